@@ -1,0 +1,436 @@
+"""CSA2 layer benchmark on GB300.
+
+One step = the whole hot path over one batch: csa2_write_cache -> csa2_index_topk ->
+csa2_attend, on seeded synthetic inputs already resident in HBM.  The headline workload is
+the T=4096 prefill from an empty cache (prefill_4k); the 1M-context decode (decode_1m,
+B=8) is measured in the same run and reported under "decode".  L2 is flushed (a 256 MiB
+write) before every timed step; each step is timed with CUDA events on the launch stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica of the workload (independent sequences,
+no data-path collective): value = all ranks' tokens / max step time over ranks.
+--impl reference times the fp64 CPU oracle on the host cores on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "CSA2 decode tok/s & prefill tok/s on 1 GB300; % of HBM / tensor-core roofline"
+H, D, DI, HI = 64, 512, 128, 32
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def seed_for_rank(base: int, rank: int) -> int:
+    """Each rank draws its own independent sequences (weak scaling)."""
+    return base + 1000 * rank
+
+
+# ------------------------------------------------------------------ work models
+def attention_rows(p0: int, T: int) -> np.ndarray:
+    t = p0 + np.arange(T, dtype=np.int64)
+    return np.minimum(128, t + 1) + np.minimum(512, (t + 1) // 2)
+
+
+def attention_flops(B: int, p0: int, T: int) -> float:
+    """QG^T and AG: 2 * 2 * 64 * n_t * 512 flops per query."""
+    return float(B * 4 * H * D * attention_rows(p0, T).sum())
+
+
+def indexer_pairs(B: int, p0: int, T: int) -> int:
+    t = p0 + np.arange(T, dtype=np.int64)
+    return int(B * ((t + 1) // 2).sum())
+
+
+def decode_bytes(B: int, p0: int) -> dict:
+    """Algorithmic HBM bytes of one decode step (T=1): indexer keys over all visible entries,
+    the 512 selected Z rows, 128 window rows, Q, Q^I, w^I, the output, the step's writes."""
+    E = (p0 + 1) // 2
+    k = min(512, E)
+    idx_keys = B * E * 68
+    rows = B * (k * 272 + min(128, p0 + 1) * 512)
+    small = B * (H * D * 2 + HI * DI * 2 + HI * 2 + H * D * 2 + 3 * D * 2 + D + 512 * 4)
+    return dict(indexer=idx_keys, step=idx_keys + rows + small)
+
+
+def launches_per_step(B: int, T: int, p0: int, num_sms: int) -> int:
+    """Kernels the three calls enqueue (mirrors the library's launch plan)."""
+    n = 0
+    new_entries = (p0 + T) // 2 - p0 // 2
+    n += (1 if new_entries > 0 else 0) + 1                    # writer: entries + window
+    emax = (p0 + T) // 2
+    ld = ((max(emax, 1) + 31) // 32) * 32
+    tq = max(1, min(T, (1 << 30) // (min(B, 128) * ld * 4)))
+    chunk = 4096
+    while chunk * 32 < ld and chunk < 32768:
+        chunk *= 2
+    for t0 in range(0, T, tq):
+        e = (p0 + t0 + min(tq, T - t0)) // 2
+        n += 1 + (1 if e > 0 else 0) + 1                      # qprep, score, top-k stage 1
+        if max(1, -(-e // chunk)) > 1:
+            n += 1                                            # top-k merge
+    nq = min(B, 128) * T
+    splits = 1 if nq >= num_sms else max(1, min(-(-2 * num_sms // nq), 20))
+    n += 1 + (1 if splits > 1 else 0)                         # attention (+ combine)
+    return n * (-(-B // 128))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = ROOT / "gpurun_out" / f"clocks_rank{gpu_index}.csv"
+
+    def __enter__(self):
+        try:
+            self.path.parent.mkdir(exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+            self.f.close()
+
+    def summary(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.path.read_text().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        busy = [s for s in sm if mx and s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our implementation
+class Step:
+    """Resident buffers and the three C-ABI calls of one workload step."""
+
+    def __init__(self, csa2, inputs, wl, seed, dev):
+        self.csa2, self.wl = csa2, wl
+        x = {}
+        x.update(inputs.layer_params(seed, dev))
+        x.update(inputs.step_inputs(wl.B, wl.T, seed, dev))
+        x.update(inputs.cache_state(wl.B, wl.T, wl.p0, wl.cap, seed, dev))
+        self.x = x
+        self.h = csa2.csa2_create()
+        self.p0 = [wl.p0] * wl.B
+        self.idx = torch.empty(wl.B, wl.T, 512, dtype=torch.int32, device=dev)
+        self.out = torch.empty(wl.B, wl.T, H, D, dtype=torch.bfloat16, device=dev)
+        self.ws_i = csa2.workspace(self.h, csa2.OP_INDEX_TOPK, wl.B, wl.T, wl.cap, dev)
+        self.ws_a = csa2.workspace(self.h, csa2.OP_ATTEND, wl.B, wl.T, 0, dev)
+
+    def write(self, s):
+        x = self.x
+        self.csa2.csa2_write_cache(self.h, x["kc"], x["gc"], x["wa"], x["gamma_c"], x["w_ik"], x["gamma_ik"],
+                                   x["gamma_w"], self.p0, x["z_codes"], x["z_scales"], x["ki_codes"], x["ki_scales"],
+                                   x["window"], x["pair_kc"], x["pair_gc"], stream=s)
+
+    def index(self, s):
+        x = self.x
+        self.csa2.csa2_index_topk(self.h, x["qi"], x["wI"], x["ki_codes"], x["ki_scales"], self.p0, self.idx,
+                                  ws=self.ws_i, stream=s)
+
+    def attend(self, s):
+        x = self.x
+        self.csa2.csa2_attend(self.h, x["q"], x["sinks"], x["z_codes"], x["z_scales"], x["window"], self.idx, self.p0,
+                              self.out, ws=self.ws_a, stream=s)
+
+
+def time_workload(step: Step, steps: int, warmup: int, ws: int, flush: torch.Tensor, clocks=None):
+    s = torch.cuda.current_stream()
+    names = ("write", "index", "attend")
+    for _ in range(warmup):
+        step.write(s); step.index(s); step.attend(s)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    ctx = clocks if clocks is not None else _Null()
+    with ctx:
+        for i in range(steps):
+            flush.zero_()  # evict L2 before each step (not timed)
+            e = ev[i]
+            e[0].record(s)
+            step.write(s)
+            e[1].record(s)
+            step.index(s)
+            e[2].record(s)
+            step.attend(s)
+            e[3].record(s)
+        torch.cuda.synchronize()
+    barrier(ws)
+    per = {n: [ev[i][k].elapsed_time(ev[i][k + 1]) for i in range(steps)] for k, n in enumerate(names)}
+    total = [sum(per[n][i] for n in names) for i in range(steps)]
+    return statistics.mean(total), {n: statistics.mean(v) for n, v in per.items()}
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def time_e2e(step: Step, steps: int, warmup: int):
+    """Same metric through the public API with HOST buffers: each step copies its inputs from
+    pinned host memory, runs the three calls, and reads the output back."""
+    x, wl = step.x, step.wl
+    keys = ("kc", "gc", "wa", "q", "qi", "wI")
+    host = {k: x[k].cpu().pin_memory() for k in keys}
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    s = torch.cuda.current_stream()
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    d2h = out_h.numel() * out_h.element_size()
+
+    def one():
+        for k in keys:
+            x[k].copy_(host[k], non_blocking=True)
+        step.write(s); step.index(s); step.attend(s)
+        out_h.copy_(step.out, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(steps):
+        one()
+    b.record(s)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": wl.B * wl.T / (ms / 1e3), "unit": "tok/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def run_ours(args, rank, ws):
+    import compressed_sparse_attention_03_gb300 as csa2
+    from compressed_sparse_attention_03_gb300 import inputs
+
+    dev = "cuda"
+    num_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    hbm, bf16, src = peaks()
+    wl = inputs.WORKLOADS[args.workload]
+    step = Step(csa2, inputs, wl, seed_for_rank(wl.seed, rank), dev)
+    clocks = ClockSampler(torch.cuda.current_device())
+    ms, per = time_workload(step, args.steps, args.warmup, ws, flush, clocks)
+    ms_max = max_over_ranks(ms, ws)
+    att_ms = max_over_ranks(per["attend"], ws)
+    flops = attention_flops(wl.B, wl.p0, wl.T)
+    achieved = flops / (att_ms / 1e3) / 1e12
+    e2e = time_e2e(step, max(2, args.steps // 2), 1)
+    e2e["value"] *= ws
+    line = {
+        "metric": METRIC, "value": ws * wl.B * wl.T / (ms_max / 1e3), "unit": "tok/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "p0": wl.p0, "seed": wl.seed,
+                   "l2": "flushed before each timed step (256 MiB write)", "parallelism": f"replicas x{ws}"},
+        "kernels_ms": per,
+        "roofline": {"kernel": "attend_kernel", "bound": "tensor", "achieved": achieved, "peak": bf16,
+                     "unit": "TFLOP/s", "frac": achieved / bf16, "peak_source": f"{src} bf16 burst",
+                     "flops_per_launch": flops, "traffic": None},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step(wl.B, wl.T, wl.p0, num_sms) * args.steps,
+        "clocks": clocks.summary(),
+    }
+    del step
+    torch.cuda.empty_cache()
+    if not args.no_decode:
+        dw = inputs.WORKLOADS[args.decode_workload]
+        dstep = Step(csa2, inputs, dw, seed_for_rank(dw.seed, rank), dev)
+        dms, dper = time_workload(dstep, args.steps, args.warmup, ws, flush)
+        dms = max_over_ranks(dms, ws)
+        idx_ms = max_over_ranks(dper["index"], ws)
+        by = decode_bytes(dw.B, dw.p0)
+        line["decode"] = {
+            "workload": dw.name, "B": dw.B, "p0": dw.p0, "value": ws * dw.B / (dms / 1e3), "unit": "tok/s",
+            "ms_per_step": dms, "kernels_ms": dper,
+            "roofline_step": {"bound": "hbm", "achieved": by["step"] / (dms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                              "frac": by["step"] / (dms / 1e3) / 1e9 / hbm, "bytes": by["step"]},
+            "roofline_index": {"bound": "hbm", "achieved": by["indexer"] / (idx_ms / 1e3) / 1e9, "peak": hbm,
+                               "unit": "GB/s", "frac": by["indexer"] / (idx_ms / 1e3) / 1e9 / hbm,
+                               "bytes": by["indexer"], "peak_source": f"{src} copy bandwidth"},
+            "gpu_launches": launches_per_step(dw.B, 1, dw.p0, num_sms) * args.steps,
+        }
+        del dstep
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------------------ the oracle (CPU baseline / reference arm)
+def cpu_baseline(wl, budget_s: float = 15.0, n_rows: int | None = None) -> dict:
+    """The fp64 oracle, as it stands, on the host cores: the writer over the whole step plus
+    indexer + top-k + attention for a sample of query rows; tokens/s extrapolated from the
+    per-row time.  Inputs are generated on the CPU (same recipe)."""
+    import oracle
+    from compressed_sparse_attention_03_gb300 import inputs
+
+    x = {}
+    x.update(inputs.layer_params(wl.seed, "cpu"))
+    x.update(inputs.step_inputs(wl.B, wl.T, wl.seed, "cpu"))
+    x.update(inputs.cache_state(wl.B, wl.T, wl.p0, wl.cap, wl.seed, "cpu"))
+    f = lambda t: t.float().numpy()
+    cores = os.cpu_count()
+    t0 = time.perf_counter()
+    w = oracle.write_seq(f(x["kc"][0]), f(x["gc"][0]), f(x["wa"][0]), f(x["gamma_c"]), f(x["w_ik"]), f(x["gamma_ik"]),
+                         f(x["gamma_w"]), wl.p0, wl.cap, z_codes=x["z_codes"][0].numpy(),
+                         z_scales=x["z_scales"][0].numpy(), ki_codes=x["ki_codes"][0].numpy(),
+                         ki_scales=x["ki_scales"][0].numpy(), pair_k=f(x["pair_kc"][0]), pair_g=f(x["pair_gc"][0]),
+                         window_prefix=x["window"][0, :127].numpy())
+    t_write = time.perf_counter() - t0
+    # rows: spread over the step; grow the sample until the budget is used
+    rows_done, t_rows = 0, 0.0
+    n = n_rows or 8
+    rng = np.random.default_rng(0)
+    while True:
+        r = np.sort(rng.choice(wl.T, size=min(n, wl.T), replace=False))
+        pos = wl.p0 + r
+        t1 = time.perf_counter()
+        sc = oracle.index_scores(pos, f(x["qi"][0][r]), f(x["wI"][0][r]), w["ki_codes"], w["ki_scales"], wl.cap)
+        oidx, _, _ = oracle.topk(sc, (pos + 1) // 2)
+        oracle.attend(pos, f(x["q"][0][r]), f(x["sinks"]), w["z_codes"], w["z_scales"], wl.cap, w["window"],
+                      wl.p0 - 127, oidx)
+        t_rows += time.perf_counter() - t1
+        rows_done += len(r)
+        if n_rows or t_write + t_rows > budget_s or rows_done >= wl.T:
+            break
+        n *= 2
+    per_row = t_rows / rows_done
+    t_step = t_write * wl.B + per_row * wl.T * wl.B  # the writer was timed on one sequence
+    return {"value": wl.B * wl.T / t_step, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"writer over all {wl.T} tokens of 1 sequence ({t_write:.2f} s) + indexer/top-k/attention "
+                      f"for {rows_done} sampled query rows ({t_rows:.2f} s); step time extrapolated per row",
+            "seconds": t_write + t_rows}
+
+
+def run_reference(args, rank, ws):
+    from compressed_sparse_attention_03_gb300 import inputs
+
+    wl = inputs.WORKLOADS[args.workload]
+    vals = []
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(wl, budget_s=min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)), n_rows=8)
+        if i >= args.warmup:
+            vals.append(cb)
+    v = statistics.mean(c["value"] for c in vals)
+    ms = wl.B * wl.T / v * 1e3
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "p0": wl.p0, "seed": wl.seed,
+                       "parallelism": "host cores (OpenMP)"},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": vals[0]["cores"], "kind": "oracle",
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill_4k")
+    ap.add_argument("--decode-workload", default="decode_1m")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    rank, ws = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, ws)), flush=True)
+        return
+    line = run_ours(args, rank, ws)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

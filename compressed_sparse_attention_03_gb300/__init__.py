@@ -1,0 +1,182 @@
+"""Python binding of libcsa2.so, the GB300 (sm_103a) CSA2 layer library.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels.
+PyTorch provides device memory and streams.  The functions carry the C-ABI names of
+``include/csa2.h`` and raise :class:`Csa2Error` on any non-OK status.  If the library has
+not been built the import of a function fails loudly; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from pathlib import Path
+
+import numpy as np
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "_build" / "libcsa2.so"
+
+OP_WRITE_CACHE, OP_INDEX_TOPK, OP_ATTEND = 0, 1, 2
+HEADS, HEAD_DIM, ROPE_DIMS, IDX_HEADS, IDX_DIM, WINDOW, TOPK = 64, 512, 64, 32, 128, 128, 512
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "inconsistent sizes", 3: "pointer not 16-byte aligned",
+           4: "workspace too small", 5: "unsupported configuration", 6: "CUDA error"}
+
+
+class Csa2Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {_STATUS.get(status, 'unknown')} (status {status})")
+        self.status = status
+
+
+class csa2_config(C.Structure):
+    _fields_ = [("heads", C.c_int), ("head_dim", C.c_int), ("rope_dims", C.c_int), ("idx_heads", C.c_int),
+                ("idx_dim", C.c_int), ("window", C.c_int), ("topk", C.c_int), ("ratio", C.c_int),
+                ("rope_base", C.c_double), ("eps", C.c_double)]
+
+
+EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_string", "csa2_workspace_bytes",
+           "csa2_write_cache", "csa2_index_topk", "csa2_attend")
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded libcsa2.so.  Raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(or python compressed_sparse_attention_03_gb300/build.py)")
+        L = C.CDLL(str(LIB_PATH))
+        p, i32, i64, sz = C.c_void_p, C.c_int, C.c_int64, C.c_size_t
+        L.csa2_default_config.argtypes = [C.POINTER(csa2_config)]
+        L.csa2_create.argtypes = [C.POINTER(csa2_config), C.POINTER(p)]
+        L.csa2_create.restype = i32
+        L.csa2_destroy.argtypes = [p]
+        L.csa2_status_string.argtypes = [i32]
+        L.csa2_status_string.restype = C.c_char_p
+        L.csa2_workspace_bytes.argtypes = [p, i32, i32, i32, i64]
+        L.csa2_workspace_bytes.restype = sz
+        L.csa2_write_cache.argtypes = [p] * 9 + [i32, i32] + [p] * 6 + [i64, p, p, sz, p]
+        L.csa2_write_cache.restype = i32
+        L.csa2_index_topk.argtypes = [p] * 5 + [i64, p, i32, i32, p, p, p, sz, p]
+        L.csa2_index_topk.restype = i32
+        L.csa2_attend.argtypes = [p] * 5 + [i64, p, p, p, i32, i32, p, p, sz, p]
+        L.csa2_attend.restype = i32
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise Csa2Error(fn, status)
+
+
+def _dev(t, dtype, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _host_p0(p0, B):
+    a = np.ascontiguousarray(np.asarray(p0.cpu() if isinstance(p0, torch.Tensor) else p0, dtype=np.int64).reshape(-1))
+    if a.size == 1 and B > 1:
+        a = np.full(B, int(a[0]), np.int64)
+    if a.size != B:
+        raise ValueError(f"p0: expected {B} positions, got {a.size}")
+    return a
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+class Handle:
+    """Owns a csa2_handle (created on the current CUDA device)."""
+
+    def __init__(self, rope_base: float = 10000.0, eps: float = 1e-20):
+        cfg = csa2_config()
+        lib().csa2_default_config(C.byref(cfg))
+        cfg.rope_base, cfg.eps = rope_base, eps
+        h = C.c_void_p()
+        _check("csa2_create", lib().csa2_create(C.byref(cfg), C.byref(h)))
+        self._h = h
+
+    @property
+    def ptr(self):
+        return self._h
+
+    def close(self):
+        if self._h:
+            lib().csa2_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def csa2_create(rope_base: float = 10000.0, eps: float = 1e-20) -> Handle:
+    return Handle(rope_base, eps)
+
+
+def csa2_workspace_bytes(h: Handle, op: int, B: int, T: int, max_entries: int) -> int:
+    return int(lib().csa2_workspace_bytes(h.ptr, op, B, T, max_entries))
+
+
+def workspace(h: Handle, op: int, B: int, T: int, max_entries: int, device=None) -> torch.Tensor:
+    """A uint8 CUDA tensor sized by csa2_workspace_bytes (at least 16 bytes)."""
+    n = max(16, csa2_workspace_bytes(h, op, B, T, max_entries))
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def csa2_write_cache(h: Handle, kc, gc, wa, gamma_c, w_ik, gamma_ik, gamma_w, p0, z_codes, z_scales, ki_codes,
+                     ki_scales, window, pair_kc=None, pair_gc=None, stream=None) -> None:
+    B, T, _ = kc.shape
+    p0a = _host_p0(p0, B)
+    cap = z_codes.shape[1]
+    _check("csa2_write_cache", lib().csa2_write_cache(
+        h.ptr, _dev(kc, torch.bfloat16, "kc"), _dev(gc, torch.bfloat16, "gc"), _dev(wa, torch.bfloat16, "wa"),
+        _dev(gamma_c, torch.float32, "gamma_c"), _dev(w_ik, torch.bfloat16, "w_ik"),
+        _dev(gamma_ik, torch.float32, "gamma_ik"), _dev(gamma_w, torch.float32, "gamma_w"),
+        p0a.ctypes.data_as(C.c_void_p), B, T, _dev(pair_kc, torch.float32, "pair_kc"),
+        _dev(pair_gc, torch.float32, "pair_gc"), _dev(z_codes, torch.uint8, "z_codes"),
+        _dev(z_scales, torch.uint8, "z_scales"), _dev(ki_codes, torch.uint8, "ki_codes"),
+        _dev(ki_scales, torch.uint8, "ki_scales"), cap, _dev(window, torch.uint8, "window"), None, 0,
+        _stream(stream)))
+
+
+def csa2_index_topk(h: Handle, qi, wI, ki_codes, ki_scales, p0, idx, top_scores=None, ws=None, stream=None) -> None:
+    B, T = qi.shape[:2]
+    p0a = _host_p0(p0, B)
+    cap = ki_codes.shape[1]
+    if ws is None:
+        ws = workspace(h, OP_INDEX_TOPK, B, T, int(((p0a + T) // 2).max()), qi.device)
+    _check("csa2_index_topk", lib().csa2_index_topk(
+        h.ptr, _dev(qi, torch.bfloat16, "qi"), _dev(wI, torch.bfloat16, "wI"), _dev(ki_codes, torch.uint8, "ki_codes"),
+        _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
+        _dev(idx, torch.int32, "idx"), _dev(top_scores, torch.float32, "top_scores"), _dev(ws, torch.uint8, "ws"),
+        ws.numel(), _stream(stream)))
+
+
+def csa2_attend(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, out, ws=None, stream=None) -> None:
+    B, T = q.shape[:2]
+    p0a = _host_p0(p0, B)
+    cap = z_codes.shape[1]
+    if ws is None:
+        ws = workspace(h, OP_ATTEND, B, T, 0, q.device)
+    _check("csa2_attend", lib().csa2_attend(
+        h.ptr, _dev(q, torch.bfloat16, "q"), _dev(sinks, torch.float32, "sinks"), _dev(z_codes, torch.uint8, "z_codes"),
+        _dev(z_scales, torch.uint8, "z_scales"), cap, _dev(window, torch.uint8, "window"),
+        _dev(idx, torch.int32, "idx"), p0a.ctypes.data_as(C.c_void_p), B, T, _dev(out, torch.bfloat16, "out"),
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))

@@ -1,0 +1,205 @@
+// C-ABI front end of libcsa2.so: argument validation, the handle, workspace sizing, and the
+// split of large batches into launches of at most kMaxSeqPerLaunch sequences.
+// The entry points and their contracts are documented in include/csa2.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "../../include/csa2.h"
+#include "csa2_internal.h"
+
+struct csa2_handle {
+  csa2_config cfg;
+  csa2::RopeFreq rf;
+  int device;
+  int num_sms;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa2::SeqPos pack_pos(const int64_t* p0, int b0, int nb) {
+  csa2::SeqPos s;
+  std::memset(&s, 0, sizeof s);
+  for (int i = 0; i < nb; ++i) s.p0[i] = p0[b0 + i];
+  return s;
+}
+
+csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+// Largest visible-entry count over the batch for queries p0..p0+T-1: floor((p0+T)/2).
+int64_t max_visible(const int64_t* p0, int B, int T) {
+  int64_t m = 0;
+  for (int b = 0; b < B; ++b) m = std::max<int64_t>(m, (p0[b] + T) / 2);
+  return m;
+}
+
+// Positions are limited so that every entry index and window row fits int32 arithmetic
+// used by the kernels and the top-k candidate domain (at most 2^20 entries per query).
+constexpr int64_t kMaxPos = (int64_t(1) << 21) - 2;
+
+csa2_status check_p0(const int64_t* p0, int B, int T) {
+  if (!p0) return CSA2_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (p0[b] < 0 || p0[b] + T > kMaxPos) return CSA2_ERR_SHAPE;
+  return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void csa2_default_config(csa2_config* c) {
+  if (!c) return;
+  c->heads = 64;
+  c->head_dim = 512;
+  c->rope_dims = 64;
+  c->idx_heads = 32;
+  c->idx_dim = 128;
+  c->window = 128;
+  c->topk = 512;
+  c->ratio = 2;
+  c->rope_base = 10000.0;
+  c->eps = 1e-20;
+}
+
+csa2_status csa2_create(const csa2_config* cfg, csa2_handle** out) {
+  if (!out) return CSA2_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg) return CSA2_ERR_INVALID_ARG;
+  if (cfg->heads != 64 || cfg->head_dim != 512 || cfg->rope_dims != 64 || cfg->idx_heads != 32 || cfg->idx_dim != 128 ||
+      cfg->window != 128 || cfg->topk != 512 || cfg->ratio != 2)
+    return CSA2_ERR_UNSUPPORTED;
+  if (!(cfg->rope_base > 1.0) || !std::isfinite(cfg->rope_base) || !(cfg->eps >= 0.0) || !std::isfinite(cfg->eps))
+    return CSA2_ERR_INVALID_ARG;
+  csa2_handle* h = new (std::nothrow) csa2_handle;
+  if (!h) return CSA2_ERR_INVALID_ARG;
+  h->cfg = *cfg;
+  for (int i = 0; i < csa2::kDR / 2; ++i) h->rf.inv_freq[i] = std::pow(cfg->rope_base, -2.0 * i / csa2::kDR);
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    delete h;
+    return CSA2_ERR_CUDA;
+  }
+  *out = h;
+  return CSA2_OK;
+}
+
+void csa2_destroy(csa2_handle* h) { delete h; }
+
+const char* csa2_status_string(csa2_status s) {
+  switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_INVALID_ARG: return "invalid argument";
+    case CSA2_ERR_SHAPE: return "inconsistent sizes";
+    case CSA2_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case CSA2_ERR_WORKSPACE: return "workspace too small";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CSA2_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+size_t csa2_workspace_bytes(const csa2_handle* h, int op, int B, int T, int64_t max_entries) {
+  if (!h || B <= 0 || T <= 0 || max_entries < 0) return 0;
+  switch (op) {
+    case CSA2_OP_WRITE_CACHE: return 0;
+    case CSA2_OP_INDEX_TOPK: return csa2::index_workspace_bytes(B, T, max_entries, h->num_sms);
+    case CSA2_OP_ATTEND: return csa2::attend_workspace_bytes(B, T, h->num_sms);
+  }
+  return 0;
+}
+
+csa2_status csa2_write_cache(csa2_handle* h, const uint16_t* kc, const uint16_t* gc, const uint16_t* wa,
+                             const float* gamma_c, const uint16_t* w_ik, const float* gamma_ik, const float* gamma_w,
+                             const int64_t* p0, int B, int T, float* pair_kc, float* pair_gc, uint8_t* z_codes,
+                             uint8_t* z_scales, uint8_t* ki_codes, uint8_t* ki_scales, int64_t cap, uint8_t* window,
+                             void* /*ws*/, size_t /*ws_bytes*/, csa2_stream_t stream) {
+  if (!h || !kc || !gc || !wa || !gamma_c || !w_ik || !gamma_ik || !gamma_w || !z_codes || !z_scales || !ki_codes ||
+      !ki_scales || !window)
+    return CSA2_ERR_INVALID_ARG;
+  if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  csa2_status st = check_p0(p0, B, T);
+  if (st != CSA2_OK) return st;
+  bool need_pair = (T & 1) != 0;
+  for (int b = 0; b < B; ++b) {
+    if (p0[b] & 1) need_pair = true;
+    if ((p0[b] + T) / 2 > cap) return CSA2_ERR_SHAPE;  // last entry index floor((p0+T)/2)-1 < cap
+  }
+  if (need_pair && (!pair_kc || !pair_gc)) return CSA2_ERR_INVALID_ARG;
+  const void* ptrs[] = {kc, gc, wa, gamma_c, w_ik, gamma_ik, gamma_w, z_codes, z_scales, ki_codes, ki_scales, window};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CSA2_ERR_ALIGN;
+  if ((pair_kc && !aligned16(pair_kc)) || (pair_gc && !aligned16(pair_gc))) return CSA2_ERR_ALIGN;
+  csa2::WriterArgs a{};
+  for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
+    const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
+    a.kc = kc; a.gc = gc; a.wa = wa; a.w_ik = w_ik;
+    a.gamma_c = gamma_c; a.gamma_ik = gamma_ik; a.gamma_w = gamma_w;
+    a.pair_kc = pair_kc; a.pair_gc = pair_gc;
+    a.z_codes = z_codes; a.z_scales = z_scales; a.ki_codes = ki_codes; a.ki_scales = ki_scales; a.window = window;
+    a.cap = cap; a.T = T; a.eps = h->cfg.eps;
+    st = cuda_status(csa2::launch_writer(a, pack_pos(p0, b0, nb), b0, nb, h->rf, reinterpret_cast<cudaStream_t>(stream)));
+    if (st != CSA2_OK) return st;
+  }
+  return CSA2_OK;
+}
+
+csa2_status csa2_index_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, const uint8_t* ki_codes,
+                            const uint8_t* ki_scales, int64_t cap, const int64_t* p0, int B, int T, int32_t* idx,
+                            float* top_scores, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  if (!h || !qi || !wI || !ki_codes || !ki_scales || !idx) return CSA2_ERR_INVALID_ARG;
+  if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  csa2_status st = check_p0(p0, B, T);
+  if (st != CSA2_OK) return st;
+  const int64_t emax = max_visible(p0, B, T);
+  if (emax > cap) return CSA2_ERR_SHAPE;
+  if (emax > (int64_t(1) << 20)) return CSA2_ERR_UNSUPPORTED;
+  const void* ptrs[] = {qi, wI, ki_codes, ki_scales, idx};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CSA2_ERR_ALIGN;
+  if (top_scores && !aligned16(top_scores)) return CSA2_ERR_ALIGN;
+  const size_t need = csa2::index_workspace_bytes(B, T, emax, h->num_sms);
+  if (ws_bytes < need || (need && !ws)) return CSA2_ERR_WORKSPACE;
+  if (!aligned16(ws)) return CSA2_ERR_ALIGN;
+  csa2::IndexArgs a{};
+  a.qi = qi; a.wI = wI; a.ki_codes = ki_codes; a.ki_scales = ki_scales; a.cap = cap; a.T = T;
+  a.idx = idx; a.top_scores = top_scores;
+  for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
+    const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
+    st = cuda_status(csa2::launch_index_topk(a, pack_pos(p0, b0, nb), b0, nb, emax, ws, ws_bytes, h->num_sms,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+    if (st != CSA2_OK) return st;
+  }
+  return CSA2_OK;
+}
+
+csa2_status csa2_attend(csa2_handle* h, const uint16_t* q, const float* sinks, const uint8_t* z_codes,
+                        const uint8_t* z_scales, int64_t cap, const uint8_t* window, const int32_t* idx,
+                        const int64_t* p0, int B, int T, uint16_t* out, void* ws, size_t ws_bytes,
+                        csa2_stream_t stream) {
+  if (!h || !q || !sinks || !z_codes || !z_scales || !window || !idx || !out) return CSA2_ERR_INVALID_ARG;
+  if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  csa2_status st = check_p0(p0, B, T);
+  if (st != CSA2_OK) return st;
+  const void* ptrs[] = {q, sinks, z_codes, z_scales, window, idx, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CSA2_ERR_ALIGN;
+  const size_t need = csa2::attend_workspace_bytes(B, T, h->num_sms);
+  if (ws_bytes < need || (need && !ws)) return CSA2_ERR_WORKSPACE;
+  if (need && !aligned16(ws)) return CSA2_ERR_ALIGN;
+  csa2::AttendArgs a{};
+  a.q = q; a.sinks = sinks; a.z_codes = z_codes; a.z_scales = z_scales; a.window = window; a.idx = idx;
+  a.cap = cap; a.T = T; a.out = out;
+  for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
+    const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
+    st = cuda_status(csa2::launch_attend(a, pack_pos(p0, b0, nb), b0, nb, h->rf, ws, ws_bytes, h->num_sms,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+    if (st != CSA2_OK) return st;
+  }
+  return CSA2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+// Device helpers shared by the CSA2 kernels: FP4 (E2M1 + UE8M0/32) and FP8 (E4M3fn)
+// codecs, RoPE angles, bf16 loads and block reductions.  Formats follow "Inside DeepSeek
+// V4.1", section "890 bytes" (FP4 entries with 8-bit scales, FP8 window) with the scale
+// rule fixed by this library (one UE8M0 per 32 values, OCP MX choice of exponent).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa2_internal.h"
+
+namespace csa2 {
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// E2M1 code (4 bits) -> value.  1 sign, 2 exponent (bias 1), 1 mantissa; exponent 0 is
+// subnormal.  Written as arithmetic on the fields.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+  uint32_t e = (c >> 1) & 3, m = c & 1;
+  float mag = e == 0 ? 0.5f * (float)m : __uint_as_float((e + 126u) << 23) * (1.0f + 0.5f * (float)m);
+  return (c & 8) ? -mag : mag;
+}
+
+// Scaled value x (already divided by the block scale) -> E2M1 code, round to nearest with
+// ties to the even code (mantissa bit 0), saturating at 6.  The decision points are the
+// midpoints 0.25 0.75 1.25 1.75 2.5 3.5 5; at a midpoint the even neighbour wins, which is
+// the lower one at 0.25 1.25 2.5 5 (codes 0 2 4 6) and the upper one at 0.75 1.75 3.5.
+__device__ __forceinline__ uint32_t f32_to_e2m1(float x) {
+  uint32_t s = (__float_as_uint(x) >> 28) & 8u;
+  float a = fabsf(x);
+  uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+  return s | m;
+}
+
+// UE8M0 exponent for a block with absolute maximum amax: floor(log2 amax) - 2, clamped to
+// [-127, 127]; amax == 0 (or subnormal) gives -127.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+  int E = (int)((__float_as_uint(amax) >> 23) & 255u);
+  if (E == 0) return -127;
+  return max(-127, E - 127 - 2);
+}
+
+// E4M3fn: value = (E + 6) * 8 + q form.  Round to nearest even within the binade of `a`
+// (subnormals share the step of the lowest binade), saturate to 448 (code 0x7E).
+__device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
+  uint32_t s = (__float_as_uint(v) >> 24) & 0x80u;
+  float a = fabsf(v);
+  if (a != a) return 0x7Fu;
+  if (!(a < 448.0f)) return s | 0x7Eu;
+  int E = (int)((__float_as_uint(a) >> 23) & 255u) - 127;  // floor(log2 a) for normal a
+  E = max(E, -6);
+  float q = rintf(ldexpf(a, 3 - E));  // exact scaling, then round half to even
+  return s | (uint32_t)((E + 6) * 8 + (int)q);
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  uint32_t e = (c >> 3) & 15, m = c & 7;
+  float mag = e == 0 ? ldexpf((float)m, -9) : ldexpf(1.0f + 0.125f * (float)m, (int)e - 7);
+  return (c & 0x80) ? -mag : mag;
+}
+
+// cos/sin of pos * inv_freq: the angle is formed and reduced modulo 2*pi in fp64 (positions
+// reach ~2^21, where an fp32 product would be off by ~0.1 rad), then evaluated in fp32.
+__device__ __forceinline__ void rope_cs(int64_t pos, double inv_freq, float sign, float& c, float& s) {
+  const double two_pi_hi = 6.283185307179586;          // nearest double to 2*pi
+  const double two_pi_lo = 2.4492935982947064e-16;     // 2*pi - two_pi_hi
+  double ang = (double)pos * inv_freq;
+  double k = rint(ang * 0.15915494309189535);
+  double r = fma(-k, two_pi_hi, ang);
+  r = fma(-k, two_pi_lo, r);
+  sincosf(sign * (float)r, &s, &c);
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Sum over a block of NT threads (NT multiple of 32, <= 1024).  `red` holds NT/32 values.
+template <int NT, typename T>
+__device__ __forceinline__ T block_sum(T v, T* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  T t = 0;
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) t += red[i];
+  return t;
+}
+
+}  // namespace csa2

@@ -1,0 +1,407 @@
+// Lightning indexer and top-512.  Page "DeepSeek V4.1 - Pooled group / Source layer, pairs
+// pooled", block "Compressed sparse attention": S^I_{t,j} = sum_h w^I_{t,h} ReLU(Q^I_{h,t} .
+// K^I_j) over j < floor((t+1)/2), and I_t = top_512 of those scores.  "Inside DeepSeek
+// V4.1", section "Attention that looks at 640 places": 32 heads of 128 numbers in FP4, one
+// key per entry, the top 512 are kept.
+//
+// Q^I is quantised to FP4 (E2M1, UE8M0 per 32) like the keys; every per-head dot product
+// is then a sum of exact products of E2M1 values times powers of two and is exact in fp32.
+// Scores are fp32.  Top-k: larger score first, equal scores -> lower j first, output
+// ascending in j, -1 padded.
+#include "csa2_common.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kQprepThreads = 128;
+constexpr int kScoreThreads = 256;  // one key per thread
+constexpr int kQT = 4;              // queries per score block
+constexpr int kTopkThreads = 512;
+constexpr int kMaxChunks = 32;
+constexpr int kMinChunk = 4096;
+constexpr int kMaxChunk = 32768;
+constexpr size_t kScoreBudget = size_t(1) << 30;  // bytes of fp32 scores per query chunk
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct IndexPlan {
+  int Tq;           // queries (per sequence) per pass
+  int64_t ld;       // score row stride (floats)
+  int chunk;        // top-k stage-1 chunk
+  int nchunks;
+  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, total;
+};
+
+IndexPlan make_plan(int nb, int T, int64_t max_entries) {
+  IndexPlan p;
+  p.ld = ((max(max_entries, (int64_t)1) + 31) / 32) * 32;
+  int64_t per_q = (int64_t)nb * p.ld * 4;
+  int64_t tq = (int64_t)(kScoreBudget / (size_t)per_q);
+  p.Tq = (int)max64(1, min64(T, tq));
+  int64_t c = kMinChunk;
+  while (c * kMaxChunks < p.ld && c < kMaxChunk) c *= 2;
+  p.chunk = (int)c;
+  p.nchunks = (int)((p.ld + c - 1) / c);
+  size_t rows = (size_t)nb * p.Tq;
+  size_t off = 0;
+  p.off_q = off; off += align256(rows * kHI * kDI * 4);
+  p.off_w = off; off += align256(rows * kHI * 4);
+  p.off_s = off; off += align256(rows * (size_t)p.ld * 4);
+  p.off_ck = off; off += align256(rows * p.nchunks * kTopK * 4);
+  p.off_cj = off; off += align256(rows * p.nchunks * kTopK * 4);
+  p.off_cn = off; off += align256(rows * p.nchunks * 4);
+  p.total = off;
+  return p;
+}
+
+// ------------------------------------------------------------------ Q^I -> FP4 -> fp32
+// grid (Tq, nb): one block per query, warp w handles heads 8w..8w+7, lane l values 4l..4l+3.
+__global__ void __launch_bounds__(kQprepThreads) qprep_kernel(IndexArgs a, int b0, int t0, int Tq, float* qdq, float* wq) {
+  const int tl = blockIdx.x, bl = blockIdx.y;
+  const int t = t0 + tl;
+  if (t >= a.T) return;
+  const int b = b0 + bl;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int64_t src = ((int64_t)b * a.T + t);
+  const int64_t dst = ((int64_t)bl * Tq + tl);
+  for (int h = 8 * w; h < 8 * w + 8; ++h) {
+    uint2 raw = *reinterpret_cast<const uint2*>(a.qi + (src * kHI + h) * kDI + 4 * l);
+    float v[4] = {bf16_to_f32(raw.x & 0xffff), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xffff), bf16_to_f32(raw.y >> 16)};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const int e = mx_scale_exp(amax);
+    float4 o;
+    o.x = ldexpf(e2m1_to_f32(f32_to_e2m1(ldexpf(v[0], -e))), e);
+    o.y = ldexpf(e2m1_to_f32(f32_to_e2m1(ldexpf(v[1], -e))), e);
+    o.z = ldexpf(e2m1_to_f32(f32_to_e2m1(ldexpf(v[2], -e))), e);
+    o.w = ldexpf(e2m1_to_f32(f32_to_e2m1(ldexpf(v[3], -e))), e);
+    *reinterpret_cast<float4*>(qdq + (dst * kHI + h) * kDI + 4 * l) = o;
+  }
+  if (threadIdx.x < kHI) wq[dst * kHI + threadIdx.x] = bf16_to_f32(a.wI[src * kHI + threadIdx.x]);
+}
+
+// ------------------------------------------------------------------ score scan (CUDA cores)
+// grid (key tiles of 256, query tiles of kQT, nb).  Thread = key j; the key's 128 FP4 values
+// are decoded one 32-block at a time and dotted with the 32 heads of each query in smem.
+__global__ void __launch_bounds__(kScoreThreads) score_kernel(IndexArgs a, SeqPos pos, int b0, int t0, int Tq,
+                                                              const float* qdq, const float* wq, float* scores, int64_t ld) {
+  extern __shared__ float4 smem4[];
+  float* sq = reinterpret_cast<float*>(smem4);  // [kQT][32][128]
+  __shared__ float sw[kQT][kHI];
+  const int bl = blockIdx.z;
+  const int b = b0 + bl;
+  const int64_t p0 = pos.p0[bl];
+  const int tq0 = blockIdx.y * kQT;
+  const int64_t j = (int64_t)blockIdx.x * kScoreThreads + threadIdx.x;
+  // visible entries of the last query of the tile bound the whole tile
+  const int tlast = min(tq0 + kQT, Tq) - 1;
+  if (t0 + tq0 >= a.T) return;
+  const int64_t Elast = (p0 + t0 + min(tlast, a.T - 1 - t0) + 1) / 2;
+  if ((int64_t)blockIdx.x * kScoreThreads >= Elast) return;
+  const int nq = min(kQT, min(Tq, a.T - t0) - tq0);
+  for (int i = threadIdx.x; i < nq * kHI * kDI / 4; i += kScoreThreads)
+    smem4[i] = reinterpret_cast<const float4*>(qdq + ((int64_t)bl * Tq + tq0) * kHI * kDI)[i];
+  for (int i = threadIdx.x; i < nq * kHI; i += kScoreThreads)
+    sw[i / kHI][i % kHI] = wq[((int64_t)bl * Tq + tq0) * kHI + i];
+  __syncthreads();
+  if (j >= Elast) return;
+  uint4 cw[4];
+  const uint4* kp = reinterpret_cast<const uint4*>(a.ki_codes + ((int64_t)b * a.cap + j) * 64);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) cw[i] = kp[i];
+  const uint32_t sc = *reinterpret_cast<const uint32_t*>(a.ki_scales + ((int64_t)b * a.cap + j) * 4);
+  for (int qq = 0; qq < nq; ++qq) {
+    const int t = t0 + tq0 + qq;
+    const int64_t E = (p0 + t + 1) / 2;
+    if (j >= E) continue;
+    float acc[kHI];
+#pragma unroll
+    for (int h = 0; h < kHI; ++h) acc[h] = 0.f;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+      const float s = ldexpf(1.0f, (int)((sc >> (8 * blk)) & 255) - 127);
+      float k[32];
+      const uint32_t words[4] = {cw[blk].x, cw[blk].y, cw[blk].z, cw[blk].w};
+#pragma unroll
+      for (int wd = 0; wd < 4; ++wd)
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) k[8 * wd + nb] = e2m1_to_f32((words[wd] >> (4 * nb)) & 15) * s;
+      const float* qb = sq + (qq * kHI) * kDI + blk * 32;
+#pragma unroll
+      for (int h = 0; h < kHI; ++h) {
+        const float4* q4 = reinterpret_cast<const float4*>(qb + h * kDI);
+        float d = acc[h];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float4 qv = q4[i];
+          d = fmaf(k[4 * i], qv.x, d);
+          d = fmaf(k[4 * i + 1], qv.y, d);
+          d = fmaf(k[4 * i + 2], qv.z, d);
+          d = fmaf(k[4 * i + 3], qv.w, d);
+        }
+        acc[h] = d;
+      }
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int h = 0; h < kHI; ++h) s = fmaf(sw[qq][h], fmaxf(acc[h], 0.f), s);
+    scores[((int64_t)bl * Tq + tq0 + qq) * ld + j] = s;
+  }
+}
+
+// ------------------------------------------------------------------ top-k
+// Order-preserving map of a float score to uint32 (larger score -> larger key, -0 == +0).
+__device__ __forceinline__ uint32_t score_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u << 1) == 0) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+struct SelectShared {
+  uint32_t hist[256];
+  int warp_tot[2][kTopkThreads / 32];
+  uint32_t bucket;
+  int krem;
+};
+
+// Radix select over keys[0..n): on return *thr is the K-th largest key and *need_eq the
+// number of keys equal to *thr that belong to the top K (the lowest-index ones).
+__device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared& sh, uint32_t* thr, int* need_eq) {
+  const int tid = threadIdx.x;
+  uint32_t prefix = 0, mask = 0;
+  int krem = K;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kTopkThreads) sh.hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kTopkThreads) {
+      const uint32_t k = keys[i];
+      if ((k & mask) == prefix) atomicAdd(&sh.hist[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // lane l owns bins 255-8l .. 248-8l (descending)
+      uint32_t c[8], tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { c[i] = sh.hist[255 - 8 * tid - i]; tot += c[i]; }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += v;
+      }
+      const uint32_t excl = incl - tot;
+      const bool mine = excl < (uint32_t)krem && incl >= (uint32_t)krem;
+      if (mine) {
+        uint32_t run = excl;
+        for (int i = 0; i < 8; ++i) {
+          if (run + c[i] >= (uint32_t)krem) {
+            sh.bucket = 255 - 8 * tid - i;
+            sh.krem = krem - (int)run;
+            break;
+          }
+          run += c[i];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= sh.bucket << shift;
+    mask |= 255u << shift;
+    krem = sh.krem;
+    __syncthreads();
+  }
+  *thr = prefix;
+  *need_eq = krem;
+}
+
+// Writes the K selected (key, j) pairs in ascending position order.  Keys > thr are all
+// taken; of the keys == thr only the first need_eq (in position order).  js == nullptr
+// means j = j0 + position.  Returns nothing; out_* receive exactly K entries.
+__device__ void compact_selected(const uint32_t* keys, const int32_t* js, int64_t j0, int n, uint32_t thr, int need_eq,
+                                 SelectShared& sh, uint32_t* out_key, int32_t* out_j) {
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+  constexpr int NW = kTopkThreads / 32;
+  int eq_base = 0, out_base = 0;
+  for (int r0 = 0; r0 < n; r0 += kTopkThreads) {
+    const int i = r0 + tid;
+    const uint32_t k = i < n ? keys[i] : 0u;
+    const bool is_gt = i < n && k > thr;
+    const bool is_eq = i < n && k == thr;
+    const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
+    if (l == 0) sh.warp_tot[0][w] = __popc(beq);
+    __syncthreads();
+    int eq_before = eq_base;
+    int eq_round = 0;
+    for (int x = 0; x < NW; ++x) {
+      const int v = sh.warp_tot[0][x];
+      if (x < w) eq_before += v;
+      eq_round += v;
+    }
+    eq_before += __popc(beq & ((1u << l) - 1u));
+    const bool take = is_gt || (is_eq && eq_before < need_eq);
+    const uint32_t bt = __ballot_sync(0xffffffffu, take);
+    if (l == 0) sh.warp_tot[1][w] = __popc(bt);
+    __syncthreads();
+    int pos = out_base, t_round = 0;
+    for (int x = 0; x < NW; ++x) {
+      const int v = sh.warp_tot[1][x];
+      if (x < w) pos += v;
+      t_round += v;
+    }
+    pos += __popc(bt & ((1u << l) - 1u));
+    if (take) {
+      out_key[pos] = k;
+      out_j[pos] = js ? js[i] : (int32_t)(j0 + i);
+    }
+    eq_base += eq_round;
+    out_base += t_round;
+    __syncthreads();
+  }
+}
+
+// Stage 1: grid (nchunks, rows, nb).  Local top-512 of one chunk of one query's scores.
+// With a single chunk the result is final and goes straight to idx / top_scores.
+__global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, SeqPos pos, int b0, int t0, int Tq,
+                                                                  const float* scores, int64_t ld, int chunk, int nchunks,
+                                                                  uint32_t* ck, int32_t* cj, int* cn) {
+  extern __shared__ uint32_t skeys[];
+  __shared__ SelectShared sh;
+  __shared__ uint32_t okey[kTopK];
+  __shared__ int32_t oj[kTopK];
+  const int c = blockIdx.x, tl = blockIdx.y, bl = blockIdx.z;
+  const int t = t0 + tl;
+  if (t >= a.T || tl >= Tq) return;
+  const int b = b0 + bl;
+  const int64_t E = (pos.p0[bl] + t + 1) / 2;
+  const int64_t cs = (int64_t)c * chunk;
+  const int n = (int)max64(0, min64(chunk, E - cs));
+  const int64_t row = (int64_t)bl * Tq + tl;
+  const float* src = scores + row * ld + cs;
+  for (int i = threadIdx.x; i < n; i += kTopkThreads) skeys[i] = score_key(src[i]);
+  __syncthreads();
+  const int K = min(kTopK, n);
+  if (K > 0) {
+    uint32_t thr;
+    int need_eq;
+    radix_select(skeys, n, K, sh, &thr, &need_eq);
+    compact_selected(skeys, nullptr, cs, n, thr, need_eq, sh, okey, oj);
+  }
+  __syncthreads();
+  if (nchunks == 1) {
+    int32_t* idx = a.idx + ((int64_t)b * a.T + t) * kTopK;
+    float* ts = a.top_scores ? a.top_scores + ((int64_t)b * a.T + t) * kTopK : nullptr;
+    for (int i = threadIdx.x; i < kTopK; i += kTopkThreads) {
+      idx[i] = i < K ? oj[i] : -1;
+      if (ts) ts[i] = i < K ? key_score(okey[i]) : __int_as_float(0x7fc00000);
+    }
+  } else {
+    const int64_t base = (row * nchunks + c) * kTopK;
+    for (int i = threadIdx.x; i < K; i += kTopkThreads) {
+      ck[base + i] = okey[i];
+      cj[base + i] = oj[i];
+    }
+    if (threadIdx.x == 0) cn[row * nchunks + c] = K;
+  }
+}
+
+// Stage 2: grid (rows, nb).  Merge the chunk candidates of one query.
+__global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(IndexArgs a, int b0, int t0, int Tq, int nchunks,
+                                                                  const uint32_t* ck, const int32_t* cj, const int* cn) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* skeys = smem;                                                // [nchunks*512]
+  int32_t* sjs = reinterpret_cast<int32_t*>(smem + nchunks * kTopK);    // [nchunks*512]
+  __shared__ SelectShared sh;
+  __shared__ uint32_t okey[kTopK];
+  __shared__ int32_t oj[kTopK];
+  __shared__ int offs[kMaxChunks + 1];
+  const int tl = blockIdx.x, bl = blockIdx.y;
+  const int t = t0 + tl;
+  if (t >= a.T) return;
+  const int b = b0 + bl;
+  const int64_t row = (int64_t)bl * Tq + tl;
+  if (threadIdx.x == 0) {
+    offs[0] = 0;
+    for (int c = 0; c < nchunks; ++c) offs[c + 1] = offs[c] + cn[row * nchunks + c];
+  }
+  __syncthreads();
+  const int n = offs[nchunks];
+  for (int c = 0; c < nchunks; ++c) {
+    const int cnt = offs[c + 1] - offs[c];
+    const int64_t base = (row * nchunks + c) * kTopK;
+    for (int i = threadIdx.x; i < cnt; i += kTopkThreads) {
+      skeys[offs[c] + i] = ck[base + i];
+      sjs[offs[c] + i] = cj[base + i];
+    }
+  }
+  __syncthreads();
+  const int K = min(kTopK, n);
+  if (K > 0) {
+    uint32_t thr;
+    int need_eq;
+    radix_select(skeys, n, K, sh, &thr, &need_eq);
+    compact_selected(skeys, sjs, 0, n, thr, need_eq, sh, okey, oj);
+  }
+  __syncthreads();
+  int32_t* idx = a.idx + ((int64_t)b * a.T + t) * kTopK;
+  float* ts = a.top_scores ? a.top_scores + ((int64_t)b * a.T + t) * kTopK : nullptr;
+  for (int i = threadIdx.x; i < kTopK; i += kTopkThreads) {
+    idx[i] = i < K ? oj[i] : -1;
+    if (ts) ts[i] = i < K ? key_score(okey[i]) : __int_as_float(0x7fc00000);
+  }
+}
+
+}  // namespace
+
+size_t index_workspace_bytes(int B, int T, int64_t max_entries, int /*num_sms*/) {
+  return make_plan(min(B, kMaxSeqPerLaunch), T, max_entries).total;
+}
+
+cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int64_t max_entries, void* ws,
+                              size_t ws_bytes, int /*num_sms*/, cudaStream_t st) {
+  const IndexPlan p = make_plan(min(nb, kMaxSeqPerLaunch), a.T, max_entries);
+  if (ws_bytes < p.total) return cudaErrorInvalidValue;
+  char* base = static_cast<char*>(ws);
+  float* qdq = reinterpret_cast<float*>(base + p.off_q);
+  float* wq = reinterpret_cast<float*>(base + p.off_w);
+  float* sc = reinterpret_cast<float*>(base + p.off_s);
+  uint32_t* ck = reinterpret_cast<uint32_t*>(base + p.off_ck);
+  int32_t* cj = reinterpret_cast<int32_t*>(base + p.off_cj);
+  int* cn = reinterpret_cast<int*>(base + p.off_cn);
+  const size_t score_smem = (size_t)kQT * kHI * kDI * 4;
+  const size_t chunk_smem = (size_t)p.chunk * 4;
+  const size_t merge_smem = (size_t)p.nchunks * kTopK * 8;
+  cudaError_t e;
+  e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)score_smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chunk_smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)merge_smem);
+  if (e != cudaSuccess) return e;
+  for (int t0 = 0; t0 < a.T; t0 += p.Tq) {
+    const int tq = min(p.Tq, a.T - t0);
+    int64_t emax = 0;
+    for (int i = 0; i < nb; ++i) emax = max(emax, (pos.p0[i] + t0 + tq) / 2);
+    qprep_kernel<<<dim3(tq, nb), kQprepThreads, 0, st>>>(a, b0, t0, p.Tq, qdq, wq);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (emax > 0) {
+      dim3 g((unsigned)((emax + kScoreThreads - 1) / kScoreThreads), (unsigned)((tq + kQT - 1) / kQT), (unsigned)nb);
+      score_kernel<<<g, kScoreThreads, score_smem, st>>>(a, pos, b0, t0, p.Tq, qdq, wq, sc, p.ld);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const int nch = (int)max64(1, (emax + p.chunk - 1) / p.chunk);
+    topk_chunk_kernel<<<dim3(nch, tq, nb), kTopkThreads, chunk_smem, st>>>(a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch,
+                                                                            ck, cj, cn);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (nch > 1) {
+      topk_merge_kernel<<<dim3(tq, nb), kTopkThreads, (size_t)nch * kTopK * 8, st>>>(a, b0, t0, p.Tq, nch, ck, cj, cn);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+  }
+  return cudaSuccess;
+}
+
+}  // namespace csa2

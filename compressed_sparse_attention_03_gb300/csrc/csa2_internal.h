@@ -1,0 +1,68 @@
+// Internal declarations shared by the C-ABI front end (csa2_api.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace csa2 {
+
+constexpr int kD = 512;      // entry / head width
+constexpr int kDR = 64;      // rotated dims (last 64 of Z, W, Q, O)
+constexpr int kDI = 128;     // indexer key width
+constexpr int kHI = 32;      // indexer heads
+constexpr int kH = 64;       // attention heads
+constexpr int kWin = 128;    // window rows
+constexpr int kTopK = 512;   // selected entries
+constexpr int kMaxSeqPerLaunch = 128;  // sequences whose p0 travels in one launch's params
+
+// Absolute start positions of up to kMaxSeqPerLaunch sequences, passed by value.
+struct SeqPos {
+  int64_t p0[kMaxSeqPerLaunch];
+};
+
+// RoPE frequencies theta_i = base^(-2i/64), i < 32, computed on the host in fp64.
+struct RopeFreq {
+  double inv_freq[kDR / 2];
+};
+
+struct WriterArgs {
+  const uint16_t *kc, *gc, *wa, *w_ik;
+  const float *gamma_c, *gamma_ik, *gamma_w;
+  float *pair_kc, *pair_gc;
+  uint8_t *z_codes, *z_scales, *ki_codes, *ki_scales, *window;
+  int64_t cap;
+  int T;
+  double eps;
+};
+
+struct IndexArgs {
+  const uint16_t *qi, *wI;
+  const uint8_t *ki_codes, *ki_scales;
+  int64_t cap;
+  int T;
+  int32_t* idx;
+  float* top_scores;
+};
+
+struct AttendArgs {
+  const uint16_t* q;
+  const float* sinks;
+  const uint8_t *z_codes, *z_scales, *window;
+  const int32_t* idx;
+  int64_t cap;
+  int T;
+  uint16_t* out;
+};
+
+// Launchers: each enqueues on `st` and returns the first CUDA launch error (or success).
+// `b0` is the batch index of the first sequence in `pos`, `nb` how many follow.
+cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf,
+                          cudaStream_t st);
+size_t index_workspace_bytes(int B, int T, int64_t max_entries, int num_sms);
+cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int64_t max_entries,
+                              void* ws, size_t ws_bytes, int num_sms, cudaStream_t st);
+size_t attend_workspace_bytes(int B, int T, int num_sms);
+cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf,
+                          void* ws, size_t ws_bytes, int num_sms, cudaStream_t st);
+
+}  // namespace csa2

@@ -1,0 +1,218 @@
+// Compressed-KV writer.  Page "DeepSeek V4.1 - Pooled group / Source layer, pairs pooled",
+// block "Compressed sparse attention": k^p_j (pair softmax pooling), c (RMSNorm, gain
+// gamma_C), Z (RoPE by 2j on dims 448..511, FP4), k^i = c W_IK, k^n (RMSNorm, gamma_IK),
+// K^I (RoPE by 2j on dims 64..127, FP4) and the window W (RMSNorm of w^a, RoPE by t, FP8).
+// RMSNorm as on "DeepSeek V4.1 - Window layer / Attention RMSNorm" (eps 1e-20).
+//
+// Precision: fp32 elementwise work, fp64 sums of squares, and a compensated (double-float)
+// dot product for c W_IK, so that the values reaching the FP4/FP8 rounding differ from an
+// fp64 evaluation by a few fp32 ulps and the codes match except at rounding midpoints.
+#include "csa2_common.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kWriterThreads = 128;
+constexpr int kEntriesPerBlock = 8;
+
+// Pack the four 4-bit codes of one thread (4 consecutive values) into two bytes.
+__device__ __forceinline__ uint16_t pack4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
+  return (uint16_t)(c0 | (c1 << 4) | (c2 << 8) | (c3 << 12));
+}
+
+// Blocks of 32 values held 4 per thread by 8 consecutive lanes: returns the 4 codes packed
+// and writes the block's scale byte from the first of the 8 lanes.
+__device__ __forceinline__ uint16_t fp4_quant4(const float v[4], uint8_t* scale_out) {
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  int e = mx_scale_exp(amax);
+  if ((threadIdx.x & 7) == 0) *scale_out = (uint8_t)(e + 127);
+  return pack4(f32_to_e2m1(ldexpf(v[0], -e)), f32_to_e2m1(ldexpf(v[1], -e)),
+               f32_to_e2m1(ldexpf(v[2], -e)), f32_to_e2m1(ldexpf(v[3], -e)));
+}
+
+// Double-float accumulation of sum(x*w): error-free product (fma) and two-sum.
+struct DF {
+  float s, c;
+  __device__ __forceinline__ void add_prod(float x, float w) {
+    float p = x * w;
+    float pe = fmaf(x, w, -p);
+    float t = s + p;
+    float bb = t - s;
+    float te = (s - (t - bb)) + (p - bb);
+    s = t;
+    c += te + pe;
+  }
+};
+
+__global__ void __launch_bounds__(kWriterThreads) writer_entries_kernel(WriterArgs a, SeqPos pos, int b0, RopeFreq rf) {
+  __shared__ float sc[kEntriesPerBlock][kD];
+  __shared__ double red[kWriterThreads / 32];
+  __shared__ int64_t sj[kEntriesPerBlock];
+
+  const int bl = blockIdx.y;
+  const int b = b0 + bl;
+  const int64_t p0 = pos.p0[bl];
+  const int T = a.T;
+  const int64_t n_new = (p0 + T) / 2 - p0 / 2;
+  const int64_t e_base = (int64_t)blockIdx.x * kEntriesPerBlock;
+  if (e_base >= n_new) return;
+  const int ne = (int)min64(kEntriesPerBlock, n_new - e_base);
+  const int tid = threadIdx.x;
+  const int ch = 4 * tid;
+
+  // ---- phase 1: pooled key, RMSNorm, Z
+  for (int e = 0; e < ne; ++e) {
+    const int64_t j = p0 / 2 + e_base + e;
+    const int64_t t1 = 2 * j + 1 - p0;  // local index of the odd token (0 <= t1 < T)
+    const uint16_t* k1p = a.kc + ((int64_t)b * T + t1) * kD + ch;
+    const uint16_t* g1p = a.gc + ((int64_t)b * T + t1) * kD + ch;
+    float k0[4], g0[4], k1[4], g1[4];
+    uint2 kk1 = *reinterpret_cast<const uint2*>(k1p), gg1 = *reinterpret_cast<const uint2*>(g1p);
+    k1[0] = bf16_to_f32(kk1.x & 0xffff); k1[1] = bf16_to_f32(kk1.x >> 16);
+    k1[2] = bf16_to_f32(kk1.y & 0xffff); k1[3] = bf16_to_f32(kk1.y >> 16);
+    g1[0] = bf16_to_f32(gg1.x & 0xffff); g1[1] = bf16_to_f32(gg1.x >> 16);
+    g1[2] = bf16_to_f32(gg1.y & 0xffff); g1[3] = bf16_to_f32(gg1.y >> 16);
+    if (t1 >= 1) {
+      uint2 kk0 = *reinterpret_cast<const uint2*>(k1p - kD), gg0 = *reinterpret_cast<const uint2*>(g1p - kD);
+      k0[0] = bf16_to_f32(kk0.x & 0xffff); k0[1] = bf16_to_f32(kk0.x >> 16);
+      k0[2] = bf16_to_f32(kk0.y & 0xffff); k0[3] = bf16_to_f32(kk0.y >> 16);
+      g0[0] = bf16_to_f32(gg0.x & 0xffff); g0[1] = bf16_to_f32(gg0.x >> 16);
+      g0[2] = bf16_to_f32(gg0.y & 0xffff); g0[3] = bf16_to_f32(gg0.y >> 16);
+    } else {  // token 2j is the one the pair buffer kept from the previous call
+      float4 kb = *reinterpret_cast<const float4*>(a.pair_kc + (int64_t)b * kD + ch);
+      float4 gb = *reinterpret_cast<const float4*>(a.pair_gc + (int64_t)b * kD + ch);
+      k0[0] = kb.x; k0[1] = kb.y; k0[2] = kb.z; k0[3] = kb.w;
+      g0[0] = gb.x; g0[1] = gb.y; g0[2] = gb.z; g0[3] = gb.w;
+    }
+    float kp[4];
+    double ss = 0.0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float m = fmaxf(g0[i], g1[i]);
+      float e0 = expf(g0[i] - m), e1 = expf(g1[i] - m);
+      float den = e0 + e1;
+      kp[i] = (e0 / den) * k0[i] + (e1 / den) * k1[i];
+      ss += (double)kp[i] * (double)kp[i];
+    }
+    ss = block_sum<kWriterThreads>(ss, red);
+    const float r = (float)(1.0 / sqrt(ss / kD + a.eps));
+    float c[4], z[4];
+    float4 gm = *reinterpret_cast<const float4*>(a.gamma_c + ch);
+    c[0] = gm.x * (kp[0] * r); c[1] = gm.y * (kp[1] * r);
+    c[2] = gm.z * (kp[2] * r); c[3] = gm.w * (kp[3] * r);
+    *reinterpret_cast<float4*>(&sc[e][ch]) = make_float4(c[0], c[1], c[2], c[3]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) z[i] = c[i];
+    if (ch >= kD - kDR) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int pi = (ch - (kD - kDR)) / 2 + q;
+        float cs, sn;
+        rope_cs(2 * j, rf.inv_freq[pi], 1.0f, cs, sn);
+        float x0 = c[2 * q], x1 = c[2 * q + 1];
+        z[2 * q] = x0 * cs - x1 * sn;
+        z[2 * q + 1] = x0 * sn + x1 * cs;
+      }
+    }
+    uint16_t packed = fp4_quant4(z, a.z_scales + ((int64_t)b * a.cap + j) * 16 + tid / 8);
+    *reinterpret_cast<uint16_t*>(a.z_codes + ((int64_t)b * a.cap + j) * 256 + 2 * tid) = packed;
+    if (tid == 0) sj[e] = j;
+  }
+  __syncthreads();
+
+  // ---- phase 2: k^i = c W_IK for the block's entries (thread = output column)
+  DF acc[kEntriesPerBlock];
+#pragma unroll
+  for (int e = 0; e < kEntriesPerBlock; ++e) acc[e] = DF{0.f, 0.f};
+  const int o = tid;
+  for (int d = 0; d < kD; ++d) {
+    const float w = bf16_to_f32(a.w_ik[d * kDI + o]);
+#pragma unroll
+    for (int e = 0; e < kEntriesPerBlock; ++e)
+      if (e < ne) acc[e].add_prod(sc[e][d], w);
+  }
+
+  // ---- phase 3: RMSNorm, RoPE by 2j on dims 64..127, FP4
+  for (int e = 0; e < ne; ++e) {
+    const int64_t j = sj[e];
+    const float ki = acc[e].s + acc[e].c;
+    double ss = block_sum<kWriterThreads>((double)ki * (double)ki, red);
+    const float r = (float)(1.0 / sqrt(ss / kDI + a.eps));
+    float kn = a.gamma_ik[o] * (ki * r);
+    const float partner = __shfl_xor_sync(0xffffffffu, kn, 1);
+    if (o >= 64) {
+      float cs, sn;
+      rope_cs(2 * j, rf.inv_freq[(o - 64) / 2], 1.0f, cs, sn);
+      kn = (o & 1) ? (partner * sn + kn * cs) : (kn * cs - partner * sn);
+    }
+    const float amax = warp_max(fabsf(kn));
+    const int ex = mx_scale_exp(amax);
+    const uint32_t code = f32_to_e2m1(ldexpf(kn, -ex));
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, code, 1);
+    if ((o & 1) == 0) a.ki_codes[((int64_t)b * a.cap + j) * 64 + o / 2] = (uint8_t)(code | (hi << 4));
+    if ((o & 31) == 0) a.ki_scales[((int64_t)b * a.cap + j) * 4 + o / 32] = (uint8_t)(ex + 127);
+  }
+}
+
+__global__ void __launch_bounds__(kWriterThreads) writer_window_kernel(WriterArgs a, SeqPos pos, int b0, RopeFreq rf) {
+  __shared__ double red[kWriterThreads / 32];
+  const int t = blockIdx.x;
+  const int bl = blockIdx.y;
+  const int b = b0 + bl;
+  const int64_t p0 = pos.p0[bl];
+  const int T = a.T;
+  const int tid = threadIdx.x;
+  const int ch = 4 * tid;
+  const int64_t row = (int64_t)b * T + t;
+  uint2 ww = *reinterpret_cast<const uint2*>(a.wa + row * kD + ch);
+  float x[4] = {bf16_to_f32(ww.x & 0xffff), bf16_to_f32(ww.x >> 16), bf16_to_f32(ww.y & 0xffff),
+                bf16_to_f32(ww.y >> 16)};
+  double ss = 0.0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ss += (double)x[i] * (double)x[i];
+  ss = block_sum<kWriterThreads>(ss, red);
+  const float r = (float)(1.0 / sqrt(ss / kD + a.eps));
+  float4 gm = *reinterpret_cast<const float4*>(a.gamma_w + ch);
+  float y[4] = {gm.x * (x[0] * r), gm.y * (x[1] * r), gm.z * (x[2] * r), gm.w * (x[3] * r)};
+  if (ch >= kD - kDR) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float cs, sn;
+      rope_cs(p0 + t, rf.inv_freq[(ch - (kD - kDR)) / 2 + q], 1.0f, cs, sn);
+      float x0 = y[2 * q], x1 = y[2 * q + 1];
+      y[2 * q] = x0 * cs - x1 * sn;
+      y[2 * q + 1] = x0 * sn + x1 * cs;
+    }
+  }
+  uint32_t packed = f32_to_e4m3(y[0]) | (f32_to_e4m3(y[1]) << 8) | (f32_to_e4m3(y[2]) << 16) | (f32_to_e4m3(y[3]) << 24);
+  *reinterpret_cast<uint32_t*>(a.window + ((int64_t)b * (127 + T) + 127 + t) * kD + ch) = packed;
+  // the last token of an unfinished pair waits in the pair buffer for its partner
+  if (t == T - 1 && ((p0 + T) & 1)) {
+    uint2 kk = *reinterpret_cast<const uint2*>(a.kc + row * kD + ch);
+    uint2 gg = *reinterpret_cast<const uint2*>(a.gc + row * kD + ch);
+    *reinterpret_cast<float4*>(a.pair_kc + (int64_t)b * kD + ch) =
+        make_float4(bf16_to_f32(kk.x & 0xffff), bf16_to_f32(kk.x >> 16), bf16_to_f32(kk.y & 0xffff), bf16_to_f32(kk.y >> 16));
+    *reinterpret_cast<float4*>(a.pair_gc + (int64_t)b * kD + ch) =
+        make_float4(bf16_to_f32(gg.x & 0xffff), bf16_to_f32(gg.x >> 16), bf16_to_f32(gg.y & 0xffff), bf16_to_f32(gg.y >> 16));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf, cudaStream_t st) {
+  int64_t max_new = 0;
+  for (int i = 0; i < nb; ++i) max_new = max(max_new, (pos.p0[i] + a.T) / 2 - pos.p0[i] / 2);
+  if (max_new > 0) {
+    dim3 grid((unsigned)((max_new + kEntriesPerBlock - 1) / kEntriesPerBlock), (unsigned)nb);
+    writer_entries_kernel<<<grid, kWriterThreads, 0, st>>>(a, pos, b0, rf);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  writer_window_kernel<<<dim3((unsigned)a.T, (unsigned)nb), kWriterThreads, 0, st>>>(a, pos, b0, rf);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

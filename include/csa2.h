@@ -1,0 +1,150 @@
+/* csa2.h - C ABI of the GB300 (sm_103a) CSA2 layer library, libcsa2.so.
+ *
+ * One DeepSeek-V4.1-style CSA2 ("compressed sparse attention 2") layer of the Full kind at
+ * compression ratio 2: the compressed-KV writer, the lightning indexer with its top-512
+ * select, and 64-head sink-softmax MQA over the 640 gathered rows.  The operations follow
+ * the equations of the page "DeepSeek V4.1 - Pooled group / Source layer, pairs pooled",
+ * block "Compressed sparse attention" (cited below as [PG]), with the RMSNorm of the page
+ * "DeepSeek V4.1 - Window layer / Attention RMSNorm" ([RN], eps = 1e-20) and the storage
+ * formats of "Inside DeepSeek V4.1", section "890 bytes" ([IN]).
+ *
+ * Conventions shared by every call
+ *  - Fixed shapes: 64 heads x 512, RoPE on the last 64 dims, indexer 32 heads x 128 (RoPE
+ *    on dims 64..127), window 128 rows, top 512, pair pooling (ratio 2).  csa2_create
+ *    rejects any other value with CSA2_ERR_UNSUPPORTED.
+ *  - Tensor arguments are DEVICE pointers, owned by the caller, row-major and densely
+ *    packed in the shapes given, 16-byte aligned.  bf16 tensors are passed as uint16_t
+ *    bit patterns.  The library allocates no device memory; scratch comes from the caller's
+ *    workspace (size from csa2_workspace_bytes).
+ *  - p0 is a HOST array of B int64 values: the absolute position of the first of the T new
+ *    tokens of each sequence (its cached length before the call).
+ *  - Every call is asynchronous on `stream` and never synchronises.  Argument errors are
+ *    returned before anything is launched; launch errors come back as CSA2_ERR_CUDA.
+ *
+ * Storage formats (fixed by this library)
+ *  - FP4 cache row of n values: n/2 code bytes (E2M1, element 2i in the low nibble of byte
+ *    i) and n/32 UE8M0 scale bytes (2^(byte-127)), kept in two separate arrays:
+ *      Z   : codes [B, cap, 256], scales [B, cap, 16]   (272 bytes per pooled entry)
+ *      K^I : codes [B, cap,  64], scales [B, cap,  4]   ( 68 bytes per pooled entry)
+ *    Scale choice follows the OCP MX rule 2^(floor(log2 amax) - 2); codes round to nearest,
+ *    ties to even, saturating at +-6.  Entry j pools tokens 2j and 2j+1.
+ *  - Window (FP8 E4M3fn, RNE, saturating at +-448, no scale): a per-call view
+ *    [B, 127+T, 512] whose row r holds position p0-127+r.  Rows 0..126 are the caller's
+ *    (the previous 127 positions; unused where the position is negative); the writer fills
+ *    rows 127..126+T.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* csa2_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad op code */
+  CSA2_ERR_SHAPE = 2,       /* sizes inconsistent (cache too small, position too large) */
+  CSA2_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+  CSA2_ERR_WORKSPACE = 4,   /* workspace smaller than csa2_workspace_bytes() */
+  CSA2_ERR_UNSUPPORTED = 5, /* configuration outside what the kernels implement */
+  CSA2_ERR_CUDA = 6         /* a CUDA launch or device query failed */
+} csa2_status;
+
+/* Layer configuration.  The integer fields must equal the defaults shown. */
+typedef struct {
+  int heads;        /* 64 */
+  int head_dim;     /* 512 */
+  int rope_dims;    /* 64 */
+  int idx_heads;    /* 32 */
+  int idx_dim;      /* 128 */
+  int window;       /* 128 */
+  int topk;         /* 512 */
+  int ratio;        /* 2 */
+  double rope_base; /* 10000: theta_i = rope_base^(-2i/64) */
+  double eps;       /* 1e-20 ([RN]) */
+} csa2_config;
+
+typedef struct csa2_handle csa2_handle;
+
+/* Fills `cfg` with the defaults above. */
+void csa2_default_config(csa2_config* cfg);
+
+/* Validates `cfg`, records the current CUDA device and its SM count, and precomputes the
+ * RoPE frequencies in fp64.  Allocates host memory only.  *out = NULL on error. */
+csa2_status csa2_create(const csa2_config* cfg, csa2_handle** out);
+void csa2_destroy(csa2_handle* h);
+const char* csa2_status_string(csa2_status s);
+
+enum { CSA2_OP_WRITE_CACHE = 0, CSA2_OP_INDEX_TOPK = 1, CSA2_OP_ATTEND = 2 };
+
+/* Bytes of workspace the call `op` needs for B sequences of T new tokens whose largest
+ * visible entry count is at most max_entries (for decode: the cached entries).  Returns 0
+ * for a bad op.  A larger workspace is always accepted. */
+size_t csa2_workspace_bytes(const csa2_handle* h, int op, int B, int T, int64_t max_entries);
+
+/* (1) Compressed-KV writer, [PG] equations for W, k^p, c, Z, k^i, k^n, K^I.
+ *  kc, gc, wa : bf16 [B, T, 512]  per-token k^c, g^c and w^a (the window source).
+ *  gamma_c    : f32 [512]   gain of the pooled-key RMSNorm.
+ *  w_ik       : bf16 [512, 128]  indexer-key projection, k^i = c W_IK (c before RoPE).
+ *  gamma_ik   : f32 [128]   gain of the indexer-key RMSNorm.
+ *  gamma_w    : f32 [512]   gain of the window RMSNorm (w^n = gamma_w RMSNorm(w^a)).
+ *  p0         : HOST int64 [B].
+ *  pair_kc, pair_gc : f32 [B, 512] pair buffer.  When p0[b] is odd it must hold token
+ *               p0[b]-1; when p0[b]+T is odd the call stores token p0[b]+T-1 there.  May be
+ *               NULL only if every p0[b] and T are even.
+ *  z_codes/z_scales, ki_codes/ki_scales : the FP4 caches with room for `cap` entries;
+ *               entries j with p0 <= 2j+1 <= p0+T-1 are written (j < cap required).
+ *  window     : u8 [B, 127+T, 512] e4m3 view; rows 127..126+T are written.
+ * Per entry: k^p = sum over the pair of softmax(g^c) * k^c per channel; c = gamma_c
+ * RMSNorm(k^p); Z = c with dims 448..511 rotated by position 2j, then FP4.  K^I = gamma_ik
+ * RMSNorm(c W_IK) with dims 64..127 rotated by 2j, then FP4.  Per token t: W = gamma_w
+ * RMSNorm(w^a) with dims 448..511 rotated by t, then FP8.
+ * Workspace: none (ws may be NULL). */
+csa2_status csa2_write_cache(csa2_handle* h, const uint16_t* kc, const uint16_t* gc,
+                             const uint16_t* wa, const float* gamma_c, const uint16_t* w_ik,
+                             const float* gamma_ik, const float* gamma_w, const int64_t* p0,
+                             int B, int T, float* pair_kc, float* pair_gc, uint8_t* z_codes,
+                             uint8_t* z_scales, uint8_t* ki_codes, uint8_t* ki_scales,
+                             int64_t cap, uint8_t* window, void* ws, size_t ws_bytes,
+                             csa2_stream_t stream);
+
+/* (2)+(3) Lightning indexer and top-512, [PG] equations for S^I and I_t.
+ *  qi  : bf16 [B, T, 32, 128]  indexer queries Q^I (quantised here to FP4, scale per 32).
+ *  wI  : bf16 [B, T, 32]       head weights w^I (already divided by sqrt(128*32)).
+ *  ki_codes/ki_scales : the K^I cache (cap entries per sequence).
+ * For query t (absolute position p0+t) the candidates are j < floor((p0+t+1)/2), which
+ * must not exceed cap.  S^I_{t,j} = sum_h w^I_h ReLU(Q^I_h . K^I_j) in fp32.
+ *  idx        : int32 [B, T, 512] the 512 largest scores (equal scores: lower j first),
+ *               ascending in j; when fewer candidates exist all are kept and the rest is -1.
+ *  top_scores : f32 [B, T, 512] or NULL: the scores of idx (NaN where idx is -1).
+ * Workspace: csa2_workspace_bytes(h, CSA2_OP_INDEX_TOPK, B, T, max_entries). */
+csa2_status csa2_index_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* wI,
+                            const uint8_t* ki_codes, const uint8_t* ki_scales, int64_t cap,
+                            const int64_t* p0, int B, int T, int32_t* idx, float* top_scores,
+                            void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* (4) Sink-softmax MQA, [PG] equations for J^w_t, Y, J, G_t, S, A, O and O-bar.
+ *  q      : bf16 [B, T, 64, 512] queries, RoPE already applied to dims 448..511.
+ *  sinks  : f32 [64] per-head sink logits s_h.
+ *  z_codes/z_scales : the Z cache (cap entries); window: the e4m3 view [B, 127+T, 512].
+ *  idx    : int32 [B, T, 512] entry indices (any source: this layer's csa2_index_topk or a
+ *           shared layer's); -1 entries are skipped, others must be < cap.
+ * G_t = window rows of positions max(0,t-127)..t followed by the Z rows idx[t] (at most
+ * 640 rows), dequantised exactly.  S = Q.G/sqrt(512), A = exp S / (exp s_h + sum exp S),
+ * O = sum A G, then dims 448..511 of O rotated by -t.
+ *  out    : bf16 [B, T, 64, 512].
+ * Workspace: csa2_workspace_bytes(h, CSA2_OP_ATTEND, B, T, 0). */
+csa2_status csa2_attend(csa2_handle* h, const uint16_t* q, const float* sinks,
+                        const uint8_t* z_codes, const uint8_t* z_scales, int64_t cap,
+                        const uint8_t* window, const int32_t* idx, const int64_t* p0, int B,
+                        int T, uint16_t* out, void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

@@ -1,0 +1,56 @@
+"""The C-ABI library loads and exports every entry point include/csa2.h declares; host-side
+checks that need no GPU (no compute call is made here)."""
+import ctypes as C
+import re
+from pathlib import Path
+
+import pytest
+
+import compressed_sparse_attention_03_gb300 as csa2
+from compressed_sparse_attention_03_gb300 import build
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "csa2.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return csa2.lib()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    return sorted(set(re.findall(r"\b(csa2_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("csa2_write_cache", "csa2_index_topk", "csa2_attend", "csa2_create", "csa2_destroy",
+              "csa2_workspace_bytes", "csa2_status_string", "csa2_default_config"):
+        assert n in names
+    assert set(names) == set(csa2.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_config_checks(lib):
+    assert lib.csa2_status_string(0) == b"ok"
+    assert lib.csa2_status_string(4) == b"workspace too small"
+    cfg = csa2.csa2_config()
+    lib.csa2_default_config(C.byref(cfg))
+    assert (cfg.heads, cfg.head_dim, cfg.rope_dims, cfg.idx_heads, cfg.idx_dim, cfg.window, cfg.topk, cfg.ratio) == \
+        (64, 512, 64, 32, 128, 128, 512, 2)
+    assert cfg.rope_base == 10000.0 and cfg.eps == 1e-20
+    h = C.c_void_p()
+    cfg.topk = 256   # the kernels are built for top-512 only
+    assert lib.csa2_create(C.byref(cfg), C.byref(h)) == 5 and not h.value
+    lib.csa2_default_config(C.byref(cfg))
+    cfg.rope_base = 0.5
+    assert lib.csa2_create(C.byref(cfg), C.byref(h)) == 1
+    assert lib.csa2_create(None, C.byref(h)) == 1
+    # no handle: every entry point refuses before touching the GPU
+    assert lib.csa2_workspace_bytes(None, 1, 1, 1, 10) == 0
+    assert lib.csa2_index_topk(*([None] * 5), 0, None, 1, 1, None, None, None, 0, None) == 1

@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, element by element on
+the same seeded inputs.  Small cases span several tiles and ragged tails; the named
+workloads run at full size with sampled query rows where the oracle would be too slow.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from compressed_sparse_attention_03_gb300 import inputs
+import compressed_sparse_attention_03_gb300 as csa2
+from parity_utils import (e4m3_compare, fp4_compare, np32, out_compare, random_indices, topk_compare)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def handle():
+    return csa2.csa2_create()
+
+
+def make_state(B, T, p0s, seed, cap=None, device=DEV):
+    p0s = np.asarray(p0s, np.int64)
+    cap = cap or int(((p0s + T) // 2).max()) + 3
+    x = {}
+    x.update(inputs.layer_params(seed, device))
+    x.update(inputs.step_inputs(B, T, seed, device))
+    st = inputs.cache_state(B, T, int(p0s.max()), cap, seed, device)
+    # sequences with shorter context: drop cached entries beyond their own length
+    for b in range(B):
+        n = int(p0s[b]) // 2
+        for k in ("z_codes", "z_scales", "ki_codes", "ki_scales"):
+            st[k][b, n:] = 0
+    x.update(st)
+    return x, cap
+
+
+def gpu_write(h, x, p0s):
+    w = {k: x[k].clone() for k in ("z_codes", "z_scales", "ki_codes", "ki_scales", "window", "pair_kc", "pair_gc")}
+    csa2.csa2_write_cache(h, x["kc"], x["gc"], x["wa"], x["gamma_c"], x["w_ik"], x["gamma_ik"], x["gamma_w"], p0s,
+                          w["z_codes"], w["z_scales"], w["ki_codes"], w["ki_scales"], w["window"], w["pair_kc"],
+                          w["pair_gc"])
+    return w
+
+
+def oracle_write(x, p0s, cap):
+    res = []
+    for b, p0 in enumerate(p0s):
+        cpu = lambda k: np32(x[k][b]) if x[k].dtype != torch.uint8 else x[k][b].cpu().numpy().copy()
+        r = oracle.write_seq(cpu("kc"), cpu("gc"), cpu("wa"), np32(x["gamma_c"]), np32(x["w_ik"]), np32(x["gamma_ik"]),
+                             np32(x["gamma_w"]), int(p0), cap, z_codes=cpu("z_codes"), z_scales=cpu("z_scales"),
+                             ki_codes=cpu("ki_codes"), ki_scales=cpu("ki_scales"), pair_k=cpu("pair_kc"),
+                             pair_g=cpu("pair_gc"), window_prefix=cpu("window")[:127])
+        res.append(r)
+    return res
+
+
+def use_oracle_state(x, ores):
+    """Replace the caches and window views in ``x`` by what the oracle's writer produced, so
+    that later stages of both sides read the same (oracle-made) state."""
+    for b, r in enumerate(ores):
+        for k in ("z_codes", "z_scales", "ki_codes", "ki_scales", "window"):
+            x[k][b] = torch.from_numpy(r[k]).to(x[k].device)
+    return x
+
+
+def check_write(w, ores, p0s, T):
+    n_code = n_scale = n_fp8 = 0
+    for b, (r, p0) in enumerate(zip(ores, p0s)):
+        j0, n = r["first_entry"], r["n_entries"]
+        sl = slice(j0, j0 + n)
+        g = {k: w[k][b].cpu().numpy() for k in ("z_codes", "z_scales", "ki_codes", "ki_scales", "window")}
+        if n:
+            c1, s1 = fp4_compare(g["z_codes"][sl], g["z_scales"][sl], r["z_codes"][sl], r["z_scales"][sl], r["z_pre"])
+            c2, s2 = fp4_compare(g["ki_codes"][sl], g["ki_scales"][sl], r["ki_codes"][sl], r["ki_scales"][sl], r["ki_pre"])
+            n_code += c1 + c2
+            n_scale += s1 + s2
+        # entries outside this call untouched
+        assert np.array_equal(g["z_codes"][:j0], r["z_codes"][:j0])
+        assert np.array_equal(g["ki_scales"][j0 + n:], r["ki_scales"][j0 + n:])
+        n_fp8 += e4m3_compare(g["window"][127:], r["window"][127:], r["win_pre"])
+        assert np.array_equal(g["window"][:127], r["window"][:127])
+        if (p0 + T) % 2 == 1:
+            assert np.array_equal(w["pair_kc"][b].cpu().numpy(), r["pair"][0])
+            assert np.array_equal(w["pair_gc"][b].cpu().numpy(), r["pair"][1])
+    return n_code, n_scale, n_fp8
+
+
+# ------------------------------------------------------------------------ writer
+@pytest.mark.parametrize("B,T,p0s", [(3, 37, [0, 5, 130]), (1, 1, [0]), (2, 1, [7, 4096]), (1, 2, [1]),
+                                     (2, 300, [0, 2001])])
+def test_writer_small(handle, B, T, p0s):
+    x, cap = make_state(B, T, p0s, seed=B * 100 + T)
+    w = gpu_write(handle, x, p0s)
+    n = check_write(w, oracle_write(x, p0s, cap), p0s, T)
+    print(f"writer B={B} T={T}: boundary exceptions codes/scales/fp8 = {n}")
+
+
+@pytest.mark.parametrize("name", ["prefill_4k", "chunk_32k"])
+def test_writer_workloads(handle, name):
+    wl = inputs.WORKLOADS[name]
+    x = inputs.workload_inputs(wl, DEV)
+    w = gpu_write(handle, x, [wl.p0])
+    n = check_write(w, oracle_write(x, [wl.p0], wl.cap), [wl.p0], wl.T)
+    print(f"writer {name}: boundary exceptions codes/scales/fp8 = {n}")
+
+
+# ------------------------------------------------------------------------ indexer + top-k
+def run_index(h, x, p0s, T):
+    B = x["qi"].shape[0]
+    idx = torch.empty(B, T, 512, dtype=torch.int32, device=DEV)
+    top = torch.empty(B, T, 512, dtype=torch.float32, device=DEV)
+    csa2.csa2_index_topk(h, x["qi"], x["wI"], x["ki_codes"], x["ki_scales"], p0s, idx, top)
+    return idx, top
+
+
+def check_index(idx, top, x, p0s, rows=None):
+    B, T = idx.shape[:2]
+    swaps = 0
+    for b, p0 in enumerate(p0s):
+        r = np.arange(T) if rows is None else np.asarray(rows)
+        pos = p0 + r
+        E = (pos + 1) // 2
+        kc = x["ki_codes"][b, : max(int(E.max()), 1)].cpu().numpy()
+        ks = x["ki_scales"][b, : max(int(E.max()), 1)].cpu().numpy()
+        sc = oracle.index_scores(pos, np32(x["qi"][b][r]), np32(x["wI"][b][r]), kc, ks, kc.shape[0])
+        oidx, otop, kth = oracle.topk(sc, E)
+        g = idx[b][r].cpu().numpy()
+        swaps += topk_compare(g, oidx, sc, kth, E)
+        # the reported scores are the fp32 scores of the chosen entries
+        gt = top[b][r].cpu().numpy()
+        for i in range(len(r)):
+            k = min(512, int(E[i]))
+            ref = sc[i, g[i, :k]]
+            assert np.allclose(gt[i, :k], ref, rtol=2e-6, atol=1e-30), f"row {r[i]} scores"
+            assert np.all(np.isnan(gt[i, k:]))
+    return swaps
+
+
+@pytest.mark.parametrize("B,T,p0s", [(2, 1, [3001, 1000]), (1, 300, [0]), (2, 64, [2000, 37]), (3, 1, [0, 1, 2]),
+                                     (1, 1, [70001])])
+def test_index_small(handle, B, T, p0s):
+    x, cap = make_state(B, T, p0s, seed=7 + T)
+    idx, top = run_index(handle, x, p0s, T)
+    swaps = check_index(idx, top, x, p0s)
+    print(f"index B={B} T={T}: near-tie swaps = {swaps}")
+
+
+def test_index_exact_ties(handle):
+    # identical keys give identical scores: the lower indices must win
+    x, cap = make_state(1, 1, [4000], seed=3)
+    x["ki_codes"][0, :2000] = x["ki_codes"][0, 5]
+    x["ki_scales"][0, :2000] = x["ki_scales"][0, 5]
+    idx, top = run_index(handle, x, [4000], 1)
+    sc = oracle.index_scores(np.array([4000]), np32(x["qi"][0]), np32(x["wI"][0]), x["ki_codes"][0].cpu().numpy(),
+                             x["ki_scales"][0].cpu().numpy(), cap)
+    oidx, _, kth = oracle.topk(sc, np.array([2000]))
+    assert np.array_equal(idx[0, 0].cpu().numpy(), oidx[0])
+
+
+@pytest.mark.parametrize("name", ["decode_8k", "decode_128k", "decode_1m", "prefill_4k"])
+def test_index_workloads(handle, name):
+    wl = inputs.WORKLOADS[name]
+    x = inputs.workload_inputs(wl, DEV)
+    if wl.p0 == 0:  # prefill from scratch: the keys come from this step's writer (the oracle's)
+        use_oracle_state(x, oracle_write(x, [wl.p0], wl.cap))
+    idx, top = run_index(handle, x, [wl.p0] * wl.B, wl.T)
+    swaps = check_index(idx, top, x, [wl.p0] * wl.B)
+    print(f"index {name}: near-tie swaps = {swaps}")
+
+
+def test_index_chunk_32k_sampled(handle):
+    wl = inputs.WORKLOADS["chunk_32k"]
+    x = inputs.workload_inputs(wl, DEV)
+    use_oracle_state(x, oracle_write(x, [wl.p0], wl.cap))
+    idx, top = run_index(handle, x, [wl.p0], wl.T)
+    rng = np.random.default_rng(4)
+    rows = np.unique(np.concatenate([[0, 1, 2, wl.T - 2, wl.T - 1], rng.integers(0, wl.T, 19)]))
+    swaps = check_index(idx, top, x, [wl.p0], rows=rows)
+    print(f"index chunk_32k ({len(rows)} rows): near-tie swaps = {swaps}")
+
+
+# ------------------------------------------------------------------------ attention
+def stratified_indices(B, T, p0s, seed):
+    """Sorted distinct visible entries per query: one draw per stratum of width E/512."""
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    idx = torch.full((B, T, 512), -1, dtype=torch.int32, device=DEV)
+    for b in range(B):
+        E = (torch.arange(T, device=DEV, dtype=torch.int64) + int(p0s[b]) + 1) // 2
+        s = torch.clamp(E // 512, min=1)
+        i = torch.arange(512, device=DEV)
+        cand = i[None, :] * s[:, None] + (torch.rand(T, 512, generator=g, device=DEV) * s[:, None]).long()
+        ok = cand < E[:, None]
+        idx[b] = torch.where(ok, cand, torch.full_like(cand, -1)).to(torch.int32)
+    return idx
+
+
+def run_attend(h, x, idx, p0s):
+    B, T = x["q"].shape[:2]
+    out = torch.empty(B, T, 64, 512, dtype=torch.bfloat16, device=DEV)
+    csa2.csa2_attend(h, x["q"], x["sinks"], x["z_codes"], x["z_scales"], x["window"], idx, p0s, out)
+    return out
+
+
+def check_attend(out, x, idx, p0s, rows=None):
+    B, T = out.shape[:2]
+    errs = []
+    for b, p0 in enumerate(p0s):
+        r = np.arange(T) if rows is None else np.asarray(rows)
+        ref = oracle.attend(p0 + r, np32(x["q"][b][r]), np32(x["sinks"]), x["z_codes"][b].cpu().numpy(),
+                            x["z_scales"][b].cpu().numpy(), x["z_codes"].shape[1], x["window"][b].cpu().numpy(),
+                            p0 - 127, idx[b][r].cpu().numpy())
+        errs.append(out_compare(np32(out[b][r]), ref))
+    return max(e[0] for e in errs), max(e[1] for e in errs)
+
+
+@pytest.mark.parametrize("B,T,p0s", [(1, 300, [0]), (3, 1, [8192, 20, 0]), (2, 40, [1000, 5001]), (1, 1, [1])])
+def test_attend_small(handle, B, T, p0s):
+    x, cap = make_state(B, T, p0s, seed=11 + T)
+    use_oracle_state(x, oracle_write(x, p0s, cap))  # this step's window rows and entries
+    idx = random_indices(B, T, p0s, seed=5, device=DEV)
+    out = run_attend(handle, x, idx, p0s)
+    print(f"attend B={B} T={T}: max abs / rel L2 = {check_attend(out, x, idx, p0s)}")
+
+
+@pytest.mark.parametrize("name", ["decode_8k", "decode_128k", "decode_1m", "prefill_4k", "chunk_32k"])
+def test_attend_workloads(handle, name):
+    wl = inputs.WORKLOADS[name]
+    x = inputs.workload_inputs(wl, DEV)
+    p0s = [wl.p0] * wl.B
+    use_oracle_state(x, oracle_write(x, p0s, wl.cap))
+    idx = stratified_indices(wl.B, wl.T, p0s, seed=wl.seed)
+    out = run_attend(handle, x, idx, p0s)
+    rows = None
+    if wl.T > 64:
+        rng = np.random.default_rng(wl.seed)
+        rows = np.unique(np.concatenate([[0, 1, 126, 127, 1023, wl.T - 1], rng.integers(0, wl.T, 58)]))
+        rows = rows[rows < wl.T]
+    print(f"attend {name}: max abs / rel L2 = {check_attend(out, x, idx, p0s, rows)}")
+
+
+# ------------------------------------------------------------------------ whole step
+@pytest.mark.parametrize("B,T,p0s", [(1, 700, [0]), (2, 1, [2049, 6000]), (2, 33, [1100, 77])])
+def test_step_end_to_end(handle, B, T, p0s):
+    """write -> index/top-k -> attend on the GPU vs the same chain in the oracle."""
+    x, cap = make_state(B, T, p0s, seed=17 + T)
+    g = gpu_write(handle, x, p0s)
+    ow = oracle_write(x, p0s, cap)
+    check_write(g, ow, p0s, T)
+    xg = dict(x, **g)
+    idx, top = run_index(handle, xg, p0s, T)
+    out = run_attend(handle, xg, idx, p0s)
+    for b, p0 in enumerate(p0s):
+        pos = p0 + np.arange(T)
+        E = (pos + 1) // 2
+        r = ow[b]
+        sc = oracle.index_scores(pos, np32(x["qi"][b]), np32(x["wI"][b]), r["ki_codes"], r["ki_scales"], cap)
+        oidx, _, kth = oracle.topk(sc, E)
+        gidx = idx[b].cpu().numpy()
+        swaps = topk_compare(gidx, oidx, sc, kth, E)
+        ref = oracle.attend(pos, np32(x["q"][b]), np32(x["sinks"]), r["z_codes"], r["z_scales"], cap, r["window"],
+                            p0 - 127, oidx)
+        same = np.array([np.array_equal(gidx[i], oidx[i]) for i in range(T)])
+        mx, rl2 = out_compare(np32(out[b])[same], ref[same])
+        print(f"step b={b}: swaps={swaps} rows compared={same.sum()} max abs={mx:.3g} rel L2={rl2:.3g}")
+
+
+# ------------------------------------------------------------------------ argument errors
+def test_argument_errors(handle):
+    x, cap = make_state(1, 4, [0], seed=1)
+    idx = torch.empty(1, 4, 512, dtype=torch.int32, device=DEV)
+    with pytest.raises(csa2.Csa2Error) as e:   # cache too small for the visible entries
+        csa2.csa2_index_topk(handle, x["qi"], x["wI"], x["ki_codes"][:, :1], x["ki_scales"][:, :1], [100], idx)
+    assert e.value.status == 2
+    with pytest.raises(csa2.Csa2Error) as e:   # workspace too small
+        csa2.csa2_index_topk(handle, x["qi"], x["wI"], x["ki_codes"], x["ki_scales"], [0], idx,
+                             ws=torch.empty(16, dtype=torch.uint8, device=DEV))
+    assert e.value.status == 4
+    with pytest.raises(csa2.Csa2Error) as e:   # odd p0 without a pair buffer
+        csa2.csa2_write_cache(handle, x["kc"], x["gc"], x["wa"], x["gamma_c"], x["w_ik"], x["gamma_ik"], x["gamma_w"],
+                              [1], x["z_codes"], x["z_scales"], x["ki_codes"], x["ki_scales"], x["window"])
+    assert e.value.status == 1
+    out = torch.empty(4 * 64 * 512 + 8, dtype=torch.bfloat16, device=DEV)
+    mis = out.view(-1)[1:1 + 4 * 64 * 512].view(1, 4, 64, 512)  # 2-byte offset: misaligned
+    with pytest.raises(csa2.Csa2Error) as e:
+        csa2.csa2_attend(handle, x["q"], x["sinks"], x["z_codes"], x["z_scales"], x["window"], idx, [0], mis)
+    assert e.value.status == 3
