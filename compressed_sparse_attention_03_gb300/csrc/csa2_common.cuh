@@ -63,7 +63,9 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
 }
 
 // cos/sin of pos * inv_freq: the angle is formed and reduced modulo 2*pi in fp64 (positions
-// reach ~2^21, where an fp32 product would be off by ~0.1 rad), then evaluated in fp32.
+// reach ~2^21, where an fp32 product would be off by ~0.1 rad) and evaluated in fp32 at the
+// rounded angle rf, then corrected to first order for d = r - rf (|d| <= 2e-7):
+// cos(r) ~ cos(rf) - d sin(rf), sin(r) ~ sin(rf) + d cos(rf).
 __device__ __forceinline__ void rope_cs(int64_t pos, double inv_freq, float sign, float& c, float& s) {
   const double two_pi_hi = 6.283185307179586;          // nearest double to 2*pi
   const double two_pi_lo = 2.4492935982947064e-16;     // 2*pi - two_pi_hi
@@ -71,7 +73,13 @@ __device__ __forceinline__ void rope_cs(int64_t pos, double inv_freq, float sign
   double k = rint(ang * 0.15915494309189535);
   double r = fma(-k, two_pi_hi, ang);
   r = fma(-k, two_pi_lo, r);
-  sincosf(sign * (float)r, &s, &c);
+  r *= (double)sign;
+  const float rf = (float)r;
+  const float d = (float)(r - (double)rf);
+  float s0, c0;
+  sincosf(rf, &s0, &c0);
+  c = fmaf(-d, s0, c0);
+  s = fmaf(d, c0, s0);
 }
 
 template <typename T>

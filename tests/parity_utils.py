@@ -3,9 +3,12 @@ comparison rules.
 
 Comparison rules
   * FP4 / FP8 codes: bit-exact, except where the oracle's fp64 value before rounding lies
-    within REL_BOUNDARY (relative) of a rounding midpoint, or (FP4 scale bytes) where the
-    block maximum lies within REL_BOUNDARY of a power of two.  Such exceptions are counted
-    and returned; any other mismatch fails.
+    within REL_BOUNDARY of a rounding midpoint, or (FP4 scale bytes) where the block maximum
+    lies within REL_BOUNDARY (relative) of a power of two.  The distance to a midpoint is
+    measured relative to max(|v|, rms of v's row): the rows are RMS-normalised and the fp32
+    error of a rotated or pooled value follows the magnitude of its operands (about the row
+    rms), not of the (possibly cancelled) result.  Exceptions are counted and returned; any
+    other mismatch fails.
   * Indices: bit-exact top-512 sets; a swap is allowed only where the oracle's scores of the
     swapped entries lie within REL_TIE (relative) of the oracle's 512th score.  Swaps are
     counted and returned.
@@ -58,7 +61,9 @@ def fp4_compare(g_codes, g_scales, o_codes, o_scales, pre):
     blk_scale_bad = np.repeat(bad_scale, 32, axis=1)
     e = np.repeat(o_scales.astype(np.int64) - 127, 32, axis=1)
     x = np.abs(pre) / 2.0 ** e
-    near_mid = (np.abs(x[..., None] - E2M1_MIDS) <= REL_BOUNDARY * E2M1_MIDS).any(-1)
+    rms = np.sqrt(np.mean(pre ** 2, axis=1, keepdims=True))
+    tol = REL_BOUNDARY * np.maximum(np.abs(pre), rms) / 2.0 ** e
+    near_mid = (np.abs(x[..., None] - E2M1_MIDS) <= tol[..., None]).any(-1)
     # a zero that differs only in its sign bit (a value rounding to 0 from either side)
     zero_sign = ((gc & 7) == 0) & ((oc & 7) == 0) & (np.abs(x) <= 0.25 * (1 + REL_BOUNDARY))
     unexplained = bad & ~(near_mid | blk_scale_bad | zero_sign)
@@ -76,7 +81,8 @@ def e4m3_compare(g, o, pre):
     ov = np.vectorize(oracle.e4m3_value)(o[bad].astype(np.int64))
     mid = (gv + ov) / 2
     p = pre[bad]
-    ok = np.abs(p - mid) <= REL_BOUNDARY * np.maximum(np.abs(mid), 1e-30)
+    rms = np.broadcast_to(np.sqrt(np.mean(pre ** 2, axis=-1, keepdims=True)), pre.shape)[bad]
+    ok = np.abs(p - mid) <= REL_BOUNDARY * np.maximum(np.abs(p), rms)
     ok |= (gv == 0) & (ov == 0)
     assert ok.all(), f"{(~ok).sum()} FP8 codes differ away from a rounding midpoint"
     return int(bad.sum())

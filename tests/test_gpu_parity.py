@@ -128,12 +128,14 @@ def check_index(idx, top, x, p0s, rows=None):
         oidx, otop, kth = oracle.topk(sc, E)
         g = idx[b][r].cpu().numpy()
         swaps += topk_compare(g, oidx, sc, kth, E)
-        # the reported scores are the fp32 scores of the chosen entries
+        # the reported scores are the fp32 scores of the chosen entries; a score is a sum of 32
+        # signed terms, so its fp32 error scales with the row's score magnitude
         gt = top[b][r].cpu().numpy()
         for i in range(len(r)):
             k = min(512, int(E[i]))
             ref = sc[i, g[i, :k]]
-            assert np.allclose(gt[i, :k], ref, rtol=2e-6, atol=1e-30), f"row {r[i]} scores"
+            scale = np.abs(sc[i, : int(E[i])]).max() if E[i] else 0.0
+            assert np.all(np.abs(gt[i, :k] - ref) <= 1e-5 * scale), f"row {r[i]} scores"
             assert np.all(np.isnan(gt[i, k:]))
     return swaps
 
