@@ -1,78 +1,137 @@
-// Sink-softmax MQA over the gathered rows.  Page "DeepSeek V4.1 - Pooled group / Source
-// layer, pairs pooled", block "Compressed sparse attention": J^w_t = {max(0,t-127)..t},
-// Y = [W; Z], J = [J^w; I + |W|], G_t = Y[J_t], S = Q.G/sqrt(512),
-// A = exp S / (exp s_h + sum exp S), O = sum A G, O-bar_{448:} = R_t^{-1} O_{448:}.
-// "Inside DeepSeek V4.1", section "Attention that looks at 640 places": 64 heads x 512, one
-// shared key/value row per place, a learned sink per head, 640 = 128 + 512 places.
+// Sink-softmax MQA over the gathered rows, on the 5th-generation tensor cores (tcgen05).
+// Page "DeepSeek V4.1 - Pooled group / Source layer, pairs pooled", block "Compressed sparse
+// attention": J^w_t = {max(0,t-127)..t}, Y = [W; Z], J = [J^w; I + |W|], G_t = Y[J_t],
+// S = Q.G/sqrt(512), A = exp S / (exp s_h + sum exp S), O = sum A G, O-bar_{448:} =
+// R_t^{-1} O_{448:}.  "Inside DeepSeek V4.1", section "Attention that looks at 640 places":
+// 64 heads x 512, one shared key/value row per place, a learned sink per head, 640 places.
 //
-// Kernel shape: one block per (query, row split).  Rows are gathered 32 at a time, decoded
-// exactly to bf16 in shared memory (E2M1 x 2^k and E4M3 are exact in bf16), and multiplied
-// with bf16 tensor-core MMAs (fp32 accumulation); the softmax is online over the chunks.
-// Decode (few queries) splits the rows across blocks and merges in a combine kernel.
+// One block per (query, row split).  The gathered rows are processed in chunks of 128:
+//   S^T[rows, heads] = G_c Q^T    (M = 128 rows, N = 64 heads, K = 512; A, B K-major)
+//   O^T[dims, heads] += G_c^T P^T (M = 128 dims x 4 tiles, N = 64, K = 128 rows; A, B MN-major)
+// so that both MMAs have M = 128 and the same shared-memory copy of G_c serves as the
+// K-major A operand of the first and the MN-major A operand of the second.  Operands are
+// fp16: E2M1 x 2^e (for scale exponents -22..12) and E4M3 values are exact in fp16 and
+// convert with one hardware instruction per pair; accumulation is fp32 in tensor memory.
+//
+// Warp roles (416 threads):
+//   warps 0-3   softmax + epilogue; thread = TMEM lane = row of S^T / dim of O^T
+//   warps 4-11  producers: Q -> smem once, then gather + decode 128 rows per chunk, two
+//               threads per row; the raw rows of chunk c+1 wait in registers while chunk c
+//               is consumed and are written as soon as the O MMAs free each 128-dim tile
+//   warp 12     TMEM allocation and the single MMA-issuing thread
+// Online softmax with a lazy reference: a head's reference m only moves when a chunk's
+// maximum exceeds it by more than kTau (log2 units), so P <= 2^kTau and O is rescaled in
+// TMEM rarely (in practice only at the first chunk, where there is nothing to rescale).
+#include <cuda_fp16.h>
+
 #include "csa2_common.cuh"
+#include "csa2_sm100.cuh"
 
 namespace csa2 {
 namespace {
 
-constexpr int kAttThreads = 256;       // 8 warps
-constexpr int kChunk = 32;             // rows per gathered chunk
-constexpr int kQStride = kD + 8;       // padded smem row (bf16 elements)
-constexpr int kPStride = kChunk + 8;
-constexpr int kMaxRows = kWin + kTopK; // 640
-constexpr float kLog2e = 1.4426950408889634f;
+using namespace sm100;
 
-struct AttSmem {
-  __nv_bfloat16 q[kH][kQStride];
-  __nv_bfloat16 g[kChunk][kQStride];
-  __nv_bfloat16 p[kH][kPStride];
-  float s[kH][kChunk + 1];
-  float m[kH], l[kH], alpha[kH];
-  int32_t rows[kMaxRows];
-  uint16_t lut8[256];  // e4m3 code -> bf16 bits
-  int nrows, nwin;
+constexpr int kThreads = 416;
+constexpr int kRows = 128;                  // rows per chunk
+constexpr int kMaxRows = kWin + kTopK;      // 640
+constexpr int kMaxChunks = kMaxRows / kRows;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kTau = 8.0f;                // lazy-rescale threshold (log2 units)
+// dynamic shared memory (1024-aligned): Q 8 atoms x [64 x 128 B], G 8 atoms x [128 x 128 B],
+// P [128 rows x 128 B]
+constexpr uint32_t kQOff = 0, kGOff = 65536, kPOff = 196608, kDynBytes = 212992 + 1024;
+// TMEM columns: O^T tiles at 0, 64, 128, 192; S^T at 256
+constexpr uint32_t kTmemCols = 512, kSCol = 256;
+
+__device__ int g_attend_error;
+
+struct Bars {
+  uint64_t q_full, s_full, p_full;
+  uint64_t atom_full[8];
+  uint64_t tile_free[4];
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n}\n" : "=r"(r) : "r"(byte));
+  return r;
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{\n .reg .b16 h0, h1;\n mov.b32 {h0, h1}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h0;\n}\n" : "=r"(r) : "r"(two));
+  return r;
 }
-__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+__device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t y) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(x), "r"(y));
+  return r;
 }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
-  __nv_bfloat16 v = __float2bfloat16_rn(x);
-  return *reinterpret_cast<uint16_t*>(&v);
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// grid (T, nb, nsplit).  nsplit == 1: writes out.  Otherwise writes the split's unnormalised
-// O, running max m (log2 units) and sum l to the workspace for attend_combine_kernel.
-__global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a, SeqPos pos, int b0, RopeFreq rf, int nsplit,
-                                                                int rows_per_split, float* part_o, float* part_ml) {
-  extern __shared__ __align__(16) unsigned char smraw[];
-  AttSmem& sm = *reinterpret_cast<AttSmem*>(smraw);
+// Reduce v[32] over the 32 lanes of the warp; lane l receives the result for entry l.
+// Each round a lane keeps half of its entries and exchanges the other half.
+template <bool kMax>
+__device__ __forceinline__ float transpose_reduce32(const float (&v)[32], int lane) {
+  auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
+  float a[16], b[8], c[4], d[2];
+  bool up = lane & 16;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float send = up ? v[i] : v[16 + i], keep = up ? v[16 + i] : v[i];
+    a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+  up = lane & 8;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = up ? a[i] : a[8 + i], keep = up ? a[8 + i] : a[i];
+    b[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+  up = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = up ? b[i] : b[4 + i], keep = up ? b[4 + i] : b[i];
+    c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+  up = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = up ? c[i] : c[2 + i], keep = up ? c[2 + i] : c[i];
+    d[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  }
+  up = lane & 1;
+  const float send = up ? d[0] : d[1], keep = up ? d[1] : d[0];
+  return op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+}
+
+// grid (T, nb, nsplit).  nsplit == 1 writes `out`; otherwise the split's unnormalised O, its
+// reference m (log2 units) and sum l go to the partial buffers for attend_combine_kernel.
+__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, SeqPos pos, int b0, RopeFreq rf,
+                                                                int nsplit, int chunks_per_split, float* part_o,
+                                                                float* part_ml) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ Bars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int32_t rows[kMaxRows];
+  __shared__ float red_max[4][64], red_sum[4][64];
+  __shared__ float m_ref[64], alpha_s[64], l_run[64], den_s[64];
+  __shared__ int nrows_sh, nwin_sh, rescale_sh;
+
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* sm = smem_raw + (sbase - smem_u32(smem_raw));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x, bl = blockIdx.y, split = blockIdx.z;
   const int b = b0 + bl;
   const int T = a.T;
-  const int64_t p0 = pos.p0[bl];
-  const int64_t p = p0 + t;
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int64_t p = pos.p0[bl] + t;
   const int64_t qrow = (int64_t)b * T + t;
+  int* err = &g_attend_error;
 
-  // ---- row list: window rows (view row index) then the selected Z entries
-  for (int i = tid; i < 256; i += kAttThreads) sm.lut8[i] = f32_to_bf16_bits(e4m3_to_f32((uint32_t)i));
-  if (tid < 32) {
+  // ---------------------------------------------------------------- setup
+  if (warp == 0) {
     const int nw = (int)min64(kWin, p + 1);
     const int32_t* ip = a.idx + qrow * kTopK;
     int base = nw;
@@ -80,204 +139,306 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(AttendArgs a, Se
       const int32_t j = ip[r0 + lane];
       const bool ok = j >= 0 && j < a.cap;  // out-of-range indices are skipped
       const uint32_t bal = __ballot_sync(0xffffffffu, ok);
-      if (ok) sm.rows[base + __popc(bal & ((1u << lane) - 1u))] = j;
+      if (ok) rows[base + __popc(bal & ((1u << lane) - 1u))] = j;
       base += __popc(bal);
     }
-    for (int i = lane; i < nw; i += 32) sm.rows[i] = t + 128 - nw + i;
+    for (int i = lane; i < nw; i += 32) rows[i] = t + 128 - nw + i;  // window-view row of position p-nw+1+i
     if (lane == 0) {
-      sm.nrows = base;
-      sm.nwin = nw;
+      nrows_sh = base;
+      nwin_sh = nw;
+      rescale_sh = 0;
     }
   }
-  for (int i = tid; i < kH; i += kAttThreads) {
-    sm.m[i] = -INFINITY;
-    sm.l[i] = 0.f;
+  if (tid == 32) {
+    mbar_init(&bars.q_full, 8);
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.p_full, 4);
+    for (int i = 0; i < 8; ++i) mbar_init(&bars.atom_full[i], 8);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars.tile_free[i], 1);
+    mbar_fence_init();
   }
-  // ---- Q [64][512] bf16 -> smem
-  {
-    const uint4* qs = reinterpret_cast<const uint4*>(a.q + qrow * kH * kD);
-    for (int i = tid; i < kH * kD / 8; i += kAttThreads) {
-      const int h = i / (kD / 8), c = i % (kD / 8);
-      *reinterpret_cast<uint4*>(&sm.q[h][c * 8]) = qs[i];
-    }
+  if (warp == 12) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
   }
+  if (tid < 64) {
+    m_ref[tid] = -INFINITY;
+    l_run[tid] = 0.f;
+  }
+  tc_fence_before();
   __syncthreads();
-  const int n = sm.nrows, nw = sm.nwin;
-  const int r_begin = split * rows_per_split;
-  const int r_end = min(n, r_begin + rows_per_split);
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int n = nrows_sh, nw = nwin_sh;
+  const int nch = (n + kRows - 1) / kRows;
+  const int c_begin = split * chunks_per_split;
+  const int nloc = max(0, min(nch, c_begin + chunks_per_split) - c_begin);
 
-  const int hg = w & 3;       // head group of 16
-  const int half = w >> 2;    // S: row half of the chunk; O: dim half
-  const int g = lane >> 2, c4 = lane & 3;
-  float o[32][4];
+  if (warp >= 4 && warp < 12) {
+    // ============================================================ producers
+    const int pidx = tid - 128;
+    if (nloc > 0) {
+      // Q (bf16 [64][512]) -> fp16, 8 K-major atoms of [64 heads x 64 dims]
+      const uint4* qs = reinterpret_cast<const uint4*>(a.q + qrow * kH * kD);
+#pragma unroll 4
+      for (int i = pidx; i < kH * kD / 8; i += 256) {
+        const int h = i >> 6, d0 = (i & 63) * 8;
+        const uint4 v = qs[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  const float scale_log2 = rsqrtf((float)kD) * kLog2e;
-
-  for (int r0 = r_begin; r0 < r_end; r0 += kChunk) {
-    const int nchunk = min(kChunk, r_end - r0);
-    // ---- gather + decode: thread -> (row tid/8, 64 dims)
-    {
-      const int rr = tid >> 3, seg = tid & 7;
-      uint32_t outw[32];
-      if (rr < nchunk) {
-        const int ri = r0 + rr;
+        for (int k = 0; k < 4; ++k) o[k] = f2_to_h2(bf16_to_f32(w[k] & 0xffffu), bf16_to_f32(w[k] >> 16));
+        *reinterpret_cast<uint4*>(sm + kQOff + (d0 >> 6) * 8192 + sw128_off(h, (d0 & 63) >> 3)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.q_full);
+    }
+    const int row = pidx >> 1, half = pidx & 1;
+    uint4 raw[16];
+    int kind = 0;  // 0: no row (zeros), 1: window (FP8), 2: Z (FP4)
+    auto load = [&](int i) {
+      const int ri = (c_begin + i) * kRows + row;
+      kind = 0;
+      if (ri < n) {
         if (ri < nw) {
-          const uint4* src = reinterpret_cast<const uint4*>(a.window + ((int64_t)b * (127 + T) + sm.rows[ri]) * kD + 64 * seg);
+          kind = 1;
+          const uint4* src = reinterpret_cast<const uint4*>(a.window + ((int64_t)b * (127 + T) + rows[ri]) * kD + 256 * half);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 x = src[v];
-            const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+          for (int k = 0; k < 16; ++k) raw[k] = src[k];
+        } else {
+          kind = 2;
+          const int64_t j = rows[ri];
+          const uint4* src = reinterpret_cast<const uint4*>(a.z_codes + ((int64_t)b * a.cap + j) * 256 + 128 * half);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              outw[8 * v + 2 * k] = (uint32_t)sm.lut8[wd[k] & 255] | ((uint32_t)sm.lut8[(wd[k] >> 8) & 255] << 16);
-              outw[8 * v + 2 * k + 1] = (uint32_t)sm.lut8[(wd[k] >> 16) & 255] | ((uint32_t)sm.lut8[wd[k] >> 24] << 16);
+          for (int k = 0; k < 8; ++k) raw[k] = src[k];
+          const uint2 s = *reinterpret_cast<const uint2*>(a.z_scales + ((int64_t)b * a.cap + j) * 16 + 8 * half);
+          raw[8] = make_uint4(s.x, s.y, 0u, 0u);
+        }
+      }
+    };
+    if (nloc > 0) load(0);
+    for (int i = 0; i < nloc; ++i) {
+#pragma unroll
+      for (int at = 0; at < 4; ++at) {
+        const int k = 4 * half + at;  // atom: 64 dims
+        if (i > 0 && (at & 1) == 0) mbar_wait(&bars.tile_free[k >> 1], (i - 1) & 1, err, 1);
+        uint32_t o[32];
+        if (kind == 1) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = raw[4 * at + q];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              o[8 * q + 2 * m] = cvt_e4m3x2_f16x2(w[m] & 0xffffu);
+              o[8 * q + 2 * m + 1] = cvt_e4m3x2_f16x2(w[m] >> 16);
             }
           }
-        } else {
-          const int64_t j = sm.rows[ri];
-          const uint4* src = reinterpret_cast<const uint4*>(a.z_codes + ((int64_t)b * a.cap + j) * 256 + 32 * seg);
-          const uint8_t* scp = a.z_scales + ((int64_t)b * a.cap + j) * 16 + 2 * seg;
+        } else if (kind == 2) {
+          const uint32_t sw = at < 2 ? raw[8].x : raw[8].y;
 #pragma unroll
-          for (int v = 0; v < 2; ++v) {
-            uint4 x = src[v];
-            const float s = ldexpf(1.0f, (int)scp[v] - 127);
-            const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+          for (int blk = 0; blk < 2; ++blk) {  // 32 dims per scale byte
+            const int e = (int)((sw >> (16 * (at & 1) + 8 * blk)) & 255u) - 127;
+            const float sf = ldexpf(1.0f, e);
+            const uint32_t s2 = f2_to_h2(sf, sf);
+            const uint4 v = raw[2 * at + blk];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
+            for (int m = 0; m < 4; ++m)
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                outw[16 * v + 4 * k + q] = pack_bf16(e2m1_to_f32((wd[k] >> (8 * q)) & 15) * s,
-                                                     e2m1_to_f32((wd[k] >> (8 * q + 4)) & 15) * s);
+              for (int by = 0; by < 4; ++by)
+                o[16 * blk + 4 * m + by] = hmul2(cvt_e2m1x2_f16x2((w[m] >> (8 * by)) & 255u), s2);
           }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) o[q] = 0u;
         }
-      } else {
+        unsigned char* dst = sm + kGOff + k * 16384;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) outw[i] = 0u;
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(dst + sw128_off(row, q)) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane < 2) mbar_arrive(&bars.atom_full[4 * lane + at]);
       }
-      uint4* dst = reinterpret_cast<uint4*>(&sm.g[rr][64 * seg]);
-#pragma unroll
-      for (int v = 0; v < 8; ++v) dst[v] = make_uint4(outw[4 * v], outw[4 * v + 1], outw[4 * v + 2], outw[4 * v + 3]);
+      if (i + 1 < nloc) load(i + 1);
     }
-    __syncthreads();
-    // ---- S = Q G^T for heads 16hg.., rows 16half..
-    {
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const int arow = 16 * hg + (lane & 7) + 8 * ((lane >> 3) & 1), acol = 8 * (lane >> 4);
-      const int brow = 16 * half + (lane & 7) + 8 * (lane >> 4), bcol = 8 * ((lane >> 3) & 1);
-#pragma unroll 4
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        uint32_t a0, a1, a2, a3, b0r, b1r, b2r, b3r;
-        ldsm_x4(smem_u32(&sm.q[arow][16 * kk + acol]), a0, a1, a2, a3);
-        ldsm_x4(smem_u32(&sm.g[brow][16 * kk + bcol]), b0r, b1r, b2r, b3r);
-        mma_bf16(s[0], a0, a1, a2, a3, b0r, b1r);
-        mma_bf16(s[1], a0, a1, a2, a3, b2r, b3r);
-      }
+  } else if (warp == 12) {
+    // ============================================================ MMA issuer
+    if (lane == 0 && nloc > 0) {
+      const uint32_t idS = idesc_f16(false, false, 128, 64);
+      const uint32_t idO = idesc_f16(true, true, 128, 64);
+      const uint32_t gq = sbase + kQOff, gg = sbase + kGOff, gp = sbase + kPOff;
+      mbar_wait(&bars.q_full, 0, err, 2);
+      for (int i = 0; i < nloc; ++i) {
+        for (int k = 0; k < 8; ++k) {
+          mbar_wait(&bars.atom_full[k], i & 1, err, 3);
+          tc_fence_after();
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_ss(tmem + kSCol, sw128_desc(gg + k * 16384 + kk * 32, 16, 1024),
+                       sw128_desc(gq + k * 8192 + kk * 32, 16, 1024), idS, (k | kk) != 0);
+        }
+        mma_commit(&bars.s_full);
+        mbar_wait(&bars.p_full, i & 1, err, 4);
+        tc_fence_after();
+        for (int m = 0; m < 4; ++m) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ss(tmem + 64 * m, sw128_desc(gg + 2 * m * 16384 + kk * 2048, 16384, 1024),
+                       sw128_desc(gp + kk * 2048, 8192, 1024), idO, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars.tile_free[m]);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ============================================================ softmax (warps 0-3)
+    const int r = 32 * warp + lane;  // row of the chunk = TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+    const float scale_log2 = rsqrtf((float)kD) * kLog2e;
+    for (int i = 0; i < nloc; ++i) {
+      mbar_wait(&bars.s_full, i & 1, err, 5);
+      tc_fence_after();
+      const bool valid = (c_begin + i) * kRows + r < n;
+      // chunk maximum per head (32 heads at a time)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t u[32];
+        tmem_ld32(lane_addr + kSCol + 32 * hh, u);
+        tmem_wait_ld();
+        float x[32];
+#pragma unroll
+        for (int h = 0; h < 32; ++h) x[h] = valid ? __uint_as_float(u[h]) * scale_log2 : -INFINITY;
+        red_max[warp][32 * hh + lane] = transpose_reduce32<true>(x, lane);
+      }
+      named_bar_sync(1, 128);
+      if (tid < 64) {
+        const float mc = fmaxf(fmaxf(red_max[0][tid], red_max[1][tid]), fmaxf(red_max[2][tid], red_max[3][tid]));
+        const float mo = m_ref[tid];
+        float al = 1.f;
+        if (mc > mo + kTau) {
+          al = exp2f(mo - mc);
+          m_ref[tid] = mc;
+          if (i > 0) rescale_sh = 1;
+        }
+        alpha_s[tid] = al;
+      }
+      named_bar_sync(1, 128);
+      if (rescale_sh) {
+        // O^T (lane = dim, column = head) *= alpha[head] once the previous chunk's MMAs are done
+        mbar_wait(&bars.tile_free[3], (i - 1) & 1, err, 6);
+        tc_fence_after();
+        for (int m = 0; m < 4; ++m)
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t u[32];
+            tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) u[h] = __float_as_uint(__uint_as_float(u[h]) * alpha_s[32 * hh + h]);
+            tmem_st32(lane_addr + 64 * m + 32 * hh, u);
+          }
+        tmem_wait_st();
+      }
+      // P row r (fp16, 64 heads) -> smem, MN-major [rows][heads]; sums of what the MMA uses
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t u[32];
+        tmem_ld32(lane_addr + kSCol + 32 * hh, u);
+        tmem_wait_ld();
+        float pr[32];
+#pragma unroll
+        for (int h = 0; h < 32; ++h)
+          pr[h] = valid ? exp2f(__uint_as_float(u[h]) * scale_log2 - m_ref[32 * hh + h]) : 0.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int h = 16 * hg + g + 8 * (q >> 1);
-          const int r = 16 * half + 8 * nt + 2 * c4 + (q & 1);
-          sm.s[h][r] = r < nchunk ? s[nt][q] * scale_log2 : -INFINITY;
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            w[k] = f2_to_h2(pr[8 * q + 2 * k], pr[8 * q + 2 * k + 1]);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+            pr[8 * q + 2 * k] = f.x;
+            pr[8 * q + 2 * k + 1] = f.y;
+          }
+          *reinterpret_cast<uint4*>(sm + kPOff + sw128_off(r, 4 * hh + q)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-    }
-    __syncthreads();
-    // ---- online softmax statistics: 4 threads per head, 8 rows each
-    {
-      const int h = tid >> 2, qd = tid & 3;
-      const float m_old = sm.m[h], l_old = sm.l[h];
-      float v[8], cmax = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[i] = sm.s[h][8 * qd + i];
-        cmax = fmaxf(cmax, v[i]);
+        red_sum[warp][32 * hh + lane] = transpose_reduce32<false>(pr, lane);
       }
-      cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
-      cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 2));
-      const float m_new = fmaxf(m_old, cmax);
-      const float alpha = exp2f(m_old - m_new);
-      float sum = 0.f;
-      uint32_t pk[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(exp2f(v[2 * i] - m_new), exp2f(v[2 * i + 1] - m_new));
-        const float2 pf = __bfloat1622float2(pb);
-        sum += pf.x + pf.y;
-        pk[i] = *reinterpret_cast<const uint32_t*>(&pb);
-      }
-      *reinterpret_cast<uint4*>(&sm.p[h][8 * qd]) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      fence_proxy_async();
+      tc_fence_before();
       __syncwarp();
-      if (qd == 0) {
-        sm.m[h] = m_new;
-        sm.l[h] = l_old * alpha + sum;
-        sm.alpha[h] = alpha;
-      }
+      if (lane == 0) mbar_arrive(&bars.p_full);
+      named_bar_sync(1, 128);
+      if (tid < 64)
+        l_run[tid] = l_run[tid] * alpha_s[tid] + ((red_sum[0][tid] + red_sum[1][tid]) + (red_sum[2][tid] + red_sum[3][tid]));
+      if (tid == 0) rescale_sh = 0;
     }
-    __syncthreads();
-    // ---- O = alpha O + P G for heads 16hg.., dims 256half..
-    {
-      const float al0 = sm.alpha[16 * hg + g], al1 = sm.alpha[16 * hg + g + 8];
+    // ------------------------------------------------------------ epilogue
+    if (nloc > 0) {
+      mbar_wait(&bars.tile_free[3], (nloc - 1) & 1, err, 7);
+      tc_fence_after();
+    }
+    if (nsplit == 1) {
+      if (tid < 64) den_s[tid] = l_run[tid] + exp2f(a.sinks[tid] * kLog2e - m_ref[tid]);
+      named_bar_sync(1, 128);
+      uint16_t* outq = a.out + qrow * kH * kD;
+      for (int m = 0; m < 4; ++m) {
+        const int d = 128 * m + r;
+        float cs = 1.f, sn = 0.f;
+        if (m == 3 && r >= 64) rope_cs(p, rf.inv_freq[(d - (kD - kDR)) >> 1], -1.0f, cs, sn);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t u[32];
+          tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
+          tmem_wait_ld();
+          float o[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        o[i][0] *= al0; o[i][1] *= al0;
-        o[i][2] *= al1; o[i][3] *= al1;
-      }
-      const int arow = 16 * hg + (lane & 7) + 8 * ((lane >> 3) & 1), acol = 8 * (lane >> 4);
-      const int brow = (lane & 7) + 8 * ((lane >> 3) & 1), bcol = 8 * (lane >> 4);
+          for (int h = 0; h < 32; ++h) o[h] = __uint_as_float(u[h]) / den_s[32 * hh + h];
+          if (m == 3 && warp >= 2) {  // dims 448..511: rotate each (even, odd) pair back by -t
+            const bool odd = d & 1;
 #pragma unroll
-      for (int kk = 0; kk < kChunk / 16; ++kk) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(smem_u32(&sm.p[arow][16 * kk + acol]), a0, a1, a2, a3);
+            for (int h = 0; h < 32; ++h) {
+              const float partner = __shfl_xor_sync(0xffffffffu, o[h], 1);
+              o[h] = odd ? fmaf(partner, sn, o[h] * cs) : fmaf(-partner, sn, o[h] * cs);
+            }
+          }
 #pragma unroll
-        for (int np = 0; np < 16; ++np) {
-          uint32_t b0r, b1r, b2r, b3r;
-          ldsm_x4_t(smem_u32(&sm.g[16 * kk + brow][256 * half + 16 * np + bcol]), b0r, b1r, b2r, b3r);
-          mma_bf16(o[2 * np], a0, a1, a2, a3, b0r, b1r);
-          mma_bf16(o[2 * np + 1], a0, a1, a2, a3, b2r, b3r);
+          for (int h = 0; h < 32; ++h) {
+            const __nv_bfloat16 v = __float2bfloat16_rn(o[h]);
+            outq[(32 * hh + h) * kD + d] = *reinterpret_cast<const uint16_t*>(&v);
+          }
         }
       }
-    }
-    __syncthreads();
-  }
-
-  const int h0 = 16 * hg + g, h1 = h0 + 8;
-  if (nsplit == 1) {
-    const float den0 = sm.l[h0] + exp2f(a.sinks[h0] * kLog2e - sm.m[h0]);
-    const float den1 = sm.l[h1] + exp2f(a.sinks[h1] * kLog2e - sm.m[h1]);
-    const float inv0 = 1.f / den0, inv1 = 1.f / den1;
-    uint16_t* out0 = a.out + (qrow * kH + h0) * kD;
-    uint16_t* out1 = a.out + (qrow * kH + h1) * kD;
+    } else {
+      const int64_t pr_row = ((int64_t)bl * T + t) * nsplit + split;
+      float* po = part_o + pr_row * kH * kD;
+      for (int m = 0; m < 4; ++m) {
+        const int d = 128 * m + r;
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t u[32];
+          if (nloc > 0) {
+            tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-    for (int nt = 0; nt < 32; ++nt) {
-      const int d = 256 * half + 8 * nt + 2 * c4;
-      float x0 = o[nt][0] * inv0, x1 = o[nt][1] * inv0, y0 = o[nt][2] * inv1, y1 = o[nt][3] * inv1;
-      if (d >= kD - kDR) {
-        float cs, sn;
-        rope_cs(p, rf.inv_freq[(d - (kD - kDR)) / 2], -1.0f, cs, sn);
-        const float rx0 = x0 * cs - x1 * sn, rx1 = x0 * sn + x1 * cs;
-        const float ry0 = y0 * cs - y1 * sn, ry1 = y0 * sn + y1 * cs;
-        x0 = rx0; x1 = rx1; y0 = ry0; y1 = ry1;
+            for (int h = 0; h < 32; ++h) u[h] = 0u;
+          }
+#pragma unroll
+          for (int h = 0; h < 32; ++h) po[(32 * hh + h) * kD + d] = __uint_as_float(u[h]);
+        }
       }
-      *reinterpret_cast<uint32_t*>(out0 + d) = pack_bf16(x0, x1);
-      *reinterpret_cast<uint32_t*>(out1 + d) = pack_bf16(y0, y1);
+      if (tid < 64) {
+        part_ml[(pr_row * kH + tid) * 2] = m_ref[tid];
+        part_ml[(pr_row * kH + tid) * 2 + 1] = l_run[tid];
+      }
     }
-  } else {
-    const int64_t pr = ((int64_t)bl * T + t) * nsplit + split;
-    float* po0 = part_o + (pr * kH + h0) * kD;
-    float* po1 = part_o + (pr * kH + h1) * kD;
-#pragma unroll
-    for (int nt = 0; nt < 32; ++nt) {
-      const int d = 256 * half + 8 * nt + 2 * c4;
-      *reinterpret_cast<float2*>(po0 + d) = make_float2(o[nt][0], o[nt][1]);
-      *reinterpret_cast<float2*>(po1 + d) = make_float2(o[nt][2], o[nt][3]);
-    }
-    if (tid < kH) {
-      part_ml[(pr * kH + tid) * 2] = sm.m[tid];
-      part_ml[(pr * kH + tid) * 2 + 1] = sm.l[tid];
-    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -290,14 +451,17 @@ __global__ void __launch_bounds__(128) attend_combine_kernel(AttendArgs a, SeqPo
   const int64_t lrow = (int64_t)bl * a.T + t;  // row within this launch's partials
   const int64_t p = pos.p0[bl] + t;
   float mstar = a.sinks[h] * kLog2e;
-  for (int s = 0; s < nsplit; ++s) mstar = fmaxf(mstar, part_ml[((lrow * nsplit + s) * kH + h) * 2]);
+  for (int s = 0; s < nsplit; ++s) {
+    const int64_t pr = lrow * nsplit + s;
+    if (part_ml[(pr * kH + h) * 2 + 1] > 0.f) mstar = fmaxf(mstar, part_ml[(pr * kH + h) * 2]);
+  }
   float den = exp2f(a.sinks[h] * kLog2e - mstar);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   const int d = 4 * threadIdx.x;
   for (int s = 0; s < nsplit; ++s) {
     const int64_t pr = lrow * nsplit + s;
     const float ms = part_ml[(pr * kH + h) * 2], ls = part_ml[(pr * kH + h) * 2 + 1];
-    if (ls == 0.f) continue;  // split without rows
+    if (!(ls > 0.f)) continue;  // split without rows
     const float wgt = exp2f(ms - mstar);
     den += wgt * ls;
     const float4 v = *reinterpret_cast<const float4*>(part_o + (pr * kH + h) * kD + d);
@@ -316,14 +480,14 @@ __global__ void __launch_bounds__(128) attend_combine_kernel(AttendArgs a, SeqPo
       acc[2 * q + 1] = x0 * sn + x1 * cs;
     }
   }
-  uint2 packed = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
-  *reinterpret_cast<uint2*>(a.out + (qrow * kH + h) * kD + d) = packed;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]), hi = __floats2bfloat162_rn(acc[2], acc[3]);
+  *reinterpret_cast<uint2*>(a.out + (qrow * kH + h) * kD + d) =
+      make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
 }
 
 int choose_splits(int nq, int num_sms) {
   if (nq >= num_sms) return 1;
-  int s = (2 * num_sms + nq - 1) / nq;
-  return max(1, min(s, kMaxRows / kChunk));
+  return max(1, min(kMaxChunks, num_sms / nq));
 }
 
 }  // namespace
@@ -339,19 +503,18 @@ size_t attend_workspace_bytes(int B, int T, int num_sms) {
 cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf, void* ws,
                           size_t ws_bytes, int num_sms, cudaStream_t st) {
   const int s = choose_splits(nb * a.T, num_sms);
-  const size_t smem = sizeof(AttSmem);
-  cudaError_t e = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynBytes);
   if (e != cudaSuccess) return e;
-  int rps = kMaxRows;
+  const int cps = (kMaxChunks + s - 1) / s;
   float *po = nullptr, *pml = nullptr;
   if (s > 1) {
-    rps = ((kMaxRows / s + kChunk - 1) / kChunk) * kChunk;
     const size_t rows = (size_t)nb * a.T * s;
     if (ws_bytes < rows * kH * kD * 4 + rows * kH * 2 * 4) return cudaErrorInvalidValue;
     po = static_cast<float*>(ws);
     pml = po + rows * kH * kD;
   }
-  attend_kernel<<<dim3((unsigned)a.T, (unsigned)nb, (unsigned)s), kAttThreads, smem, st>>>(a, pos, b0, rf, s, rps, po, pml);
+  attend_tc_kernel<<<dim3((unsigned)a.T, (unsigned)nb, (unsigned)s), kThreads, kDynBytes, st>>>(a, pos, b0, rf, s, cps,
+                                                                                                 po, pml);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (s > 1) {
     attend_combine_kernel<<<dim3((unsigned)a.T, (unsigned)nb, kH), 128, 0, st>>>(a, pos, b0, rf, s, po, pml);
