@@ -1,0 +1,299 @@
+// Lightning-indexer scores for prefill on the tcgen05 tensor cores.
+// Page "DeepSeek V4.1 - Pooled group / Source layer, pairs pooled", block "Compressed sparse
+// attention": S^I_{t,j} = sum_h w^I_{t,h} ReLU(Q^I_{h,t} . K^I_j).
+//
+// As a GEMM: D[j, (t,h)] = K^I_j . Q^I_{t,h} with M = 128 keys, N = 256 = 8 queries x 32 heads,
+// K = 128; the epilogue thread that owns key j (one TMEM lane) forms the 8 scores
+// sum_h w_{t,h} ReLU(D[j, (t,h)]) in registers.  Both operands are the FP4 values decoded to
+// fp16 (E2M1 x 2^e is exact in fp16 for scale exponents -22..12): Q^I is quantised to FP4
+// here exactly as in the CUDA-core path, then written as 64 KB "images" per query tile, K^I
+// as 32 KB images per key tile, each image already in the 128B-swizzled K-major layout the
+// MMA reads, so that one bulk copy (cp.async.bulk) stages it.  Products of two E2M1 values
+// times powers of two are exact, and the fp32 accumulation of 128 of them is exact while
+// the block exponents of a row stay within ~10 of each other, as for the CUDA-core path.
+//
+// Persistent kernel, 256 threads: warp 0 issues the bulk copies, warp 1 allocates TMEM and
+// issues the MMAs, warps 4-7 run the epilogue.  A query tile's image stays resident
+// (double-buffered) while its causal key tiles stream through a 2-stage ring; accumulators
+// are double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile overlaps the
+// MMAs of the next.
+#include <cuda_fp16.h>
+
+#include "csa2_common.cuh"
+#include "csa2_sm100.cuh"
+
+namespace csa2 {
+namespace {
+
+using namespace sm100;
+
+constexpr int kQPerTile = 8;                       // queries per query tile (N = 256)
+constexpr uint32_t kQImg = 65536, kKImg = 32768;   // bytes per image
+constexpr int kThreadsTC = 256;
+// dynamic smem: B (query images) 2 x 64 KB, A (key images) 2 x 32 KB, w^I 2 x [8][32] floats
+constexpr uint32_t kBOff = 0, kAOff = 131072, kWOff = 196608, kDynTC = 196608 + 2048 + 1024;
+
+__device__ int g_index_error;
+
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Q^I (bf16) -> FP4 (E2M1, UE8M0 per 32) -> fp16 image.  grid (Tq, nb), 128 threads: warp w
+// handles heads 8w..8w+7, lane l values 4l..4l+3.  Query t of the chunk lives in tile t/8,
+// rows (t%8)*32 + h of the tile's [256 x 128] K-major image (2 atoms of 64 dims).
+__global__ void __launch_bounds__(128) qimage_kernel(IndexArgs a, int b0, int t0, int Tq, int nqt, uint8_t* qimg,
+                                                     float* wq) {
+  const int tl = blockIdx.x, bl = blockIdx.y;
+  const int t = t0 + tl;
+  const int b = b0 + bl;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int64_t src = (int64_t)b * a.T + t;
+  uint8_t* tile = qimg + ((int64_t)bl * nqt + tl / kQPerTile) * kQImg;
+  for (int h = 8 * w; h < 8 * w + 8; ++h) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(a.qi + (src * kHI + h) * kDI + 4 * l);
+    float v[4] = {bf16_to_f32(raw.x & 0xffff), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xffff), bf16_to_f32(raw.y >> 16)};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const int e = mx_scale_exp(amax);
+    float q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = ldexpf(e2m1_to_f32(f32_to_e2m1(ldexpf(v[i], -e))), e);
+    const int n = (tl % kQPerTile) * kHI + h, d = 4 * l;
+    *reinterpret_cast<uint2*>(tile + (d >> 6) * 32768 + sw128_off(n, (d & 63) >> 3) + (d & 7) * 2) =
+        make_uint2(f2_to_h2(q[0], q[1]), f2_to_h2(q[2], q[3]));
+  }
+  if (threadIdx.x < kHI) wq[((int64_t)bl * Tq + tl) * kHI + threadIdx.x] = bf16_to_f32(a.wI[src * kHI + threadIdx.x]);
+}
+
+// K^I (FP4) -> fp16 image.  grid (key tiles, nb), 128 threads: thread = key of the tile.
+__global__ void __launch_bounds__(128) kimage_kernel(IndexArgs a, int b0, int64_t n_keys, int nkt, uint8_t* kimg) {
+  const int kt = blockIdx.x, bl = blockIdx.y;
+  const int b = b0 + bl;
+  const int r = threadIdx.x;
+  const int64_t j = (int64_t)kt * 128 + r;
+  uint8_t* tile = kimg + ((int64_t)bl * nkt + kt) * kKImg;
+  uint4 c[4];
+  uint32_t sc = 0;
+  if (j < n_keys) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.ki_codes + ((int64_t)b * a.cap + j) * 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = src[i];
+    sc = *reinterpret_cast<const uint32_t*>(a.ki_scales + ((int64_t)b * a.cap + j) * 4);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int blk = 0; blk < 4; ++blk) {  // 32 values: 16 bytes of codes, one scale byte
+    const float s = ldexpf(1.0f, (int)((sc >> (8 * blk)) & 255u) - 127);
+    const uint32_t wd[4] = {c[blk].x, c[blk].y, c[blk].z, c[blk].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // 8 values = one 16-byte chunk of fp16
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t byte = (wd[q] >> (8 * k)) & 255u;
+        o[k] = f2_to_h2(e2m1_to_f32(byte & 15u) * s, e2m1_to_f32(byte >> 4) * s);
+      }
+      const int d = 32 * blk + 8 * q;
+      *reinterpret_cast<uint4*>(tile + (d >> 6) * 16384 + sw128_off(r, (d & 63) >> 3)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+struct TcBars {
+  uint64_t b_full[2], b_free[2], a_full[2], a_free[2], d_full[2], d_free[2];
+};
+
+// The static schedule: in round r CTA c takes query tile r*G + c (even rounds) or
+// r*G + G-1-c (odd rounds), a zig-zag that balances the causal work (key tiles grow with the
+// query index) across CTAs.  -1 past the last tile.
+__device__ __forceinline__ int tile_of(int round, int G, int ntiles) {
+  const int idx = round * G + ((round & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  return idx < ntiles ? idx : -1;
+}
+
+__global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexArgs a, SeqPos pos, int t0, int tq, int nqt,
+                                                                         int nkt, const uint8_t* qimg, const uint8_t* kimg,
+                                                                         const float* wq, float* scores, int64_t ld,
+                                                                         int nb, int Tq) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ TcBars bars;
+  __shared__ uint32_t tmem_base_sh;
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* sm = smem_raw + (sbase - smem_u32(smem_raw));
+  float* sw = reinterpret_cast<float*>(sm + kWOff);  // [2][8][32]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nqt_act = (tq + kQPerTile - 1) / kQPerTile;  // query tiles of this pass (image stride: nqt)
+  const int G = gridDim.x, ntiles = nb * nqt_act;
+  int* err = &g_index_error;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.b_full[i], 1);
+      mbar_init(&bars.b_free[i], 1);
+      mbar_init(&bars.a_full[i], 1);
+      mbar_init(&bars.a_free[i], 1);
+      mbar_init(&bars.d_full[i], 1);
+      mbar_init(&bars.d_free[i], 4);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  // key tiles needed by query tile qt of sequence bl: entries visible to its last query
+  auto n_key_tiles = [&](int bl, int qt) {
+    const int tlast = min(tq, (qt + 1) * kQPerTile) - 1;
+    const int64_t E = (pos.p0[bl] + t0 + tlast + 1) / 2;
+    return (int)((E + 127) / 128);
+  };
+
+  if (warp == 0) {
+    // ============================================================ bulk-copy producer
+    if (lane == 0) {
+      int it = 0, qi = 0;
+      for (int k = 0; k * G < ntiles; ++k) {
+        const int tile = tile_of(k, G, ntiles);
+        if (tile < 0) continue;
+        const int bl = tile / nqt_act, qt = tile % nqt_act;
+        const int nk = n_key_tiles(bl, qt);
+        if (nk == 0) continue;
+        const int sB = qi & 1;
+        if (qi >= 2) mbar_wait(&bars.b_free[sB], ((qi >> 1) - 1) & 1, err, 11);
+        mbar_arrive_expect_tx(&bars.b_full[sB], kQImg);
+        const uint8_t* qsrc = qimg + ((int64_t)bl * nqt + qt) * kQImg;
+        for (int c = 0; c < 4; ++c) bulk_g2s(sm + kBOff + sB * kQImg + c * 16384, qsrc + c * 16384, 16384, &bars.b_full[sB]);
+        for (int kt = 0; kt < nk; ++kt, ++it) {
+          const int sA = it & 1;
+          if (it >= 2) mbar_wait(&bars.a_free[sA], ((it >> 1) - 1) & 1, err, 12);
+          mbar_arrive_expect_tx(&bars.a_full[sA], kKImg);
+          const uint8_t* ksrc = kimg + ((int64_t)bl * nkt + kt) * kKImg;
+          for (int c = 0; c < 2; ++c) bulk_g2s(sm + kAOff + sA * kKImg + c * 16384, ksrc + c * 16384, 16384, &bars.a_full[sA]);
+        }
+        ++qi;
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(false, false, 128, 256);
+      int it = 0, qi = 0, dc = 0;
+      for (int k = 0; k * G < ntiles; ++k) {
+        const int tile = tile_of(k, G, ntiles);
+        if (tile < 0) continue;
+        const int bl = tile / nqt_act, qt = tile % nqt_act;
+        const int nk = n_key_tiles(bl, qt);
+        if (nk == 0) continue;
+        const int sB = qi & 1;
+        mbar_wait(&bars.b_full[sB], (qi >> 1) & 1, err, 13);
+        for (int kt = 0; kt < nk; ++kt, ++it, ++dc) {
+          const int sA = it & 1, sD = dc & 1;
+          mbar_wait(&bars.a_full[sA], (it >> 1) & 1, err, 14);
+          if (dc >= 2) mbar_wait(&bars.d_free[sD], ((dc >> 1) - 1) & 1, err, 15);
+          tc_fence_after();
+          const uint32_t abase = sbase + kAOff + sA * kKImg, bbase = sbase + kBOff + sB * kQImg;
+#pragma unroll
+          for (int k16 = 0; k16 < 8; ++k16) {
+            const uint32_t atom = k16 >> 2, off = (k16 & 3) * 32;
+            mma_f16_ss(tmem + 256 * sD, sw128_desc(abase + atom * 16384 + off, 16, 1024),
+                       sw128_desc(bbase + atom * 32768 + off, 16, 1024), idesc, k16 > 0);
+          }
+          mma_commit(&bars.a_free[sA]);
+          mma_commit(&bars.d_full[sD]);
+        }
+        mma_commit(&bars.b_free[sB]);
+        ++qi;
+      }
+    }
+  } else if (warp >= 4) {
+    // ============================================================ epilogue
+    const int ew = warp - 4, r = 32 * ew + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * ew) << 16);
+    int dc = 0, qi = 0;
+    for (int k = 0; k * G < ntiles; ++k) {
+      const int tile = tile_of(k, G, ntiles);
+      if (tile < 0) continue;
+      const int bl = tile / nqt_act, qt = tile % nqt_act;
+      const int nk = n_key_tiles(bl, qt);
+      if (nk == 0) continue;
+      float* wsm = sw + (qi & 1) * 256;
+      named_bar_sync(2, 128);  // the previous use of this w buffer is finished
+      for (int i = r; i < 256; i += 128) {
+        const int tl = qt * kQPerTile + i / kHI;
+        wsm[i] = tl < tq ? wq[((int64_t)bl * Tq + tl) * kHI + (i % kHI)] : 0.f;
+      }
+      named_bar_sync(2, 128);
+      const int64_t p0 = pos.p0[bl] + t0;
+      for (int kt = 0; kt < nk; ++kt, ++dc) {
+        const int sD = dc & 1;
+        mbar_wait(&bars.d_full[sD], (dc >> 1) & 1, err, 16);
+        tc_fence_after();
+        const int64_t j = (int64_t)kt * 128 + r;
+#pragma unroll 1
+        for (int q = 0; q < kQPerTile; ++q) {
+          const int tl = qt * kQPerTile + q;
+          uint32_t u[32];
+          tmem_ld32(lane_addr + 256 * sD + 32 * q, u);
+          tmem_wait_ld();
+          float s = 0.f;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) s = fmaf(wsm[32 * q + h], fmaxf(__uint_as_float(u[h]), 0.f), s);
+          if (tl < tq && j < (p0 + tl + 1) / 2) scores[((int64_t)bl * Tq + tl) * ld + j] = s;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.d_free[sD]);
+      }
+      ++qi;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+size_t index_tc_image_bytes(int nb, int Tq, int64_t max_entries) {
+  const size_t nqt = (size_t)(Tq + kQPerTile - 1) / kQPerTile;
+  const size_t nkt = (size_t)((max_entries + 127) / 128);
+  return (size_t)nb * (nqt * kQImg + nkt * kKImg);
+}
+
+cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq, int Tq,
+                                   int64_t emax, uint8_t* img, float* wq, float* scores, int64_t ld, int num_sms,
+                                   cudaStream_t st) {
+  const int nqt = (Tq + kQPerTile - 1) / kQPerTile;
+  const int nkt = (int)((emax + 127) / 128);
+  uint8_t* qimg = img;
+  uint8_t* kimg = img + (size_t)nb * nqt * kQImg;
+  qimage_kernel<<<dim3((unsigned)tq, (unsigned)nb), 128, 0, st>>>(a, b0, t0, Tq, nqt, qimg, wq);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (nkt > 0) {
+    kimage_kernel<<<dim3((unsigned)nkt, (unsigned)nb), 128, 0, st>>>(a, b0, emax, nkt, kimg);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  e = cudaFuncSetAttribute(index_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynTC);
+  if (e != cudaSuccess) return e;
+  const int ntiles = nb * ((tq + kQPerTile - 1) / kQPerTile);
+  const int grid = max(1, min(num_sms, ntiles));
+  index_prefill_tc_kernel<<<grid, kThreadsTC, kDynTC, st>>>(a, pos, t0, tq, nqt, nkt, qimg, kimg, wq, scores, ld, nb, Tq);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -29,8 +29,11 @@ struct IndexPlan {
   int64_t ld;       // score row stride (floats)
   int chunk;        // top-k stage-1 chunk
   int nchunks;
-  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, total;
+  bool tc;          // prefill: tensor-core score GEMM (queries per pass >= kMinTcQueries)
+  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, off_img, total;
 };
+
+constexpr int kMinTcQueries = 8;
 
 IndexPlan make_plan(int nb, int T, int64_t max_entries) {
   IndexPlan p;
@@ -43,13 +46,15 @@ IndexPlan make_plan(int nb, int T, int64_t max_entries) {
   p.chunk = (int)c;
   p.nchunks = (int)((p.ld + c - 1) / c);
   size_t rows = (size_t)nb * p.Tq;
+  p.tc = T >= kMinTcQueries;
   size_t off = 0;
-  p.off_q = off; off += align256(rows * kHI * kDI * 4);
+  p.off_q = off; off += p.tc ? 0 : align256(rows * kHI * kDI * 4);
   p.off_w = off; off += align256(rows * kHI * 4);
   p.off_s = off; off += align256(rows * (size_t)p.ld * 4);
   p.off_ck = off; off += align256(rows * p.nchunks * kTopK * 4);
   p.off_cj = off; off += align256(rows * p.nchunks * kTopK * 4);
   p.off_cn = off; off += align256(rows * p.nchunks * 4);
+  p.off_img = off; off += p.tc ? align256(index_tc_image_bytes(nb, p.Tq, p.ld)) : 0;
   p.total = off;
   return p;
 }
@@ -361,7 +366,7 @@ size_t index_workspace_bytes(int B, int T, int64_t max_entries, int /*num_sms*/)
 }
 
 cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int64_t max_entries, void* ws,
-                              size_t ws_bytes, int /*num_sms*/, cudaStream_t st) {
+                              size_t ws_bytes, int num_sms, cudaStream_t st) {
   const IndexPlan p = make_plan(min(nb, kMaxSeqPerLaunch), a.T, max_entries);
   if (ws_bytes < p.total) return cudaErrorInvalidValue;
   char* base = static_cast<char*>(ws);
@@ -385,9 +390,15 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
     const int tq = min(p.Tq, a.T - t0);
     int64_t emax = 0;
     for (int i = 0; i < nb; ++i) emax = max(emax, (pos.p0[i] + t0 + tq) / 2);
-    qprep_kernel<<<dim3(tq, nb), kQprepThreads, 0, st>>>(a, b0, t0, p.Tq, qdq, wq);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (emax > 0) {
+    if (p.tc) {
+      e = launch_index_scores_tc(a, pos, b0, nb, t0, tq, p.Tq, emax, reinterpret_cast<uint8_t*>(base + p.off_img), wq, sc,
+                                 p.ld, num_sms, st);
+      if (e != cudaSuccess) return e;
+    } else {
+      qprep_kernel<<<dim3(tq, nb), kQprepThreads, 0, st>>>(a, b0, t0, p.Tq, qdq, wq);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (!p.tc && emax > 0) {
       dim3 g((unsigned)((emax + kScoreThreads - 1) / kScoreThreads), (unsigned)((tq + kQT - 1) / kQT), (unsigned)nb);
       score_kernel<<<g, kScoreThreads, score_smem, st>>>(a, pos, b0, t0, p.Tq, qdq, wq, sc, p.ld);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
