@@ -124,7 +124,9 @@ def launches_per_step(B: int, T: int, p0: int, num_sms: int) -> int:
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampled every 50 ms from before the timed region; summary() keeps the samples
+    whose timestamps fall inside the window marked by mark_start() / mark_end()."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -138,11 +140,19 @@ class ClockSampler:
             self.path.parent.mkdir(exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
+            time.sleep(0.5)  # nvidia-smi start-up
         except Exception:
             self.proc = None
+        self.t0 = self.t1 = None
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *a):
         if self.proc:
@@ -153,23 +163,32 @@ class ClockSampler:
     def summary(self) -> dict:
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, mx, reasons = [], None, set()
+        import datetime as _dt
+
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.path.read_text().splitlines():
             p = [x.strip() for x in line.split(",")]
-            if len(p) < 9:
+            if len(p) < 10:
                 continue
             try:
-                sm.append(float(p[1]))
-                mx = float(p[2])
+                ts = _dt.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(p[2]), float(p[3]), p[6:10]))
             except ValueError:
                 continue
-            for nm, v in zip(names, p[5:9]):
+        inside = [r for r in rows if self.t0 and self.t1 and self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        note = "samples within the timed region"
+        if not inside:  # region shorter than the sampling period: nearest samples around it
+            inside = sorted(rows, key=lambda r: abs(r[0] - (self.t0 or 0)))[:3]
+            note = "timed region shorter than the 50 ms sampling period: nearest samples"
+        reasons = set()
+        for r in inside:
+            for nm, v in zip(names, r[3]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
-        busy = [s for s in sm if mx and s > 0.5 * mx] or sm
-        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        mx = inside[0][2] if inside else None
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(inside), "note": note}
 
 
 # ------------------------------------------------------------------ our implementation
@@ -218,6 +237,8 @@ def time_workload(step: Step, steps: int, warmup: int, ws: int, flush: torch.Ten
     torch.cuda.synchronize()
     ctx = clocks if clocks is not None else _Null()
     with ctx:
+        if clocks is not None:
+            clocks.mark_start()
         for i in range(steps):
             flush.zero_()  # evict L2 before each step (not timed)
             e = ev[i]
@@ -229,6 +250,8 @@ def time_workload(step: Step, steps: int, warmup: int, ws: int, flush: torch.Ten
             step.attend(s)
             e[3].record(s)
         torch.cuda.synchronize()
+        if clocks is not None:
+            clocks.mark_end()
     barrier(ws)
     per = {n: [ev[i][k].elapsed_time(ev[i][k + 1]) for i in range(steps)] for k, n in enumerate(names)}
     total = [sum(per[n][i] for n in names) for i in range(steps)]
@@ -409,8 +432,8 @@ def run_reference(args, rank, ws):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_4k")
     ap.add_argument("--decode-workload", default="decode_1m")

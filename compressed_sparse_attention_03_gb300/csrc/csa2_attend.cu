@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   __shared__ uint32_t tmem_base_sh;
   __shared__ int32_t rows[kMaxRows];
   __shared__ float red_max[4][64], red_sum[4][64];
-  __shared__ float m_ref[64], alpha_s[64], l_run[64], den_s[64];
+  __shared__ float m_ref[64], alpha_s[64], l_run[64], den_s[64];  // den_s: 1 / denominator
   __shared__ int nrows_sh, nwin_sh, rescale_sh;
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -132,16 +132,30 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
 
   // ---------------------------------------------------------------- setup
   if (warp == 0) {
+    // all 512 indices in one round trip (16 per lane); the order of the gathered rows does not
+    // matter to the result, so each lane appends its valid entries after a warp prefix sum
     const int nw = (int)min64(kWin, p + 1);
-    const int32_t* ip = a.idx + qrow * kTopK;
-    int base = nw;
-    for (int r0 = 0; r0 < kTopK; r0 += 32) {
-      const int32_t j = ip[r0 + lane];
-      const bool ok = j >= 0 && j < a.cap;  // out-of-range indices are skipped
-      const uint32_t bal = __ballot_sync(0xffffffffu, ok);
-      if (ok) rows[base + __popc(bal & ((1u << lane) - 1u))] = j;
-      base += __popc(bal);
+    const int4* ip = reinterpret_cast<const int4*>(a.idx + qrow * kTopK);
+    int32_t jv[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int4 x = ip[v * 32 + lane];
+      jv[4 * v] = x.x; jv[4 * v + 1] = x.y; jv[4 * v + 2] = x.z; jv[4 * v + 3] = x.w;
     }
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) cnt += (jv[k] >= 0 && jv[k] < a.cap) ? 1 : 0;  // out-of-range entries are skipped
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int wpos = nw + incl - cnt;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      if (jv[k] >= 0 && jv[k] < a.cap) rows[wpos++] = jv[k];
+    const int base = nw + __shfl_sync(0xffffffffu, incl, 31);
     for (int i = lane; i < nw; i += 32) rows[i] = t + 128 - nw + i;  // window-view row of position p-nw+1+i
     if (lane == 0) {
       nrows_sh = base;
@@ -177,24 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   if (warp >= 4 && warp < 12) {
     // ============================================================ producers
     const int pidx = tid - 128;
-    if (nloc > 0) {
-      // Q (bf16 [64][512]) -> fp16, 8 K-major atoms of [64 heads x 64 dims]
-      const uint4* qs = reinterpret_cast<const uint4*>(a.q + qrow * kH * kD);
-#pragma unroll 4
-      for (int i = pidx; i < kH * kD / 8; i += 256) {
-        const int h = i >> 6, d0 = (i & 63) * 8;
-        const uint4 v = qs[i];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) o[k] = f2_to_h2(bf16_to_f32(w[k] & 0xffffu), bf16_to_f32(w[k] >> 16));
-        *reinterpret_cast<uint4*>(sm + kQOff + (d0 >> 6) * 8192 + sw128_off(h, (d0 & 63) >> 3)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.q_full);
-    }
     const int row = pidx >> 1, half = pidx & 1;
     uint4 raw[16];
     int kind = 0;  // 0: no row (zeros), 1: window (FP8), 2: Z (FP4)
@@ -218,7 +214,33 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         }
       }
     };
-    if (nloc > 0) load(0);
+    if (nloc > 0) {
+      // Q (bf16 [64][512]) -> fp16, 8 K-major atoms of [64 heads x 64 dims].  A thread's 16
+      // loads are in flight together, and the first chunk's rows are requested before the
+      // conversion so that both latencies overlap.
+      const uint4* qs = reinterpret_cast<const uint4*>(a.q + qrow * kH * kD);
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint4 qv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) qv[k] = qs[pidx + 256 * (8 * part + k)];
+        if (part == 0) load(0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int i = pidx + 256 * (8 * part + k);
+          const int h = i >> 6, d0 = (i & 63) * 8;
+          const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) o[m] = f2_to_h2(bf16_to_f32(w[m] & 0xffffu), bf16_to_f32(w[m] >> 16));
+          *reinterpret_cast<uint4*>(sm + kQOff + (d0 >> 6) * 8192 + sw128_off(h, (d0 & 63) >> 3)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.q_full);
+    }
     for (int i = 0; i < nloc; ++i) {
 #pragma unroll
       for (int at = 0; at < 4; ++at) {
@@ -303,30 +325,47 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       mbar_wait(&bars.s_full, i & 1, err, 5);
       tc_fence_after();
       const bool valid = (c_begin + i) * kRows + r < n;
-      // chunk maximum per head (32 heads at a time)
+      // After the first chunk the per-head reference only moves if some score exceeds it by
+      // more than kTau; each thread checks its own row and one barrier ORs the answers.
+      bool need_max = (i == 0);
+      if (!need_max) {
+        bool over = false;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t u[32];
-        tmem_ld32(lane_addr + kSCol + 32 * hh, u);
-        tmem_wait_ld();
-        float x[32];
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t u[32];
+          tmem_ld32(lane_addr + kSCol + 32 * hh, u);
+          tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) x[h] = valid ? __uint_as_float(u[h]) * scale_log2 : -INFINITY;
-        red_max[warp][32 * hh + lane] = transpose_reduce32<true>(x, lane);
-      }
-      named_bar_sync(1, 128);
-      if (tid < 64) {
-        const float mc = fmaxf(fmaxf(red_max[0][tid], red_max[1][tid]), fmaxf(red_max[2][tid], red_max[3][tid]));
-        const float mo = m_ref[tid];
-        float al = 1.f;
-        if (mc > mo + kTau) {
-          al = exp2f(mo - mc);
-          m_ref[tid] = mc;
-          if (i > 0) rescale_sh = 1;
+          for (int h = 0; h < 32; ++h) over |= valid && (__uint_as_float(u[h]) * scale_log2 > m_ref[32 * hh + h] + kTau);
         }
-        alpha_s[tid] = al;
+        need_max = bar_red_or(1, 128, over);
       }
-      named_bar_sync(1, 128);
+      if (need_max) {
+        // chunk maximum per head (32 heads at a time)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t u[32];
+          tmem_ld32(lane_addr + kSCol + 32 * hh, u);
+          tmem_wait_ld();
+          float x[32];
+#pragma unroll
+          for (int h = 0; h < 32; ++h) x[h] = valid ? __uint_as_float(u[h]) * scale_log2 : -INFINITY;
+          red_max[warp][32 * hh + lane] = transpose_reduce32<true>(x, lane);
+        }
+        named_bar_sync(1, 128);
+        if (tid < 64) {
+          const float mc = fmaxf(fmaxf(red_max[0][tid], red_max[1][tid]), fmaxf(red_max[2][tid], red_max[3][tid]));
+          const float mo = m_ref[tid];
+          float al = 1.f;
+          if (mc > mo + kTau) {
+            al = exp2f(mo - mc);
+            m_ref[tid] = mc;
+            if (i > 0) rescale_sh = 1;
+          }
+          alpha_s[tid] = al;
+        }
+        named_bar_sync(1, 128);
+      }
       if (rescale_sh) {
         // O^T (lane = dim, column = head) *= alpha[head] once the previous chunk's MMAs are done
         mbar_wait(&bars.tile_free[3], (i - 1) & 1, err, 6);
@@ -372,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       if (lane == 0) mbar_arrive(&bars.p_full);
       named_bar_sync(1, 128);
       if (tid < 64)
-        l_run[tid] = l_run[tid] * alpha_s[tid] + ((red_sum[0][tid] + red_sum[1][tid]) + (red_sum[2][tid] + red_sum[3][tid]));
+        l_run[tid] = l_run[tid] * (need_max ? alpha_s[tid] : 1.f) +
+                     ((red_sum[0][tid] + red_sum[1][tid]) + (red_sum[2][tid] + red_sum[3][tid]));
       if (tid == 0) rescale_sh = 0;
     }
     // ------------------------------------------------------------ epilogue
@@ -381,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       tc_fence_after();
     }
     if (nsplit == 1) {
-      if (tid < 64) den_s[tid] = l_run[tid] + exp2f(a.sinks[tid] * kLog2e - m_ref[tid]);
+      if (tid < 64) den_s[tid] = 1.f / (l_run[tid] + exp2f(a.sinks[tid] * kLog2e - m_ref[tid]));
       named_bar_sync(1, 128);
       uint16_t* outq = a.out + qrow * kH * kD;
       for (int m = 0; m < 4; ++m) {
@@ -394,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
           tmem_wait_ld();
           float o[32];
 #pragma unroll
-          for (int h = 0; h < 32; ++h) o[h] = __uint_as_float(u[h]) / den_s[32 * hh + h];
+          for (int h = 0; h < 32; ++h) o[h] = __uint_as_float(u[h]) * den_s[32 * hh + h];
           if (m == 3 && warp >= 2) {  // dims 448..511: rotate each (even, odd) pair back by -t
             const bool odd = d & 1;
 #pragma unroll

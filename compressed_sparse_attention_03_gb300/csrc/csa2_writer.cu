@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kWriterThreads) writer_entries_kernel(WriterAr
   const int ne = (int)min64(kEntriesPerBlock, n_new - e_base);
   const int tid = threadIdx.x;
   const int ch = 4 * tid;
+  for (int e = ne; e < kEntriesPerBlock; ++e) *reinterpret_cast<float4*>(&sc[e][ch]) = make_float4(0.f, 0.f, 0.f, 0.f);
 
   // ---- phase 1: pooled key, RMSNorm, Z
   for (int e = 0; e < ne; ++e) {
@@ -123,20 +124,25 @@ __global__ void __launch_bounds__(kWriterThreads) writer_entries_kernel(WriterAr
   }
   __syncthreads();
 
-  // ---- phase 2: k^i = c W_IK for the block's entries (thread = output column)
+  // ---- phase 2: k^i = c W_IK for the block's entries (thread = output column).  Rows of
+  // sc beyond `ne` hold zeros, so all kEntriesPerBlock accumulators run unconditionally and
+  // stay in registers.
   DF acc[kEntriesPerBlock];
 #pragma unroll
   for (int e = 0; e < kEntriesPerBlock; ++e) acc[e] = DF{0.f, 0.f};
   const int o = tid;
+#pragma unroll 4
   for (int d = 0; d < kD; ++d) {
     const float w = bf16_to_f32(a.w_ik[d * kDI + o]);
 #pragma unroll
-    for (int e = 0; e < kEntriesPerBlock; ++e)
-      if (e < ne) acc[e].add_prod(sc[e][d], w);
+    for (int e = 0; e < kEntriesPerBlock; ++e) acc[e].add_prod(sc[e][d], w);
   }
 
-  // ---- phase 3: RMSNorm, RoPE by 2j on dims 64..127, FP4
-  for (int e = 0; e < ne; ++e) {
+  // ---- phase 3: RMSNorm, RoPE by 2j on dims 64..127, FP4 (unrolled so that acc[] is
+  // indexed at compile time; the guard is uniform across the block)
+#pragma unroll
+  for (int e = 0; e < kEntriesPerBlock; ++e) {
+    if (e >= ne) break;
     const int64_t j = sj[e];
     const float ki = acc[e].s + acc[e].c;
     double ss = block_sum<kWriterThreads>((double)ki * (double)ki, red);
