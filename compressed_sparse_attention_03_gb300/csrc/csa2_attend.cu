@@ -13,6 +13,13 @@
 // fp16: E2M1 x 2^e (for scale exponents -22..12) and E4M3 values are exact in fp16 and
 // convert with one hardware instruction per pair; accumulation is fp32 in tensor memory.
 //
+// The per-head row sums l_h = sum_rows P[row, h] come from the tensor core too: a fifth O-phase
+// accumulator multiplies P^T by an all-ones A operand (one 1 KB swizzle atom addressed with a
+// zero row-group stride), so the softmax never reduces across lanes after the first chunk.
+// S^T is accumulated in two independent halves (dims 0..255 and 256..511) and the O-phase
+// MMAs run K-step-major over the five tiles, so consecutive MMAs never wait on each other's
+// accumulator.
+//
 // Warp roles (416 threads):
 //   warps 0-3   softmax + epilogue; thread = TMEM lane = row of S^T / dim of O^T
 //   warps 4-11  producers: Q -> smem once, then gather + decode 128 rows per chunk, two
@@ -39,10 +46,12 @@ constexpr int kMaxChunks = kMaxRows / kRows;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.0f;                // lazy-rescale threshold (log2 units)
 // dynamic shared memory (1024-aligned): Q 8 atoms x [64 x 128 B], G 8 atoms x [128 x 128 B],
-// P [128 rows x 128 B]
-constexpr uint32_t kQOff = 0, kGOff = 65536, kPOff = 196608, kDynBytes = 212992 + 1024;
-// TMEM columns: O^T tiles at 0, 64, 128, 192; S^T at 256
-constexpr uint32_t kTmemCols = 512, kSCol = 256;
+// P [128 rows x 128 B], one 1 KB swizzle atom of fp16 ones
+constexpr uint32_t kQOff = 0, kGOff = 65536, kPOff = 196608, kOnesOff = 212992, kDynBytes = 214016 + 1024;
+// TMEM columns: O^T tiles at 0, 64, 128, 192; row sums at 256; S^T halves at 320 and 384
+constexpr uint32_t kTmemCols = 512, kLCol = 256, kSCol = 320;
+// epilogue staging of one O^T tile in the (then free) G region: [128 dims][kStage floats]
+constexpr int kStage = 68;
 
 __device__ int g_attend_error;
 
@@ -116,9 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int32_t rows[kMaxRows];
-  __shared__ float red_max[4][64], red_sum[4][64];
+  __shared__ float red_max[4][64];
   __shared__ float m_ref[64], alpha_s[64], l_run[64], den_s[64];  // den_s: 1 / denominator
-  __shared__ int nrows_sh, nwin_sh, rescale_sh;
+  __shared__ int nrows_sh, nwin_sh;
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   unsigned char* sm = smem_raw + (sbase - smem_u32(smem_raw));
@@ -160,7 +169,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     if (lane == 0) {
       nrows_sh = base;
       nwin_sh = nw;
-      rescale_sh = 0;
     }
   }
   if (tid == 32) {
@@ -237,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
               make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
+      if (pidx < 64) *reinterpret_cast<uint4*>(sm + kOnesOff + 16 * pidx) = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.q_full);
@@ -292,27 +301,36 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     if (lane == 0 && nloc > 0) {
       const uint32_t idS = idesc_f16(false, false, 128, 64);
       const uint32_t idO = idesc_f16(true, true, 128, 64);
+      const uint32_t idL = idesc_f16(false, true, 128, 64);  // ones (any layout) x P^T (MN-major)
       const uint32_t gq = sbase + kQOff, gg = sbase + kGOff, gp = sbase + kPOff;
       mbar_wait(&bars.q_full, 0, err, 2);
+      const uint64_t ones_desc = sw128_desc(sbase + kOnesOff, 16, 0);  // every row group reads the same atom
       for (int i = 0; i < nloc; ++i) {
-        for (int k = 0; k < 8; ++k) {
-          mbar_wait(&bars.atom_full[k], i & 1, err, 3);
-          tc_fence_after();
+        // S^T: two independent accumulators (dims 0..255 and 256..511), issued alternately
+        for (int k2 = 0; k2 < 4; ++k2)
+          for (int hf = 0; hf < 2; ++hf) {
+            const int k = 4 * hf + k2;
+            mbar_wait(&bars.atom_full[k], i & 1, err, 3);
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16_ss(tmem + kSCol, sw128_desc(gg + k * 16384 + kk * 32, 16, 1024),
-                       sw128_desc(gq + k * 8192 + kk * 32, 16, 1024), idS, (k | kk) != 0);
-        }
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(tmem + kSCol + 64 * hf, sw128_desc(gg + k * 16384 + kk * 32, 16, 1024),
+                         sw128_desc(gq + k * 8192 + kk * 32, 16, 1024), idS, (k2 | kk) != 0);
+          }
         mma_commit(&bars.s_full);
         mbar_wait(&bars.p_full, i & 1, err, 4);
         tc_fence_after();
-        for (int m = 0; m < 4; ++m) {
+        // O^T tiles and the row sums, K-step-major over the five independent accumulators
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t pd = sw128_desc(gp + kk * 2048, 8192, 1024);
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_f16_ss(tmem + 64 * m, sw128_desc(gg + 2 * m * 16384 + kk * 2048, 16384, 1024),
-                       sw128_desc(gp + kk * 2048, 8192, 1024), idO, (i > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.tile_free[m]);
+          for (int m = 0; m < 4; ++m)
+            mma_f16_ss(tmem + 64 * m, sw128_desc(gg + 2 * m * 16384 + kk * 2048, 16384, 1024), pd, idO, acc);
+          mma_f16_ss(tmem + kLCol, ones_desc, pd, idL, acc);
         }
+        for (int m = 0; m < 4; ++m) mma_commit(&bars.tile_free[m]);
       }
     }
     __syncwarp();
@@ -321,35 +339,50 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     const int r = 32 * warp + lane;  // row of the chunk = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
     const float scale_log2 = rsqrtf((float)kD) * kLog2e;
+    // x[32] = scaled scores of heads 32hh..32hh+31 for this thread's row (sum of the S halves)
+    auto load_x = [&](int hh, bool valid, float (&x)[32]) {
+      uint32_t u[32], v[32];
+      tmem_ld32(lane_addr + kSCol + 32 * hh, u);
+      tmem_ld32(lane_addr + kSCol + 64 + 32 * hh, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int h = 0; h < 32; ++h) x[h] = valid ? (__uint_as_float(u[h]) + __uint_as_float(v[h])) * scale_log2 : -INFINITY;
+    };
+    // P = exp2(x - m) as fp16 into the MN-major [rows][heads] operand; true if some score
+    // exceeds its head's reference by more than kTau
+    auto write_p = [&](bool valid) {
+      bool over = false;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float x[32];
+        load_x(hh, valid, x);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int h0 = 8 * q + 2 * k;
+            const float m0 = m_ref[32 * hh + h0], m1 = m_ref[32 * hh + h0 + 1];
+            over |= (x[h0] > m0 + kTau) | (x[h0 + 1] > m1 + kTau);
+            w[k] = f2_to_h2(exp2f(x[h0] - m0), exp2f(x[h0 + 1] - m1));
+          }
+          *reinterpret_cast<uint4*>(sm + kPOff + sw128_off(r, 4 * hh + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      return over;
+    };
     for (int i = 0; i < nloc; ++i) {
       mbar_wait(&bars.s_full, i & 1, err, 5);
       tc_fence_after();
       const bool valid = (c_begin + i) * kRows + r < n;
-      // After the first chunk the per-head reference only moves if some score exceeds it by
-      // more than kTau; each thread checks its own row and one barrier ORs the answers.
-      bool need_max = (i == 0);
-      if (!need_max) {
-        bool over = false;
+      // Optimistic pass with the current references (for the first chunk they are -inf, so the
+      // check always fails there); one barrier ORs whether any head needs a new reference.
+      const bool over = write_p(valid);
+      if (bar_red_or(1, 128, over)) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          uint32_t u[32];
-          tmem_ld32(lane_addr + kSCol + 32 * hh, u);
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < 32; ++h) over |= valid && (__uint_as_float(u[h]) * scale_log2 > m_ref[32 * hh + h] + kTau);
-        }
-        need_max = bar_red_or(1, 128, over);
-      }
-      if (need_max) {
-        // chunk maximum per head (32 heads at a time)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t u[32];
-          tmem_ld32(lane_addr + kSCol + 32 * hh, u);
-          tmem_wait_ld();
           float x[32];
-#pragma unroll
-          for (int h = 0; h < 32; ++h) x[h] = valid ? __uint_as_float(u[h]) * scale_log2 : -INFINITY;
+          load_x(hh, valid, x);
           red_max[warp][32 * hh + lane] = transpose_reduce32<true>(x, lane);
         }
         named_bar_sync(1, 128);
@@ -360,118 +393,111 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
           if (mc > mo + kTau) {
             al = exp2f(mo - mc);
             m_ref[tid] = mc;
-            if (i > 0) rescale_sh = 1;
           }
           alpha_s[tid] = al;
         }
         named_bar_sync(1, 128);
-      }
-      if (rescale_sh) {
-        // O^T (lane = dim, column = head) *= alpha[head] once the previous chunk's MMAs are done
-        mbar_wait(&bars.tile_free[3], (i - 1) & 1, err, 6);
-        tc_fence_after();
-        for (int m = 0; m < 4; ++m)
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t u[32];
-            tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
-            tmem_wait_ld();
+        if (i > 0) {
+          // O^T tiles and row sums (lane = dim, column = head) *= alpha[head], once the previous
+          // chunk's MMAs are done
+          mbar_wait(&bars.tile_free[3], (i - 1) & 1, err, 6);
+          tc_fence_after();
+          for (int m = 0; m < 5; ++m)
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t u[32];
+              tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
+              tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 32; ++h) u[h] = __float_as_uint(__uint_as_float(u[h]) * alpha_s[32 * hh + h]);
-            tmem_st32(lane_addr + 64 * m + 32 * hh, u);
-          }
-        tmem_wait_st();
-      }
-      // P row r (fp16, 64 heads) -> smem, MN-major [rows][heads]; sums of what the MMA uses
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t u[32];
-        tmem_ld32(lane_addr + kSCol + 32 * hh, u);
-        tmem_wait_ld();
-        float pr[32];
-#pragma unroll
-        for (int h = 0; h < 32; ++h)
-          pr[h] = valid ? exp2f(__uint_as_float(u[h]) * scale_log2 - m_ref[32 * hh + h]) : 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            w[k] = f2_to_h2(pr[8 * q + 2 * k], pr[8 * q + 2 * k + 1]);
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-            pr[8 * q + 2 * k] = f.x;
-            pr[8 * q + 2 * k + 1] = f.y;
-          }
-          *reinterpret_cast<uint4*>(sm + kPOff + sw128_off(r, 4 * hh + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+              for (int h = 0; h < 32; ++h) u[h] = __float_as_uint(__uint_as_float(u[h]) * alpha_s[32 * hh + h]);
+              tmem_st32(lane_addr + 64 * m + 32 * hh, u);
+            }
+          tmem_wait_st();
         }
-        red_sum[warp][32 * hh + lane] = transpose_reduce32<false>(pr, lane);
+        write_p(valid);
       }
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.p_full);
-      named_bar_sync(1, 128);
-      if (tid < 64)
-        l_run[tid] = l_run[tid] * (need_max ? alpha_s[tid] : 1.f) +
-                     ((red_sum[0][tid] + red_sum[1][tid]) + (red_sum[2][tid] + red_sum[3][tid]));
-      if (tid == 0) rescale_sh = 0;
     }
     // ------------------------------------------------------------ epilogue
     if (nloc > 0) {
       mbar_wait(&bars.tile_free[3], (nloc - 1) & 1, err, 7);
       tc_fence_after();
     }
-    if (nsplit == 1) {
-      if (tid < 64) den_s[tid] = 1.f / (l_run[tid] + exp2f(a.sinks[tid] * kLog2e - m_ref[tid]));
-      named_bar_sync(1, 128);
-      uint16_t* outq = a.out + qrow * kH * kD;
-      for (int m = 0; m < 4; ++m) {
-        const int d = 128 * m + r;
-        float cs = 1.f, sn = 0.f;
-        if (m == 3 && r >= 64) rope_cs(p, rf.inv_freq[(d - (kD - kDR)) >> 1], -1.0f, cs, sn);
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t u[32];
+    // row sums: every lane of the sum tile holds sum_rows P[row, h]
+    if (tid < 64) {
+      float l = 0.f;
+      if (nloc > 0) {
+        uint32_t u[32];
+        tmem_ld32(lane_addr + kLCol + 32 * (tid >> 5), u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 32; ++h)
+          if (h == lane) l = __uint_as_float(u[h]);
+      }
+      l_run[tid] = l;
+      den_s[tid] = nsplit == 1 ? 1.f / (l + exp2f(a.sinks[tid] * kLog2e - m_ref[tid])) : 1.f;
+    }
+    named_bar_sync(1, 128);
+    // O^T tile by tile through smem: thread = dim writes its 64 heads as a row, then tasks
+    // (head, 8 dims) read columns and store 16 bytes (bf16 out) or 32 bytes (fp32 partials)
+    float* stage = reinterpret_cast<float*>(sm + kGOff);
+    const int64_t pr_row = ((int64_t)bl * T + t) * nsplit + split;
+    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t u[32];
+        if (nloc > 0) {
           tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
           tmem_wait_ld();
-          float o[32];
+        } else {
 #pragma unroll
-          for (int h = 0; h < 32; ++h) o[h] = __uint_as_float(u[h]) * den_s[32 * hh + h];
-          if (m == 3 && warp >= 2) {  // dims 448..511: rotate each (even, odd) pair back by -t
-            const bool odd = d & 1;
+          for (int h = 0; h < 32; ++h) u[h] = 0u;
+        }
 #pragma unroll
-            for (int h = 0; h < 32; ++h) {
-              const float partner = __shfl_xor_sync(0xffffffffu, o[h], 1);
-              o[h] = odd ? fmaf(partner, sn, o[h] * cs) : fmaf(-partner, sn, o[h] * cs);
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(stage + r * kStage + 32 * hh + 4 * q) =
+              make_float4(__uint_as_float(u[4 * q]) * den_s[32 * hh + 4 * q], __uint_as_float(u[4 * q + 1]) * den_s[32 * hh + 4 * q + 1],
+                          __uint_as_float(u[4 * q + 2]) * den_s[32 * hh + 4 * q + 2], __uint_as_float(u[4 * q + 3]) * den_s[32 * hh + 4 * q + 3]);
+      }
+      named_bar_sync(1, 128);
+#pragma unroll 2
+      for (int task = tid; task < 64 * 16; task += 128) {
+        const int h = task & 63, g = task >> 6;  // head, group of 8 dims
+        float o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = stage[(8 * g + k) * kStage + h];
+        const int d0 = 128 * m + 8 * g;
+        if (nsplit == 1) {
+          if (d0 >= kD - kDR) {  // rotate each (even, odd) pair back by -t
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float cs, sn;
+              rope_cs(p, rf.inv_freq[(d0 - (kD - kDR)) / 2 + k], -1.0f, cs, sn);
+              const float x0 = o[2 * k], x1 = o[2 * k + 1];
+              o[2 * k] = x0 * cs - x1 * sn;
+              o[2 * k + 1] = x0 * sn + x1 * cs;
             }
           }
+          uint32_t w[4];
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            const __nv_bfloat16 v = __float2bfloat16_rn(o[h]);
-            outq[(32 * hh + h) * kD + d] = *reinterpret_cast<const uint16_t*>(&v);
+          for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(o[2 * k], o[2 * k + 1]);
+            w[k] = *reinterpret_cast<const uint32_t*>(&v);
           }
+          *reinterpret_cast<uint4*>(a.out + (qrow * kH + h) * kD + d0) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+          float4* po = reinterpret_cast<float4*>(part_o + (pr_row * kH + h) * kD + d0);
+          po[0] = make_float4(o[0], o[1], o[2], o[3]);
+          po[1] = make_float4(o[4], o[5], o[6], o[7]);
         }
       }
-    } else {
-      const int64_t pr_row = ((int64_t)bl * T + t) * nsplit + split;
-      float* po = part_o + pr_row * kH * kD;
-      for (int m = 0; m < 4; ++m) {
-        const int d = 128 * m + r;
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t u[32];
-          if (nloc > 0) {
-            tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int h = 0; h < 32; ++h) u[h] = 0u;
-          }
-#pragma unroll
-          for (int h = 0; h < 32; ++h) po[(32 * hh + h) * kD + d] = __uint_as_float(u[h]);
-        }
-      }
-      if (tid < 64) {
-        part_ml[(pr_row * kH + tid) * 2] = m_ref[tid];
-        part_ml[(pr_row * kH + tid) * 2 + 1] = l_run[tid];
-      }
+      named_bar_sync(1, 128);
+    }
+    if (nsplit > 1 && tid < 64) {
+      part_ml[(pr_row * kH + tid) * 2] = m_ref[tid];
+      part_ml[(pr_row * kH + tid) * 2 + 1] = l_run[tid];
     }
   }
   tc_fence_before();
