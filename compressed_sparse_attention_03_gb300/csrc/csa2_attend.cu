@@ -5,30 +5,28 @@
 // R_t^{-1} O_{448:}.  "Inside DeepSeek V4.1", section "Attention that looks at 640 places":
 // 64 heads x 512, one shared key/value row per place, a learned sink per head, 640 places.
 //
-// One block per (query, row split).  The gathered rows are processed in chunks of 128:
-//   S^T[rows, heads] = G_c Q^T    (M = 128 rows, N = 64 heads, K = 512; A, B K-major)
-//   O^T[dims, heads] += G_c^T P^T (M = 128 dims x 4 tiles, N = 64, K = 128 rows; A, B MN-major)
-// so that both MMAs have M = 128 and the same shared-memory copy of G_c serves as the
-// K-major A operand of the first and the MN-major A operand of the second.  Operands are
-// fp16: E2M1 x 2^e (for scale exponents -22..12) and E4M3 values are exact in fp16 and
-// convert with one hardware instruction per pair; accumulation is fp32 in tensor memory.
-//
-// The per-head row sums l_h = sum_rows P[row, h] come from the tensor core too: a fifth O-phase
-// accumulator multiplies P^T by an all-ones A operand (one 1 KB swizzle atom addressed with a
-// zero row-group stride), so the softmax never reduces across lanes after the first chunk.
-// S^T is accumulated in two independent halves (dims 0..255 and 256..511) and the O-phase
-// MMAs run K-step-major over the five tiles, so consecutive MMAs never wait on each other's
-// accumulator.
+// One block per (query, row split).  The gathered rows form chunks of 128 (at most 5), and
+// G is decoded twice into a 4-slot ring of "atoms" (128 rows x 64 dims, fp16, 128B-swizzled):
+//   pass 1  S^T_c[rows, heads] = G_c Q^T    M=128 rows, N=64 heads, K=512 (8 atoms, K-major)
+//           into its own TMEM tile per chunk; the softmax turns each S tile into
+//           P_c = exp2(S - m) (fp16, kept in smem for all chunks) while the next chunk's MMAs run
+//   pass 2  O^T[dims, heads] += G_c^T P_c^T  M=128 dims, N=64, K=128 rows (atom pairs, MN-major)
+//           for dims 0..255 over all chunks, then dims 256..511, plus l_h = sum_rows P
+//           from a ones x P^T MMA (one 1 KB swizzle atom of ones, zero row-group stride).
+// Operands are fp16: E2M1 x 2^e (scale exponents -22..12) and E4M3 values are exact in fp16
+// and convert with one hardware instruction per pair; accumulation is fp32 in TMEM.
+// Measured on GB300: a 128 x 64 x 16 fp16 MMA takes ~50 cycles and alternating accumulators
+// costs more, so every accumulator receives its MMAs consecutively.
 //
 // Warp roles (416 threads):
 //   warps 0-3   softmax + epilogue; thread = TMEM lane = row of S^T / dim of O^T
-//   warps 4-11  producers: Q -> smem once, then gather + decode 128 rows per chunk, two
-//               threads per row; the raw rows of chunk c+1 wait in registers while chunk c
-//               is consumed and are written as soon as the O MMAs free each 128-dim tile
+//   warps 4-11  producers: Q -> smem, then the atom sequence (pass 1: chunk-major, 8 atoms per
+//               chunk; pass 2: dims 0..255 then 256..511), two threads per row and atom, raw
+//               rows fetched 4 atoms ahead into registers
 //   warp 12     TMEM allocation and the single MMA-issuing thread
 // Online softmax with a lazy reference: a head's reference m only moves when a chunk's
-// maximum exceeds it by more than kTau (log2 units), so P <= 2^kTau and O is rescaled in
-// TMEM rarely (in practice only at the first chunk, where there is nothing to rescale).
+// maximum exceeds it by more than kTau (log2 units), so P <= 2^kTau; when it moves, the
+// earlier chunks' P (still in smem, before any O MMA) are rescaled.
 #include <cuda_fp16.h>
 
 #include "csa2_common.cuh"
@@ -43,22 +41,24 @@ constexpr int kThreads = 416;
 constexpr int kRows = 128;                  // rows per chunk
 constexpr int kMaxRows = kWin + kTopK;      // 640
 constexpr int kMaxChunks = kMaxRows / kRows;
+constexpr int kSlots = 4;                   // G atom ring
+constexpr int kAhead = 4;                   // raw atoms prefetched per producer thread
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.0f;                // lazy-rescale threshold (log2 units)
-// dynamic shared memory (1024-aligned): Q 8 atoms x [64 x 128 B], G 8 atoms x [128 x 128 B],
-// P [128 rows x 128 B], one 1 KB swizzle atom of fp16 ones
-constexpr uint32_t kQOff = 0, kGOff = 65536, kPOff = 196608, kOnesOff = 212992, kDynBytes = 214016 + 1024;
-// TMEM columns: O^T tiles at 0, 64, 128, 192; row sums at 256; S^T halves at 320 and 384
-constexpr uint32_t kTmemCols = 512, kLCol = 256, kSCol = 320;
-// epilogue staging of one O^T tile in the (then free) G region: [128 dims][kStage floats]
-constexpr int kStage = 68;
+// dynamic shared memory (1024-aligned): Q 8 atoms x [64 heads x 128 B] (later: epilogue
+// staging), P 5 chunks x [128 rows x 128 B], G ring 4 atoms x [128 rows x 128 B], ones 1 KB
+constexpr uint32_t kQOff = 0, kPOff = 65536, kGOff = 147456, kOnesOff = 212992, kDynBytes = 214016 + 1024;
+// TMEM columns: O^T dims 0..127 at 0, 128..255 at 64, row sums at 128, S^T chunk c at 192+64c;
+// pass 2b puts O^T dims 256..383 / 384..511 into the S columns of chunks 0 / 1
+constexpr uint32_t kTmemCols = 512, kLCol = 128, kSCol = 192;
+constexpr int kStage = 68;                  // epilogue staging row (floats) in the Q region
 
 __device__ int g_attend_error;
 
 struct Bars {
-  uint64_t q_full, s_full, p_full;
-  uint64_t atom_full[8];
-  uint64_t tile_free[4];
+  uint64_t q_full, p_all, o_lo, o_hi;
+  uint64_t s_full[kMaxChunks];
+  uint64_t atom_full[kSlots], atom_free[kSlots];
 };
 
 __device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
@@ -116,6 +116,18 @@ __device__ __forceinline__ float transpose_reduce32(const float (&v)[32], int la
   return op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
 }
 
+// Atom `seq` of the sequence, in the order the MMAs consume them: pass 1 (seq < 8n) chunk
+// seq/8, dims block seq%8; pass 2, for each 128-dim tile (blocks 2u, 2u+1, u = 0..3), the
+// block pair of every chunk in turn.
+struct AtomId {
+  int chunk, blk;
+};
+__device__ __forceinline__ AtomId atom_of(int seq, int nloc) {
+  if (seq < 8 * nloc) return {seq >> 3, seq & 7};
+  const int s2 = seq - 8 * nloc, tile = s2 / (2 * nloc), w = s2 % (2 * nloc);
+  return {w >> 1, 2 * tile + (w & 1)};
+}
+
 // grid (T, nb, nsplit).  nsplit == 1 writes `out`; otherwise the split's unnormalised O, its
 // reference m (log2 units) and sum l go to the partial buffers for attend_combine_kernel.
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, SeqPos pos, int b0, RopeFreq rf,
@@ -126,7 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   __shared__ uint32_t tmem_base_sh;
   __shared__ int32_t rows[kMaxRows];
   __shared__ float red_max[4][64];
-  __shared__ float m_ref[64], alpha_s[64], l_run[64], den_s[64];  // den_s: 1 / denominator
+  __shared__ float m_ref[64], alpha_s[64], den_s[64], l_s[64];  // den_s: 1 / denominator
+  __shared__ float2 rope_s[kDR / 2];                            // cos, sin of -t per rotated pair
   __shared__ int nrows_sh, nwin_sh;
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -171,22 +184,28 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       nwin_sh = nw;
     }
   }
-  if (tid == 32) {
+  if (warp == 1) {
+    float cs, sn;
+    rope_cs(p, rf.inv_freq[lane], -1.0f, cs, sn);
+    rope_s[lane] = make_float2(cs, sn);
+  }
+  if (tid == 64) {
     mbar_init(&bars.q_full, 8);
-    mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_full, 4);
-    for (int i = 0; i < 8; ++i) mbar_init(&bars.atom_full[i], 8);
-    for (int i = 0; i < 4; ++i) mbar_init(&bars.tile_free[i], 1);
+    mbar_init(&bars.p_all, 4);
+    mbar_init(&bars.o_lo, 1);
+    mbar_init(&bars.o_hi, 1);
+    for (int i = 0; i < kMaxChunks; ++i) mbar_init(&bars.s_full[i], 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&bars.atom_full[i], 8);
+      mbar_init(&bars.atom_free[i], 1);
+    }
     mbar_fence_init();
   }
   if (warp == 12) {
     tmem_alloc(&tmem_base_sh, kTmemCols);
     tmem_relinquish();
   }
-  if (tid < 64) {
-    m_ref[tid] = -INFINITY;
-    l_run[tid] = 0.f;
-  }
+  if (tid < 64) m_ref[tid] = -INFINITY;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -195,44 +214,46 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   const int nch = (n + kRows - 1) / kRows;
   const int c_begin = split * chunks_per_split;
   const int nloc = max(0, min(nch, c_begin + chunks_per_split) - c_begin);
+  const int n_atoms = 16 * nloc;
 
   if (warp >= 4 && warp < 12) {
     // ============================================================ producers
     const int pidx = tid - 128;
-    const int row = pidx >> 1, half = pidx & 1;
-    uint4 raw[16];
-    int kind = 0;  // 0: no row (zeros), 1: window (FP8), 2: Z (FP4)
-    auto load = [&](int i) {
-      const int ri = (c_begin + i) * kRows + row;
-      kind = 0;
-      if (ri < n) {
-        if (ri < nw) {
-          kind = 1;
-          const uint4* src = reinterpret_cast<const uint4*>(a.window + ((int64_t)b * (127 + T) + rows[ri]) * kD + 256 * half);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) raw[k] = src[k];
-        } else {
-          kind = 2;
-          const int64_t j = rows[ri];
-          const uint4* src = reinterpret_cast<const uint4*>(a.z_codes + ((int64_t)b * a.cap + j) * 256 + 128 * half);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) raw[k] = src[k];
-          const uint2 s = *reinterpret_cast<const uint2*>(a.z_scales + ((int64_t)b * a.cap + j) * 16 + 8 * half);
-          raw[8] = make_uint4(s.x, s.y, 0u, 0u);
-        }
+    const int row = pidx >> 1, sub = pidx & 1;  // row of the chunk, 32-dim half of the atom
+    uint4 raw[kAhead][2];
+    uint32_t sc[kAhead];
+    int kind[kAhead];  // 0: no row (zeros), 1: window (FP8), 2: Z (FP4)
+    auto fetch = [&](int seq, int s) {  // s == seq % kAhead, a compile-time constant at every call
+      kind[s] = 0;
+      if (seq >= n_atoms) return;
+      const AtomId id = atom_of(seq, nloc);
+      const int ri = (c_begin + id.chunk) * kRows + row;
+      if (ri >= n) return;
+      const int d0 = 64 * id.blk + 32 * sub;
+      if (ri < nw) {
+        kind[s] = 1;
+        const uint4* src = reinterpret_cast<const uint4*>(a.window + ((int64_t)b * (127 + T) + rows[ri]) * kD + d0);
+        raw[s][0] = src[0];
+        raw[s][1] = src[1];
+      } else {
+        kind[s] = 2;
+        const int64_t j = rows[ri];
+        raw[s][0] = *reinterpret_cast<const uint4*>(a.z_codes + ((int64_t)b * a.cap + j) * 256 + d0 / 2);
+        sc[s] = a.z_scales[((int64_t)b * a.cap + j) * 16 + d0 / 32];
       }
     };
     if (nloc > 0) {
-      // Q (bf16 [64][512]) -> fp16, 8 K-major atoms of [64 heads x 64 dims].  A thread's 16
-      // loads are in flight together, and the first chunk's rows are requested before the
-      // conversion so that both latencies overlap.
+      // Q (bf16 [64][512]) -> fp16, 8 K-major atoms of [64 heads x 64 dims]; the first raw atoms
+      // are requested between the two halves so that the latencies overlap
       const uint4* qs = reinterpret_cast<const uint4*>(a.q + qrow * kH * kD);
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint4 qv[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) qv[k] = qs[pidx + 256 * (8 * part + k)];
-        if (part == 0) load(0);
+        if (part == 0)
+#pragma unroll
+          for (int s = 0; s < kAhead; ++s) fetch(s, s);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int i = pidx + 256 * (8 * part + k);
@@ -250,51 +271,42 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.q_full);
     }
-    for (int i = 0; i < nloc; ++i) {
+    static_assert(kAhead == kSlots, "the producer loop is unrolled by the ring depth");
+    for (int seq0 = 0; seq0 < n_atoms; seq0 += kSlots) {  // n_atoms is a multiple of 4
 #pragma unroll
-      for (int at = 0; at < 4; ++at) {
-        const int k = 4 * half + at;  // atom: 64 dims
-        if (i > 0 && (at & 1) == 0) mbar_wait(&bars.tile_free[k >> 1], (i - 1) & 1, err, 1);
-        uint32_t o[32];
-        if (kind == 1) {
+      for (int s = 0; s < kSlots; ++s) {
+        const int seq = seq0 + s, slot = s;
+        if (seq >= kSlots) mbar_wait(&bars.atom_free[slot], ((seq / kSlots) - 1) & 1, err, 1);
+        uint32_t o[16];
+        if (kind[s] == 1) {
+          const uint32_t w[8] = {raw[s][0].x, raw[s][0].y, raw[s][0].z, raw[s][0].w,
+                                 raw[s][1].x, raw[s][1].y, raw[s][1].z, raw[s][1].w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 v = raw[4 * at + q];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              o[8 * q + 2 * m] = cvt_e4m3x2_f16x2(w[m] & 0xffffu);
-              o[8 * q + 2 * m + 1] = cvt_e4m3x2_f16x2(w[m] >> 16);
-            }
+          for (int m = 0; m < 8; ++m) {
+            o[2 * m] = cvt_e4m3x2_f16x2(w[m] & 0xffffu);
+            o[2 * m + 1] = cvt_e4m3x2_f16x2(w[m] >> 16);
           }
-        } else if (kind == 2) {
-          const uint32_t sw = at < 2 ? raw[8].x : raw[8].y;
+        } else if (kind[s] == 2) {
+          const float sf = ldexpf(1.0f, (int)sc[s] - 127);
+          const uint32_t s2 = f2_to_h2(sf, sf);
+          const uint32_t w[4] = {raw[s][0].x, raw[s][0].y, raw[s][0].z, raw[s][0].w};
 #pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {  // 32 dims per scale byte
-            const int e = (int)((sw >> (16 * (at & 1) + 8 * blk)) & 255u) - 127;
-            const float sf = ldexpf(1.0f, e);
-            const uint32_t s2 = f2_to_h2(sf, sf);
-            const uint4 v = raw[2 * at + blk];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          for (int m = 0; m < 4; ++m)
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
-#pragma unroll
-              for (int by = 0; by < 4; ++by)
-                o[16 * blk + 4 * m + by] = hmul2(cvt_e2m1x2_f16x2((w[m] >> (8 * by)) & 255u), s2);
-          }
+            for (int by = 0; by < 4; ++by) o[4 * m + by] = hmul2(cvt_e2m1x2_f16x2((w[m] >> (8 * by)) & 255u), s2);
         } else {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) o[q] = 0u;
+          for (int q = 0; q < 16; ++q) o[q] = 0u;
         }
-        unsigned char* dst = sm + kGOff + k * 16384;
+        unsigned char* dst = sm + kGOff + slot * 16384;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<uint4*>(dst + sw128_off(row, q)) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(dst + sw128_off(row, 4 * sub + q)) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
         fence_proxy_async();
         __syncwarp();
-        if (lane < 2) mbar_arrive(&bars.atom_full[4 * lane + at]);
+        if (lane == 0) mbar_arrive(&bars.atom_full[slot]);
+        fetch(seq + kAhead, s);
       }
-      if (i + 1 < nloc) load(i + 1);
     }
   } else if (warp == 12) {
     // ============================================================ MMA issuer
@@ -303,34 +315,56 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       const uint32_t idO = idesc_f16(true, true, 128, 64);
       const uint32_t idL = idesc_f16(false, true, 128, 64);  // ones (any layout) x P^T (MN-major)
       const uint32_t gq = sbase + kQOff, gg = sbase + kGOff, gp = sbase + kPOff;
-      mbar_wait(&bars.q_full, 0, err, 2);
       const uint64_t ones_desc = sw128_desc(sbase + kOnesOff, 16, 0);  // every row group reads the same atom
-      for (int i = 0; i < nloc; ++i) {
-        // S^T: two independent accumulators (dims 0..255 and 256..511), issued alternately
-        for (int k2 = 0; k2 < 4; ++k2)
-          for (int hf = 0; hf < 2; ++hf) {
-            const int k = 4 * hf + k2;
-            mbar_wait(&bars.atom_full[k], i & 1, err, 3);
-            tc_fence_after();
+      mbar_wait(&bars.q_full, 0, err, 2);
+      int seq = 0;
+      // pass 1: S^T of every chunk
+      for (int c = 0; c < nloc; ++c) {
+        for (int k = 0; k < 8; ++k, ++seq) {
+          const int slot = seq % kSlots;
+          mbar_wait(&bars.atom_full[slot], (seq / kSlots) & 1, err, 3);
+          tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(tmem + kSCol + 64 * hf, sw128_desc(gg + k * 16384 + kk * 32, 16, 1024),
-                         sw128_desc(gq + k * 8192 + kk * 32, 16, 1024), idS, (k2 | kk) != 0);
-          }
-        mma_commit(&bars.s_full);
-        mbar_wait(&bars.p_full, i & 1, err, 4);
-        tc_fence_after();
-        // O^T tiles and the row sums, K-step-major over the five independent accumulators
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t pd = sw128_desc(gp + kk * 2048, 8192, 1024);
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            mma_f16_ss(tmem + 64 * m, sw128_desc(gg + 2 * m * 16384 + kk * 2048, 16384, 1024), pd, idO, acc);
-          mma_f16_ss(tmem + kLCol, ones_desc, pd, idL, acc);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_ss(tmem + kSCol + 64 * c, sw128_desc(gg + slot * 16384 + kk * 32, 16, 1024),
+                       sw128_desc(gq + k * 8192 + kk * 32, 16, 1024), idS, (k | kk) != 0);
+          mma_commit(&bars.atom_free[slot]);
         }
-        for (int m = 0; m < 4; ++m) mma_commit(&bars.tile_free[m]);
+        mma_commit(&bars.s_full[c]);
+      }
+      mbar_wait(&bars.p_all, 0, err, 4);
+      tc_fence_after();
+      // pass 2: O^T 128-dim tiles over all chunks; atoms come in (even, odd) slot pairs
+      for (int half = 0; half < 2; ++half) {
+        for (int tile = 0; tile < 2; ++tile) {
+          // dims 128*(2*half+tile) ..: accumulator column
+          const uint32_t ocol = half == 0 ? 64u * tile : kSCol + 64u * tile;
+          for (int c = 0; c < nloc; ++c) {
+            const int s0 = 8 * nloc + 2 * nloc * (2 * half + tile) + 2 * c;  // first atom of the pair (even)
+            const int slot = s0 % kSlots;
+            mbar_wait(&bars.atom_full[slot], (s0 / kSlots) & 1, err, 3);
+            mbar_wait(&bars.atom_full[slot + 1], ((s0 + 1) / kSlots) & 1, err, 3);
+            tc_fence_after();
+            const uint32_t pc = gp + c * 16384;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ss(tmem + ocol, sw128_desc(gg + slot * 16384 + kk * 2048, 16384, 1024),
+                         sw128_desc(pc + kk * 2048, 8192, 1024), idO, (c > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bars.atom_free[slot]);
+            mma_commit(&bars.atom_free[slot + 1]);
+          }
+        }
+        if (half == 0) {
+          // row sums l_h = sum over all rows of P[row, h]
+          for (int c = 0; c < nloc; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ss(tmem + kLCol, ones_desc, sw128_desc(gp + c * 16384 + kk * 2048, 8192, 1024), idL,
+                         (c > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars.o_lo);
+        } else {
+          mma_commit(&bars.o_hi);
+        }
       }
     }
     __syncwarp();
@@ -339,23 +373,21 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     const int r = 32 * warp + lane;  // row of the chunk = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
     const float scale_log2 = rsqrtf((float)kD) * kLog2e;
-    // x[32] = scaled scores of heads 32hh..32hh+31 for this thread's row (sum of the S halves)
-    auto load_x = [&](int hh, bool valid, float (&x)[32]) {
-      uint32_t u[32], v[32];
-      tmem_ld32(lane_addr + kSCol + 32 * hh, u);
-      tmem_ld32(lane_addr + kSCol + 64 + 32 * hh, v);
+    auto load_x = [&](int c, int hh, bool valid, float (&x)[32]) {
+      uint32_t u[32];
+      tmem_ld32(lane_addr + kSCol + 64 * c + 32 * hh, u);
       tmem_wait_ld();
 #pragma unroll
-      for (int h = 0; h < 32; ++h) x[h] = valid ? (__uint_as_float(u[h]) + __uint_as_float(v[h])) * scale_log2 : -INFINITY;
+      for (int h = 0; h < 32; ++h) x[h] = valid ? __uint_as_float(u[h]) * scale_log2 : -INFINITY;
     };
-    // P = exp2(x - m) as fp16 into the MN-major [rows][heads] operand; true if some score
-    // exceeds its head's reference by more than kTau
-    auto write_p = [&](bool valid) {
+    // P_c = exp2(x - m) as fp16, MN-major [rows][heads]; true if some score exceeds its head's
+    // reference by more than kTau
+    auto write_p = [&](int c, bool valid) {
       bool over = false;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float x[32];
-        load_x(hh, valid, x);
+        load_x(c, hh, valid, x);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t w[4];
@@ -366,23 +398,22 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
             over |= (x[h0] > m0 + kTau) | (x[h0 + 1] > m1 + kTau);
             w[k] = f2_to_h2(exp2f(x[h0] - m0), exp2f(x[h0 + 1] - m1));
           }
-          *reinterpret_cast<uint4*>(sm + kPOff + sw128_off(r, 4 * hh + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(sm + kPOff + c * 16384 + sw128_off(r, 4 * hh + q)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       return over;
     };
-    for (int i = 0; i < nloc; ++i) {
-      mbar_wait(&bars.s_full, i & 1, err, 5);
+    for (int c = 0; c < nloc; ++c) {
+      mbar_wait(&bars.s_full[c], 0, err, 5);
       tc_fence_after();
-      const bool valid = (c_begin + i) * kRows + r < n;
-      // Optimistic pass with the current references (for the first chunk they are -inf, so the
-      // check always fails there); one barrier ORs whether any head needs a new reference.
-      const bool over = write_p(valid);
-      if (bar_red_or(1, 128, over)) {
+      const bool valid = (c_begin + c) * kRows + r < n;
+      // optimistic pass with the current references (-inf before the first chunk, so the check
+      // always fails there); one barrier ORs whether any head needs a new reference
+      if (bar_red_or(1, 128, write_p(c, valid))) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float x[32];
-          load_x(hh, valid, x);
+          load_x(c, hh, valid, x);
           red_max[warp][32 * hh + lane] = transpose_reduce32<true>(x, lane);
         }
         named_bar_sync(1, 128);
@@ -397,35 +428,33 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
           alpha_s[tid] = al;
         }
         named_bar_sync(1, 128);
-        if (i > 0) {
-          // O^T tiles and row sums (lane = dim, column = head) *= alpha[head], once the previous
-          // chunk's MMAs are done
-          mbar_wait(&bars.tile_free[3], (i - 1) & 1, err, 6);
-          tc_fence_after();
-          for (int m = 0; m < 5; ++m)
-            for (int hh = 0; hh < 2; ++hh) {
-              uint32_t u[32];
-              tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
-              tmem_wait_ld();
+        // earlier chunks' P (this thread's rows) *= alpha[head]; no O MMA has read them yet
+        for (int c2 = 0; c2 < c; ++c2)
 #pragma unroll
-              for (int h = 0; h < 32; ++h) u[h] = __float_as_uint(__uint_as_float(u[h]) * alpha_s[32 * hh + h]);
-              tmem_st32(lane_addr + 64 * m + 32 * hh, u);
+          for (int q = 0; q < 8; ++q) {
+            uint4* pp = reinterpret_cast<uint4*>(sm + kPOff + c2 * 16384 + sw128_off(r, q));
+            uint4 v = *pp;
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+              w[k] = f2_to_h2(f.x * alpha_s[8 * q + 2 * k], f.y * alpha_s[8 * q + 2 * k + 1]);
             }
-          tmem_wait_st();
-        }
-        write_p(valid);
+            *pp = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        write_p(c, valid);
       }
-      fence_proxy_async();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_full);
     }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0 && nloc > 0) mbar_arrive(&bars.p_all);
     // ------------------------------------------------------------ epilogue
+    // row sums: every lane of the sum tile holds sum_rows P[row, h]
     if (nloc > 0) {
-      mbar_wait(&bars.tile_free[3], (nloc - 1) & 1, err, 7);
+      mbar_wait(&bars.o_lo, 0, err, 7);
       tc_fence_after();
     }
-    // row sums: every lane of the sum tile holds sum_rows P[row, h]
     if (tid < 64) {
       float l = 0.f;
       if (nloc > 0) {
@@ -436,20 +465,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         for (int h = 0; h < 32; ++h)
           if (h == lane) l = __uint_as_float(u[h]);
       }
-      l_run[tid] = l;
+      l_s[tid] = l;
       den_s[tid] = nsplit == 1 ? 1.f / (l + exp2f(a.sinks[tid] * kLog2e - m_ref[tid])) : 1.f;
     }
     named_bar_sync(1, 128);
-    // O^T tile by tile through smem: thread = dim writes its 64 heads as a row, then tasks
-    // (head, 8 dims) read columns and store 16 bytes (bf16 out) or 32 bytes (fp32 partials)
-    float* stage = reinterpret_cast<float*>(sm + kGOff);
+    // O^T tile by tile through smem (the Q region): thread = dim writes its 64 heads as a row,
+    // then tasks (head, 8 dims) read columns and store 16 bytes (bf16 out) or 32 (fp32 partials)
+    float* stage = reinterpret_cast<float*>(sm + kQOff);
     const int64_t pr_row = ((int64_t)bl * T + t) * nsplit + split;
     for (int m = 0; m < 4; ++m) {
+      if (m == 2 && nloc > 0) {
+        mbar_wait(&bars.o_hi, 0, err, 8);
+        tc_fence_after();
+      }
+      const uint32_t ocol = m < 2 ? 64u * m : kSCol + 64u * (m - 2);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t u[32];
         if (nloc > 0) {
-          tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
+          tmem_ld32(lane_addr + ocol + 32 * hh, u);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -473,11 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
           if (d0 >= kD - kDR) {  // rotate each (even, odd) pair back by -t
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              float cs, sn;
-              rope_cs(p, rf.inv_freq[(d0 - (kD - kDR)) / 2 + k], -1.0f, cs, sn);
+              const float2 cs = rope_s[(d0 - (kD - kDR)) / 2 + k];
               const float x0 = o[2 * k], x1 = o[2 * k + 1];
-              o[2 * k] = x0 * cs - x1 * sn;
-              o[2 * k + 1] = x0 * sn + x1 * cs;
+              o[2 * k] = x0 * cs.x - x1 * cs.y;
+              o[2 * k + 1] = x0 * cs.y + x1 * cs.x;
             }
           }
           uint32_t w[4];
@@ -497,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     }
     if (nsplit > 1 && tid < 64) {
       part_ml[(pr_row * kH + tid) * 2] = m_ref[tid];
-      part_ml[(pr_row * kH + tid) * 2 + 1] = l_run[tid];
+      part_ml[(pr_row * kH + tid) * 2 + 1] = l_s[tid];
     }
   }
   tc_fence_before();
