@@ -5,28 +5,31 @@
 // R_t^{-1} O_{448:}.  "Inside DeepSeek V4.1", section "Attention that looks at 640 places":
 // 64 heads x 512, one shared key/value row per place, a learned sink per head, 640 places.
 //
-// One block per (query, row split).  The gathered rows form chunks of 128 (at most 5), and
-// G is decoded twice into a 4-slot ring of "atoms" (128 rows x 64 dims, fp16, 128B-swizzled):
-//   pass 1  S^T_c[rows, heads] = G_c Q^T    M=128 rows, N=64 heads, K=512 (8 atoms, K-major)
-//           into its own TMEM tile per chunk; the softmax turns each S tile into
-//           P_c = exp2(S - m) (fp16, kept in smem for all chunks) while the next chunk's MMAs run
-//   pass 2  O^T[dims, heads] += G_c^T P_c^T  M=128 dims, N=64, K=128 rows (atom pairs, MN-major)
-//           for dims 0..255 over all chunks, then dims 256..511, plus l_h = sum_rows P
-//           from a ones x P^T MMA (one 1 KB swizzle atom of ones, zero row-group stride).
-// Operands are fp16: E2M1 x 2^e (scale exponents -22..12) and E4M3 values are exact in fp16
-// and convert with one hardware instruction per pair; accumulation is fp32 in TMEM.
-// Measured on GB300: a 128 x 64 x 16 fp16 MMA takes ~50 cycles and alternating accumulators
-// costs more, so every accumulator receives its MMAs consecutively.
+// One block per (query, row split).  The gathered rows form chunks of 128 (at most 5):
+//   S^T_c[rows, heads] = G_c Q^T     M=128 rows, N=64 heads, K=512 (8 K-major atoms)
+//   O^T[dims, heads] += G_c^T P_c^T  M=128 dims x 4 tiles, N=64, K=128 rows (MN-major)
+//   l_h += sum_rows P_c[row, h]      a ones x P^T MMA (one 1 KB swizzle atom of ones read
+//                                    for every row group through a zero row-group stride)
+// An "atom" is 128 rows x 64 dims of G in fp16, 128B-swizzled; the same atom serves as the
+// K-major A operand of S and, in (even, odd) pairs, the MN-major A operand of one O tile.
+// The MMA stream is software-pipelined: S(0), then S(c) and O(c-1) for c = 1..n-1, then
+// O(n-1), so the softmax of chunk c (S -> P_c in smem) overlaps the MMAs of S(c+1).  G is
+// decoded twice (for S and for O) from FP4 / FP8 rows: E2M1 x 2^e (scale exponents -22..12)
+// and E4M3 are exact in fp16 and convert with one hardware instruction per pair.
+//
+// Measured on GB300: a 128x64x16 fp16 MMA takes ~50 cycles and alternating accumulators
+// costs more, so each accumulator receives its MMAs consecutively; and a barrier arrive with
+// release semantics waits for the arriving thread's outstanding loads, so raw rows are staged
+// with cp.async (not ordered by the arrive) several atoms ahead.
 //
 // Warp roles (416 threads):
 //   warps 0-3   softmax + epilogue; thread = TMEM lane = row of S^T / dim of O^T
-//   warps 4-11  producers: Q -> smem, then the atom sequence (pass 1: chunk-major, 8 atoms per
-//               chunk; pass 2: dims 0..255 then 256..511), two threads per row and atom, raw
-//               rows fetched 4 atoms ahead into registers
+//   warps 4-11  producers: Q -> smem, then every atom: raw 32 dims per thread (cp.async into a
+//               5-deep staging ring) -> decode -> 4-slot atom ring; two threads per row
 //   warp 12     TMEM allocation and the single MMA-issuing thread
 // Online softmax with a lazy reference: a head's reference m only moves when a chunk's
-// maximum exceeds it by more than kTau (log2 units), so P <= 2^kTau; when it moves, the
-// earlier chunks' P (still in smem, before any O MMA) are rescaled.
+// maximum exceeds it by more than kTau (log2 units), so P <= 2^kTau; when it moves, O and l
+// are rescaled in TMEM after the previous chunk's MMAs complete.
 #include <cuda_fp16.h>
 
 #include "csa2_common.cuh"
@@ -41,23 +44,28 @@ constexpr int kThreads = 416;
 constexpr int kRows = 128;                  // rows per chunk
 constexpr int kMaxRows = kWin + kTopK;      // 640
 constexpr int kMaxChunks = kMaxRows / kRows;
-constexpr int kSlots = 4;                   // G atom ring
-constexpr int kAhead = 4;                   // raw atoms prefetched per producer thread
+constexpr int kSlots = 4;                   // decoded atom ring
+constexpr int kStg = 5;                     // raw staging ring (cp.async depth)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.0f;                // lazy-rescale threshold (log2 units)
-// dynamic shared memory (1024-aligned): Q 8 atoms x [64 heads x 128 B] (later: epilogue
-// staging), P 5 chunks x [128 rows x 128 B], G ring 4 atoms x [128 rows x 128 B], ones 1 KB
-constexpr uint32_t kQOff = 0, kPOff = 65536, kGOff = 147456, kOnesOff = 212992, kDynBytes = 214016 + 1024;
-// TMEM columns: O^T dims 0..127 at 0, 128..255 at 64, row sums at 128, S^T chunk c at 192+64c;
-// pass 2b puts O^T dims 256..383 / 384..511 into the S columns of chunks 0 / 1
-constexpr uint32_t kTmemCols = 512, kLCol = 128, kSCol = 192;
-constexpr int kStage = 68;                  // epilogue staging row (floats) in the Q region
+// dynamic shared memory (1024-aligned)
+constexpr uint32_t kQOff = 0;                        // Q: 8 atoms x [64 heads x 128 B]
+constexpr uint32_t kPOff = 65536;                    // P: 2 x [128 rows x 128 B]
+constexpr uint32_t kGOff = 98304;                    // atoms: 4 x [128 rows x 128 B] (epilogue staging later)
+constexpr uint32_t kStgOff = 163840;                 // raw: 5 x [128 rows x 64 B]
+constexpr uint32_t kScOff = 204800;                  // Z scale rows: 3 chunks x [128 x 16 B]
+constexpr uint32_t kOnesOff = 210944;                // 1 KB of fp16 ones
+constexpr uint32_t kDynBytes = 211968 + 1024;
+// TMEM columns: O^T dims tiles at 0, 64, 128, 192; row sums at 256; S^T buffers at 320, 384
+constexpr uint32_t kTmemCols = 512, kLCol = 256, kSCol = 320;
+constexpr int kStage = 68;                           // epilogue staging row (floats)
 
 __device__ int g_attend_error;
 
 struct Bars {
-  uint64_t q_full, p_all, o_lo, o_hi;
+  uint64_t q_full;
   uint64_t s_full[kMaxChunks];
+  uint64_t p_full[2], o_done[2];
   uint64_t atom_full[kSlots], atom_free[kSlots];
 };
 
@@ -116,16 +124,17 @@ __device__ __forceinline__ float transpose_reduce32(const float (&v)[32], int la
   return op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
 }
 
-// Atom `seq` of the sequence, in the order the MMAs consume them: pass 1 (seq < 8n) chunk
-// seq/8, dims block seq%8; pass 2, for each 128-dim tile (blocks 2u, 2u+1, u = 0..3), the
-// block pair of every chunk in turn.
+// Atom `pos` of the stream S(0); S(1), O(0); ...; S(n-1), O(n-2); O(n-1): chunk, dims block
+// (0..7), and whether it belongs to an S pass.  O atoms come in tile order (pairs 0-1, ..., 6-7).
 struct AtomId {
   int chunk, blk;
+  bool s;
 };
-__device__ __forceinline__ AtomId atom_of(int seq, int nloc) {
-  if (seq < 8 * nloc) return {seq >> 3, seq & 7};
-  const int s2 = seq - 8 * nloc, tile = s2 / (2 * nloc), w = s2 % (2 * nloc);
-  return {w >> 1, 2 * tile + (w & 1)};
+__device__ __forceinline__ AtomId atom_of(int pos, int n) {
+  if (pos < 8) return {0, pos, true};
+  if (pos >= 16 * n - 8) return {n - 1, pos - (16 * n - 8), false};
+  const int q = (pos - 8) >> 4, r = (pos - 8) & 15;
+  return r < 8 ? AtomId{q + 1, r, true} : AtomId{q, r - 8, false};
 }
 
 // grid (T, nb, nsplit).  nsplit == 1 writes `out`; otherwise the split's unnormalised O, its
@@ -140,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   __shared__ float red_max[4][64];
   __shared__ float m_ref[64], alpha_s[64], den_s[64], l_s[64];  // den_s: 1 / denominator
   __shared__ float2 rope_s[kDR / 2];                            // cos, sin of -t per rotated pair
-  __shared__ int nrows_sh, nwin_sh;
+  __shared__ int nrows_sh, nwin_sh, moved_sh;
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   unsigned char* sm = smem_raw + (sbase - smem_u32(smem_raw));
@@ -182,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     if (lane == 0) {
       nrows_sh = base;
       nwin_sh = nw;
+      moved_sh = 0;
     }
   }
   if (warp == 1) {
@@ -191,10 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   }
   if (tid == 64) {
     mbar_init(&bars.q_full, 8);
-    mbar_init(&bars.p_all, 4);
-    mbar_init(&bars.o_lo, 1);
-    mbar_init(&bars.o_hi, 1);
     for (int i = 0; i < kMaxChunks; ++i) mbar_init(&bars.s_full[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.p_full[i], 4);
+      mbar_init(&bars.o_done[i], 1);
+    }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&bars.atom_full[i], 8);
       mbar_init(&bars.atom_free[i], 1);
@@ -219,41 +230,42 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   if (warp >= 4 && warp < 12) {
     // ============================================================ producers
     const int pidx = tid - 128;
-    const int row = pidx >> 1, sub = pidx & 1;  // row of the chunk, 32-dim half of the atom
-    uint4 raw[kAhead][2];
-    uint32_t sc[kAhead];
-    int kind[kAhead];  // 0: no row (zeros), 1: window (FP8), 2: Z (FP4)
-    auto fetch = [&](int seq, int s) {  // s == seq % kAhead, a compile-time constant at every call
-      kind[s] = 0;
-      if (seq >= n_atoms) return;
-      const AtomId id = atom_of(seq, nloc);
-      const int ri = (c_begin + id.chunk) * kRows + row;
-      if (ri >= n) return;
-      const int d0 = 64 * id.blk + 32 * sub;
-      if (ri < nw) {
-        kind[s] = 1;
-        const uint4* src = reinterpret_cast<const uint4*>(a.window + ((int64_t)b * (127 + T) + rows[ri]) * kD + d0);
-        raw[s][0] = src[0];
-        raw[s][1] = src[1];
-      } else {
-        kind[s] = 2;
-        const int64_t j = rows[ri];
-        raw[s][0] = *reinterpret_cast<const uint4*>(a.z_codes + ((int64_t)b * a.cap + j) * 256 + d0 / 2);
-        sc[s] = a.z_scales[((int64_t)b * a.cap + j) * 16 + d0 / 32];
+    const int row = pidx >> 1, sub = pidx & 1;  // row of the chunk, 32-dim half of each atom
+    // raw bytes of atom `at` (this thread's 32 dims) -> staging slot at % kStg, asynchronously
+    auto issue = [&](int at) {
+      if (at < n_atoms) {
+        const AtomId id = atom_of(at, nloc);
+        const int ri = (c_begin + id.chunk) * kRows + row;
+        unsigned char* st = sm + kStgOff + (at % kStg) * 8192 + row * 64 + 32 * sub;
+        if (ri < n) {
+          const int d0 = 64 * id.blk + 32 * sub;
+          if (ri < nw) {
+            const unsigned char* src = a.window + ((int64_t)b * (127 + T) + rows[ri]) * kD + d0;
+            cp_async16(st, src);
+            cp_async16(st + 16, src + 16);
+          } else {
+            const int64_t j = rows[ri];
+            cp_async16(st, a.z_codes + ((int64_t)b * a.cap + j) * 256 + d0 / 2);
+            // the chunk's scale row, with its first atom; both threads of the row copy the same 16
+            // bytes so that each only depends on its own copies
+            if (id.s && id.blk == 0)
+              cp_async16(sm + kScOff + (id.chunk % 3) * 2048 + row * 16, a.z_scales + ((int64_t)b * a.cap + j) * 16);
+          }
+        }
       }
+      cp_async_commit();  // one group per atom, possibly empty
     };
     if (nloc > 0) {
       // Q (bf16 [64][512]) -> fp16, 8 K-major atoms of [64 heads x 64 dims]; the first raw atoms
-      // are requested between the two halves so that the latencies overlap
+      // are requested first so that the latencies overlap
+#pragma unroll 1
+      for (int at = 0; at < kStg; ++at) issue(at);
       const uint4* qs = reinterpret_cast<const uint4*>(a.q + qrow * kH * kD);
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint4 qv[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) qv[k] = qs[pidx + 256 * (8 * part + k)];
-        if (part == 0)
-#pragma unroll
-          for (int s = 0; s < kAhead; ++s) fetch(s, s);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int i = pidx + 256 * (8 * part + k);
@@ -271,43 +283,47 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.q_full);
     }
-    static_assert(kAhead == kSlots, "the producer loop is unrolled by the ring depth");
-    for (int seq0 = 0; seq0 < n_atoms; seq0 += kSlots) {  // n_atoms is a multiple of 4
+#pragma unroll 1
+    for (int at = 0; at < n_atoms; ++at) {
+      cp_async_wait<kStg - 1>();  // this thread's copies for atom `at` have landed
+      const AtomId id = atom_of(at, nloc);
+      const int ri = (c_begin + id.chunk) * kRows + row;
+      const unsigned char* st = sm + kStgOff + (at % kStg) * 8192 + row * 64 + 32 * sub;
+      uint32_t o[16];
+      if (ri < n && ri < nw) {
+        const uint4 v0 = *reinterpret_cast<const uint4*>(st), v1 = *reinterpret_cast<const uint4*>(st + 16);
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-      for (int s = 0; s < kSlots; ++s) {
-        const int seq = seq0 + s, slot = s;
-        if (seq >= kSlots) mbar_wait(&bars.atom_free[slot], ((seq / kSlots) - 1) & 1, err, 1);
-        uint32_t o[16];
-        if (kind[s] == 1) {
-          const uint32_t w[8] = {raw[s][0].x, raw[s][0].y, raw[s][0].z, raw[s][0].w,
-                                 raw[s][1].x, raw[s][1].y, raw[s][1].z, raw[s][1].w};
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            o[2 * m] = cvt_e4m3x2_f16x2(w[m] & 0xffffu);
-            o[2 * m + 1] = cvt_e4m3x2_f16x2(w[m] >> 16);
-          }
-        } else if (kind[s] == 2) {
-          const float sf = ldexpf(1.0f, (int)sc[s] - 127);
-          const uint32_t s2 = f2_to_h2(sf, sf);
-          const uint32_t w[4] = {raw[s][0].x, raw[s][0].y, raw[s][0].z, raw[s][0].w};
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int by = 0; by < 4; ++by) o[4 * m + by] = hmul2(cvt_e2m1x2_f16x2((w[m] >> (8 * by)) & 255u), s2);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 16; ++q) o[q] = 0u;
+        for (int m = 0; m < 8; ++m) {
+          o[2 * m] = cvt_e4m3x2_f16x2(w[m] & 0xffffu);
+          o[2 * m + 1] = cvt_e4m3x2_f16x2(w[m] >> 16);
         }
-        unsigned char* dst = sm + kGOff + slot * 16384;
+      } else if (ri < n) {
+        const uint4 v = *reinterpret_cast<const uint4*>(st);
+        const int e = (int)sm[kScOff + (id.chunk % 3) * 2048 + row * 16 + 2 * id.blk + sub] - 127;
+        const float sf = ldexpf(1.0f, e);
+        const uint32_t s2 = f2_to_h2(sf, sf);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(dst + sw128_off(row, 4 * sub + q)) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.atom_full[slot]);
-        fetch(seq + kAhead, s);
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int by = 0; by < 4; ++by) o[4 * m + by] = hmul2(cvt_e2m1x2_f16x2((w[m] >> (8 * by)) & 255u), s2);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) o[q] = 0u;
       }
+      const int slot = at % kSlots;
+      if (at >= kSlots) mbar_wait(&bars.atom_free[slot], ((at / kSlots) - 1) & 1, err, 1);
+      unsigned char* dst = sm + kGOff + slot * 16384;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(dst + sw128_off(row, 4 * sub + q)) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.atom_full[slot]);
+      issue(at + kStg);
     }
+    cp_async_wait<0>();
   } else if (warp == 12) {
     // ============================================================ MMA issuer
     if (lane == 0 && nloc > 0) {
@@ -317,55 +333,47 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       const uint32_t gq = sbase + kQOff, gg = sbase + kGOff, gp = sbase + kPOff;
       const uint64_t ones_desc = sw128_desc(sbase + kOnesOff, 16, 0);  // every row group reads the same atom
       mbar_wait(&bars.q_full, 0, err, 2);
-      int seq = 0;
-      // pass 1: S^T of every chunk
-      for (int c = 0; c < nloc; ++c) {
-        for (int k = 0; k < 8; ++k, ++seq) {
-          const int slot = seq % kSlots;
-          mbar_wait(&bars.atom_full[slot], (seq / kSlots) & 1, err, 3);
+      int at = 0;
+      auto s_pass = [&](int c) {
+        for (int k = 0; k < 8; ++k, ++at) {
+          const int slot = at % kSlots;
+          mbar_wait(&bars.atom_full[slot], (at / kSlots) & 1, err, 3);
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f16_ss(tmem + kSCol + 64 * c, sw128_desc(gg + slot * 16384 + kk * 32, 16, 1024),
+            mma_f16_ss(tmem + kSCol + 64 * (c & 1), sw128_desc(gg + slot * 16384 + kk * 32, 16, 1024),
                        sw128_desc(gq + k * 8192 + kk * 32, 16, 1024), idS, (k | kk) != 0);
           mma_commit(&bars.atom_free[slot]);
         }
         mma_commit(&bars.s_full[c]);
-      }
-      mbar_wait(&bars.p_all, 0, err, 4);
-      tc_fence_after();
-      // pass 2: O^T 128-dim tiles over all chunks; atoms come in (even, odd) slot pairs
-      for (int half = 0; half < 2; ++half) {
-        for (int tile = 0; tile < 2; ++tile) {
-          // dims 128*(2*half+tile) ..: accumulator column
-          const uint32_t ocol = half == 0 ? 64u * tile : kSCol + 64u * tile;
-          for (int c = 0; c < nloc; ++c) {
-            const int s0 = 8 * nloc + 2 * nloc * (2 * half + tile) + 2 * c;  // first atom of the pair (even)
-            const int slot = s0 % kSlots;
-            mbar_wait(&bars.atom_full[slot], (s0 / kSlots) & 1, err, 3);
-            mbar_wait(&bars.atom_full[slot + 1], ((s0 + 1) / kSlots) & 1, err, 3);
-            tc_fence_after();
-            const uint32_t pc = gp + c * 16384;
+      };
+      auto o_pass = [&](int c) {
+        mbar_wait(&bars.p_full[c & 1], (c >> 1) & 1, err, 4);
+        tc_fence_after();
+        const uint32_t pc = gp + (c & 1) * 16384;
+        for (int tile = 0; tile < 4; ++tile, at += 2) {
+          const int slot = at % kSlots;  // even: the pair is (slot, slot + 1)
+          mbar_wait(&bars.atom_full[slot], (at / kSlots) & 1, err, 3);
+          mbar_wait(&bars.atom_full[slot + 1], ((at + 1) / kSlots) & 1, err, 3);
+          tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ss(tmem + ocol, sw128_desc(gg + slot * 16384 + kk * 2048, 16384, 1024),
-                         sw128_desc(pc + kk * 2048, 8192, 1024), idO, (c > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&bars.atom_free[slot]);
-            mma_commit(&bars.atom_free[slot + 1]);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            mma_f16_ss(tmem + 64 * tile, sw128_desc(gg + slot * 16384 + kk * 2048, 16384, 1024),
+                       sw128_desc(pc + kk * 2048, 8192, 1024), idO, (c > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars.atom_free[slot]);
+          mma_commit(&bars.atom_free[slot + 1]);
         }
-        if (half == 0) {
-          // row sums l_h = sum over all rows of P[row, h]
-          for (int c = 0; c < nloc; ++c)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ss(tmem + kLCol, ones_desc, sw128_desc(gp + c * 16384 + kk * 2048, 8192, 1024), idL,
-                         (c > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bars.o_lo);
-        } else {
-          mma_commit(&bars.o_hi);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ss(tmem + kLCol, ones_desc, sw128_desc(pc + kk * 2048, 8192, 1024), idL, (c > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.o_done[c & 1]);
+      };
+      s_pass(0);
+      for (int c = 1; c < nloc; ++c) {
+        s_pass(c);
+        o_pass(c - 1);
       }
+      o_pass(nloc - 1);
     }
     __syncwarp();
   } else {
@@ -375,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     const float scale_log2 = rsqrtf((float)kD) * kLog2e;
     auto load_x = [&](int c, int hh, bool valid, float (&x)[32]) {
       uint32_t u[32];
-      tmem_ld32(lane_addr + kSCol + 64 * c + 32 * hh, u);
+      tmem_ld32(lane_addr + kSCol + 64 * (c & 1) + 32 * hh, u);
       tmem_wait_ld();
 #pragma unroll
       for (int h = 0; h < 32; ++h) x[h] = valid ? __uint_as_float(u[h]) * scale_log2 : -INFINITY;
@@ -398,13 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
             over |= (x[h0] > m0 + kTau) | (x[h0 + 1] > m1 + kTau);
             w[k] = f2_to_h2(exp2f(x[h0] - m0), exp2f(x[h0 + 1] - m1));
           }
-          *reinterpret_cast<uint4*>(sm + kPOff + c * 16384 + sw128_off(r, 4 * hh + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(sm + kPOff + (c & 1) * 16384 + sw128_off(r, 4 * hh + q)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       return over;
     };
     for (int c = 0; c < nloc; ++c) {
       mbar_wait(&bars.s_full[c], 0, err, 5);
+      if (c >= 2) mbar_wait(&bars.o_done[c & 1], ((c - 2) >> 1) & 1, err, 6);  // O(c-2) has read P buffer
       tc_fence_after();
       const bool valid = (c_begin + c) * kRows + r < n;
       // optimistic pass with the current references (-inf before the first chunk, so the check
@@ -424,37 +433,41 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
           if (mc > mo + kTau) {
             al = exp2f(mo - mc);
             m_ref[tid] = mc;
+            if (c > 0) moved_sh = 1;
           }
           alpha_s[tid] = al;
         }
         named_bar_sync(1, 128);
-        // earlier chunks' P (this thread's rows) *= alpha[head]; no O MMA has read them yet
-        for (int c2 = 0; c2 < c; ++c2)
+        if (moved_sh) {
+          // O^T tiles and row sums (lane = dim, column = head) *= alpha[head] once O(c-1) is done
+          mbar_wait(&bars.o_done[(c - 1) & 1], ((c - 1) >> 1) & 1, err, 7);
+          tc_fence_after();
+          for (int m = 0; m < 5; ++m)
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t u[32];
+              tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
+              tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            uint4* pp = reinterpret_cast<uint4*>(sm + kPOff + c2 * 16384 + sw128_off(r, q));
-            uint4 v = *pp;
-            uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-              w[k] = f2_to_h2(f.x * alpha_s[8 * q + 2 * k], f.y * alpha_s[8 * q + 2 * k + 1]);
+              for (int h = 0; h < 32; ++h) u[h] = __float_as_uint(__uint_as_float(u[h]) * alpha_s[32 * hh + h]);
+              tmem_st32(lane_addr + 64 * m + 32 * hh, u);
             }
-            *pp = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          tmem_wait_st();
+        }
         write_p(c, valid);
+        named_bar_sync(1, 128);
+        if (tid == 0) moved_sh = 0;
       }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full[c & 1]);
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0 && nloc > 0) mbar_arrive(&bars.p_all);
     // ------------------------------------------------------------ epilogue
-    // row sums: every lane of the sum tile holds sum_rows P[row, h]
     if (nloc > 0) {
-      mbar_wait(&bars.o_lo, 0, err, 7);
+      mbar_wait(&bars.o_done[(nloc - 1) & 1], ((nloc - 1) >> 1) & 1, err, 8);
       tc_fence_after();
     }
+    // row sums: every lane of the sum tile holds sum_rows P[row, h]
     if (tid < 64) {
       float l = 0.f;
       if (nloc > 0) {
@@ -469,21 +482,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       den_s[tid] = nsplit == 1 ? 1.f / (l + exp2f(a.sinks[tid] * kLog2e - m_ref[tid])) : 1.f;
     }
     named_bar_sync(1, 128);
-    // O^T tile by tile through smem (the Q region): thread = dim writes its 64 heads as a row,
-    // then tasks (head, 8 dims) read columns and store 16 bytes (bf16 out) or 32 (fp32 partials)
-    float* stage = reinterpret_cast<float*>(sm + kQOff);
+    // O^T tile by tile through smem (the atom ring, idle now): thread = dim writes its 64 heads
+    // as a row, then tasks (head, 8 dims) read columns and store 16 bytes (bf16) or 32 (fp32)
+    float* stage = reinterpret_cast<float*>(sm + kGOff);
     const int64_t pr_row = ((int64_t)bl * T + t) * nsplit + split;
     for (int m = 0; m < 4; ++m) {
-      if (m == 2 && nloc > 0) {
-        mbar_wait(&bars.o_hi, 0, err, 8);
-        tc_fence_after();
-      }
-      const uint32_t ocol = m < 2 ? 64u * m : kSCol + 64u * (m - 2);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t u[32];
         if (nloc > 0) {
-          tmem_ld32(lane_addr + ocol + 32 * hh, u);
+          tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
           tmem_wait_ld();
         } else {
 #pragma unroll
