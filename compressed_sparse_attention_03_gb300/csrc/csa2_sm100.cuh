@@ -12,7 +12,11 @@
 namespace csa2 {
 namespace sm100 {
 
-constexpr uint32_t kSpinLimit = 1u << 24;
+// Each poll may suspend the thread for up to kSuspendNs (it resumes as soon as the phase
+// completes), so a waiting warp does not take issue slots from the working ones; kSpinLimit
+// polls bound a wait to a few seconds.
+constexpr uint32_t kSuspendNs = 20000;
+constexpr uint32_t kSpinLimit = 1u << 18;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -30,9 +34,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
