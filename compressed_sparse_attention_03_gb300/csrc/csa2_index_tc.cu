@@ -35,6 +35,16 @@ constexpr uint32_t kBOff = 0, kAOff = 131072, kWOff = 196608, kDynTC = 196608 + 
 
 __device__ int g_index_error;
 
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n}\n" : "=r"(r) : "r"(byte));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t y) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(x), "r"(y));
+  return r;
+}
 __device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -266,7 +276,204 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
   }
 }
 
+// ------------------------------------------------------------------ decode (one query)
+// Scores of one query per sequence against all its visible keys: M = 128 keys, N = 32 heads,
+// K = 128 per tile.  The FP4 keys are decoded inside the kernel (a fp16 image of all keys
+// would cost 4x the key bytes in extra HBM traffic): 128 producer threads (one key each)
+// stage the raw 68-byte keys with cp.async kDStg tiles ahead, decode them exactly to fp16
+// into a kDSlots-deep ring of 32 KB operand tiles, and one thread issues the MMAs into
+// double-buffered TMEM accumulators read by 128 epilogue threads.  Each sequence's key tiles
+// are split evenly over gridDim.x / nb persistent blocks.
+constexpr int kDSlots = 4, kDStg = 4, kDThreads = 288;  // warps 0-3 producers, 4 MMA, 5-8 epilogue
+constexpr uint32_t kDAOff = 0;                     // operand tiles: kDSlots x 32 KB
+constexpr uint32_t kDRawOff = 131072;              // raw codes: kDStg x [128 keys x 64 B]
+constexpr uint32_t kDScOff = 163840;               // raw scales: kDStg x [128 keys x 4 B]
+constexpr uint32_t kDQOff = 165888;                // Q^I image: 2 atoms x [32 heads x 128 B]
+constexpr uint32_t kDynDec = 174080 + 1024;
+
+struct DecBars {
+  uint64_t a_full[kDSlots], a_free[kDSlots], d_full[2], d_free[2];
+};
+
+__global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs a, SeqPos pos, int b0, int nb,
+                                                                       float* scores, int64_t ld) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ DecBars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ float wsh[kHI];
+  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  unsigned char* sm = smem_raw + (sbase - smem_u32(smem_raw));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* err = &g_index_error;
+  // this block's sequence and key-tile range
+  const int per_seq = max(1, (int)gridDim.x / nb);
+  const int bl = blockIdx.x / per_seq, part = blockIdx.x % per_seq;
+  const bool active = bl < nb;
+  const int b = b0 + (active ? bl : 0);
+  const int64_t E = active ? (pos.p0[bl] + 1) / 2 : 0;  // visible entries of the one query
+  const int ntile = (int)((E + 127) / 128);
+  const int tpb = (ntile + per_seq - 1) / per_seq;
+  const int t_begin = min(ntile, part * tpb), t_end = min(ntile, t_begin + tpb);
+  const int nt = active ? t_end - t_begin : 0;
+
+  if (tid == 0) {
+    for (int i = 0; i < kDSlots; ++i) {
+      mbar_init(&bars.a_full[i], 4);
+      mbar_init(&bars.a_free[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.d_full[i], 1);
+      mbar_init(&bars.d_free[i], 4);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(&tmem_base_sh, 64);
+    tmem_relinquish();
+  }
+  // Q^I -> FP4 -> fp16 image (warps 0-3: warp w heads 8w..8w+7, lane l values 4l..4l+3), w^I
+  if (warp < 4 && active) {
+    const int64_t src = (int64_t)b * a.T;  // T == 1
+    for (int h = 8 * warp; h < 8 * warp + 8; ++h) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(a.qi + (src * kHI + h) * kDI + 4 * lane);
+      float v[4] = {bf16_to_f32(raw.x & 0xffff), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xffff), bf16_to_f32(raw.y >> 16)};
+      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+      const int e = mx_scale_exp(amax);
+      float q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = ldexpf(e2m1_to_f32(f32_to_e2m1(ldexpf(v[i], -e))), e);
+      const int d = 4 * lane;
+      *reinterpret_cast<uint2*>(sm + kDQOff + (d >> 6) * 4096 + sw128_off(h, (d & 63) >> 3) + (d & 7) * 2) =
+          make_uint2(f2_to_h2(q[0], q[1]), f2_to_h2(q[2], q[3]));
+    }
+    if (tid < kHI) wsh[tid] = bf16_to_f32(a.wI[src * kHI + tid]);
+    fence_proxy_async();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp < 4) {
+    // ============================================================ producers: thread = key row
+    const int r = tid;
+    auto issue = [&](int i) {
+      if (i < nt) {
+        const int64_t j = (int64_t)(t_begin + i) * 128 + r;
+        if (j < E) {
+          const int st = i % kDStg;
+          const uint8_t* src = a.ki_codes + ((int64_t)b * a.cap + j) * 64;
+          unsigned char* dst = sm + kDRawOff + st * 8192 + r * 64;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) cp_async16(dst + 16 * k, src + 16 * k);
+          cp_async4(sm + kDScOff + st * 512 + r * 4, a.ki_scales + ((int64_t)b * a.cap + j) * 4);
+        }
+      }
+      cp_async_commit();
+    };
+    for (int i = 0; i < kDStg; ++i) issue(i);
+#pragma unroll 1
+    for (int i = 0; i < nt; ++i) {
+      cp_async_wait<kDStg - 1>();
+      const int st = i % kDStg, slot = i % kDSlots;
+      const int64_t j = (int64_t)(t_begin + i) * 128 + r;
+      uint4 c[4];
+      uint32_t sc = 0;
+      if (j < E) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[k] = *reinterpret_cast<const uint4*>(sm + kDRawOff + st * 8192 + r * 64 + 16 * k);
+        sc = *reinterpret_cast<const uint32_t*>(sm + kDScOff + st * 512 + r * 4);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[k] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (i >= kDSlots) mbar_wait(&bars.a_free[slot], ((i / kDSlots) - 1) & 1, err, 21);
+      unsigned char* tile = sm + kDAOff + slot * 32768;
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {  // 32 values: 16 code bytes, one scale byte
+        const float sf = ldexpf(1.0f, (int)((sc >> (8 * blk)) & 255u) - 127);
+        const uint32_t s2 = f2_to_h2(sf, sf);
+        const uint32_t wd[4] = {c[blk].x, c[blk].y, c[blk].z, c[blk].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // 8 values = one 16-byte chunk of fp16
+          uint32_t o[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[k] = hmul2(cvt_e2m1x2_f16x2((wd[q] >> (8 * k)) & 255u), s2);
+          const int d = 32 * blk + 8 * q;
+          *reinterpret_cast<uint4*>(tile + (d >> 6) * 16384 + sw128_off(r, (d & 63) >> 3)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.a_full[slot]);
+      issue(i + kDStg);
+    }
+    cp_async_wait<0>();
+  } else if (warp == 4) {
+    // ============================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(false, false, 128, 32);
+      for (int i = 0; i < nt; ++i) {
+        const int slot = i % kDSlots, sD = i & 1;
+        mbar_wait(&bars.a_full[slot], (i / kDSlots) & 1, err, 22);
+        if (i >= 2) mbar_wait(&bars.d_free[sD], ((i >> 1) - 1) & 1, err, 23);
+        tc_fence_after();
+        const uint32_t abase = sbase + kDAOff + slot * 32768, bbase = sbase + kDQOff;
+#pragma unroll
+        for (int k16 = 0; k16 < 8; ++k16) {
+          const uint32_t atom = k16 >> 2, off = (k16 & 3) * 32;
+          mma_f16_ss(tmem + 32 * sD, sw128_desc(abase + atom * 16384 + off, 16, 1024),
+                     sw128_desc(bbase + atom * 4096 + off, 16, 1024), idesc, k16 > 0);
+        }
+        mma_commit(&bars.a_free[slot]);
+        mma_commit(&bars.d_full[sD]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ============================================================ epilogue: thread = key lane
+    const int q4 = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
+    float* out = scores + (int64_t)bl * ld;
+    for (int i = 0; i < nt; ++i) {
+      const int sD = i & 1;
+      mbar_wait(&bars.d_full[sD], (i >> 1) & 1, err, 24);
+      tc_fence_after();
+      uint32_t u[32];
+      tmem_ld32(lane_addr + 32 * sD, u);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.d_free[sD]);
+      float s = 0.f;
+#pragma unroll
+      for (int h = 0; h < 32; ++h) s = fmaf(wsh[h], fmaxf(__uint_as_float(u[h]), 0.f), s);
+      const int64_t j = (int64_t)(t_begin + i) * 128 + r;
+      if (j < E) out[j] = s;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, float* scores,
+                                          int64_t ld, int num_sms, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(index_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynDec);
+  if (e != cudaSuccess) return e;
+  const int grid = nb >= num_sms ? nb : (num_sms / nb) * nb;
+  index_decode_tc_kernel<<<grid, kDThreads, kDynDec, st>>>(a, pos, b0, nb, scores, ld);
+  return cudaGetLastError();
+}
 
 size_t index_tc_image_bytes(int nb, int Tq, int64_t max_entries) {
   const size_t nqt = (size_t)(Tq + kQPerTile - 1) / kQPerTile;

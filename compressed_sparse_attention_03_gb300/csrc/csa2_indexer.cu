@@ -394,11 +394,16 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
       e = launch_index_scores_tc(a, pos, b0, nb, t0, tq, p.Tq, emax, reinterpret_cast<uint8_t*>(base + p.off_img), wq, sc,
                                  p.ld, num_sms, st);
       if (e != cudaSuccess) return e;
+    } else if (a.T == 1) {
+      if (emax > 0) {
+        e = launch_index_scores_decode_tc(a, pos, b0, nb, sc, p.ld, num_sms, st);
+        if (e != cudaSuccess) return e;
+      }
     } else {
       qprep_kernel<<<dim3(tq, nb), kQprepThreads, 0, st>>>(a, b0, t0, p.Tq, qdq, wq);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (!p.tc && emax > 0) {
+    if (!p.tc && a.T > 1 && emax > 0) {
       dim3 g((unsigned)((emax + kScoreThreads - 1) / kScoreThreads), (unsigned)((tq + kQT - 1) / kQT), (unsigned)nb);
       score_kernel<<<g, kScoreThreads, score_smem, st>>>(a, pos, b0, t0, p.Tq, qdq, wq, sc, p.ld);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;

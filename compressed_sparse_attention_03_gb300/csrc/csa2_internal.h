@@ -65,6 +65,8 @@ size_t index_tc_image_bytes(int nb, int Tq, int64_t max_entries);
 cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq, int Tq,
                                    int64_t emax, uint8_t* img, float* wq, float* scores, int64_t ld, int num_sms,
                                    cudaStream_t st);
+cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, float* scores,
+                                          int64_t ld, int num_sms, cudaStream_t st);
 size_t attend_workspace_bytes(int B, int T, int num_sms);
 cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf,
                           void* ws, size_t ws_bytes, int num_sms, cudaStream_t st);
