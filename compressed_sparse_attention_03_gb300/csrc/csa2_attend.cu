@@ -30,6 +30,8 @@
 // TMEM rarely (in practice only at the first chunk, where there is nothing to rescale).
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "csa2_common.cuh"
 #include "csa2_sm100.cuh"
 
@@ -547,12 +549,22 @@ int choose_splits(int nq, int num_sms) {
 
 }  // namespace
 
-size_t attend_workspace_bytes(int B, int T, int num_sms) {
-  const int nb = min(B, kMaxSeqPerLaunch);
+namespace {
+size_t attend_group_bytes(int nb, int T, int num_sms) {
   const int s = choose_splits(nb * T, num_sms);
   if (s == 1) return 0;
   const size_t rows = (size_t)nb * T * s;
   return rows * kH * kD * 4 + rows * kH * 2 * 4;
+}
+}  // namespace
+
+// Launches take groups of kMaxSeqPerLaunch sequences; a smaller tail group may split more, so the
+// need is the larger of the two group sizes.
+size_t attend_workspace_bytes(int B, int T, int num_sms) {
+  size_t need = attend_group_bytes(min(B, kMaxSeqPerLaunch), T, num_sms);
+  if (B > kMaxSeqPerLaunch && B % kMaxSeqPerLaunch)
+    need = std::max(need, attend_group_bytes(B % kMaxSeqPerLaunch, T, num_sms));
+  return need;
 }
 
 cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf, void* ws,

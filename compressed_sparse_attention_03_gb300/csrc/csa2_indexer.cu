@@ -8,6 +8,8 @@
 // is then a sum of exact products of E2M1 values times powers of two and is exact in fp32.
 // Scores are fp32.  Top-k: larger score first, equal scores -> lower j first, output
 // ascending in j, -1 padded.
+#include <algorithm>
+
 #include "csa2_common.cuh"
 
 namespace csa2 {
@@ -361,8 +363,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(IndexArgs a, i
 
 }  // namespace
 
+// Launches take groups of kMaxSeqPerLaunch sequences; a smaller tail group may take more queries
+// per pass, so the need is the larger of the two group plans.
 size_t index_workspace_bytes(int B, int T, int64_t max_entries, int /*num_sms*/) {
-  return make_plan(min(B, kMaxSeqPerLaunch), T, max_entries).total;
+  size_t need = make_plan(min(B, kMaxSeqPerLaunch), T, max_entries).total;
+  if (B > kMaxSeqPerLaunch && B % kMaxSeqPerLaunch)
+    need = std::max(need, make_plan(B % kMaxSeqPerLaunch, T, max_entries).total);
+  return need;
 }
 
 cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int64_t max_entries, void* ws,

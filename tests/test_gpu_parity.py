@@ -183,6 +183,19 @@ def test_index_chunk_32k_sampled(handle):
     print(f"index chunk_32k ({len(rows)} rows): near-tie swaps = {swaps}")
 
 
+def test_tail_group_workspace(handle):
+    # 130 sequences run as a group of 128 and a tail of 2; the tail takes more queries per pass
+    # (indexer) and more splits (attention), so the workspace must cover it too
+    B, T = 130, 1
+    p0s = np.random.default_rng(2).integers(0, 900, B)
+    x, cap = make_state(B, T, p0s, seed=21)
+    use_oracle_state(x, oracle_write(x, p0s, cap))
+    idx, top = run_index(handle, x, p0s, T)
+    check_index(idx, top, x, p0s)
+    out = run_attend(handle, x, idx, p0s)
+    print(f"tail group: max abs / rel L2 = {check_attend(out, x, idx, p0s)}")
+
+
 # ------------------------------------------------------------------------ attention
 def stratified_indices(B, T, p0s, seed):
     """Sorted distinct visible entries per query: one draw per stratum of width E/512."""
