@@ -20,7 +20,8 @@ OP_WRITE_CACHE, OP_INDEX_TOPK, OP_ATTEND = 0, 1, 2
 HEADS, HEAD_DIM, ROPE_DIMS, IDX_HEADS, IDX_DIM, WINDOW, TOPK = 64, 512, 64, 32, 128, 128, 512
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "inconsistent sizes", 3: "pointer not 16-byte aligned",
-           4: "workspace too small", 5: "unsupported configuration", 6: "CUDA error"}
+           4: "workspace too small", 5: "unsupported configuration", 6: "CUDA error",
+           7: "batch exceeds the fixed scratch of csa2_attend_static"}
 
 
 class Csa2Error(RuntimeError):
@@ -36,7 +37,7 @@ class csa2_config(C.Structure):
 
 
 EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_string", "csa2_workspace_bytes",
-           "csa2_write_cache", "csa2_index_topk", "csa2_attend")
+           "csa2_write_cache", "csa2_index_topk", "csa2_attend", "csa2_attend_static")
 
 _lib = None
 
@@ -64,6 +65,8 @@ def lib() -> C.CDLL:
         L.csa2_index_topk.restype = i32
         L.csa2_attend.argtypes = [p] * 5 + [i64, p, p, p, i32, i32, p, p, sz, p]
         L.csa2_attend.restype = i32
+        L.csa2_attend_static.argtypes = [p] * 5 + [i64, p, p, p, i32, i32, p, p]
+        L.csa2_attend_static.restype = i32
         _lib = L
     return _lib
 
@@ -180,3 +183,17 @@ def csa2_attend(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, out, ws
         _dev(z_scales, torch.uint8, "z_scales"), cap, _dev(window, torch.uint8, "window"),
         _dev(idx, torch.int32, "idx"), p0a.ctypes.data_as(C.c_void_p), B, T, _dev(out, torch.bfloat16, "out"),
         _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+
+
+def csa2_attend_static(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, out, stream=None) -> None:
+    """csa2_attend without a workspace: the library's fixed device scratch holds the split
+    partials, and no call here allocates device memory (the tensors are the caller's).  Calls
+    that can overlap in time share that scratch and race; see include/csa2.h."""
+    B, T = q.shape[:2]
+    p0a = _host_p0(p0, B)
+    cap = z_codes.shape[1]
+    _check("csa2_attend_static", lib().csa2_attend_static(
+        h.ptr, _dev(q, torch.bfloat16, "q"), _dev(sinks, torch.float32, "sinks"), _dev(z_codes, torch.uint8, "z_codes"),
+        _dev(z_scales, torch.uint8, "z_scales"), cap, _dev(window, torch.uint8, "window"),
+        _dev(idx, torch.int32, "idx"), p0a.ctypes.data_as(C.c_void_p), B, T, _dev(out, torch.bfloat16, "out"),
+        _stream(stream)))

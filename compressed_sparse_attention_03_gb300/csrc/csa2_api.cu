@@ -98,6 +98,7 @@ const char* csa2_status_string(csa2_status s) {
     case CSA2_ERR_WORKSPACE: return "workspace too small";
     case CSA2_ERR_UNSUPPORTED: return "unsupported configuration";
     case CSA2_ERR_CUDA: return "CUDA error";
+    case CSA2_ERR_TOO_LARGE: return "batch exceeds the fixed scratch of csa2_attend_static";
   }
   return "unknown status";
 }
@@ -196,6 +197,40 @@ csa2_status csa2_attend(csa2_handle* h, const uint16_t* q, const float* sinks, c
   for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
     const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
     st = cuda_status(csa2::launch_attend(a, pack_pos(p0, b0, nb), b0, nb, h->rf, ws, ws_bytes, h->num_sms,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+    if (st != CSA2_OK) return st;
+  }
+  return CSA2_OK;
+}
+
+// Allocation-free variant of csa2_attend (see include/csa2.h): identical validation and
+// launches, with the split partials in the library's fixed device array.
+csa2_status csa2_attend_static(csa2_handle* h, const uint16_t* q, const float* sinks, const uint8_t* z_codes,
+                               const uint8_t* z_scales, int64_t cap, const uint8_t* window, const int32_t* idx,
+                               const int64_t* p0, int B, int T, uint16_t* out, csa2_stream_t stream) {
+  if (!h || !q || !sinks || !z_codes || !z_scales || !window || !idx || !out) return CSA2_ERR_INVALID_ARG;
+  if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  csa2_status st = check_p0(p0, B, T);
+  if (st != CSA2_OK) return st;
+  const void* ptrs[] = {q, sinks, z_codes, z_scales, window, idx, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CSA2_ERR_ALIGN;
+  const size_t need = csa2::attend_workspace_bytes(B, T, h->num_sms);
+  if (need > csa2::attend_static_scratch_bytes()) return CSA2_ERR_TOO_LARGE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (dev != h->device) return CSA2_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  if (need) {  // a batch that is not split needs no scratch and never touches the array
+    if (csa2::attend_static_scratch(dev, &ws) != cudaSuccess) return CSA2_ERR_CUDA;
+  }
+  csa2::AttendArgs a{};
+  a.q = q; a.sinks = sinks; a.z_codes = z_codes; a.z_scales = z_scales; a.window = window; a.idx = idx;
+  a.cap = cap; a.T = T; a.out = out;
+  // Launches of successive groups of sequences reuse the array; they are ordered on `stream`.
+  for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
+    const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
+    st = cuda_status(csa2::launch_attend(a, pack_pos(p0, b0, nb), b0, nb, h->rf, ws, need, h->num_sms,
                                          reinterpret_cast<cudaStream_t>(stream)));
     if (st != CSA2_OK) return st;
   }

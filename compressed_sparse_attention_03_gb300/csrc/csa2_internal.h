@@ -71,4 +71,10 @@ size_t attend_workspace_bytes(int B, int T, int num_sms);
 cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf,
                           void* ws, size_t ws_bytes, int num_sms, cudaStream_t st);
 
+// Fixed device scratch of csa2_attend_static: room for this many split-partial rows (one row =
+// 64 heads x 514 fp32), the most a launch needs on a device with at most 152 SMs.
+constexpr size_t kStaticAttendRows = 152;
+size_t attend_static_scratch_bytes();
+cudaError_t attend_static_scratch(int device, void** out);
+
 }  // namespace csa2

@@ -15,7 +15,8 @@
  *  - Tensor arguments are DEVICE pointers, owned by the caller, row-major and densely
  *    packed in the shapes given, 16-byte aligned.  bf16 tensors are passed as uint16_t
  *    bit patterns.  The library allocates no device memory; scratch comes from the caller's
- *    workspace (size from csa2_workspace_bytes).
+ *    workspace (size from csa2_workspace_bytes), except for csa2_attend_static, whose
+ *    scratch is a fixed array of the library (see there).
  *  - p0 is a HOST array of B int64 values: the absolute position of the first of the T new
  *    tokens of each sequence (its cached length before the call).
  *  - Every call is asynchronous on `stream` and never synchronises.  Argument errors are
@@ -52,7 +53,8 @@ typedef enum {
   CSA2_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
   CSA2_ERR_WORKSPACE = 4,   /* workspace smaller than csa2_workspace_bytes() */
   CSA2_ERR_UNSUPPORTED = 5, /* configuration outside what the kernels implement */
-  CSA2_ERR_CUDA = 6         /* a CUDA launch or device query failed */
+  CSA2_ERR_CUDA = 6,        /* a CUDA launch or device query failed */
+  CSA2_ERR_TOO_LARGE = 7    /* batch needs more than csa2_attend_static's fixed scratch */
 } csa2_status;
 
 /* Layer configuration.  The integer fields must equal the defaults shown. */
@@ -143,6 +145,30 @@ csa2_status csa2_attend(csa2_handle* h, const uint16_t* q, const float* sinks,
                         const uint8_t* z_codes, const uint8_t* z_scales, int64_t cap,
                         const uint8_t* window, const int32_t* idx, const int64_t* p0, int B,
                         int T, uint16_t* out, void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* csa2_attend with no workspace argument.  Not an operation of the pages (they have no
+ * counterpart): an interface for callers that cannot allocate device memory at call time,
+ * e.g. a serving process that hands all free HBM to its KV-cache pool at start-up, or code
+ * that must not call cudaMalloc/cudaFree because those can synchronise the device and stall
+ * the work of other streams.
+ * Same arguments, results and launches as csa2_attend (bit-identical output), but the split
+ * partials live in one fixed device array of the library: 152 rows x 64 heads x 514 fp32 =
+ * 20,000,768 bytes, enough for every batch on a device with at most 152 SMs.  A batch whose
+ * split partials need more (only possible on a larger device) is rejected with
+ * CSA2_ERR_TOO_LARGE before anything is launched.  Nothing in the array has to start at
+ * zero: every split writes all of its partial row, also when it received no rows.
+ *  - Set-up: the first call on a device resolves the array's address there with
+ *    cudaGetSymbolAddress (which may load the library's module and so allocate the array);
+ *    later calls reuse the cached address and make no allocating call at all.  Make the
+ *    first call on each device before any stream capture.  The handle's device must be the
+ *    current device (else CSA2_ERR_INVALID_ARG).
+ *  - The array is shared: calls that may overlap in time (different streams, or different
+ *    threads without ordering) race on it and corrupt each other's output.  Calls queued on
+ *    one stream are ordered and safe. */
+csa2_status csa2_attend_static(csa2_handle* h, const uint16_t* q, const float* sinks,
+                               const uint8_t* z_codes, const uint8_t* z_scales, int64_t cap,
+                               const uint8_t* window, const int32_t* idx, const int64_t* p0,
+                               int B, int T, uint16_t* out, csa2_stream_t stream);
 
 #ifdef __cplusplus
 }

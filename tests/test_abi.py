@@ -39,6 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_config_checks(lib):
     assert lib.csa2_status_string(0) == b"ok"
     assert lib.csa2_status_string(4) == b"workspace too small"
+    assert lib.csa2_status_string(7) == b"batch exceeds the fixed scratch of csa2_attend_static"
     cfg = csa2.csa2_config()
     lib.csa2_default_config(C.byref(cfg))
     assert (cfg.heads, cfg.head_dim, cfg.rope_dims, cfg.idx_heads, cfg.idx_dim, cfg.window, cfg.topk, cfg.ratio) == \
@@ -54,3 +55,4 @@ def test_status_strings_and_config_checks(lib):
     # no handle: every entry point refuses before touching the GPU
     assert lib.csa2_workspace_bytes(None, 1, 1, 1, 10) == 0
     assert lib.csa2_index_topk(*([None] * 5), 0, None, 1, 1, None, None, None, 0, None) == 1
+    assert lib.csa2_attend_static(*([None] * 5), 0, None, None, None, 1, 1, None, None) == 1
