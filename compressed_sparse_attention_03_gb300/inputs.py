@@ -73,13 +73,17 @@ def _bytes(shape, g, device):
     return torch.randint(0, 256, shape, generator=g, device=device, dtype=torch.int32)
 
 
+def _e2m1_nibbles(shape, g, device):
+    """Random E2M1 codes: a magnitude code from the full 256-entry table, then a sign bit."""
+    mag = _E2M1_MAG.to(device)[_bytes(shape, g, device)]
+    sign = ((_bytes(shape, g, device) & 1) << 3).to(torch.uint8)
+    return mag | sign
+
+
 def random_fp4(rows_shape, n: int, g, device):
     """Random FP4 rows: (codes [..., n/2] u8, scales [..., n/32] u8)."""
-    u0 = _bytes((*rows_shape, n // 2), g, device)
-    u1 = _bytes((*rows_shape, n // 2), g, device)
-    mag = _E2M1_MAG.to(device)
-    lo = mag[u0 & 127] | ((u0 >> 7) << 3).to(torch.uint8)
-    hi = mag[u1 & 127] | ((u1 >> 7) << 3).to(torch.uint8)
+    lo = _e2m1_nibbles((*rows_shape, n // 2), g, device)
+    hi = _e2m1_nibbles((*rows_shape, n // 2), g, device)
     codes = (lo | (hi << 4)).to(torch.uint8)
     scales = _SCALE.to(device)[_bytes((*rows_shape, n // 32), g, device)]
     return codes, scales
