@@ -36,7 +36,8 @@ class csa2_config(C.Structure):
                 ("rope_base", C.c_double), ("eps", C.c_double)]
 
 
-EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_string", "csa2_workspace_bytes",
+EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_string", "csa2_kernel_launches",
+           "csa2_workspace_bytes",
            "csa2_write_cache", "csa2_index_topk", "csa2_attend", "csa2_attend_static")
 
 _lib = None
@@ -57,6 +58,8 @@ def lib() -> C.CDLL:
         L.csa2_destroy.argtypes = [p]
         L.csa2_status_string.argtypes = [i32]
         L.csa2_status_string.restype = C.c_char_p
+        L.csa2_kernel_launches.argtypes = []
+        L.csa2_kernel_launches.restype = C.c_uint64
         L.csa2_workspace_bytes.argtypes = [p, i32, i32, i32, i64]
         L.csa2_workspace_bytes.restype = sz
         L.csa2_write_cache.argtypes = [p] * 9 + [i32, i32] + [p] * 6 + [i64, p, p, sz, p]
@@ -131,6 +134,11 @@ class Handle:
 
 def csa2_create(rope_base: float = 10000.0, eps: float = 1e-20) -> Handle:
     return Handle(rope_base, eps)
+
+
+def csa2_kernel_launches() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib().csa2_kernel_launches())
 
 
 def csa2_workspace_bytes(h: Handle, op: int, B: int, T: int, max_entries: int) -> int:

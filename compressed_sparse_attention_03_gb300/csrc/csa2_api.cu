@@ -1,6 +1,7 @@
 // C-ABI front end of libcsa2.so: argument validation, the handle, workspace sizing, and the
 // split of large batches into launches of at most kMaxSeqPerLaunch sequences.
 // The entry points and their contracts are documented in include/csa2.h.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -15,6 +16,14 @@ struct csa2_handle {
   int device;
   int num_sms;
 };
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+}  // namespace
+
+void csa2::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 
@@ -88,6 +97,8 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_handle** out) {
 }
 
 void csa2_destroy(csa2_handle* h) { delete h; }
+
+uint64_t csa2_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* csa2_status_string(csa2_status s) {
   switch (s) {

@@ -582,9 +582,11 @@ cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, int b0, int nb
   }
   attend_tc_kernel<<<dim3((unsigned)a.T, (unsigned)nb, (unsigned)s), kThreads, kDynBytes, st>>>(a, pos, b0, rf, s, cps,
                                                                                                  po, pml);
+  note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (s > 1) {
     attend_combine_kernel<<<dim3((unsigned)a.T, (unsigned)nb, kH), 128, 0, st>>>(a, pos, b0, rf, s, po, pml);
+    note_launch();
     e = cudaGetLastError();
   }
   return e;

@@ -472,6 +472,7 @@ cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos,
   if (e != cudaSuccess) return e;
   const int grid = nb >= num_sms ? nb : (num_sms / nb) * nb;
   index_decode_tc_kernel<<<grid, kDThreads, kDynDec, st>>>(a, pos, b0, nb, scores, ld);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -489,10 +490,12 @@ cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0
   uint8_t* qimg = img;
   uint8_t* kimg = img + (size_t)nb * nqt * kQImg;
   qimage_kernel<<<dim3((unsigned)tq, (unsigned)nb), 128, 0, st>>>(a, b0, t0, Tq, nqt, qimg, wq);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (nkt > 0) {
     kimage_kernel<<<dim3((unsigned)nkt, (unsigned)nb), 128, 0, st>>>(a, b0, emax, nkt, kimg);
+    note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   e = cudaFuncSetAttribute(index_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynTC);
@@ -500,6 +503,7 @@ cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0
   const int ntiles = nb * ((tq + kQPerTile - 1) / kQPerTile);
   const int grid = max(1, min(num_sms, ntiles));
   index_prefill_tc_kernel<<<grid, kThreadsTC, kDynTC, st>>>(a, pos, t0, tq, nqt, nkt, qimg, kimg, wq, scores, ld, nb, Tq);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -408,19 +408,23 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
       }
     } else {
       qprep_kernel<<<dim3(tq, nb), kQprepThreads, 0, st>>>(a, b0, t0, p.Tq, qdq, wq);
+      note_launch();
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (!p.tc && a.T > 1 && emax > 0) {
       dim3 g((unsigned)((emax + kScoreThreads - 1) / kScoreThreads), (unsigned)((tq + kQT - 1) / kQT), (unsigned)nb);
       score_kernel<<<g, kScoreThreads, score_smem, st>>>(a, pos, b0, t0, p.Tq, qdq, wq, sc, p.ld);
+      note_launch();
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const int nch = (int)max64(1, (emax + p.chunk - 1) / p.chunk);
     topk_chunk_kernel<<<dim3(nch, tq, nb), kTopkThreads, chunk_smem, st>>>(a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch,
                                                                             ck, cj, cn);
+    note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (nch > 1) {
       topk_merge_kernel<<<dim3(tq, nb), kTopkThreads, (size_t)nch * kTopK * 8, st>>>(a, b0, t0, p.Tq, nch, ck, cj, cn);
+      note_launch();
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }

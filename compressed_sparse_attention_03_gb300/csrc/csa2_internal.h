@@ -67,6 +67,9 @@ cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0
                                    cudaStream_t st);
 cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, float* scores,
                                           int64_t ld, int num_sms, cudaStream_t st);
+// Counts one kernel enqueued by this library (read back by csa2_kernel_launches).
+void note_launch();
+
 size_t attend_workspace_bytes(int B, int T, int num_sms);
 cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf,
                           void* ws, size_t ws_bytes, int num_sms, cudaStream_t st);

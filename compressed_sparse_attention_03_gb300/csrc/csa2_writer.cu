@@ -214,10 +214,12 @@ cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb
   if (max_new > 0) {
     dim3 grid((unsigned)((max_new + kEntriesPerBlock - 1) / kEntriesPerBlock), (unsigned)nb);
     writer_entries_kernel<<<grid, kWriterThreads, 0, st>>>(a, pos, b0, rf);
+    note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   writer_window_kernel<<<dim3((unsigned)a.T, (unsigned)nb), kWriterThreads, 0, st>>>(a, pos, b0, rf);
+  note_launch();
   return cudaGetLastError();
 }
 

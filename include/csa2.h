@@ -82,6 +82,10 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_handle** out);
 void csa2_destroy(csa2_handle* h);
 const char* csa2_status_string(csa2_status s);
 
+/* Number of kernels this library has enqueued in this process so far (every handle and
+ * device; a launch that failed is counted too).  Host-side counter; never synchronises. */
+uint64_t csa2_kernel_launches(void);
+
 enum { CSA2_OP_WRITE_CACHE = 0, CSA2_OP_INDEX_TOPK = 1, CSA2_OP_ATTEND = 2 };
 
 /* Bytes of workspace the call `op` needs for B sequences of T new tokens whose largest

@@ -52,7 +52,9 @@ def test_status_strings_and_config_checks(lib):
     cfg.rope_base = 0.5
     assert lib.csa2_create(C.byref(cfg), C.byref(h)) == 1
     assert lib.csa2_create(None, C.byref(h)) == 1
-    # no handle: every entry point refuses before touching the GPU
+    # no handle: every entry point refuses before touching the GPU (and launches nothing)
+    launches = lib.csa2_kernel_launches()
     assert lib.csa2_workspace_bytes(None, 1, 1, 1, 10) == 0
     assert lib.csa2_index_topk(*([None] * 5), 0, None, 1, 1, None, None, None, 0, None) == 1
     assert lib.csa2_attend_static(*([None] * 5), 0, None, None, None, 1, 1, None, None) == 1
+    assert lib.csa2_kernel_launches() == launches
