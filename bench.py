@@ -100,28 +100,6 @@ def decode_bytes(B: int, p0: int) -> dict:
     return dict(indexer=idx_keys, step=idx_keys + rows + small)
 
 
-def launches_per_step(B: int, T: int, p0: int, num_sms: int) -> int:
-    """Kernels the three calls enqueue (mirrors the library's launch plan)."""
-    n = 0
-    new_entries = (p0 + T) // 2 - p0 // 2
-    n += (1 if new_entries > 0 else 0) + 1                    # writer: entries + window
-    emax = (p0 + T) // 2
-    ld = ((max(emax, 1) + 31) // 32) * 32
-    tq = max(1, min(T, (1 << 30) // (min(B, 128) * ld * 4)))
-    chunk = 4096
-    while chunk * 32 < ld and chunk < 32768:
-        chunk *= 2
-    for t0 in range(0, T, tq):
-        e = (p0 + t0 + min(tq, T - t0)) // 2
-        n += 1 + (1 if e > 0 else 0) + 1                      # qprep, score, top-k stage 1
-        if max(1, -(-e // chunk)) > 1:
-            n += 1                                            # top-k merge
-    nq = min(B, 128) * T
-    splits = 1 if nq >= num_sms else max(1, min(-(-2 * num_sms // nq), 20))
-    n += 1 + (1 if splits > 1 else 0)                         # attention (+ combine)
-    return n * (-(-B // 128))
-
-
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi sampled every 50 ms from before the timed region; summary() keeps the samples
@@ -236,6 +214,7 @@ def time_workload(step: Step, steps: int, warmup: int, ws: int, flush: torch.Ten
     barrier(ws)
     torch.cuda.synchronize()
     ctx = clocks if clocks is not None else _Null()
+    launches0 = step.csa2.csa2_kernel_launches()
     with ctx:
         if clocks is not None:
             clocks.mark_start()
@@ -252,10 +231,11 @@ def time_workload(step: Step, steps: int, warmup: int, ws: int, flush: torch.Ten
         torch.cuda.synchronize()
         if clocks is not None:
             clocks.mark_end()
+    launches = step.csa2.csa2_kernel_launches() - launches0  # the library's own kernels, timed steps only
     barrier(ws)
     per = {n: [ev[i][k].elapsed_time(ev[i][k + 1]) for i in range(steps)] for k, n in enumerate(names)}
     total = [sum(per[n][i] for n in names) for i in range(steps)]
-    return statistics.mean(total), {n: statistics.mean(v) for n, v in per.items()}
+    return statistics.mean(total), {n: statistics.mean(v) for n, v in per.items()}, launches
 
 
 class _Null:
@@ -310,13 +290,12 @@ def run_ours(args, rank, ws):
     from compressed_sparse_attention_03_gb300 import inputs
 
     dev = "cuda"
-    num_sms = torch.cuda.get_device_properties(0).multi_processor_count
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     hbm, bf16, src = peaks()
     wl = inputs.WORKLOADS[args.workload]
     step = Step(csa2, inputs, wl, seed_for_rank(wl.seed, rank), dev)
     clocks = ClockSampler(torch.cuda.current_device())
-    ms, per = time_workload(step, args.steps, args.warmup, ws, flush, clocks)
+    ms, per, launches = time_workload(step, args.steps, args.warmup, ws, flush, clocks)
     ms_max = max_over_ranks(ms, ws)
     att_ms = max_over_ranks(per["attend"], ws)
     flops = attention_flops(wl.B, wl.p0, wl.T)
@@ -334,7 +313,7 @@ def run_ours(args, rank, ws):
                      "unit": "TFLOP/s", "frac": achieved / bf16, "peak_source": f"{src} bf16 burst",
                      "flops_per_launch": flops, "traffic": None},
         "e2e": e2e,
-        "gpu_launches": launches_per_step(wl.B, wl.T, wl.p0, num_sms) * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks.summary(),
     }
     del step
@@ -342,7 +321,7 @@ def run_ours(args, rank, ws):
     if not args.no_decode:
         dw = inputs.WORKLOADS[args.decode_workload]
         dstep = Step(csa2, inputs, dw, seed_for_rank(dw.seed, rank), dev)
-        dms, dper = time_workload(dstep, args.steps, args.warmup, ws, flush)
+        dms, dper, dlaunches = time_workload(dstep, args.steps, args.warmup, ws, flush)
         dms = max_over_ranks(dms, ws)
         idx_ms = max_over_ranks(dper["index"], ws)
         by = decode_bytes(dw.B, dw.p0)
@@ -354,7 +333,7 @@ def run_ours(args, rank, ws):
             "roofline_index": {"bound": "hbm", "achieved": by["indexer"] / (idx_ms / 1e3) / 1e9, "peak": hbm,
                                "unit": "GB/s", "frac": by["indexer"] / (idx_ms / 1e3) / 1e9 / hbm,
                                "bytes": by["indexer"], "peak_source": f"{src} copy bandwidth"},
-            "gpu_launches": launches_per_step(dw.B, 1, dw.p0, num_sms) * args.steps,
+            "gpu_launches": dlaunches,
         }
         del dstep
     if rank == 0 and not args.no_cpu_baseline:
@@ -441,11 +420,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
-    rank, ws = dist_setup()
     if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only; the other ranks exit without work
+        rank, ws = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
         if rank == 0:
             print(json.dumps(run_reference(args, rank, ws)), flush=True)
         return
+    rank, ws = dist_setup()
     line = run_ours(args, rank, ws)
     if rank == 0:
         print(json.dumps(line), flush=True)
