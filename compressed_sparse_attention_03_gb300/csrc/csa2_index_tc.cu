@@ -279,20 +279,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
 // ------------------------------------------------------------------ decode (one query)
 // Scores of one query per sequence against all its visible keys: M = 128 keys, N = 32 heads,
 // K = 128 per tile.  The FP4 keys are decoded inside the kernel (a fp16 image of all keys
-// would cost 4x the key bytes in extra HBM traffic): 128 producer threads (one key each)
-// stage the raw 68-byte keys with cp.async kDStg tiles ahead, decode them exactly to fp16
-// into a kDSlots-deep ring of 32 KB operand tiles, and one thread issues the MMAs into
-// double-buffered TMEM accumulators read by 128 epilogue threads.  Each sequence's key tiles
-// are split evenly over gridDim.x / nb persistent blocks.
-constexpr int kDSlots = 4, kDStg = 4, kDThreads = 288;  // warps 0-3 producers, 4 MMA, 5-8 epilogue
+// would cost 4x the key bytes in extra HBM traffic).
+//  - warp 0 (loader): per tile one bulk copy of the 128 x 64 code bytes and, lane by lane,
+//    4-byte cp.async copies of the scale words (their rows are only 4-byte aligned), all
+//    completing on the stage's mbarrier; kDStg stages in flight.
+//  - warps 1-8 (decoders, two per SM sub-partition so that one hides the other's latency): a
+//    warp reads 8 consecutive 64-byte code rows per load (conflict free), lane = (row, 32-value
+//    block); decodes exactly to fp16 into a kDSlots-deep ring of 32 KB swizzled operand tiles.
+//  - warp 9 (one thread): the MMAs, into double-buffered TMEM accumulators.
+//  - warps 10-13 (epilogue): ReLU, the w^I weighting and the fp32 score stores.
+// Each sequence's key tiles are split evenly over gridDim.x / nb persistent blocks.
+constexpr int kDSlots = 4, kDStg = 8, kDDec = 8, kDThreads = 32 * (2 + kDDec + 4);
 constexpr uint32_t kDAOff = 0;                     // operand tiles: kDSlots x 32 KB
 constexpr uint32_t kDRawOff = 131072;              // raw codes: kDStg x [128 keys x 64 B]
-constexpr uint32_t kDScOff = 163840;               // raw scales: kDStg x [128 keys x 4 B]
-constexpr uint32_t kDQOff = 165888;                // Q^I image: 2 atoms x [32 heads x 128 B]
-constexpr uint32_t kDynDec = 174080 + 1024;
+constexpr uint32_t kDScOff = kDRawOff + kDStg * 8192;  // raw scales: kDStg x [128 keys x 4 B]
+constexpr uint32_t kDQOff = kDScOff + kDStg * 512;     // Q^I image: 2 atoms x [32 heads x 128 B]
+constexpr uint32_t kDynDec = kDQOff + 8192 + 1024;
+static_assert(kDQOff % 1024 == 0, "swizzled Q^I atoms need 1024-byte alignment");
 
 struct DecBars {
-  uint64_t a_full[kDSlots], a_free[kDSlots], d_full[2], d_free[2];
+  uint64_t raw_full[kDStg], raw_free[kDStg], a_full[kDSlots], a_free[kDSlots], d_full[2], d_free[2];
 };
 
 __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs a, SeqPos pos, int b0, int nb,
@@ -317,8 +323,12 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   const int nt = active ? t_end - t_begin : 0;
 
   if (tid == 0) {
+    for (int i = 0; i < kDStg; ++i) {
+      mbar_init(&bars.raw_full[i], 1 + 32);  // the loader's expect_tx + one cp.async arrival per lane
+      mbar_init(&bars.raw_free[i], kDDec);
+    }
     for (int i = 0; i < kDSlots; ++i) {
-      mbar_init(&bars.a_full[i], 4);
+      mbar_init(&bars.a_full[i], kDDec);
       mbar_init(&bars.a_free[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -327,14 +337,14 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
     }
     mbar_fence_init();
   }
-  if (warp == 4) {
+  if (warp == kDDec + 1) {
     tmem_alloc(&tmem_base_sh, 64);
     tmem_relinquish();
   }
-  // Q^I -> FP4 -> fp16 image (warps 0-3: warp w heads 8w..8w+7, lane l values 4l..4l+3), w^I
-  if (warp < 4 && active) {
+  // Q^I -> FP4 -> fp16 image (warps 1-4: warp w heads 8(w-1)..+7, lane l values 4l..4l+3), w^I
+  if (warp >= 1 && warp <= 4 && active) {
     const int64_t src = (int64_t)b * a.T;  // T == 1
-    for (int h = 8 * warp; h < 8 * warp + 8; ++h) {
+    for (int h = 8 * (warp - 1); h < 8 * warp; ++h) {
       const uint2 raw = *reinterpret_cast<const uint2*>(a.qi + (src * kHI + h) * kDI + 4 * lane);
       float v[4] = {bf16_to_f32(raw.x & 0xffff), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xffff), bf16_to_f32(raw.y >> 16)};
       float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
@@ -349,7 +359,7 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
       *reinterpret_cast<uint2*>(sm + kDQOff + (d >> 6) * 4096 + sw128_off(h, (d & 63) >> 3) + (d & 7) * 2) =
           make_uint2(f2_to_h2(q[0], q[1]), f2_to_h2(q[2], q[3]));
     }
-    if (tid < kHI) wsh[tid] = bf16_to_f32(a.wI[src * kHI + tid]);
+    if (warp == 1) wsh[lane] = bf16_to_f32(a.wI[src * kHI + lane]);
     fence_proxy_async();
   }
   tc_fence_before();
@@ -357,62 +367,75 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp < 4) {
-    // ============================================================ producers: thread = key row
-    const int r = tid;
-    auto issue = [&](int i) {
-      if (i < nt) {
-        const int64_t j = (int64_t)(t_begin + i) * 128 + r;
-        if (j < E) {
-          const int st = i % kDStg;
-          const uint8_t* src = a.ki_codes + ((int64_t)b * a.cap + j) * 64;
-          unsigned char* dst = sm + kDRawOff + st * 8192 + r * 64;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) cp_async16(dst + 16 * k, src + 16 * k);
-          cp_async4(sm + kDScOff + st * 512 + r * 4, a.ki_scales + ((int64_t)b * a.cap + j) * 4);
-        }
-      }
-      cp_async_commit();
-    };
-    for (int i = 0; i < kDStg; ++i) issue(i);
+  if (warp == 0) {
+    // ============================================================ loader
+    const uint8_t* codes = a.ki_codes + (int64_t)b * a.cap * 64;
+    const uint8_t* scl = a.ki_scales + (int64_t)b * a.cap * 4;
 #pragma unroll 1
     for (int i = 0; i < nt; ++i) {
-      cp_async_wait<kDStg - 1>();
-      const int st = i % kDStg, slot = i % kDSlots;
-      const int64_t j = (int64_t)(t_begin + i) * 128 + r;
-      uint4 c[4];
-      uint32_t sc = 0;
-      if (j < E) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) c[k] = *reinterpret_cast<const uint4*>(sm + kDRawOff + st * 8192 + r * 64 + 16 * k);
-        sc = *reinterpret_cast<const uint32_t*>(sm + kDScOff + st * 512 + r * 4);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) c[k] = make_uint4(0u, 0u, 0u, 0u);
+      const int st = i % kDStg;
+      if (i >= kDStg) mbar_wait(&bars.raw_free[st], ((i / kDStg) - 1) & 1, err, 31);
+      const int64_t j0 = (int64_t)(t_begin + i) * 128;
+      const int n = (int)min64(128, E - j0);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars.raw_full[st], (uint32_t)n * 64u);
+        bulk_g2s(sm + kDRawOff + st * 8192, codes + j0 * 64, (uint32_t)n * 64u, &bars.raw_full[st]);
       }
-      if (i >= kDSlots) mbar_wait(&bars.a_free[slot], ((i / kDSlots) - 1) & 1, err, 21);
-      unsigned char* tile = sm + kDAOff + slot * 32768;
 #pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {  // 32 values: 16 code bytes, one scale byte
-        const float sf = ldexpf(1.0f, (int)((sc >> (8 * blk)) & 255u) - 127);
+      for (int k = 4 * lane; k < 4 * lane + 4; ++k)
+        if (k < n) cp_async4(sm + kDScOff + st * 512 + 4 * k, scl + (j0 + k) * 4);
+      cp_async_mbar_arrive_noinc(&bars.raw_full[st]);
+    }
+    // leave no copy in flight, also after a wait that gave up
+    for (int i = max(0, nt - kDStg); i < nt; ++i) mbar_wait(&bars.raw_full[i % kDStg], (i / kDStg) & 1, err, 32);
+    cp_async_commit();
+    cp_async_wait<0>();
+  } else if (warp <= kDDec) {
+    // ============================================================ decoders
+    const int dw = warp - 1;
+    const int blk = lane & 3;  // 32-value block of the row: 16 code bytes, one scale byte
+#pragma unroll 1
+    for (int i = 0; i < nt; ++i) {
+      const int st = i % kDStg, slot = i % kDSlots;
+      const int n = (int)min64(128, E - (int64_t)(t_begin + i) * 128);
+      mbar_wait(&bars.raw_full[st], (i / kDStg) & 1, err, 33);
+      constexpr int kIt = 128 / (8 * kDDec);  // 8-row groups per decoder warp
+      uint4 c[kIt];
+      uint32_t sc[kIt];
+#pragma unroll
+      for (int it = 0; it < kIt; ++it) {
+        const int key = 8 * (kIt * dw + it) + (lane >> 2);
+        if (key < n) {
+          c[it] = *reinterpret_cast<const uint4*>(sm + kDRawOff + st * 8192 + key * 64 + blk * 16);
+          sc[it] = sm[kDScOff + st * 512 + key * 4 + blk];
+        } else {
+          c[it] = make_uint4(0u, 0u, 0u, 0u);  // rows past the last key: zero operands
+          sc[it] = 127u;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.raw_free[st]);
+      if (i >= kDSlots) mbar_wait(&bars.a_free[slot], ((i / kDSlots) - 1) & 1, err, 34);
+      unsigned char* tile = sm + kDAOff + slot * 32768 + (blk >> 1) * 16384;
+#pragma unroll
+      for (int it = 0; it < kIt; ++it) {
+        const int key = 8 * (kIt * dw + it) + (lane >> 2);
+        const float sf = ldexpf(1.0f, (int)sc[it] - 127);
         const uint32_t s2 = f2_to_h2(sf, sf);
-        const uint32_t wd[4] = {c[blk].x, c[blk].y, c[blk].z, c[blk].w};
+        const uint32_t wd[4] = {c[it].x, c[it].y, c[it].z, c[it].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {  // 8 values = one 16-byte chunk of fp16
           uint32_t o[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) o[k] = hmul2(cvt_e2m1x2_f16x2((wd[q] >> (8 * k)) & 255u), s2);
-          const int d = 32 * blk + 8 * q;
-          *reinterpret_cast<uint4*>(tile + (d >> 6) * 16384 + sw128_off(r, (d & 63) >> 3)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(tile + sw128_off(key, 4 * (blk & 1) + q)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.a_full[slot]);
-      issue(i + kDStg);
     }
-    cp_async_wait<0>();
-  } else if (warp == 4) {
+  } else if (warp == kDDec + 1) {
     // ============================================================ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(false, false, 128, 32);
@@ -458,7 +481,7 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kDDec + 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 64);
   }

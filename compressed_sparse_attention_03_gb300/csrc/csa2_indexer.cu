@@ -169,32 +169,73 @@ __device__ __forceinline__ float key_score(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
+constexpr int kTopkWarps = kTopkThreads / 32;
+
 struct SelectShared {
-  uint32_t hist[256];
-  int warp_tot[2][kTopkThreads / 32];
+  uint32_t hist[kTopkWarps][256];  // one histogram per warp: fewer same-address atomics
+  uint32_t red[2][kTopkWarps];
+  int warp_tot[2][kTopkWarps];
   uint32_t bucket;
   int krem;
 };
 
 // Radix select over keys[0..n): on return *thr is the K-th largest key and *need_eq the
-// number of keys equal to *thr that belong to the top K (the lowest-index ones).
+// number of keys equal to *thr that belong to the top K (the lowest-index ones).  The digits
+// start at the highest bit in which the smallest and largest key differ (the bits above are
+// common to every key and would put all keys into one bin).
 __device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared& sh, uint32_t* thr, int* need_eq) {
-  const int tid = threadIdx.x;
-  uint32_t prefix = 0, mask = 0;
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+  uint32_t mn = 0xffffffffu, mx = 0u;
+  for (int i = tid; i < n; i += kTopkThreads) {
+    const uint32_t k = keys[i];
+    mn = min(mn, k);
+    mx = max(mx, k);
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (l == 0) {
+    sh.red[0][w] = mn;
+    sh.red[1][w] = mx;
+  }
+  __syncthreads();
+  mn = 0xffffffffu;
+  mx = 0u;
+  for (int x = 0; x < kTopkWarps; ++x) {
+    mn = min(mn, sh.red[0][x]);
+    mx = max(mx, sh.red[1][x]);
+  }
+  __syncthreads();
+  if (mn == mx) {  // every key equal: the K lowest positions
+    *thr = mx;
+    *need_eq = K;
+    return;
+  }
+  const int top = 31 - __clz(mn ^ mx);
+  uint32_t mask = top == 31 ? 0u : ~((2u << top) - 1u);
+  uint32_t prefix = mx & mask;
   int krem = K;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kTopkThreads) sh.hist[i] = 0;
+  for (int hi = top; hi >= 0; hi -= 8) {
+    const int lo = max(hi - 7, 0);
+    const uint32_t dmask = (2u << (hi - lo)) - 1u;
+    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&sh.hist[0][0])[i] = 0;
     __syncthreads();
     for (int i = tid; i < n; i += kTopkThreads) {
       const uint32_t k = keys[i];
-      if ((k & mask) == prefix) atomicAdd(&sh.hist[(k >> shift) & 255u], 1u);
+      if ((k & mask) == prefix) atomicAdd(&sh.hist[w][(k >> lo) & dmask], 1u);
+    }
+    __syncthreads();
+    for (int b = tid; b < 256; b += kTopkThreads) {  // fold the per-warp histograms into warp 0's
+      uint32_t c = 0;
+#pragma unroll
+      for (int x = 0; x < kTopkWarps; ++x) c += sh.hist[x][b];
+      sh.hist[0][b] = c;
     }
     __syncthreads();
     if (tid < 32) {
       // lane l owns bins 255-8l .. 248-8l (descending)
       uint32_t c[8], tot = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) { c[i] = sh.hist[255 - 8 * tid - i]; tot += c[i]; }
+      for (int i = 0; i < 8; ++i) { c[i] = sh.hist[0][255 - 8 * tid - i]; tot += c[i]; }
       uint32_t incl = tot;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -216,8 +257,8 @@ __device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared& s
       }
     }
     __syncthreads();
-    prefix |= sh.bucket << shift;
-    mask |= 255u << shift;
+    prefix |= sh.bucket << lo;
+    mask |= dmask << lo;
     krem = sh.krem;
     __syncthreads();
   }
@@ -227,47 +268,62 @@ __device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared& s
 
 // Writes the K selected (key, j) pairs in ascending position order.  Keys > thr are all
 // taken; of the keys == thr only the first need_eq (in position order).  js == nullptr
-// means j = j0 + position.  Returns nothing; out_* receive exactly K entries.
+// means j = j0 + position.  Each warp owns one contiguous segment: a counting pass, one scan
+// of the per-warp counts, then an ordered writing pass.
 __device__ void compact_selected(const uint32_t* keys, const int32_t* js, int64_t j0, int n, uint32_t thr, int need_eq,
                                  SelectShared& sh, uint32_t* out_key, int32_t* out_j) {
-  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
-  constexpr int NW = kTopkThreads / 32;
-  int eq_base = 0, out_base = 0;
-  for (int r0 = 0; r0 < n; r0 += kTopkThreads) {
-    const int i = r0 + tid;
-    const uint32_t k = i < n ? keys[i] : 0u;
-    const bool is_gt = i < n && k > thr;
-    const bool is_eq = i < n && k == thr;
-    const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
-    if (l == 0) sh.warp_tot[0][w] = __popc(beq);
-    __syncthreads();
-    int eq_before = eq_base;
-    int eq_round = 0;
-    for (int x = 0; x < NW; ++x) {
-      const int v = sh.warp_tot[0][x];
-      if (x < w) eq_before += v;
-      eq_round += v;
-    }
-    eq_before += __popc(beq & ((1u << l) - 1u));
-    const bool take = is_gt || (is_eq && eq_before < need_eq);
-    const uint32_t bt = __ballot_sync(0xffffffffu, take);
-    if (l == 0) sh.warp_tot[1][w] = __popc(bt);
-    __syncthreads();
-    int pos = out_base, t_round = 0;
-    for (int x = 0; x < NW; ++x) {
-      const int v = sh.warp_tot[1][x];
-      if (x < w) pos += v;
-      t_round += v;
-    }
-    pos += __popc(bt & ((1u << l) - 1u));
-    if (take) {
-      out_key[pos] = k;
-      out_j[pos] = js ? js[i] : (int32_t)(j0 + i);
-    }
-    eq_base += eq_round;
-    out_base += t_round;
-    __syncthreads();
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const uint32_t lt = (1u << l) - 1u;
+  const int seg = (((n + kTopkWarps - 1) / kTopkWarps) + 31) & ~31;
+  const int s0 = min(n, w * seg), s1 = min(n, s0 + seg);
+  int gt = 0, eq = 0;
+  for (int i0 = s0; i0 < s1; i0 += 32) {
+    const int i = i0 + l;
+    const bool v = i < s1;
+    const uint32_t k = v ? keys[i] : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, v && k > thr));
+    eq += __popc(__ballot_sync(0xffffffffu, v && k == thr));
   }
+  if (l == 0) {
+    sh.warp_tot[0][w] = gt;
+    sh.warp_tot[1][w] = eq;
+  }
+  __syncthreads();
+  // lane x holds warp x's counts; exclusive scans give this warp's equal-key rank and output base
+  const int g = l < kTopkWarps ? sh.warp_tot[0][l] : 0, e = l < kTopkWarps ? sh.warp_tot[1][l] : 0;
+  int e_inc = e;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, e_inc, o);
+    if (l >= o) e_inc += y;
+  }
+  const int e_exc = e_inc - e;
+  const int taken = g + min(max(need_eq - e_exc, 0), e);
+  int t_inc = taken;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, t_inc, o);
+    if (l >= o) t_inc += y;
+  }
+  int run_eq = __shfl_sync(0xffffffffu, e_exc, w);
+  int pos = __shfl_sync(0xffffffffu, t_inc - taken, w);
+  for (int i0 = s0; i0 < s1; i0 += 32) {
+    const int i = i0 + l;
+    const bool v = i < s1;
+    const uint32_t k = v ? keys[i] : 0u;
+    const bool is_eq = v && k == thr;
+    const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
+    const bool take = (v && k > thr) || (is_eq && run_eq + __popc(beq & lt) < need_eq);
+    const uint32_t bt = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const int p = pos + __popc(bt & lt);
+      out_key[p] = k;
+      out_j[p] = js ? js[i] : (int32_t)(j0 + i);
+    }
+    run_eq += __popc(beq);
+    pos += __popc(bt);
+  }
+  __syncthreads();
 }
 
 // Stage 1: grid (nchunks, rows, nb).  Local top-512 of one chunk of one query's scores.
@@ -287,11 +343,22 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, S
   const int64_t cs = (int64_t)c * chunk;
   const int n = (int)max64(0, min64(chunk, E - cs));
   const int64_t row = (int64_t)bl * Tq + tl;
-  const float* src = scores + row * ld + cs;
-  for (int i = threadIdx.x; i < n; i += kTopkThreads) skeys[i] = score_key(src[i]);
+  const float* src = scores + row * ld + cs;  // 16-byte aligned: ld and the chunk are multiples of 32
+  const int n4 = n >> 2;
+#pragma unroll 4
+  for (int v = threadIdx.x; v < n4; v += kTopkThreads) {
+    const float4 f = reinterpret_cast<const float4*>(src)[v];
+    reinterpret_cast<uint4*>(skeys)[v] = make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+  }
+  for (int i = 4 * n4 + threadIdx.x; i < n; i += kTopkThreads) skeys[i] = score_key(src[i]);
   __syncthreads();
   const int K = min(kTopK, n);
-  if (K > 0) {
+  if (n <= kTopK) {  // every candidate is kept, already in position order
+    for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+      okey[i] = skeys[i];
+      oj[i] = (int32_t)(cs + i);
+    }
+  } else {
     uint32_t thr;
     int need_eq;
     radix_select(skeys, n, K, sh, &thr, &need_eq);
@@ -330,23 +397,32 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(IndexArgs a, i
   if (t >= a.T) return;
   const int b = b0 + bl;
   const int64_t row = (int64_t)bl * Tq + tl;
+  __shared__ int cnt_s[kMaxChunks];
+  if (threadIdx.x < nchunks) cnt_s[threadIdx.x] = cn[row * nchunks + threadIdx.x];
+  __syncthreads();
   if (threadIdx.x == 0) {
     offs[0] = 0;
-    for (int c = 0; c < nchunks; ++c) offs[c + 1] = offs[c] + cn[row * nchunks + c];
+    for (int c = 0; c < nchunks; ++c) offs[c + 1] = offs[c] + cnt_s[c];
   }
   __syncthreads();
   const int n = offs[nchunks];
-  for (int c = 0; c < nchunks; ++c) {
-    const int cnt = offs[c + 1] - offs[c];
-    const int64_t base = (row * nchunks + c) * kTopK;
-    for (int i = threadIdx.x; i < cnt; i += kTopkThreads) {
-      skeys[offs[c] + i] = ck[base + i];
-      sjs[offs[c] + i] = cj[base + i];
+  // every (chunk, slot) pair at once, so that all loads are in flight together
+  for (int q = threadIdx.x; q < nchunks * kTopK; q += kTopkThreads) {
+    const int c = q / kTopK, i = q % kTopK;
+    if (i < cnt_s[c]) {
+      const int64_t src = (row * nchunks + c) * kTopK + i;
+      skeys[offs[c] + i] = ck[src];
+      sjs[offs[c] + i] = cj[src];
     }
   }
   __syncthreads();
   const int K = min(kTopK, n);
-  if (K > 0) {
+  if (n <= kTopK) {  // chunk lists are consecutive in position order
+    for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+      okey[i] = skeys[i];
+      oj[i] = sjs[i];
+    }
+  } else {
     uint32_t thr;
     int need_eq;
     radix_select(skeys, n, K, sh, &thr, &need_eq);
