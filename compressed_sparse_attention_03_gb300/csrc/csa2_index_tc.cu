@@ -50,6 +50,17 @@ __device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Both halves = 2^e as fp16 bits, built without arithmetic: normal for -14 <= e <= 15,
+// subnormal down to 2^-24, 0 below, +inf above (the values an fp32 2^e rounds to in fp16).
+__device__ __forceinline__ uint32_t pow2_h2(int e) {
+  uint32_t h;
+  if (e > 15) h = 0x7C00u;
+  else if (e >= -14) h = (uint32_t)(e + 15) << 10;
+  else if (e >= -24) h = 1u << (e + 24);
+  else h = 0u;
+  return h | (h << 16);
+}
+
 // Q^I (bf16) -> FP4 (E2M1, UE8M0 per 32) -> fp16 image.  grid (Tq, nb), 128 threads: warp w
 // handles heads 8w..8w+7, lane l values 4l..4l+3.  Query t of the chunk lives in tile t/8,
 // rows (t%8)*32 + h of the tile's [256 x 128] K-major image (2 atoms of 64 dims).
@@ -279,26 +290,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
 // ------------------------------------------------------------------ decode (one query)
 // Scores of one query per sequence against all its visible keys: M = 128 keys, N = 32 heads,
 // K = 128 per tile.  The FP4 keys are decoded inside the kernel (a fp16 image of all keys
-// would cost 4x the key bytes in extra HBM traffic).
-//  - warp 0 (loader): per tile one bulk copy of the 128 x 64 code bytes and, lane by lane,
-//    4-byte cp.async copies of the scale words (their rows are only 4-byte aligned), all
-//    completing on the stage's mbarrier; kDStg stages in flight.
-//  - warps 1-8 (decoders, two per SM sub-partition so that one hides the other's latency): a
-//    warp reads 8 consecutive 64-byte code rows per load (conflict free), lane = (row, 32-value
-//    block); decodes exactly to fp16 into a kDSlots-deep ring of 32 KB swizzled operand tiles.
-//  - warp 9 (one thread): the MMAs, into double-buffered TMEM accumulators.
-//  - warps 10-13 (epilogue): ReLU, the w^I weighting and the fp32 score stores.
+// would cost 4x the key bytes in extra HBM traffic) and the decoded tile goes to tensor
+// memory, where the MMA reads its A operand: staging it in shared memory made the 32 KB
+// store + 32 KB operand read per tile the bottleneck of the shared-memory port.
+//  - warps 0-7 (epilogue, group = warp / 4, TMEM lane quarter = warp % 4): ReLU, the w^I
+//    weighting and the fp32 score stores for the tiles of their parity (accumulator = parity).
+//  - warps 8-15 (decoders, group = (warp - 8) / 4): thread = key row of the tiles of the
+//    group's parity; loads its 64 code bytes and 4 scale bytes straight from global memory two
+//    tiles ahead, decodes exactly to fp16 and writes the row into TMEM (kDSlots tiles).
+//  - warp 16 (one thread): the MMAs, A from TMEM, B (Q^I) from shared memory.
 // Each sequence's key tiles are split evenly over gridDim.x / nb persistent blocks.
-constexpr int kDSlots = 4, kDStg = 8, kDDec = 8, kDThreads = 32 * (2 + kDDec + 4);
-constexpr uint32_t kDAOff = 0;                     // operand tiles: kDSlots x 32 KB
-constexpr uint32_t kDRawOff = 131072;              // raw codes: kDStg x [128 keys x 64 B]
-constexpr uint32_t kDScOff = kDRawOff + kDStg * 8192;  // raw scales: kDStg x [128 keys x 4 B]
-constexpr uint32_t kDQOff = kDScOff + kDStg * 512;     // Q^I image: 2 atoms x [32 heads x 128 B]
+constexpr int kDSlots = 4, kDThreads = 32 * 17;
+constexpr int kDDec0 = 8, kDMma = 16;
+constexpr uint32_t kDACol = 0;                    // TMEM: A tiles kDSlots x 64 columns
+constexpr uint32_t kDDCol = kDSlots * 64;          // TMEM: two 32-column accumulators
+constexpr uint32_t kDTmemCols = 512;
+constexpr uint32_t kDQOff = 0;                     // smem: Q^I image, 2 atoms x [32 heads x 128 B]
 constexpr uint32_t kDynDec = kDQOff + 8192 + 1024;
-static_assert(kDQOff % 1024 == 0, "swizzled Q^I atoms need 1024-byte alignment");
+static_assert(kDSlots % 2 == 0, "a decoder group keeps the parity of its tiles");
+static_assert(kDDCol + 64 <= kDTmemCols, "TMEM columns");
 
+// a_full[slot]: the tile in a slot is decoded (4 decoder warps).  done[slot]: the MMAs of the
+// tile in a slot completed (one commit): the slot is free and accumulator slot & 1 holds its
+// scores.  d_free[k]: the epilogue group of parity k has read accumulator k (4 warps).
 struct DecBars {
-  uint64_t raw_full[kDStg], raw_free[kDStg], a_full[kDSlots], a_free[kDSlots], d_full[2], d_free[2];
+  uint64_t a_full[kDSlots], done[kDSlots], d_free[2];
 };
 
 __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs a, SeqPos pos, int b0, int nb,
@@ -323,28 +339,22 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   const int nt = active ? t_end - t_begin : 0;
 
   if (tid == 0) {
-    for (int i = 0; i < kDStg; ++i) {
-      mbar_init(&bars.raw_full[i], 1 + 32);  // the loader's expect_tx + one cp.async arrival per lane
-      mbar_init(&bars.raw_free[i], kDDec);
-    }
     for (int i = 0; i < kDSlots; ++i) {
-      mbar_init(&bars.a_full[i], kDDec);
-      mbar_init(&bars.a_free[i], 1);
+      mbar_init(&bars.a_full[i], 4);  // the four warps of one decoder group
+      mbar_init(&bars.done[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.d_full[i], 1);
-      mbar_init(&bars.d_free[i], 4);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(&bars.d_free[i], 4);  // the four warps of one epilogue group
     mbar_fence_init();
   }
-  if (warp == kDDec + 1) {
-    tmem_alloc(&tmem_base_sh, 64);
+  if (warp == kDMma) {
+    tmem_alloc(&tmem_base_sh, kDTmemCols);
     tmem_relinquish();
   }
-  // Q^I -> FP4 -> fp16 image (warps 1-4: warp w heads 8(w-1)..+7, lane l values 4l..4l+3), w^I
-  if (warp >= 1 && warp <= 4 && active) {
+  // Q^I -> FP4 -> fp16 image (warps 8-11: warp heads 8(w-8)..+7, lane l values 4l..4l+3), w^I
+  if (warp >= kDDec0 && warp < kDDec0 + 4 && active) {
+    const int hw = warp - kDDec0;
     const int64_t src = (int64_t)b * a.T;  // T == 1
-    for (int h = 8 * (warp - 1); h < 8 * warp; ++h) {
+    for (int h = 8 * hw; h < 8 * hw + 8; ++h) {
       const uint2 raw = *reinterpret_cast<const uint2*>(a.qi + (src * kHI + h) * kDI + 4 * lane);
       float v[4] = {bf16_to_f32(raw.x & 0xffff), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xffff), bf16_to_f32(raw.y >> 16)};
       float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
@@ -359,7 +369,7 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
       *reinterpret_cast<uint2*>(sm + kDQOff + (d >> 6) * 4096 + sw128_off(h, (d & 63) >> 3) + (d & 7) * 2) =
           make_uint2(f2_to_h2(q[0], q[1]), f2_to_h2(q[2], q[3]));
     }
-    if (warp == 1) wsh[lane] = bf16_to_f32(a.wI[src * kHI + lane]);
+    if (hw == 0) wsh[lane] = bf16_to_f32(a.wI[src * kHI + lane]);
     fence_proxy_async();
   }
   tc_fence_before();
@@ -367,123 +377,114 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 0) {
-    // ============================================================ loader
+  if (warp >= kDDec0 && warp < kDDec0 + 8) {
+    // ============================================================ decoders: thread = key row
+    const int grp = (warp - kDDec0) >> 2, q4 = warp & 3;
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
     const uint8_t* codes = a.ki_codes + (int64_t)b * a.cap * 64;
     const uint8_t* scl = a.ki_scales + (int64_t)b * a.cap * 4;
+    auto load = [&](int i, uint4 (&c)[4], uint32_t& sc) {
+      const int64_t j = (int64_t)(t_begin + i) * 128 + r;
+      if (i < nt && j < E) {
+        const uint4* p = reinterpret_cast<const uint4*>(codes + j * 64);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[k] = __ldg(p + k);
+        sc = __ldg(reinterpret_cast<const uint32_t*>(scl + j * 4));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[k] = make_uint4(0u, 0u, 0u, 0u);  // rows past the last key: zero
+        sc = 0x7f7f7f7fu;
+      }
+    };
+    uint4 ca[4], cb[4];
+    uint32_t sa, sb;
+    load(grp, ca, sa);
+    load(grp + 2, cb, sb);
 #pragma unroll 1
-    for (int i = 0; i < nt; ++i) {
-      const int st = i % kDStg;
-      if (i >= kDStg) mbar_wait(&bars.raw_free[st], ((i / kDStg) - 1) & 1, err, 31);
-      const int64_t j0 = (int64_t)(t_begin + i) * 128;
-      const int n = (int)min64(128, E - j0);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars.raw_full[st], (uint32_t)n * 64u);
-        bulk_g2s(sm + kDRawOff + st * 8192, codes + j0 * 64, (uint32_t)n * 64u, &bars.raw_full[st]);
+    for (int i = grp; i < nt; i += 2) {
+      uint4 cc[4];
+      uint32_t scc;
+      load(i + 4, cc, scc);  // two tiles of this group ahead
+      const int slot = i % kDSlots;
+      if (i >= kDSlots) mbar_wait(&bars.done[slot], ((i / kDSlots) - 1) & 1, err, 34);  // slot's last tile done
+      tc_fence_after();
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {  // 32 values: 16 code bytes, one scale byte
+        const uint32_t s2 = pow2_h2((int)((sa >> (8 * blk)) & 255u) - 127);
+        const uint32_t wd[4] = {ca[blk].x, ca[blk].y, ca[blk].z, ca[blk].w};
+        uint32_t o[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[4 * q + k] = hmul2(cvt_e2m1x2_f16x2((wd[q] >> (8 * k)) & 255u), s2);
+        tmem_st16(lane_addr + kDACol + slot * 64 + 16 * blk, o);
       }
-#pragma unroll
-      for (int k = 4 * lane; k < 4 * lane + 4; ++k)
-        if (k < n) cp_async4(sm + kDScOff + st * 512 + 4 * k, scl + (j0 + k) * 4);
-      cp_async_mbar_arrive_noinc(&bars.raw_full[st]);
-    }
-    // leave no copy in flight, also after a wait that gave up
-    for (int i = max(0, nt - kDStg); i < nt; ++i) mbar_wait(&bars.raw_full[i % kDStg], (i / kDStg) & 1, err, 32);
-    cp_async_commit();
-    cp_async_wait<0>();
-  } else if (warp <= kDDec) {
-    // ============================================================ decoders
-    const int dw = warp - 1;
-    const int blk = lane & 3;  // 32-value block of the row: 16 code bytes, one scale byte
-#pragma unroll 1
-    for (int i = 0; i < nt; ++i) {
-      const int st = i % kDStg, slot = i % kDSlots;
-      const int n = (int)min64(128, E - (int64_t)(t_begin + i) * 128);
-      mbar_wait(&bars.raw_full[st], (i / kDStg) & 1, err, 33);
-      constexpr int kIt = 128 / (8 * kDDec);  // 8-row groups per decoder warp
-      uint4 c[kIt];
-      uint32_t sc[kIt];
-#pragma unroll
-      for (int it = 0; it < kIt; ++it) {
-        const int key = 8 * (kIt * dw + it) + (lane >> 2);
-        if (key < n) {
-          c[it] = *reinterpret_cast<const uint4*>(sm + kDRawOff + st * 8192 + key * 64 + blk * 16);
-          sc[it] = sm[kDScOff + st * 512 + key * 4 + blk];
-        } else {
-          c[it] = make_uint4(0u, 0u, 0u, 0u);  // rows past the last key: zero operands
-          sc[it] = 127u;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.raw_free[st]);
-      if (i >= kDSlots) mbar_wait(&bars.a_free[slot], ((i / kDSlots) - 1) & 1, err, 34);
-      unsigned char* tile = sm + kDAOff + slot * 32768 + (blk >> 1) * 16384;
-#pragma unroll
-      for (int it = 0; it < kIt; ++it) {
-        const int key = 8 * (kIt * dw + it) + (lane >> 2);
-        const float sf = ldexpf(1.0f, (int)sc[it] - 127);
-        const uint32_t s2 = f2_to_h2(sf, sf);
-        const uint32_t wd[4] = {c[it].x, c[it].y, c[it].z, c[it].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {  // 8 values = one 16-byte chunk of fp16
-          uint32_t o[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) o[k] = hmul2(cvt_e2m1x2_f16x2((wd[q] >> (8 * k)) & 255u), s2);
-          *reinterpret_cast<uint4*>(tile + sw128_off(key, 4 * (blk & 1) + q)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-      fence_proxy_async();
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.a_full[slot]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        ca[k] = cb[k];
+        cb[k] = cc[k];
+      }
+      sa = sb;
+      sb = scc;
     }
-  } else if (warp == kDDec + 1) {
+  } else if (warp == kDMma) {
     // ============================================================ MMA issuer
     if (lane == 0) {
+      // The MMA thread shares its sub-partition with four busy warps: keep its instruction
+      // stream short (the Q^I descriptors never change; A and D are plain TMEM offsets).
       const uint32_t idesc = idesc_f16(false, false, 128, 32);
+      uint64_t bdesc[8];
+#pragma unroll
+      for (int k16 = 0; k16 < 8; ++k16)
+        bdesc[k16] = sw128_desc(sbase + kDQOff + (k16 >> 2) * 4096 + (k16 & 3) * 32, 16, 1024);
       for (int i = 0; i < nt; ++i) {
         const int slot = i % kDSlots, sD = i & 1;
         mbar_wait(&bars.a_full[slot], (i / kDSlots) & 1, err, 22);
         if (i >= 2) mbar_wait(&bars.d_free[sD], ((i >> 1) - 1) & 1, err, 23);
         tc_fence_after();
-        const uint32_t abase = sbase + kDAOff + slot * 32768, bbase = sbase + kDQOff;
+        const uint32_t ta = tmem + kDACol + slot * 64, td = tmem + kDDCol + 32 * sD;
+        mma_f16_ts(td, ta, bdesc[0], idesc, 0u);
 #pragma unroll
-        for (int k16 = 0; k16 < 8; ++k16) {
-          const uint32_t atom = k16 >> 2, off = (k16 & 3) * 32;
-          mma_f16_ss(tmem + 32 * sD, sw128_desc(abase + atom * 16384 + off, 16, 1024),
-                     sw128_desc(bbase + atom * 4096 + off, 16, 1024), idesc, k16 > 0);
-        }
-        mma_commit(&bars.a_free[slot]);
-        mma_commit(&bars.d_full[sD]);
+        for (int k16 = 1; k16 < 8; ++k16) mma_f16_ts(td, ta + 8 * k16, bdesc[k16], idesc, 1u);
+        mma_commit(&bars.done[slot]);
       }
     }
     __syncwarp();
   } else {
     // ============================================================ epilogue: thread = key lane
-    const int q4 = warp & 3;  // TMEM lane quarter this warp may access
+    const int grp = warp >> 2, q4 = warp & 3;  // tile parity, TMEM lane quarter
     const int r = 32 * q4 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16) + kDDCol + 32 * grp;
     float* out = scores + (int64_t)bl * ld;
-    for (int i = 0; i < nt; ++i) {
-      const int sD = i & 1;
-      mbar_wait(&bars.d_full[sD], (i >> 1) & 1, err, 24);
+    float wr[kHI];
+#pragma unroll
+    for (int h = 0; h < kHI; ++h) wr[h] = wsh[h];
+    for (int i = grp; i < nt; i += 2) {
+      mbar_wait(&bars.done[i % kDSlots], (i / kDSlots) & 1, err, 24);
       tc_fence_after();
       uint32_t u[32];
-      tmem_ld32(lane_addr + 32 * sD, u);
+      tmem_ld32(lane_addr, u);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.d_free[sD]);
-      float s = 0.f;
+      if (lane == 0) mbar_arrive(&bars.d_free[grp]);
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains of 8
 #pragma unroll
-      for (int h = 0; h < 32; ++h) s = fmaf(wsh[h], fmaxf(__uint_as_float(u[h]), 0.f), s);
+      for (int h = 0; h < 32; ++h) s4[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(u[h]), 0.f), s4[h & 3]);
       const int64_t j = (int64_t)(t_begin + i) * 128 + r;
-      if (j < E) out[j] = s;
+      if (j < E) out[j] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kDDec + 1) {
+  if (warp == kDMma) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, kDTmemCols);
   }
 }
 

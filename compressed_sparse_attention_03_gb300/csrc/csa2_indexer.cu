@@ -345,10 +345,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, S
   const int64_t row = (int64_t)bl * Tq + tl;
   const float* src = scores + row * ld + cs;  // 16-byte aligned: ld and the chunk are multiples of 32
   const int n4 = n >> 2;
-#pragma unroll 4
-  for (int v = threadIdx.x; v < n4; v += kTopkThreads) {
-    const float4 f = reinterpret_cast<const float4*>(src)[v];
-    reinterpret_cast<uint4*>(skeys)[v] = make_uint4(score_key(f.x), score_key(f.y), score_key(f.z), score_key(f.w));
+  constexpr int kLB = 4;  // 16-byte loads in flight per thread
+  for (int v0 = threadIdx.x; v0 < n4; v0 += kLB * kTopkThreads) {
+    float4 f[kLB];
+#pragma unroll
+    for (int u = 0; u < kLB; ++u)
+      if (v0 + u * kTopkThreads < n4) f[u] = __ldg(reinterpret_cast<const float4*>(src) + v0 + u * kTopkThreads);
+#pragma unroll
+    for (int u = 0; u < kLB; ++u)
+      if (v0 + u * kTopkThreads < n4)
+        reinterpret_cast<uint4*>(skeys)[v0 + u * kTopkThreads] =
+            make_uint4(score_key(f[u].x), score_key(f[u].y), score_key(f[u].z), score_key(f[u].w));
   }
   for (int i = 4 * n4 + threadIdx.x; i < n; i += kTopkThreads) skeys[i] = score_key(src[i]);
   __syncthreads();
@@ -406,13 +413,25 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(IndexArgs a, i
   }
   __syncthreads();
   const int n = offs[nchunks];
-  // every (chunk, slot) pair at once, so that all loads are in flight together
-  for (int q = threadIdx.x; q < nchunks * kTopK; q += kTopkThreads) {
-    const int c = q / kTopK, i = q % kTopK;
-    if (i < cnt_s[c]) {
+  // all (chunk, slot) loads of a thread are issued before any of its shared-memory stores
+  constexpr int kLB = kMaxChunks * kTopK / kTopkThreads;
+  uint32_t kk[kLB];
+  int32_t jj[kLB];
+#pragma unroll
+  for (int u = 0; u < kLB; ++u) {
+    const int q = threadIdx.x + u * kTopkThreads, c = q / kTopK, i = q % kTopK;
+    if (c < nchunks && i < cnt_s[c]) {
       const int64_t src = (row * nchunks + c) * kTopK + i;
-      skeys[offs[c] + i] = ck[src];
-      sjs[offs[c] + i] = cj[src];
+      kk[u] = __ldg(ck + src);
+      jj[u] = __ldg(cj + src);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kLB; ++u) {
+    const int q = threadIdx.x + u * kTopkThreads, c = q / kTopK, i = q % kTopK;
+    if (c < nchunks && i < cnt_s[c]) {
+      skeys[offs[c] + i] = kk[u];
+      sjs[offs[c] + i] = jj[u];
     }
   }
   __syncthreads();
