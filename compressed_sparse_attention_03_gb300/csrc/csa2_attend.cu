@@ -306,14 +306,21 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       mbar_wait(&bars.q_full, 0, err, 2);
       const uint64_t ones_desc = sw128_desc(sbase + kOnesOff, 16, 0);  // every row group reads the same atom
       for (int i = 0; i < nloc; ++i) {
-        // S^T = G_c Q^T, the atoms in order into one accumulator
-        for (int k = 0; k < 8; ++k) {
-          mbar_wait(&bars.atom_full[k], i & 1, err, 3);
+        // S^T = G_c Q^T into one accumulator.  Every wait of this thread stalls until its MMAs in
+        // flight drain, so it waits for atoms k and k+4 together (the two producer halves write
+        // them at the same time).
+        for (int k2 = 0; k2 < 4; ++k2) {
+          mbar_wait(&bars.atom_full[k2], i & 1, err, 3);
+          mbar_wait(&bars.atom_full[k2 + 4], i & 1, err, 3);
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16_ss(tmem + kSCol, sw128_desc(gg + k * 16384 + kk * 32, 16, 1024),
-                       sw128_desc(gq + k * 8192 + kk * 32, 16, 1024), idS, (k | kk) != 0);
+          for (int hk = 0; hk < 2; ++hk) {
+            const int k = k2 + 4 * hk;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(tmem + kSCol, sw128_desc(gg + k * 16384 + kk * 32, 16, 1024),
+                         sw128_desc(gq + k * 8192 + kk * 32, 16, 1024), idS, (k2 | hk | kk) != 0);
+          }
         }
         mma_commit(&bars.s_full);
         mbar_wait(&bars.p_full, i & 1, err, 4);
