@@ -15,8 +15,10 @@ no data-path collective): value = all ranks' tokens / max step time over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -277,6 +279,24 @@ def time_e2e(step: Step, steps: int, warmup: int):
             "d2h_bytes_per_step": d2h}
 
 
+def profiled_traffic(profile: str, sources) -> int | None:
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu summary
+    under profiles/, or None when the kernel sources changed since that capture."""
+    p = ROOT / "profiles" / profile
+    if not p.exists():
+        return None
+    txt = p.read_text()
+    sha = re.search(r"source_sha256_16: ([0-9a-f]{16})", txt)
+    byt = re.search(r"traffic_bytes_per_launch: (\d+)", txt)
+    if not sha or not byt:
+        return None
+    now = hashlib.sha256(b"".join((ROOT / s).read_bytes() for s in sources)).hexdigest()[:16]
+    return int(byt.group(1)) if now == sha.group(1) else None
+
+
+CSRC = "compressed_sparse_attention_03_gb300/csrc/"
+
+
 def peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -311,7 +331,9 @@ def run_ours(args, rank, ws):
         "kernels_ms": per,
         "roofline": {"kernel": "attend_kernel", "bound": "tensor", "achieved": achieved, "peak": bf16,
                      "unit": "TFLOP/s", "frac": achieved / bf16, "peak_source": f"{src} bf16 burst",
-                     "flops_per_launch": flops, "traffic": None},
+                     "flops_per_launch": flops,
+                     "traffic": profiled_traffic("attend_tc_kernel_prefill_4k.md", [CSRC + "csa2_attend.cu"]),
+                     "traffic_source": "profiles/attend_tc_kernel_prefill_4k.md (null once the kernel changed)"},
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks.summary(),
@@ -332,7 +354,9 @@ def run_ours(args, rank, ws):
                               "frac": by["step"] / (dms / 1e3) / 1e9 / hbm, "bytes": by["step"]},
             "roofline_index": {"bound": "hbm", "achieved": by["indexer"] / (idx_ms / 1e3) / 1e9, "peak": hbm,
                                "unit": "GB/s", "frac": by["indexer"] / (idx_ms / 1e3) / 1e9 / hbm,
-                               "bytes": by["indexer"], "peak_source": f"{src} copy bandwidth"},
+                               "bytes": by["indexer"], "peak_source": f"{src} copy bandwidth",
+                               "traffic": profiled_traffic("index_decode_decode_1m.md",
+                                                           [CSRC + "csa2_index_tc.cu", CSRC + "csa2_indexer.cu"])},
             "gpu_launches": dlaunches,
         }
         del dstep

@@ -62,3 +62,20 @@ def test_single_rank_needs_no_process_group():
                          timeout=120)
     assert out.returncode == 0, out.stderr
     assert out.stdout.split() == ["0", "1", "2.5", "4"]
+
+
+def test_profiled_traffic_is_dropped_when_the_kernel_source_changes(tmp_path, monkeypatch):
+    import importlib
+    sys.path.insert(0, str(ROOT))
+    bench = importlib.import_module("bench")
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    import hashlib
+    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "p.md").write_text(f"source_sha256_16: {h}\ntraffic_bytes_per_launch: 1234\n")
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    assert bench.profiled_traffic("p.md", ["k.cu"]) == 1234
+    src.write_text("kernel v2")
+    assert bench.profiled_traffic("p.md", ["k.cu"]) is None
+    assert bench.profiled_traffic("missing.md", ["k.cu"]) is None
