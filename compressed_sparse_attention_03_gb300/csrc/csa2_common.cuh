@@ -37,6 +37,14 @@ __device__ __forceinline__ uint32_t f32_to_e2m1(float x) {
 
 // UE8M0 exponent for a block with absolute maximum amax: floor(log2 amax) - 2, clamped to
 // [-127, 127]; amax == 0 (or subnormal) gives -127.
+// 2^k as a float built from its bits: exact for -149 <= k <= 127 (subnormal below -126).
+__device__ __forceinline__ float pow2f(int k) {
+  if (k > 127) return __uint_as_float(0x7f800000u);
+  if (k >= -126) return __uint_as_float((uint32_t)(k + 127) << 23);
+  if (k >= -149) return __uint_as_float(1u << (k + 149));
+  return 0.f;
+}
+
 __device__ __forceinline__ int mx_scale_exp(float amax) {
   int E = (int)((__float_as_uint(amax) >> 23) & 255u);
   if (E == 0) return -127;
@@ -80,6 +88,44 @@ __device__ __forceinline__ void rope_cs(int64_t pos, double inv_freq, float sign
   sincosf(rf, &s0, &c0);
   c = fmaf(-d, s0, c0);
   s = fmaf(d, c0, s0);
+}
+
+// Double-float (s + c) accumulation in fp32: error-free two-sum of each addend, so that a
+// sum of squares keeps ~2^-44 relative accuracy without fp64 arithmetic (slow on this GPU).
+struct DFSum {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float t = s + x;
+    const float bb = t - s;
+    c += (s - (t - bb)) + (x - bb);
+    s = t;
+  }
+  __device__ __forceinline__ void add_sq(float x) {  // x * x exactly (product + fma error)
+    const float p = x * x;
+    add(p);
+    c += fmaf(x, x, -p);
+  }
+  __device__ __forceinline__ void add(const DFSum& o) {
+    add(o.s);
+    c += o.c;
+  }
+  __device__ __forceinline__ float value() const { return s + c; }
+};
+
+__device__ __forceinline__ DFSum warp_sum_df(DFSum v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    DFSum p;
+    p.s = __shfl_xor_sync(0xffffffffu, v.s, o);
+    p.c = __shfl_xor_sync(0xffffffffu, v.c, o);
+    v.add(p);
+  }
+  return v;
+}
+
+// 1 / sqrt(ss / n + eps) in fp32 with correctly rounded division and square root.
+__device__ __forceinline__ float rms_inv(float ss, float n, double eps) {
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n), (float)eps)));
 }
 
 template <typename T>

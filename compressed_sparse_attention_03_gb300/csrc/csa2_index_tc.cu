@@ -72,8 +72,13 @@ __global__ void __launch_bounds__(128) qimage_kernel(IndexArgs a, int b0, int t0
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int64_t src = (int64_t)b * a.T + t;
   uint8_t* tile = qimg + ((int64_t)bl * nqt + tl / kQPerTile) * kQImg;
-  for (int h = 8 * w; h < 8 * w + 8; ++h) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(a.qi + (src * kHI + h) * kDI + 4 * l);
+  uint2 rawv[8];  // the warp's eight head rows, all loads in flight before any store
+#pragma unroll
+  for (int k = 0; k < 8; ++k) rawv[k] = __ldg(reinterpret_cast<const uint2*>(a.qi + (src * kHI + 8 * w + k) * kDI + 4 * l));
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int h = 8 * w + k;
+    const uint2 raw = rawv[k];
     float v[4] = {bf16_to_f32(raw.x & 0xffff), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xffff), bf16_to_f32(raw.y >> 16)};
     float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
@@ -81,8 +86,9 @@ __global__ void __launch_bounds__(128) qimage_kernel(IndexArgs a, int b0, int t0
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     const int e = mx_scale_exp(amax);
     float q[4];
+    const float down = pow2f(-e), up = pow2f(e);  // exact powers of two
 #pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = ldexpf(e2m1_to_f32(f32_to_e2m1(ldexpf(v[i], -e))), e);
+    for (int i = 0; i < 4; ++i) q[i] = e2m1_to_f32(f32_to_e2m1(v[i] * down)) * up;
     const int n = (tl % kQPerTile) * kHI + h, d = 4 * l;
     *reinterpret_cast<uint2*>(tile + (d >> 6) * 32768 + sw128_off(n, (d & 63) >> 3) + (d & 7) * 2) =
         make_uint2(f2_to_h2(q[0], q[1]), f2_to_h2(q[2], q[3]));

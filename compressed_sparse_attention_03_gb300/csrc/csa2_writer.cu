@@ -8,12 +8,14 @@
 // dot product for c W_IK, so that the values reaching the FP4/FP8 rounding differ from an
 // fp64 evaluation by a few fp32 ulps and the codes match except at rounding midpoints.
 #include "csa2_common.cuh"
+#include "csa2_sm100.cuh"
 
 namespace csa2 {
 namespace {
 
-constexpr int kWriterThreads = 128;
-constexpr int kEntriesPerBlock = 8;
+constexpr int kWriterThreads = 128;       // window kernel: one token per block
+constexpr int kEntryThreads = 512;        // entries kernel: four groups of 128
+constexpr int kEntriesPerBlock = 4;       // one per group
 
 // Pack the four 4-bit codes of one thread (4 consecutive values) into two bytes.
 __device__ __forceinline__ uint16_t pack4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
@@ -29,8 +31,8 @@ __device__ __forceinline__ uint16_t fp4_quant4(const float v[4], uint8_t* scale_
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
   int e = mx_scale_exp(amax);
   if ((threadIdx.x & 7) == 0) *scale_out = (uint8_t)(e + 127);
-  return pack4(f32_to_e2m1(ldexpf(v[0], -e)), f32_to_e2m1(ldexpf(v[1], -e)),
-               f32_to_e2m1(ldexpf(v[2], -e)), f32_to_e2m1(ldexpf(v[3], -e)));
+  const float s = pow2f(-e);  // exact: -e is in [-125, 127]
+  return pack4(f32_to_e2m1(v[0] * s), f32_to_e2m1(v[1] * s), f32_to_e2m1(v[2] * s), f32_to_e2m1(v[3] * s));
 }
 
 // Double-float accumulation of sum(x*w): error-free product (fma) and two-sum.
@@ -47,10 +49,30 @@ struct DF {
   }
 };
 
-__global__ void __launch_bounds__(kWriterThreads) writer_entries_kernel(WriterArgs a, SeqPos pos, int b0, RopeFreq rf) {
+// Double-float sum over the 128 threads of group g (four whole warps), on named barrier 1 + g.
+__device__ __forceinline__ float group_sum(DFSum v, float2* red, int g) {
+  v = warp_sum_df(v);
+  const int wg = (threadIdx.x >> 5) & 3;
+  sm100::named_bar_sync(1 + g, 128);  // earlier readers of red[] are done
+  if ((threadIdx.x & 31) == 0) red[wg] = make_float2(v.s, v.c);
+  sm100::named_bar_sync(1 + g, 128);
+  DFSum t;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    t.add(red[i].x);
+    t.c += red[i].y;
+  }
+  return t.value();
+}
+
+// grid (entry groups of 4, sequences), 512 threads.  Group g = tid / 128 pools, normalises and
+// quantises entry g (thread = 4 channels); the k^i = c W_IK products are split over the
+// groups by K quarter (thread = output column), each a double-float partial, combined in
+// phase 3 where group g again owns entry g (thread = output column).
+__global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArgs a, SeqPos pos, int b0, RopeFreq rf) {
   __shared__ float sc[kEntriesPerBlock][kD];
-  __shared__ double red[kWriterThreads / 32];
-  __shared__ int64_t sj[kEntriesPerBlock];
+  __shared__ float2 part[4][kEntriesPerBlock][kDI];  // (s, c) of each K quarter
+  __shared__ float2 red[kEntriesPerBlock][4];
 
   const int bl = blockIdx.y;
   const int b = b0 + bl;
@@ -60,13 +82,12 @@ __global__ void __launch_bounds__(kWriterThreads) writer_entries_kernel(WriterAr
   const int64_t e_base = (int64_t)blockIdx.x * kEntriesPerBlock;
   if (e_base >= n_new) return;
   const int ne = (int)min64(kEntriesPerBlock, n_new - e_base);
-  const int tid = threadIdx.x;
-  const int ch = 4 * tid;
-  for (int e = ne; e < kEntriesPerBlock; ++e) *reinterpret_cast<float4*>(&sc[e][ch]) = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int tid = threadIdx.x, g = tid >> 7, gt = tid & 127;
+  const int ch = 4 * gt;
+  const int64_t j = p0 / 2 + e_base + g;  // this group's entry (valid when g < ne)
 
-  // ---- phase 1: pooled key, RMSNorm, Z
-  for (int e = 0; e < ne; ++e) {
-    const int64_t j = p0 / 2 + e_base + e;
+  // ---- phase 1: pooled key, RMSNorm, Z (the branch is uniform over a group)
+  if (g < ne) {
     const int64_t t1 = 2 * j + 1 - p0;  // local index of the odd token (0 <= t1 < T)
     const uint16_t* k1p = a.kc + ((int64_t)b * T + t1) * kD + ch;
     const uint16_t* g1p = a.gc + ((int64_t)b * T + t1) * kD + ch;
@@ -89,22 +110,21 @@ __global__ void __launch_bounds__(kWriterThreads) writer_entries_kernel(WriterAr
       g0[0] = gb.x; g0[1] = gb.y; g0[2] = gb.z; g0[3] = gb.w;
     }
     float kp[4];
-    double ss = 0.0;
+    DFSum ssq;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float m = fmaxf(g0[i], g1[i]);
       float e0 = expf(g0[i] - m), e1 = expf(g1[i] - m);
       float den = e0 + e1;
       kp[i] = (e0 / den) * k0[i] + (e1 / den) * k1[i];
-      ss += (double)kp[i] * (double)kp[i];
+      ssq.add_sq(kp[i]);
     }
-    ss = block_sum<kWriterThreads>(ss, red);
-    const float r = (float)(1.0 / sqrt(ss / kD + a.eps));
+    const float r = rms_inv(group_sum(ssq, red[g], g), (float)kD, a.eps);
     float c[4], z[4];
     float4 gm = *reinterpret_cast<const float4*>(a.gamma_c + ch);
     c[0] = gm.x * (kp[0] * r); c[1] = gm.y * (kp[1] * r);
     c[2] = gm.z * (kp[2] * r); c[3] = gm.w * (kp[3] * r);
-    *reinterpret_cast<float4*>(&sc[e][ch]) = make_float4(c[0], c[1], c[2], c[3]);
+    *reinterpret_cast<float4*>(&sc[g][ch]) = make_float4(c[0], c[1], c[2], c[3]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) z[i] = c[i];
     if (ch >= kD - kDR) {
@@ -118,35 +138,43 @@ __global__ void __launch_bounds__(kWriterThreads) writer_entries_kernel(WriterAr
         z[2 * q + 1] = x0 * sn + x1 * cs;
       }
     }
-    uint16_t packed = fp4_quant4(z, a.z_scales + ((int64_t)b * a.cap + j) * 16 + tid / 8);
-    *reinterpret_cast<uint16_t*>(a.z_codes + ((int64_t)b * a.cap + j) * 256 + 2 * tid) = packed;
-    if (tid == 0) sj[e] = j;
+    uint16_t packed = fp4_quant4(z, a.z_scales + ((int64_t)b * a.cap + j) * 16 + gt / 8);
+    *reinterpret_cast<uint16_t*>(a.z_codes + ((int64_t)b * a.cap + j) * 256 + 2 * gt) = packed;
+  } else {
+    *reinterpret_cast<float4*>(&sc[g][ch]) = make_float4(0.f, 0.f, 0.f, 0.f);  // no entry: zero row
   }
   __syncthreads();
 
-  // ---- phase 2: k^i = c W_IK for the block's entries (thread = output column).  Rows of
-  // sc beyond `ne` hold zeros, so all kEntriesPerBlock accumulators run unconditionally and
-  // stay in registers.
-  DF acc[kEntriesPerBlock];
+  // ---- phase 2: quarter g of k^i = c W_IK for the block's entries (thread = output column)
+  {
+    DF acc[kEntriesPerBlock];
 #pragma unroll
-  for (int e = 0; e < kEntriesPerBlock; ++e) acc[e] = DF{0.f, 0.f};
-  const int o = tid;
+    for (int e = 0; e < kEntriesPerBlock; ++e) acc[e] = DF{0.f, 0.f};
+    const int o = gt;
 #pragma unroll 4
-  for (int d = 0; d < kD; ++d) {
-    const float w = bf16_to_f32(a.w_ik[d * kDI + o]);
+    for (int d = 128 * g; d < 128 * g + 128; ++d) {
+      const float w = bf16_to_f32(a.w_ik[d * kDI + o]);
 #pragma unroll
-    for (int e = 0; e < kEntriesPerBlock; ++e) acc[e].add_prod(sc[e][d], w);
+      for (int e = 0; e < kEntriesPerBlock; ++e) acc[e].add_prod(sc[e][d], w);
+    }
+#pragma unroll
+    for (int e = 0; e < kEntriesPerBlock; ++e) part[g][e][o] = make_float2(acc[e].s, acc[e].c);
   }
+  __syncthreads();
 
-  // ---- phase 3: RMSNorm, RoPE by 2j on dims 64..127, FP4 (unrolled so that acc[] is
-  // indexed at compile time; the guard is uniform across the block)
+  // ---- phase 3: RMSNorm, RoPE by 2j on dims 64..127, FP4 for entry g (thread = output column)
+  if (g < ne) {
+    const int o = gt;
+    DF t{0.f, 0.f};
 #pragma unroll
-  for (int e = 0; e < kEntriesPerBlock; ++e) {
-    if (e >= ne) break;
-    const int64_t j = sj[e];
-    const float ki = acc[e].s + acc[e].c;
-    double ss = block_sum<kWriterThreads>((double)ki * (double)ki, red);
-    const float r = (float)(1.0 / sqrt(ss / kDI + a.eps));
+    for (int q = 0; q < 4; ++q) {
+      t.add_prod(part[q][g][o].x, 1.f);
+      t.add_prod(part[q][g][o].y, 1.f);
+    }
+    const float ki = t.s + t.c;
+    DFSum ssq;
+    ssq.add_sq(ki);
+    const float r = rms_inv(group_sum(ssq, red[g], g), (float)kDI, a.eps);
     float kn = a.gamma_ik[o] * (ki * r);
     const float partner = __shfl_xor_sync(0xffffffffu, kn, 1);
     if (o >= 64) {
@@ -156,7 +184,7 @@ __global__ void __launch_bounds__(kWriterThreads) writer_entries_kernel(WriterAr
     }
     const float amax = warp_max(fabsf(kn));
     const int ex = mx_scale_exp(amax);
-    const uint32_t code = f32_to_e2m1(ldexpf(kn, -ex));
+    const uint32_t code = f32_to_e2m1(kn * pow2f(-ex));
     const uint32_t hi = __shfl_xor_sync(0xffffffffu, code, 1);
     if ((o & 1) == 0) a.ki_codes[((int64_t)b * a.cap + j) * 64 + o / 2] = (uint8_t)(code | (hi << 4));
     if ((o & 31) == 0) a.ki_scales[((int64_t)b * a.cap + j) * 4 + o / 32] = (uint8_t)(ex + 127);
@@ -164,7 +192,8 @@ __global__ void __launch_bounds__(kWriterThreads) writer_entries_kernel(WriterAr
 }
 
 __global__ void __launch_bounds__(kWriterThreads) writer_window_kernel(WriterArgs a, SeqPos pos, int b0, RopeFreq rf) {
-  __shared__ double red[kWriterThreads / 32];
+  __shared__ float2 red[kWriterThreads / 32];
+  __shared__ float r_sh;
   const int t = blockIdx.x;
   const int bl = blockIdx.y;
   const int b = b0 + bl;
@@ -176,11 +205,23 @@ __global__ void __launch_bounds__(kWriterThreads) writer_window_kernel(WriterArg
   uint2 ww = *reinterpret_cast<const uint2*>(a.wa + row * kD + ch);
   float x[4] = {bf16_to_f32(ww.x & 0xffff), bf16_to_f32(ww.x >> 16), bf16_to_f32(ww.y & 0xffff),
                 bf16_to_f32(ww.y >> 16)};
-  double ss = 0.0;
+  DFSum ssq;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) ss += (double)x[i] * (double)x[i];
-  ss = block_sum<kWriterThreads>(ss, red);
-  const float r = (float)(1.0 / sqrt(ss / kD + a.eps));
+  for (int i = 0; i < 4; ++i) ssq.add_sq(x[i]);
+  ssq = warp_sum_df(ssq);
+  if ((tid & 31) == 0) red[tid >> 5] = make_float2(ssq.s, ssq.c);
+  __syncthreads();
+  if (tid == 0) {
+    DFSum tot;
+#pragma unroll
+    for (int i = 0; i < kWriterThreads / 32; ++i) {
+      tot.add(red[i].x);
+      tot.c += red[i].y;
+    }
+    r_sh = rms_inv(tot.value(), (float)kD, a.eps);
+  }
+  __syncthreads();
+  const float r = r_sh;
   float4 gm = *reinterpret_cast<const float4*>(a.gamma_w + ch);
   float y[4] = {gm.x * (x[0] * r), gm.y * (x[1] * r), gm.z * (x[2] * r), gm.w * (x[3] * r)};
   if (ch >= kD - kDR) {
@@ -213,7 +254,7 @@ cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb
   for (int i = 0; i < nb; ++i) max_new = max(max_new, (pos.p0[i] + a.T) / 2 - pos.p0[i] / 2);
   if (max_new > 0) {
     dim3 grid((unsigned)((max_new + kEntriesPerBlock - 1) / kEntriesPerBlock), (unsigned)nb);
-    writer_entries_kernel<<<grid, kWriterThreads, 0, st>>>(a, pos, b0, rf);
+    writer_entries_kernel<<<grid, kEntryThreads, 0, st>>>(a, pos, b0, rf);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
