@@ -64,10 +64,10 @@ def _declare(L: C.CDLL) -> None:
     L.csa2o_rmsnorm.argtypes = [p, p, i32, f64, p]
     L.csa2o_rope.argtypes = [p, i32, f64, f64, i32]
     L.csa2o_write_seq.restype = i64
-    L.csa2o_write_seq.argtypes = [i32, i64, p, p, p, p, p, p, p, f64, f64, p, p, p, p, i64,
+    L.csa2o_write_seq.argtypes = [i32, i32, i64, p, p, p, p, p, p, p, f64, f64, p, p, p, p, i64,
                                   p, p, p, p, p, p, p, p]
     L.csa2o_index_scores.restype = i32
-    L.csa2o_index_scores.argtypes = [i32, p, p, p, p, p, i64, p, i64, p, p]
+    L.csa2o_index_scores.argtypes = [i32, i32, p, p, p, p, p, i64, p, i64, p, p]
     L.csa2o_topk.restype = i32
     L.csa2o_topk.argtypes = [i32, p, p, i64, i32, p, p, p]
     L.csa2o_attend.restype = i32
@@ -140,8 +140,9 @@ def rope(x, pos, base=10000.0, inverse=False):
 # ------------------------------------------------------------------ layer pieces
 def write_seq(kc, gc, wa, gamma_c, w_ik, gamma_ik, gamma_w, p0, cap, *, z_codes=None,
               z_scales=None, ki_codes=None, ki_scales=None, pair_k=None, pair_g=None,
-              window_prefix=None, base=10000.0, eps=1e-20):
-    """Append T tokens (positions p0..p0+T-1) to one sequence's caches.
+              window_prefix=None, base=10000.0, eps=1e-20, ratio=2):
+    """Append T tokens (positions p0..p0+T-1) to one sequence's caches.  ``ratio`` is the
+    layer's compression ratio: 2 (entry j pools tokens 2j, 2j+1) or 1 (entry j is token j).
 
     kc, gc, wa: [T, 512] float arrays.  The caches are created (zero) when not given and
     updated in place.  ``pair_k``/``pair_g`` hold the buffered token p0-1 when p0 is odd.
@@ -158,45 +159,46 @@ def write_seq(kc, gc, wa, gamma_c, w_ik, gamma_ik, gamma_w, p0, cap, *, z_codes=
     window = np.zeros((127 + T, D), np.uint8)
     if window_prefix is not None:
         window[:127] = window_prefix
-    n_new = sum(1 for t in range(T) if (p0 + t) % 2 == 1)
+    n_new = sum(1 for t in range(T) if (p0 + t) % ratio == ratio - 1)
     z_pre = np.zeros((max(n_new, 1), D))
     ki_pre = np.zeros((max(n_new, 1), DI))
     win_pre = np.zeros((T, D))
     pk_in = None if pair_k is None else _c(pair_k, np.float32)
     pg_in = None if pair_g is None else _c(pair_g, np.float32)
-    if p0 % 2 == 1 and pk_in is None:
+    if ratio == 2 and p0 % 2 == 1 and pk_in is None:
         raise ValueError("p0 is odd: the pair buffer (token p0-1) is required")
     pk_out = np.zeros(D, np.float32)
     pg_out = np.zeros(D, np.float32)
     g = [_c(a, np.float32) for a in (gamma_c, w_ik, gamma_ik, gamma_w)]
-    n = lib().csa2o_write_seq(T, int(p0), _ptr(kc), _ptr(gc), _ptr(wa), *(_ptr(a) for a in g),
+    n = lib().csa2o_write_seq(int(ratio), T, int(p0), _ptr(kc), _ptr(gc), _ptr(wa), *(_ptr(a) for a in g),
                               base, eps, _ptr(pk_in), _ptr(pg_in), _ptr(pk_out), _ptr(pg_out),
                               cap, _ptr(z_codes), _ptr(z_scales), _ptr(ki_codes),
                               _ptr(ki_scales), _ptr(window), _ptr(z_pre), _ptr(ki_pre),
                               _ptr(win_pre))
     if n < 0:
         raise ValueError("cache capacity too small")
-    pair = (pk_out, pg_out) if (p0 + T) % 2 == 1 else None
+    pair = (pk_out, pg_out) if ratio == 2 and (p0 + T) % 2 == 1 else None
     return dict(z_codes=z_codes, z_scales=z_scales, ki_codes=ki_codes, ki_scales=ki_scales,
                 window=window, pair=pair, z_pre=z_pre[:n], ki_pre=ki_pre[:n], win_pre=win_pre,
-                first_entry=p0 // 2, n_entries=int(n))
+                first_entry=p0 // ratio, n_entries=int(n))
 
 
-def index_scores(pos, qi, wI, ki_codes, ki_scales, n_entries, return_qi_codes=False):
+def index_scores(pos, qi, wI, ki_codes, ki_scales, n_entries, return_qi_codes=False, ratio=2):
     """fp64 indexer scores for query rows at absolute positions ``pos``.
 
-    qi [nq,32,128], wI [nq,32].  Returns scores [nq, max E] with NaN beyond E_r.
+    qi [nq,32,128], wI [nq,32].  Returns scores [nq, max E] with NaN beyond E_r =
+    floor((pos+1)/ratio).
     """
     pos = _c(pos, np.int64)
     qi = _c(qi, np.float32)
     wI = _c(wI, np.float32)
     nq = pos.size
-    E = (pos + 1) // 2
+    E = (pos + 1) // ratio
     ld = max(int(E.max()) if nq else 0, 1)
     scores = np.full((nq, ld), np.nan)
     qc = np.empty((nq, HI, 64), np.uint8) if return_qi_codes else None
     qs = np.empty((nq, HI, 4), np.uint8) if return_qi_codes else None
-    rc = lib().csa2o_index_scores(nq, _ptr(pos), _ptr(qi), _ptr(wI), _ptr(_c(ki_codes, np.uint8)),
+    rc = lib().csa2o_index_scores(int(ratio), nq, _ptr(pos), _ptr(qi), _ptr(wI), _ptr(_c(ki_codes, np.uint8)),
                                   _ptr(_c(ki_scales, np.uint8)), int(n_entries), _ptr(scores), ld,
                                   _ptr(qc), _ptr(qs))
     if rc != 0:

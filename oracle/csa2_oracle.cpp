@@ -154,13 +154,20 @@ constexpr int H = 64;      // attention heads
 constexpr int WIN = 128;   // window rows
 constexpr int TOPK = 512;  // selected entries
 
-// One pooled entry j from tokens (2j, 2j+1): [PG] k^p, c, Z, k^i, k^n, K^I.
-void write_entry(const float* k0, const float* g0, const float* k1, const float* g1, int64_t j,
+// One compressed entry from its tokens: [PG] k^p, c, Z, k^i, k^n, K^I.  At compression
+// ratio 2 the entry j pools tokens (2j, 2j+1) (k0/g0 and k1/g1); at ratio 1 it is token j
+// itself (k0 == nullptr: the softmax over one token is 1, so k^p = k^c).  rope_pos is the
+// position the entry is rotated by: r * j.
+void write_entry(const float* k0, const float* g0, const float* k1, const float* g1, double rope_pos,
                  const float* gamma_c, const float* w_ik, const float* gamma_ik, double base,
                  double eps, uint8_t* zc, uint8_t* zs, uint8_t* kc, uint8_t* ks, double* z_pre,
                  double* ki_pre) {
   double kp[D], c[D], z[D], ki[DI], kn[DI];
   for (int ch = 0; ch < D; ++ch) {
+    if (!k0) {
+      kp[ch] = k1[ch];
+      continue;
+    }
     // softmax over the two tokens of the pair, per channel
     double a = g0[ch], b = g1[ch], m = std::max(a, b);
     double ea = std::exp(a - m), eb = std::exp(b - m);
@@ -169,7 +176,7 @@ void write_entry(const float* k0, const float* g0, const float* k1, const float*
   }
   rmsnorm(kp, gamma_c, D, eps, c);
   std::memcpy(z, c, sizeof z);
-  rope(z + (D - DR), DR, 2.0 * j, base, 1.0);
+  rope(z + (D - DR), DR, rope_pos, base, 1.0);
   if (z_pre) std::memcpy(z_pre, z, sizeof z);
   mx_row(z, D, zc, zs);
   for (int o = 0; o < DI; ++o) {
@@ -178,7 +185,7 @@ void write_entry(const float* k0, const float* g0, const float* k1, const float*
     ki[o] = s;
   }
   rmsnorm(ki, gamma_ik, DI, eps, kn);
-  rope(kn + 64, DI - 64, 2.0 * j, base, 1.0);
+  rope(kn + 64, DI - 64, rope_pos, base, 1.0);
   if (ki_pre) std::memcpy(ki_pre, kn, sizeof kn);
   mx_row(kn, DI, kc, ks);
 }
@@ -205,7 +212,8 @@ void csa2o_rmsnorm(const double* x, const float* gamma, int n, double eps, doubl
 void csa2o_rope(double* x, int d, double pos, double base, int inverse) { rope(x, d, pos, base, inverse ? -1.0 : 1.0); }
 
 // ---------------------------------------------------------------- writer, one sequence
-// Appends T tokens at absolute positions p0 .. p0+T-1.
+// Appends T tokens at absolute positions p0 .. p0+T-1 to a layer of compression ratio
+// `ratio` (2: entry j pools tokens 2j, 2j+1; 1: entry j is token j, no pair buffer).
 //  kc, gc, wa: [T, 512]; pair_k_in/pair_g_in: the buffered token p0-1 (needed iff p0 odd);
 //  pair_k_out/pair_g_out: receive token p0+T-1 iff p0+T is odd (may alias the inputs).
 //  z_codes [cap,256], z_scales [cap,16], ki_codes [cap,64], ki_scales [cap,4]: this
@@ -213,19 +221,20 @@ void csa2o_rope(double* x, int d, double pos, double base, int inverse) { rope(x
 //  window [127+T, 512]: row r holds position p0-127+r; rows 127.. are written here.
 //  z_pre [n_new,512], ki_pre [n_new,128], win_pre [T,512] (optional): the fp64 values just
 //  before FP4 / FP8, for the near-boundary rule of the parity tests.
-// Returns the number of entries written; their first index is floor(p0/2).
-int64_t csa2o_write_seq(int T, int64_t p0, const float* kc, const float* gc, const float* wa,
+// Returns the number of entries written; their first index is floor(p0/ratio).
+int64_t csa2o_write_seq(int ratio, int T, int64_t p0, const float* kc, const float* gc, const float* wa,
                         const float* gamma_c, const float* w_ik, const float* gamma_ik,
                         const float* gamma_w, double base, double eps, const float* pair_k_in,
                         const float* pair_g_in, float* pair_k_out, float* pair_g_out,
                         int64_t cap, uint8_t* z_codes, uint8_t* z_scales, uint8_t* ki_codes,
                         uint8_t* ki_scales, uint8_t* window, double* z_pre, double* ki_pre,
                         double* win_pre) {
-  int64_t j0 = p0 / 2;
-  // entries completed by this call: j with p0 <= 2j+1 <= p0+T-1
+  if (ratio != 1 && ratio != 2) return -1;
+  int64_t j0 = p0 / ratio;
+  // entries completed by this call: j whose last token ratio*j + ratio-1 is in p0 .. p0+T-1
   std::vector<int64_t> js;
   for (int t = 0; t < T; ++t)
-    if ((p0 + t) % 2 == 1) js.push_back((p0 + t - 1) / 2);
+    if ((p0 + t) % ratio == ratio - 1) js.push_back((p0 + t) / ratio);
   for (int64_t j : js)
     if (j >= cap) return -1;
   std::vector<float> keep_k(D), keep_g(D);
@@ -237,16 +246,18 @@ int64_t csa2o_write_seq(int T, int64_t p0, const float* kc, const float* gc, con
 #pragma omp parallel for schedule(dynamic)
   for (int64_t n = 0; n < (int64_t)js.size(); ++n) {
     int64_t j = js[n];
-    int64_t t1 = 2 * j + 1 - p0;  // local index of the odd token
-    const float *k0, *g0;
-    if (t1 >= 1) {
-      k0 = kc + (t1 - 1) * D;
-      g0 = gc + (t1 - 1) * D;
-    } else {
-      k0 = keep_k.data();
-      g0 = keep_g.data();
+    int64_t t1 = ratio * j + ratio - 1 - p0;  // local index of the entry's last token
+    const float *k0 = nullptr, *g0 = nullptr;
+    if (ratio == 2) {
+      if (t1 >= 1) {
+        k0 = kc + (t1 - 1) * D;
+        g0 = gc + (t1 - 1) * D;
+      } else {
+        k0 = keep_k.data();
+        g0 = keep_g.data();
+      }
     }
-    write_entry(k0, g0, kc + t1 * D, gc + t1 * D, j, gamma_c, w_ik, gamma_ik, base, eps,
+    write_entry(k0, g0, kc + t1 * D, gc + t1 * D, (double)(ratio * j), gamma_c, w_ik, gamma_ik, base, eps,
                 z_codes + j * 256, z_scales + j * 16, ki_codes + j * 64, ki_scales + j * 4,
                 z_pre ? z_pre + (j - j0) * D : nullptr, ki_pre ? ki_pre + (j - j0) * DI : nullptr);
   }
@@ -261,7 +272,7 @@ int64_t csa2o_write_seq(int T, int64_t p0, const float* kc, const float* gc, con
     uint8_t* row = window + (int64_t)(127 + t) * D;
     for (int i = 0; i < D; ++i) row[i] = (uint8_t)e4m3_encode(y[i]);
   }
-  if ((p0 + T) % 2 == 1 && pair_k_out && pair_g_out) {
+  if (ratio == 2 && (p0 + T) % 2 == 1 && pair_k_out && pair_g_out) {
     std::memcpy(pair_k_out, kc + (int64_t)(T - 1) * D, D * sizeof(float));
     std::memcpy(pair_g_out, gc + (int64_t)(T - 1) * D, D * sizeof(float));
   }
@@ -270,14 +281,16 @@ int64_t csa2o_write_seq(int T, int64_t p0, const float* kc, const float* gc, con
 
 // ---------------------------------------------------------------- indexer scores
 // Query rows at absolute positions pos[r]: Q^I qi [nq,32,128], w^I wI [nq,32].
-// S^I_{t,j} = sum_h w^I_{t,h} ReLU(Q^I_{h,t} . K^I_j) for j < floor((t+1)/2)  ([PG] S^I, I_t).
-// scores [nq, ld]: row r gets E_r = floor((pos+1)/2) values; the rest is left untouched.
+// S^I_{t,j} = sum_h w^I_{t,h} ReLU(Q^I_{h,t} . K^I_j) for j < floor((t+1)/ratio)  ([PG] S^I,
+// I_t; an entry is visible once its last token is).
+// scores [nq, ld]: row r gets E_r = floor((pos+1)/ratio) values; the rest is left untouched.
 // qi_codes [nq,32,64] / qi_scales [nq,32,4] (optional): the FP4 form of Q^I.
-int csa2o_index_scores(int nq, const int64_t* pos, const float* qi, const float* wI,
+int csa2o_index_scores(int ratio, int nq, const int64_t* pos, const float* qi, const float* wI,
                        const uint8_t* ki_codes, const uint8_t* ki_scales, int64_t n_entries,
                        double* scores, int64_t ld, uint8_t* qi_codes, uint8_t* qi_scales) {
+  if (ratio != 1 && ratio != 2) return -1;
   for (int r = 0; r < nq; ++r)
-    if ((pos[r] + 1) / 2 > n_entries || (pos[r] + 1) / 2 > ld) return -1;
+    if ((pos[r] + 1) / ratio > n_entries || (pos[r] + 1) / ratio > ld) return -1;
 #pragma omp parallel for schedule(dynamic)
   for (int r = 0; r < nq; ++r) {
     std::vector<double> qv(HI * DI), kv(DI), q64(DI);
@@ -289,7 +302,7 @@ int csa2o_index_scores(int nq, const int64_t* pos, const float* qi, const float*
       if (qi_codes) std::memcpy(qi_codes + ((int64_t)r * HI + h) * 64, c, 64);
       if (qi_scales) std::memcpy(qi_scales + ((int64_t)r * HI + h) * 4, s, 4);
     }
-    int64_t E = (pos[r] + 1) / 2;
+    int64_t E = (pos[r] + 1) / ratio;
     for (int64_t j = 0; j < E; ++j) {
       mx_row_decode(ki_codes + j * 64, ki_scales + j * 4, DI, kv.data());
       double sc = 0.0;

@@ -216,6 +216,63 @@ def test_writer_entries_and_pair_buffer_split_calls():
     assert full["n_entries"] == T // 2
 
 
+def test_writer_ratio1_matches_ratio2_pool_of_equal_tokens():
+    # Compression ratio 1 (decoder owner layers): entry j is token j itself, rotated by j.
+    # A ratio-2 entry m pooled from two copies of the same token has softmax weights summing
+    # to 1, so it equals that token's ratio-1 entry when both are rotated by the same position:
+    # ratio-1 entry 2m (token at position 2m) vs ratio-2 entry m (tokens 2m, 2m+1 equal).
+    rng = np.random.default_rng(11)
+    T = 8
+    kc = rng.standard_normal((T, 512)).astype(np.float32)
+    gc = rng.standard_normal((T, 512)).astype(np.float32)
+    wa = rng.standard_normal((T, 512)).astype(np.float32)
+    prm = _writer_params(seed=11)
+    r1 = oracle.write_seq(kc, gc, wa, p0=0, cap=T, ratio=1, **prm)
+    assert r1["n_entries"] == T and r1["first_entry"] == 0 and r1["pair"] is None
+    kc2 = np.repeat(kc[0::2], 2, axis=0)   # tokens 2m and 2m+1 both = token 2m
+    gc2 = rng.standard_normal((T, 512)).astype(np.float32)  # any gates: the weights sum to 1
+    r2 = oracle.write_seq(kc2, gc2, wa, p0=0, cap=T, ratio=2, **prm)
+    assert r2["n_entries"] == T // 2
+    # equal up to fp64 rounding of the pooled sum (w0 k + w1 k vs k)
+    assert np.allclose(r1["z_pre"][0::2], r2["z_pre"], rtol=0, atol=1e-12)
+    assert np.allclose(r1["ki_pre"][0::2], r2["ki_pre"], rtol=0, atol=1e-12)
+    # the window does not depend on the ratio
+    assert np.array_equal(r1["window"], r2["window"])
+
+
+def test_writer_ratio1_ignores_gates_and_splits_anywhere():
+    rng = np.random.default_rng(12)
+    T = 9
+    kc, gc, wa = (rng.standard_normal((T, 512)).astype(np.float32) for _ in range(3))
+    prm = _writer_params(seed=12)
+    full = oracle.write_seq(kc, gc, wa, p0=5, cap=20, ratio=1, **prm)
+    other_gates = oracle.write_seq(kc, -3 * gc, wa, p0=5, cap=20, ratio=1, **prm)
+    for k in ("z_codes", "z_scales", "ki_codes", "ki_scales"):
+        assert np.array_equal(full[k], other_gates[k])
+    assert full["first_entry"] == 5 and full["n_entries"] == T
+    # entries are single tokens: any split point, no pair buffer
+    a = oracle.write_seq(kc[:4], gc[:4], wa[:4], p0=5, cap=20, ratio=1, **prm)
+    b = oracle.write_seq(kc[4:], gc[4:], wa[4:], p0=9, cap=20, ratio=1, z_codes=a["z_codes"],
+                         z_scales=a["z_scales"], ki_codes=a["ki_codes"], ki_scales=a["ki_scales"], **prm)
+    for k in ("z_codes", "z_scales", "ki_codes", "ki_scales"):
+        assert np.array_equal(full[k], b[k])
+
+
+def test_index_causal_bound_ratio1():
+    rng = np.random.default_rng(13)
+    kc, ks = oracle.mx_quantize(rng.standard_normal((60, 128)))
+    pos = np.array([0, 1, 2, 58, 59])
+    s = oracle.index_scores(pos, rng.standard_normal((5, 32, 128)).astype(np.float32),
+                            rng.standard_normal((5, 32)).astype(np.float32), kc, ks, 60, ratio=1)
+    for r, p in enumerate(pos):
+        E = p + 1   # at ratio 1 every token is an entry: j <= t
+        assert np.all(np.isfinite(s[r, :E])) and np.all(np.isnan(s[r, E:]))
+    # the same keys at ratio 2 see only floor((t+1)/2) of them
+    s2 = oracle.index_scores(pos, rng.standard_normal((5, 32, 128)).astype(np.float32),
+                             rng.standard_normal((5, 32)).astype(np.float32), kc, ks, 60, ratio=2)
+    assert np.isnan(s2[-1, 30:]).all() and np.isfinite(s2[-1, :30]).all()
+
+
 # ---------------------------------------------------------------- indexer + top-k
 def _const_keys(vals):
     """K^I rows whose 128 values all equal vals[j] (a value on the E2M1 grid, scale 1)."""
