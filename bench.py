@@ -76,25 +76,25 @@ def seed_for_rank(base: int, rank: int) -> int:
 
 
 # ------------------------------------------------------------------ work models
-def attention_rows(p0: int, T: int) -> np.ndarray:
+def attention_rows(p0: int, T: int, ratio: int = 2) -> np.ndarray:
     t = p0 + np.arange(T, dtype=np.int64)
-    return np.minimum(128, t + 1) + np.minimum(512, (t + 1) // 2)
+    return np.minimum(128, t + 1) + np.minimum(512, (t + 1) // ratio)
 
 
-def attention_flops(B: int, p0: int, T: int) -> float:
+def attention_flops(B: int, p0: int, T: int, ratio: int = 2) -> float:
     """QG^T and AG: 2 * 2 * 64 * n_t * 512 flops per query."""
-    return float(B * 4 * H * D * attention_rows(p0, T).sum())
+    return float(B * 4 * H * D * attention_rows(p0, T, ratio).sum())
 
 
-def indexer_pairs(B: int, p0: int, T: int) -> int:
+def indexer_pairs(B: int, p0: int, T: int, ratio: int = 2) -> int:
     t = p0 + np.arange(T, dtype=np.int64)
-    return int(B * ((t + 1) // 2).sum())
+    return int(B * ((t + 1) // ratio).sum())
 
 
-def decode_bytes(B: int, p0: int) -> dict:
+def decode_bytes(B: int, p0: int, ratio: int = 2) -> dict:
     """Algorithmic HBM bytes of one decode step (T=1): indexer keys over all visible entries,
     the 512 selected Z rows, 128 window rows, Q, Q^I, w^I, the output, the step's writes."""
-    E = (p0 + 1) // 2
+    E = (p0 + 1) // ratio
     k = min(512, E)
     idx_keys = B * E * 68
     rows = B * (k * 272 + min(128, p0 + 1) * 512)
@@ -180,9 +180,9 @@ class Step:
         x = {}
         x.update(inputs.layer_params(seed, dev))
         x.update(inputs.step_inputs(wl.B, wl.T, seed, dev))
-        x.update(inputs.cache_state(wl.B, wl.T, wl.p0, wl.cap, seed, dev))
+        x.update(inputs.cache_state(wl.B, wl.T, wl.p0, wl.cap, seed, dev, wl.ratio))
         self.x = x
-        self.h = csa2.csa2_create()
+        self.h = csa2.csa2_create(ratio=wl.ratio)
         self.p0 = [wl.p0] * wl.B
         self.idx = torch.empty(wl.B, wl.T, 512, dtype=torch.int32, device=dev)
         self.out = torch.empty(wl.B, wl.T, H, D, dtype=torch.bfloat16, device=dev)
@@ -318,7 +318,7 @@ def run_ours(args, rank, ws):
     ms, per, launches = time_workload(step, args.steps, args.warmup, ws, flush, clocks)
     ms_max = max_over_ranks(ms, ws)
     att_ms = max_over_ranks(per["attend"], ws)
-    flops = attention_flops(wl.B, wl.p0, wl.T)
+    flops = attention_flops(wl.B, wl.p0, wl.T, wl.ratio)
     achieved = flops / (att_ms / 1e3) / 1e12
     e2e = time_e2e(step, max(2, args.steps // 2), 1)
     e2e["value"] *= ws
@@ -340,23 +340,27 @@ def run_ours(args, rank, ws):
     }
     del step
     torch.cuda.empty_cache()
-    if not args.no_decode:
-        dw = inputs.WORKLOADS[args.decode_workload]
+    # decode objects: the ratio-2 layer at 1M tokens, and a ratio-1 (decoder owner) layer
+    for key, name in (("decode", args.decode_workload), ("decode_ratio1", args.ratio1_workload)):
+        if args.no_decode or not name:
+            continue
+        dw = inputs.WORKLOADS[name]
         dstep = Step(csa2, inputs, dw, seed_for_rank(dw.seed, rank), dev)
         dms, dper, dlaunches = time_workload(dstep, args.steps, args.warmup, ws, flush)
         dms = max_over_ranks(dms, ws)
         idx_ms = max_over_ranks(dper["index"], ws)
-        by = decode_bytes(dw.B, dw.p0)
-        line["decode"] = {
-            "workload": dw.name, "B": dw.B, "p0": dw.p0, "value": ws * dw.B / (dms / 1e3), "unit": "tok/s",
-            "ms_per_step": dms, "kernels_ms": dper,
+        by = decode_bytes(dw.B, dw.p0, dw.ratio)
+        line[key] = {
+            "workload": dw.name, "B": dw.B, "p0": dw.p0, "ratio": dw.ratio, "value": ws * dw.B / (dms / 1e3),
+            "unit": "tok/s", "ms_per_step": dms, "kernels_ms": dper,
             "roofline_step": {"bound": "hbm", "achieved": by["step"] / (dms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
                               "frac": by["step"] / (dms / 1e3) / 1e9 / hbm, "bytes": by["step"]},
             "roofline_index": {"bound": "hbm", "achieved": by["indexer"] / (idx_ms / 1e3) / 1e9, "peak": hbm,
                                "unit": "GB/s", "frac": by["indexer"] / (idx_ms / 1e3) / 1e9 / hbm,
                                "bytes": by["indexer"], "peak_source": f"{src} copy bandwidth",
                                "traffic": profiled_traffic("index_decode_decode_1m.md",
-                                                           [CSRC + "csa2_index_tc.cu", CSRC + "csa2_indexer.cu"])},
+                                                           [CSRC + "csa2_index_tc.cu", CSRC + "csa2_indexer.cu"])
+                               if name == "decode_1m" else None},
             "gpu_launches": dlaunches,
         }
         del dstep
@@ -376,7 +380,7 @@ def cpu_baseline(wl, budget_s: float = 15.0, n_rows: int | None = None) -> dict:
     x = {}
     x.update(inputs.layer_params(wl.seed, "cpu"))
     x.update(inputs.step_inputs(wl.B, wl.T, wl.seed, "cpu"))
-    x.update(inputs.cache_state(wl.B, wl.T, wl.p0, wl.cap, wl.seed, "cpu"))
+    x.update(inputs.cache_state(wl.B, wl.T, wl.p0, wl.cap, wl.seed, "cpu", wl.ratio))
     f = lambda t: t.float().numpy()
     cores = os.cpu_count()
     t0 = time.perf_counter()
@@ -384,7 +388,7 @@ def cpu_baseline(wl, budget_s: float = 15.0, n_rows: int | None = None) -> dict:
                          f(x["gamma_w"]), wl.p0, wl.cap, z_codes=x["z_codes"][0].numpy(),
                          z_scales=x["z_scales"][0].numpy(), ki_codes=x["ki_codes"][0].numpy(),
                          ki_scales=x["ki_scales"][0].numpy(), pair_k=f(x["pair_kc"][0]), pair_g=f(x["pair_gc"][0]),
-                         window_prefix=x["window"][0, :127].numpy())
+                         window_prefix=x["window"][0, :127].numpy(), ratio=wl.ratio)
     t_write = time.perf_counter() - t0
     # rows: spread over the step; grow the sample until the budget is used
     rows_done, t_rows = 0, 0.0
@@ -394,8 +398,9 @@ def cpu_baseline(wl, budget_s: float = 15.0, n_rows: int | None = None) -> dict:
         r = np.sort(rng.choice(wl.T, size=min(n, wl.T), replace=False))
         pos = wl.p0 + r
         t1 = time.perf_counter()
-        sc = oracle.index_scores(pos, f(x["qi"][0][r]), f(x["wI"][0][r]), w["ki_codes"], w["ki_scales"], wl.cap)
-        oidx, _, _ = oracle.topk(sc, (pos + 1) // 2)
+        sc = oracle.index_scores(pos, f(x["qi"][0][r]), f(x["wI"][0][r]), w["ki_codes"], w["ki_scales"], wl.cap,
+                                 ratio=wl.ratio)
+        oidx, _, _ = oracle.topk(sc, (pos + 1) // wl.ratio)
         oracle.attend(pos, f(x["q"][0][r]), f(x["sinks"]), w["z_codes"], w["z_scales"], wl.cap, w["window"],
                       wl.p0 - 127, oidx)
         t_rows += time.perf_counter() - t1
@@ -440,6 +445,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_4k")
     ap.add_argument("--decode-workload", default="decode_1m")
+    ap.add_argument("--ratio1-workload", default="decode_512k_r1", help="empty: skip the ratio-1 decode object")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

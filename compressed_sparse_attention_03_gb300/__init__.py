@@ -108,10 +108,11 @@ def _stream(stream):
 class Handle:
     """Owns a csa2_handle (created on the current CUDA device)."""
 
-    def __init__(self, rope_base: float = 10000.0, eps: float = 1e-20):
+    def __init__(self, rope_base: float = 10000.0, eps: float = 1e-20, ratio: int = 2):
         cfg = csa2_config()
         lib().csa2_default_config(C.byref(cfg))
-        cfg.rope_base, cfg.eps = rope_base, eps
+        cfg.rope_base, cfg.eps, cfg.ratio = rope_base, eps, ratio
+        self.ratio = ratio
         h = C.c_void_p()
         _check("csa2_create", lib().csa2_create(C.byref(cfg), C.byref(h)))
         self._h = h
@@ -132,8 +133,8 @@ class Handle:
             pass
 
 
-def csa2_create(rope_base: float = 10000.0, eps: float = 1e-20) -> Handle:
-    return Handle(rope_base, eps)
+def csa2_create(rope_base: float = 10000.0, eps: float = 1e-20, ratio: int = 2) -> Handle:
+    return Handle(rope_base, eps, ratio)
 
 
 def csa2_kernel_launches() -> int:
@@ -172,7 +173,7 @@ def csa2_index_topk(h: Handle, qi, wI, ki_codes, ki_scales, p0, idx, top_scores=
     p0a = _host_p0(p0, B)
     cap = ki_codes.shape[1]
     if ws is None:
-        ws = workspace(h, OP_INDEX_TOPK, B, T, int(((p0a + T) // 2).max()), qi.device)
+        ws = workspace(h, OP_INDEX_TOPK, B, T, int(((p0a + T) // h.ratio).max()), qi.device)
     _check("csa2_index_topk", lib().csa2_index_topk(
         h.ptr, _dev(qi, torch.bfloat16, "qi"), _dev(wI, torch.bfloat16, "wI"), _dev(ki_codes, torch.uint8, "ki_codes"),
         _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,

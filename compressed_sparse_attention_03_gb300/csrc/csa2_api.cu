@@ -15,6 +15,7 @@ struct csa2_handle {
   csa2::RopeFreq rf;
   int device;
   int num_sms;
+  int rshift;  // log2 of the compression ratio (0: ratio 1, 1: ratio 2)
 };
 
 namespace {
@@ -38,10 +39,10 @@ csa2::SeqPos pack_pos(const int64_t* p0, int b0, int nb) {
 
 csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
 
-// Largest visible-entry count over the batch for queries p0..p0+T-1: floor((p0+T)/2).
-int64_t max_visible(const int64_t* p0, int B, int T) {
+// Largest visible-entry count over the batch for queries p0..p0+T-1: floor((p0+T)/ratio).
+int64_t max_visible(const int64_t* p0, int B, int T, int rshift) {
   int64_t m = 0;
-  for (int b = 0; b < B; ++b) m = std::max<int64_t>(m, (p0[b] + T) / 2);
+  for (int b = 0; b < B; ++b) m = std::max<int64_t>(m, (p0[b] + T) >> rshift);
   return m;
 }
 
@@ -79,13 +80,14 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_handle** out) {
   *out = nullptr;
   if (!cfg) return CSA2_ERR_INVALID_ARG;
   if (cfg->heads != 64 || cfg->head_dim != 512 || cfg->rope_dims != 64 || cfg->idx_heads != 32 || cfg->idx_dim != 128 ||
-      cfg->window != 128 || cfg->topk != 512 || cfg->ratio != 2)
+      cfg->window != 128 || cfg->topk != 512 || (cfg->ratio != 1 && cfg->ratio != 2))
     return CSA2_ERR_UNSUPPORTED;
   if (!(cfg->rope_base > 1.0) || !std::isfinite(cfg->rope_base) || !(cfg->eps >= 0.0) || !std::isfinite(cfg->eps))
     return CSA2_ERR_INVALID_ARG;
   csa2_handle* h = new (std::nothrow) csa2_handle;
   if (!h) return CSA2_ERR_INVALID_ARG;
   h->cfg = *cfg;
+  h->rshift = cfg->ratio == 2 ? 1 : 0;
   for (int i = 0; i < csa2::kDR / 2; ++i) h->rf.inv_freq[i] = std::pow(cfg->rope_base, -2.0 * i / csa2::kDR);
   if (cudaGetDevice(&h->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
@@ -135,10 +137,11 @@ csa2_status csa2_write_cache(csa2_handle* h, const uint16_t* kc, const uint16_t*
   if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
   csa2_status st = check_p0(p0, B, T);
   if (st != CSA2_OK) return st;
-  bool need_pair = (T & 1) != 0;
+  const int rs = h->rshift;
+  bool need_pair = rs == 1 && (T & 1) != 0;  // the pair buffer exists at ratio 2 only
   for (int b = 0; b < B; ++b) {
-    if (p0[b] & 1) need_pair = true;
-    if ((p0[b] + T) / 2 > cap) return CSA2_ERR_SHAPE;  // last entry index floor((p0+T)/2)-1 < cap
+    if (rs == 1 && (p0[b] & 1)) need_pair = true;
+    if ((p0[b] + T) >> rs > cap) return CSA2_ERR_SHAPE;  // last entry floor((p0+T)/ratio)-1 < cap
   }
   if (need_pair && (!pair_kc || !pair_gc)) return CSA2_ERR_INVALID_ARG;
   const void* ptrs[] = {kc, gc, wa, gamma_c, w_ik, gamma_ik, gamma_w, z_codes, z_scales, ki_codes, ki_scales, window};
@@ -152,7 +155,7 @@ csa2_status csa2_write_cache(csa2_handle* h, const uint16_t* kc, const uint16_t*
     a.gamma_c = gamma_c; a.gamma_ik = gamma_ik; a.gamma_w = gamma_w;
     a.pair_kc = pair_kc; a.pair_gc = pair_gc;
     a.z_codes = z_codes; a.z_scales = z_scales; a.ki_codes = ki_codes; a.ki_scales = ki_scales; a.window = window;
-    a.cap = cap; a.T = T; a.eps = h->cfg.eps;
+    a.cap = cap; a.T = T; a.rshift = rs; a.eps = h->cfg.eps;
     st = cuda_status(csa2::launch_writer(a, pack_pos(p0, b0, nb), b0, nb, h->rf, reinterpret_cast<cudaStream_t>(stream)));
     if (st != CSA2_OK) return st;
   }
@@ -166,7 +169,7 @@ csa2_status csa2_index_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* 
   if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
   csa2_status st = check_p0(p0, B, T);
   if (st != CSA2_OK) return st;
-  const int64_t emax = max_visible(p0, B, T);
+  const int64_t emax = max_visible(p0, B, T, h->rshift);
   if (emax > cap) return CSA2_ERR_SHAPE;
   if (emax > (int64_t(1) << 20)) return CSA2_ERR_UNSUPPORTED;
   const void* ptrs[] = {qi, wI, ki_codes, ki_scales, idx};
@@ -178,6 +181,7 @@ csa2_status csa2_index_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* 
   if (!aligned16(ws)) return CSA2_ERR_ALIGN;
   csa2::IndexArgs a{};
   a.qi = qi; a.wI = wI; a.ki_codes = ki_codes; a.ki_scales = ki_scales; a.cap = cap; a.T = T;
+  a.rshift = h->rshift;
   a.idx = idx; a.top_scores = top_scores;
   for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
     const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);

@@ -326,8 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         mbar_wait(&bars.p_full, i & 1, err, 4);
         tc_fence_after();
         // O^T tiles one after the other (each frees its two atoms for the next chunk), then the
-        // row sums
-        for (int m = 0; m < 4; ++m) {
+        // row sums.  Order 0, 2, 1, 3: the two producer halves refill tiles {0,1} and {2,3}, so
+        // both get a free tile early and the paired atom waits above are met sooner.
+        for (int mi = 0; mi < 4; ++mi) {
+          const int m = ((mi & 1) << 1) | (mi >> 1);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_f16_ss(tmem + 64 * m, sw128_desc(gg + 2 * m * 16384 + kk * 2048, 16384, 1024),

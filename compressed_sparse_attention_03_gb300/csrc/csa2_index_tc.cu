@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
   // key tiles needed by query tile qt of sequence bl: entries visible to its last query
   auto n_key_tiles = [&](int bl, int qt) {
     const int tlast = min(tq, (qt + 1) * kQPerTile) - 1;
-    const int64_t E = (pos.p0[bl] + t0 + tlast + 1) / 2;
+    const int64_t E = (pos.p0[bl] + t0 + tlast + 1) >> a.rshift;
     return (int)((E + 127) / 128);
   };
 
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
           float s = 0.f;
 #pragma unroll
           for (int h = 0; h < 32; ++h) s = fmaf(wsm[32 * q + h], fmaxf(__uint_as_float(u[h]), 0.f), s);
-          if (tl < tq && j < (p0 + tl + 1) / 2) scores[((int64_t)bl * Tq + tl) * ld + j] = s;
+          if (tl < tq && j < ((p0 + tl + 1) >> a.rshift)) scores[((int64_t)bl * Tq + tl) * ld + j] = s;
         }
         tc_fence_before();
         __syncwarp();
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   const int bl = blockIdx.x / per_seq, part = blockIdx.x % per_seq;
   const bool active = bl < nb;
   const int b = b0 + (active ? bl : 0);
-  const int64_t E = active ? (pos.p0[bl] + 1) / 2 : 0;  // visible entries of the one query
+  const int64_t E = active ? (pos.p0[bl] + 1) >> a.rshift : 0;  // visible entries of the one query
   const int ntile = (int)((E + 127) / 128);
   const int tpb = (ntile + per_seq - 1) / per_seq;
   const int t_begin = min(ntile, part * tpb), t_end = min(ntile, t_begin + tpb);

@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(IndexArgs a, SeqPo
   // visible entries of the last query of the tile bound the whole tile
   const int tlast = min(tq0 + kQT, Tq) - 1;
   if (t0 + tq0 >= a.T) return;
-  const int64_t Elast = (p0 + t0 + min(tlast, a.T - 1 - t0) + 1) / 2;
+  const int64_t Elast = (p0 + t0 + min(tlast, a.T - 1 - t0) + 1) >> a.rshift;
   if ((int64_t)blockIdx.x * kScoreThreads >= Elast) return;
   const int nq = min(kQT, min(Tq, a.T - t0) - tq0);
   for (int i = threadIdx.x; i < nq * kHI * kDI / 4; i += kScoreThreads)
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(IndexArgs a, SeqPo
   const uint32_t sc = *reinterpret_cast<const uint32_t*>(a.ki_scales + ((int64_t)b * a.cap + j) * 4);
   for (int qq = 0; qq < nq; ++qq) {
     const int t = t0 + tq0 + qq;
-    const int64_t E = (p0 + t + 1) / 2;
+    const int64_t E = (p0 + t + 1) >> a.rshift;
     if (j >= E) continue;
     float acc[kHI];
 #pragma unroll
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, S
   const int t = t0 + tl;
   if (t >= a.T || tl >= Tq) return;
   const int b = b0 + bl;
-  const int64_t E = (pos.p0[bl] + t + 1) / 2;
+  const int64_t E = (pos.p0[bl] + t + 1) >> a.rshift;
   const int64_t cs = (int64_t)c * chunk;
   const int n = (int)max64(0, min64(chunk, E - cs));
   const int64_t row = (int64_t)bl * Tq + tl;
@@ -491,7 +491,7 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
   for (int t0 = 0; t0 < a.T; t0 += p.Tq) {
     const int tq = min(p.Tq, a.T - t0);
     int64_t emax = 0;
-    for (int i = 0; i < nb; ++i) emax = max(emax, (pos.p0[i] + t0 + tq) / 2);
+    for (int i = 0; i < nb; ++i) emax = max(emax, (pos.p0[i] + t0 + tq) >> a.rshift);
     if (p.tc) {
       e = launch_index_scores_tc(a, pos, b0, nb, t0, tq, p.Tq, emax, reinterpret_cast<uint8_t*>(base + p.off_img), wq, sc,
                                  p.ld, num_sms, st);

@@ -32,6 +32,7 @@ struct WriterArgs {
   uint8_t *z_codes, *z_scales, *ki_codes, *ki_scales, *window;
   int64_t cap;
   int T;
+  int rshift;  // log2 of the compression ratio: entry j covers tokens (j << rshift) .. + ratio-1
   double eps;
 };
 
@@ -40,6 +41,7 @@ struct IndexArgs {
   const uint8_t *ki_codes, *ki_scales;
   int64_t cap;
   int T;
+  int rshift;  // log2 of the compression ratio: query t sees entries j < (t+1) >> rshift
   int32_t* idx;
   float* top_scores;
 };

@@ -78,17 +78,19 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
   const int b = b0 + bl;
   const int64_t p0 = pos.p0[bl];
   const int T = a.T;
-  const int64_t n_new = (p0 + T) / 2 - p0 / 2;
+  const int rs = a.rshift;
+  const int64_t n_new = ((p0 + T) >> rs) - (p0 >> rs);
   const int64_t e_base = (int64_t)blockIdx.x * kEntriesPerBlock;
   if (e_base >= n_new) return;
   const int ne = (int)min64(kEntriesPerBlock, n_new - e_base);
   const int tid = threadIdx.x, g = tid >> 7, gt = tid & 127;
   const int ch = 4 * gt;
-  const int64_t j = p0 / 2 + e_base + g;  // this group's entry (valid when g < ne)
+  const int64_t j = (p0 >> rs) + e_base + g;  // this group's entry (valid when g < ne)
+  const int64_t jpos = j << rs;                // the position the entry is rotated by
 
   // ---- phase 1: pooled key, RMSNorm, Z (the branch is uniform over a group)
   if (g < ne) {
-    const int64_t t1 = 2 * j + 1 - p0;  // local index of the odd token (0 <= t1 < T)
+    const int64_t t1 = jpos + (1 << rs) - 1 - p0;  // local index of the entry's last token
     const uint16_t* k1p = a.kc + ((int64_t)b * T + t1) * kD + ch;
     const uint16_t* g1p = a.gc + ((int64_t)b * T + t1) * kD + ch;
     float k0[4], g0[4], k1[4], g1[4];
@@ -97,7 +99,13 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
     k1[2] = bf16_to_f32(kk1.y & 0xffff); k1[3] = bf16_to_f32(kk1.y >> 16);
     g1[0] = bf16_to_f32(gg1.x & 0xffff); g1[1] = bf16_to_f32(gg1.x >> 16);
     g1[2] = bf16_to_f32(gg1.y & 0xffff); g1[3] = bf16_to_f32(gg1.y >> 16);
-    if (t1 >= 1) {
+    if (rs == 0) {  // ratio 1: the entry is the token itself (a softmax over one token is 1)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        k0[i] = 0.f;
+        g0[i] = -INFINITY;
+      }
+    } else if (t1 >= 1) {
       uint2 kk0 = *reinterpret_cast<const uint2*>(k1p - kD), gg0 = *reinterpret_cast<const uint2*>(g1p - kD);
       k0[0] = bf16_to_f32(kk0.x & 0xffff); k0[1] = bf16_to_f32(kk0.x >> 16);
       k0[2] = bf16_to_f32(kk0.y & 0xffff); k0[3] = bf16_to_f32(kk0.y >> 16);
@@ -113,10 +121,14 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
     DFSum ssq;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float m = fmaxf(g0[i], g1[i]);
-      float e0 = expf(g0[i] - m), e1 = expf(g1[i] - m);
-      float den = e0 + e1;
-      kp[i] = (e0 / den) * k0[i] + (e1 / den) * k1[i];
+      if (rs == 0) {
+        kp[i] = k1[i];
+      } else {
+        float m = fmaxf(g0[i], g1[i]);
+        float e0 = expf(g0[i] - m), e1 = expf(g1[i] - m);
+        float den = e0 + e1;
+        kp[i] = (e0 / den) * k0[i] + (e1 / den) * k1[i];
+      }
       ssq.add_sq(kp[i]);
     }
     const float r = rms_inv(group_sum(ssq, red[g], g), (float)kD, a.eps);
@@ -132,7 +144,7 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
       for (int q = 0; q < 2; ++q) {
         const int pi = (ch - (kD - kDR)) / 2 + q;
         float cs, sn;
-        rope_cs(2 * j, rf.inv_freq[pi], 1.0f, cs, sn);
+        rope_cs(jpos, rf.inv_freq[pi], 1.0f, cs, sn);
         float x0 = c[2 * q], x1 = c[2 * q + 1];
         z[2 * q] = x0 * cs - x1 * sn;
         z[2 * q + 1] = x0 * sn + x1 * cs;
@@ -146,7 +158,23 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
   __syncthreads();
 
   // ---- phase 2: quarter g of k^i = c W_IK for the block's entries (thread = output column)
-  {
+  if (ne == 1) {  // one entry (decode): accumulate it alone, in two chains (even / odd K)
+    DF acc0{0.f, 0.f}, acc1{0.f, 0.f};
+    const int o = gt;
+    for (int d0 = 128 * g; d0 < 128 * g + 128; d0 += 16) {
+      uint32_t wv[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) wv[u] = __ldg(a.w_ik + (d0 + u) * kDI + o);
+#pragma unroll
+      for (int u = 0; u < 16; u += 2) {
+        acc0.add_prod(sc[0][d0 + u], __uint_as_float(wv[u] << 16));
+        acc1.add_prod(sc[0][d0 + u + 1], __uint_as_float(wv[u + 1] << 16));
+      }
+    }
+    acc0.add_prod(acc1.s, 1.f);
+    acc0.c += acc1.c;
+    part[g][0][o] = make_float2(acc0.s, acc0.c);
+  } else {
     DF acc[kEntriesPerBlock];
 #pragma unroll
     for (int e = 0; e < kEntriesPerBlock; ++e) acc[e] = DF{0.f, 0.f};
@@ -179,7 +207,7 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
     const float partner = __shfl_xor_sync(0xffffffffu, kn, 1);
     if (o >= 64) {
       float cs, sn;
-      rope_cs(2 * j, rf.inv_freq[(o - 64) / 2], 1.0f, cs, sn);
+      rope_cs(jpos, rf.inv_freq[(o - 64) / 2], 1.0f, cs, sn);
       kn = (o & 1) ? (partner * sn + kn * cs) : (kn * cs - partner * sn);
     }
     const float amax = warp_max(fabsf(kn));
@@ -236,8 +264,8 @@ __global__ void __launch_bounds__(kWriterThreads) writer_window_kernel(WriterArg
   }
   uint32_t packed = f32_to_e4m3(y[0]) | (f32_to_e4m3(y[1]) << 8) | (f32_to_e4m3(y[2]) << 16) | (f32_to_e4m3(y[3]) << 24);
   *reinterpret_cast<uint32_t*>(a.window + ((int64_t)b * (127 + T) + 127 + t) * kD + ch) = packed;
-  // the last token of an unfinished pair waits in the pair buffer for its partner
-  if (t == T - 1 && ((p0 + T) & 1)) {
+  // the last token of an unfinished pair waits in the pair buffer for its partner (ratio 2)
+  if (a.rshift == 1 && t == T - 1 && ((p0 + T) & 1)) {
     uint2 kk = *reinterpret_cast<const uint2*>(a.kc + row * kD + ch);
     uint2 gg = *reinterpret_cast<const uint2*>(a.gc + row * kD + ch);
     *reinterpret_cast<float4*>(a.pair_kc + (int64_t)b * kD + ch) =
@@ -251,7 +279,7 @@ __global__ void __launch_bounds__(kWriterThreads) writer_window_kernel(WriterArg
 
 cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf, cudaStream_t st) {
   int64_t max_new = 0;
-  for (int i = 0; i < nb; ++i) max_new = max(max_new, (pos.p0[i] + a.T) / 2 - pos.p0[i] / 2);
+  for (int i = 0; i < nb; ++i) max_new = max(max_new, ((pos.p0[i] + a.T) >> a.rshift) - (pos.p0[i] >> a.rshift));
   if (max_new > 0) {
     dim3 grid((unsigned)((max_new + kEntriesPerBlock - 1) / kEntriesPerBlock), (unsigned)nb);
     writer_entries_kernel<<<grid, kEntryThreads, 0, st>>>(a, pos, b0, rf);

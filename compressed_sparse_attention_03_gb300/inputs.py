@@ -9,6 +9,8 @@ Workloads (B sequences, T new tokens, p0 cached positions before the step):
   decode_128k    B=64, p0=131072,  T=1   (65536 entries per sequence)          seed 2
   decode_1m      B=8,  p0=1048576, T=1   (524288 entries per sequence)         seed 3
   chunk_32k      B=1,  p0=262144,  T=32768 (131072 cached + 16384 new entries) seed 4
+  decode_512k_r1 B=8,  p0=524288,  T=1   compression ratio 1 (524288 entries)  seed 5
+  prefill_4k_r1  B=1,  p0=0,       T=4096 compression ratio 1                  seed 6
 """
 from __future__ import annotations
 
@@ -26,15 +28,16 @@ class Workload:
     T: int
     p0: int
     seed: int
+    ratio: int = 2  # compression ratio of the layer (entries per token: 1 / ratio)
 
     @property
     def cap(self) -> int:
         """Cache capacity (entries) that holds every entry visible to the step."""
-        return (self.p0 + self.T) // 2
+        return (self.p0 + self.T) // self.ratio
 
     @property
     def cached_entries(self) -> int:
-        return self.p0 // 2
+        return self.p0 // self.ratio
 
 
 WORKLOADS = {
@@ -43,6 +46,8 @@ WORKLOADS = {
     "decode_128k": Workload("decode_128k", 64, 1, 131072, 2),
     "decode_1m": Workload("decode_1m", 8, 1, 1048576, 3),
     "chunk_32k": Workload("chunk_32k", 1, 32768, 262144, 4),
+    "decode_512k_r1": Workload("decode_512k_r1", 8, 1, 524288, 5, ratio=1),
+    "prefill_4k_r1": Workload("prefill_4k_r1", 1, 4096, 0, 6, ratio=1),
 }
 
 
@@ -123,12 +128,12 @@ def step_inputs(B: int, T: int, seed: int, device="cpu"):
     return dict(kc=kc, gc=gc, wa=wa, q=q, qi=qi, wI=wI)
 
 
-def cache_state(B: int, T: int, p0: int, cap: int, seed: int, device="cpu"):
-    """Synthetic state before the step: FP4 caches with the p0//2 cached entries drawn at
+def cache_state(B: int, T: int, p0: int, cap: int, seed: int, device="cpu", ratio: int = 2):
+    """Synthetic state before the step: FP4 caches with the p0//ratio cached entries drawn at
     random (rest zero), the window view [B,127+T,512] with random E4M3 codes in the rows of
     positions p0-127..p0-1 that exist, and a random pair buffer (used when p0 is odd)."""
     g = _gen(30_000 + seed, device)
-    n = p0 // 2
+    n = p0 // ratio
     z_codes = torch.zeros(B, cap, D // 2, dtype=torch.uint8, device=device)
     z_scales = torch.zeros(B, cap, D // 32, dtype=torch.uint8, device=device)
     ki_codes = torch.zeros(B, cap, DI // 2, dtype=torch.uint8, device=device)
@@ -153,5 +158,5 @@ def workload_inputs(w: Workload, device="cpu"):
     out = {}
     out.update(layer_params(w.seed, device))
     out.update(step_inputs(w.B, w.T, w.seed, device))
-    out.update(cache_state(w.B, w.T, w.p0, w.cap, w.seed, device))
+    out.update(cache_state(w.B, w.T, w.p0, w.cap, w.seed, device, w.ratio))
     return out

@@ -1,7 +1,7 @@
 /* csa2.h - C ABI of the GB300 (sm_103a) CSA2 layer library, libcsa2.so.
  *
  * One DeepSeek-V4.1-style CSA2 ("compressed sparse attention 2") layer of the Full kind at
- * compression ratio 2: the compressed-KV writer, the lightning indexer with its top-512
+ * compression ratio 2 (or 1): the compressed-KV writer, the lightning indexer with its top-512
  * select, and 64-head sink-softmax MQA over the 640 gathered rows.  The operations follow
  * the equations of the page "DeepSeek V4.1 - Pooled group / Source layer, pairs pooled",
  * block "Compressed sparse attention" (cited below as [PG]), with the RMSNorm of the page
@@ -10,8 +10,13 @@
  *
  * Conventions shared by every call
  *  - Fixed shapes: 64 heads x 512, RoPE on the last 64 dims, indexer 32 heads x 128 (RoPE
- *    on dims 64..127), window 128 rows, top 512, pair pooling (ratio 2).  csa2_create
- *    rejects any other value with CSA2_ERR_UNSUPPORTED.
+ *    on dims 64..127), window 128 rows, top 512.  csa2_create rejects any other value with
+ *    CSA2_ERR_UNSUPPORTED.
+ *  - Compression ratio r (config.ratio): 2 for the encoder owner layers (entry j pools
+ *    tokens 2j, 2j+1), or 1 for the decoder owner layers ("Inside DeepSeek V4.1 Flash:
+ *    Deriving the 890-Byte KV Cache", decoder layers of ratio one): entry j is token j
+ *    itself (a softmax over one token is 1, so k^p = k^c), there is no pair buffer.  Entry j
+ *    is rotated by position r*j and is visible to query t iff j < floor((t+1)/r).
  *  - Tensor arguments are DEVICE pointers, owned by the caller, row-major and densely
  *    packed in the shapes given, 16-byte aligned.  bf16 tensors are passed as uint16_t
  *    bit patterns.  The library allocates no device memory; scratch comes from the caller's
@@ -66,7 +71,7 @@ typedef struct {
   int idx_dim;      /* 128 */
   int window;       /* 128 */
   int topk;         /* 512 */
-  int ratio;        /* 2 */
+  int ratio;        /* 2 (default) or 1 */
   double rope_base; /* 10000: theta_i = rope_base^(-2i/64) */
   double eps;       /* 1e-20 ([RN]) */
 } csa2_config;
@@ -100,15 +105,16 @@ size_t csa2_workspace_bytes(const csa2_handle* h, int op, int B, int T, int64_t 
  *  gamma_ik   : f32 [128]   gain of the indexer-key RMSNorm.
  *  gamma_w    : f32 [512]   gain of the window RMSNorm (w^n = gamma_w RMSNorm(w^a)).
  *  p0         : HOST int64 [B].
- *  pair_kc, pair_gc : f32 [B, 512] pair buffer.  When p0[b] is odd it must hold token
- *               p0[b]-1; when p0[b]+T is odd the call stores token p0[b]+T-1 there.  May be
- *               NULL only if every p0[b] and T are even.
+ *  pair_kc, pair_gc : f32 [B, 512] pair buffer (ratio 2 only).  When p0[b] is odd it must
+ *               hold token p0[b]-1; when p0[b]+T is odd the call stores token p0[b]+T-1
+ *               there.  May be NULL if every p0[b] and T are even, or at ratio 1.
  *  z_codes/z_scales, ki_codes/ki_scales : the FP4 caches with room for `cap` entries;
- *               entries j with p0 <= 2j+1 <= p0+T-1 are written (j < cap required).
+ *               entries j whose last token r*j + r-1 is in p0..p0+T-1 are written (j < cap).
  *  window     : u8 [B, 127+T, 512] e4m3 view; rows 127..126+T are written.
- * Per entry: k^p = sum over the pair of softmax(g^c) * k^c per channel; c = gamma_c
- * RMSNorm(k^p); Z = c with dims 448..511 rotated by position 2j, then FP4.  K^I = gamma_ik
- * RMSNorm(c W_IK) with dims 64..127 rotated by 2j, then FP4.  Per token t: W = gamma_w
+ * Per entry: k^p = sum over the pair of softmax(g^c) * k^c per channel (ratio 1: the token's
+ * k^c); c = gamma_c RMSNorm(k^p); Z = c with dims 448..511 rotated by position r*j, then
+ * FP4.  K^I = gamma_ik RMSNorm(c W_IK) with dims 64..127 rotated by r*j, then FP4.  Per
+ * token t: W = gamma_w
  * RMSNorm(w^a) with dims 448..511 rotated by t, then FP8.
  * Workspace: none (ws may be NULL). */
 csa2_status csa2_write_cache(csa2_handle* h, const uint16_t* kc, const uint16_t* gc,

@@ -49,6 +49,9 @@ def test_status_strings_and_config_checks(lib):
     cfg.topk = 256   # the kernels are built for top-512 only
     assert lib.csa2_create(C.byref(cfg), C.byref(h)) == 5 and not h.value
     lib.csa2_default_config(C.byref(cfg))
+    cfg.ratio = 3    # compression ratio 1 or 2 only
+    assert lib.csa2_create(C.byref(cfg), C.byref(h)) == 5 and not h.value
+    lib.csa2_default_config(C.byref(cfg))
     cfg.rope_base = 0.5
     assert lib.csa2_create(C.byref(cfg), C.byref(h)) == 1
     assert lib.csa2_create(None, C.byref(h)) == 1

@@ -20,16 +20,21 @@ def handle():
     return csa2.csa2_create()
 
 
-def make_state(B, T, p0s, seed, cap=None, device=DEV):
+@pytest.fixture(scope="module")
+def handle_r1():
+    return csa2.csa2_create(ratio=1)
+
+
+def make_state(B, T, p0s, seed, cap=None, device=DEV, ratio=2):
     p0s = np.asarray(p0s, np.int64)
-    cap = cap or int(((p0s + T) // 2).max()) + 3
+    cap = cap or int(((p0s + T) // ratio).max()) + 3
     x = {}
     x.update(inputs.layer_params(seed, device))
     x.update(inputs.step_inputs(B, T, seed, device))
-    st = inputs.cache_state(B, T, int(p0s.max()), cap, seed, device)
+    st = inputs.cache_state(B, T, int(p0s.max()), cap, seed, device, ratio)
     # sequences with shorter context: drop cached entries beyond their own length
     for b in range(B):
-        n = int(p0s[b]) // 2
+        n = int(p0s[b]) // ratio
         for k in ("z_codes", "z_scales", "ki_codes", "ki_scales"):
             st[k][b, n:] = 0
     x.update(st)
@@ -44,14 +49,14 @@ def gpu_write(h, x, p0s):
     return w
 
 
-def oracle_write(x, p0s, cap):
+def oracle_write(x, p0s, cap, ratio=2):
     res = []
     for b, p0 in enumerate(p0s):
         cpu = lambda k: np32(x[k][b]) if x[k].dtype != torch.uint8 else x[k][b].cpu().numpy().copy()
         r = oracle.write_seq(cpu("kc"), cpu("gc"), cpu("wa"), np32(x["gamma_c"]), np32(x["w_ik"]), np32(x["gamma_ik"]),
                              np32(x["gamma_w"]), int(p0), cap, z_codes=cpu("z_codes"), z_scales=cpu("z_scales"),
                              ki_codes=cpu("ki_codes"), ki_scales=cpu("ki_scales"), pair_k=cpu("pair_kc"),
-                             pair_g=cpu("pair_gc"), window_prefix=cpu("window")[:127])
+                             pair_g=cpu("pair_gc"), window_prefix=cpu("window")[:127], ratio=ratio)
         res.append(r)
     return res
 
@@ -65,7 +70,7 @@ def use_oracle_state(x, ores):
     return x
 
 
-def check_write(w, ores, p0s, T):
+def check_write(w, ores, p0s, T, ratio=2):
     n_code = n_scale = n_fp8 = 0
     for b, (r, p0) in enumerate(zip(ores, p0s)):
         j0, n = r["first_entry"], r["n_entries"]
@@ -81,7 +86,7 @@ def check_write(w, ores, p0s, T):
         assert np.array_equal(g["ki_scales"][j0 + n:], r["ki_scales"][j0 + n:])
         n_fp8 += e4m3_compare(g["window"][127:], r["window"][127:], r["win_pre"])
         assert np.array_equal(g["window"][:127], r["window"][:127])
-        if (p0 + T) % 2 == 1:
+        if ratio == 2 and (p0 + T) % 2 == 1:
             assert np.array_equal(w["pair_kc"][b].cpu().numpy(), r["pair"][0])
             assert np.array_equal(w["pair_gc"][b].cpu().numpy(), r["pair"][1])
     return n_code, n_scale, n_fp8
@@ -115,16 +120,16 @@ def run_index(h, x, p0s, T):
     return idx, top
 
 
-def check_index(idx, top, x, p0s, rows=None):
+def check_index(idx, top, x, p0s, rows=None, ratio=2):
     B, T = idx.shape[:2]
     swaps = 0
     for b, p0 in enumerate(p0s):
         r = np.arange(T) if rows is None else np.asarray(rows)
         pos = p0 + r
-        E = (pos + 1) // 2
+        E = (pos + 1) // ratio
         kc = x["ki_codes"][b, : max(int(E.max()), 1)].cpu().numpy()
         ks = x["ki_scales"][b, : max(int(E.max()), 1)].cpu().numpy()
-        sc = oracle.index_scores(pos, np32(x["qi"][b][r]), np32(x["wI"][b][r]), kc, ks, kc.shape[0])
+        sc = oracle.index_scores(pos, np32(x["qi"][b][r]), np32(x["wI"][b][r]), kc, ks, kc.shape[0], ratio=ratio)
         oidx, otop, kth = oracle.topk(sc, E)
         g = idx[b][r].cpu().numpy()
         swaps += topk_compare(g, oidx, sc, kth, E)
@@ -280,6 +285,61 @@ def test_step_end_to_end(handle, B, T, p0s):
         same = np.array([np.array_equal(gidx[i], oidx[i]) for i in range(T)])
         mx, rl2 = out_compare(np32(out[b])[same], ref[same])
         print(f"step b={b}: swaps={swaps} rows compared={same.sum()} max abs={mx:.3g} rel L2={rl2:.3g}")
+
+
+# ------------------------------------------------------------------------ compression ratio 1
+@pytest.mark.parametrize("B,T,p0s", [(3, 37, [0, 5, 130]), (1, 1, [0]), (2, 1, [7, 4096]), (2, 300, [0, 2001])])
+def test_writer_small_ratio1(handle_r1, B, T, p0s):
+    x, cap = make_state(B, T, p0s, seed=B * 100 + T + 1, ratio=1)
+    w = gpu_write(handle_r1, x, p0s)
+    n = check_write(w, oracle_write(x, p0s, cap, ratio=1), p0s, T, ratio=1)
+    print(f"writer ratio 1 B={B} T={T}: boundary exceptions codes/scales/fp8 = {n}")
+
+
+@pytest.mark.parametrize("B,T,p0s", [(2, 1, [3001, 1000]), (1, 300, [0]), (2, 64, [2000, 37]), (3, 1, [0, 1, 2])])
+def test_index_small_ratio1(handle_r1, B, T, p0s):
+    x, cap = make_state(B, T, p0s, seed=9 + T, ratio=1)
+    idx, top = run_index(handle_r1, x, p0s, T)
+    swaps = check_index(idx, top, x, p0s, ratio=1)
+    print(f"index ratio 1 B={B} T={T}: near-tie swaps = {swaps}")
+
+
+@pytest.mark.parametrize("name", ["decode_512k_r1", "prefill_4k_r1"])
+def test_index_workloads_ratio1(handle_r1, name):
+    wl = inputs.WORKLOADS[name]
+    x = inputs.workload_inputs(wl, DEV)
+    rows = None
+    if wl.p0 == 0:  # prefill from scratch: the keys come from this step's writer (the oracle's)
+        use_oracle_state(x, oracle_write(x, [wl.p0], wl.cap, ratio=1))
+        rng = np.random.default_rng(wl.seed)
+        rows = np.unique(np.concatenate([[0, 1, 510, 511, 512, wl.T - 1], rng.integers(0, wl.T, 40)]))
+    idx, top = run_index(handle_r1, x, [wl.p0] * wl.B, wl.T)
+    swaps = check_index(idx, top, x, [wl.p0] * wl.B, rows=rows, ratio=1)
+    print(f"index {name}: near-tie swaps = {swaps}")
+
+
+def test_step_end_to_end_ratio1(handle_r1):
+    B, T, p0s = 2, 33, [1100, 77]
+    x, cap = make_state(B, T, p0s, seed=23, ratio=1)
+    g = gpu_write(handle_r1, x, p0s)
+    ow = oracle_write(x, p0s, cap, ratio=1)
+    check_write(g, ow, p0s, T, ratio=1)
+    xg = dict(x, **g)
+    idx, top = run_index(handle_r1, xg, p0s, T)
+    out = run_attend(handle_r1, xg, idx, p0s)
+    for b, p0 in enumerate(p0s):
+        pos = p0 + np.arange(T)
+        E = pos + 1
+        r = ow[b]
+        sc = oracle.index_scores(pos, np32(x["qi"][b]), np32(x["wI"][b]), r["ki_codes"], r["ki_scales"], cap, ratio=1)
+        oidx, _, kth = oracle.topk(sc, E)
+        gidx = idx[b].cpu().numpy()
+        swaps = topk_compare(gidx, oidx, sc, kth, E)
+        ref = oracle.attend(pos, np32(x["q"][b]), np32(x["sinks"]), r["z_codes"], r["z_scales"], cap, r["window"],
+                            p0 - 127, oidx)
+        same = np.array([np.array_equal(gidx[i], oidx[i]) for i in range(T)])
+        mx, rl2 = out_compare(np32(out[b])[same], ref[same])
+        print(f"step ratio 1 b={b}: swaps={swaps} rows compared={same.sum()} max abs={mx:.3g} rel L2={rl2:.3g}")
 
 
 # ------------------------------------------------------------------------ argument errors
