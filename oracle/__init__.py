@@ -71,7 +71,7 @@ def _declare(L: C.CDLL) -> None:
     L.csa2o_topk.restype = i32
     L.csa2o_topk.argtypes = [i32, p, p, i64, i32, p, p, p]
     L.csa2o_attend.restype = i32
-    L.csa2o_attend.argtypes = [i32, p, p, p, p, p, i64, p, i64, i64, p, f64, p, p, p]
+    L.csa2o_attend.argtypes = [i32, p, p, p, p, p, i64, p, i64, i64, p, f64, i64, p, p, p]
 
 
 def _ptr(a):
@@ -219,11 +219,12 @@ def topk(scores, E, k=TOPK):
 
 
 def attend(pos, q, sinks, z_codes, z_scales, n_entries, window, win_p0, idx, base=10000.0,
-           return_mass=False):
+           return_mass=False, win_start=0):
     """fp64 sink-softmax MQA for query rows at absolute positions ``pos``.
 
     q [nq,64,512] (already rotated), sinks [64], window [rows,512] u8 with row r <->
-    position win_p0 + r, idx [nq,512].  Returns out [nq,64,512] (fp64).
+    position win_p0 + r, idx [nq,512].  ``win_start`` = s bounds the window rows to positions
+    max(s, t-127)..t (replay from s).  Returns out [nq,64,512] (fp64).
     """
     pos = _c(pos, np.int64)
     q = _c(q, np.float32)
@@ -236,8 +237,8 @@ def attend(pos, q, sinks, z_codes, z_scales, n_entries, window, win_p0, idx, bas
     nrows = np.empty(nq, np.int32)
     rc = lib().csa2o_attend(nq, _ptr(pos), _ptr(q), _ptr(sinks), _ptr(_c(z_codes, np.uint8)),
                             _ptr(_c(z_scales, np.uint8)), int(n_entries), _ptr(window),
-                            int(win_p0), window.shape[0], _ptr(idx), float(base), _ptr(out),
-                            _ptr(mass), _ptr(nrows))
+                            int(win_p0), window.shape[0], _ptr(idx), float(base), int(win_start),
+                            _ptr(out), _ptr(mass), _ptr(nrows))
     if rc != 0:
         raise ValueError(f"attend: bad arguments ({rc})")
     return (out, mass, nrows) if return_mass else out

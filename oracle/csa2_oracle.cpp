@@ -350,15 +350,19 @@ int csa2o_topk(int nq, const int64_t* E, const double* scores, int64_t ld, int k
 // ---------------------------------------------------------------- sink-softmax MQA
 // Query rows at absolute positions pos[r] with Q q [nq,64,512] (already rotated), sinks [64].
 // G_t = [window rows for positions max(0,t-127)..t ; Z rows idx[r, i] (>= 0)]   ([PG] J, G_t)
+// With a replay start win_start = s ("Inside DeepSeek V4.1 Flash: Deriving the 890-Byte KV
+// Cache", section "Bounded replay trades exact state for cheaper resumption") the window
+// rows are positions max(s, t-127)..t; s = 0 is the plain window.
 // S = Q.G/sqrt(512);  A = exp S / (exp s_h + sum exp S);  O = sum A G;  O[448:] <- R_t^-1 O.
 // window: rows of positions win_p0 .. win_p0+win_rows-1 (row r <-> position win_p0 + r).
 // out [nq,64,512]; mass [nq,64] (optional) = sum_i A; nrows [nq] (optional) = |G_t|.
 int csa2o_attend(int nq, const int64_t* pos, const float* q, const float* sinks,
                  const uint8_t* z_codes, const uint8_t* z_scales, int64_t n_entries,
                  const uint8_t* window, int64_t win_p0, int64_t win_rows, const int32_t* idx,
-                 double base, double* out, double* mass, int32_t* nrows) {
+                 double base, int64_t win_start, double* out, double* mass, int32_t* nrows) {
   for (int r = 0; r < nq; ++r) {
-    int64_t lo = std::max<int64_t>(0, pos[r] - (WIN - 1));
+    int64_t lo = std::max<int64_t>(std::max<int64_t>(0, win_start), pos[r] - (WIN - 1));
+    if (win_start > pos[r]) return -3;
     if (lo < win_p0 || pos[r] >= win_p0 + win_rows) return -1;
     for (int i = 0; i < TOPK; ++i)
       if (idx[(int64_t)r * TOPK + i] >= n_entries) return -2;
@@ -366,7 +370,7 @@ int csa2o_attend(int nq, const int64_t* pos, const float* q, const float* sinks,
 #pragma omp parallel for schedule(dynamic)
   for (int r = 0; r < nq; ++r) {
     int64_t p = pos[r];
-    int64_t lo = std::max<int64_t>(0, p - (WIN - 1));
+    int64_t lo = std::max<int64_t>(std::max<int64_t>(0, win_start), p - (WIN - 1));
     std::vector<double> G;
     for (int64_t x = lo; x <= p; ++x) {
       const uint8_t* row = window + (x - win_p0) * D;

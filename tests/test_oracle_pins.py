@@ -415,6 +415,35 @@ def test_attend_row_counts():
         assert nrows[0] == want
 
 
+def test_attend_replay_bound():
+    # "Deriving the 890-Byte KV Cache", bounded replay: after a replay starting at s, query t
+    # sees window positions max(s, t-127)..t only.
+    zc, zs, win, q, sinks, idx, pos = _attend_case(nq=1, seed=14)
+    p = int(pos[0])
+    plain = oracle.attend(pos, q, sinks, zc, zs, len(zc), win, p - 127, idx)
+    # a bound at or below t-127 changes nothing
+    same = oracle.attend(pos, q, sinks, zc, zs, len(zc), win, p - 127, idx, win_start=p - 127)
+    assert np.array_equal(plain, same)
+    # row counts: min(128, t+1-s) window rows + the selected entries
+    for s_, want in ((p - 127, 640), (p - 100, 613), (p - 1, 514), (p, 513)):
+        _, _, nrows = oracle.attend(pos, q, sinks, zc, zs, len(zc), win, p - 127, idx, return_mass=True,
+                                    win_start=s_)
+        assert nrows[0] == want
+    # s = t: only the query's own window row -- SDPA with the sink as a zero key/value row
+    out = oracle.attend(pos, q, sinks, zc, zs, len(zc), win, p - 127, idx, win_start=p)
+    G = torch.from_numpy(_gathered(zc, zs, win[-1:], idx[0]))
+    K = torch.cat([G, torch.zeros(1, 512, dtype=torch.float64)])
+    mask = torch.zeros(64, 1, K.shape[0], dtype=torch.float64)
+    mask[:, 0, -1] = torch.from_numpy(sinks.astype(np.float64))
+    Q = torch.from_numpy(q[0].astype(np.float64))[:, None, :]
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K[None].expand(64, -1, -1), K[None].expand(64, -1, -1),
+                                                           attn_mask=mask)[:, 0, :].numpy()
+    ref = np.stack([np.concatenate([ref[h, :448], oracle.rope(ref[h, 448:], p, inverse=True)]) for h in range(64)])
+    assert np.abs(out[0] - ref).max() < 1e-12
+    with pytest.raises(ValueError):  # a replay start after the query is not a valid bound
+        oracle.attend(pos, q, sinks, zc, zs, len(zc), win, p - 127, idx, win_start=p + 1)
+
+
 # ---------------------------------------------------------------- page arithmetic
 def test_kv_bytes_and_work_ratios():
     gd = golden()
