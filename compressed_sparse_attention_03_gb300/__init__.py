@@ -38,7 +38,7 @@ class csa2_config(C.Structure):
 
 EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_string", "csa2_kernel_launches",
            "csa2_workspace_bytes",
-           "csa2_write_cache", "csa2_index_topk", "csa2_attend", "csa2_attend_static")
+           "csa2_write_cache", "csa2_index_topk", "csa2_attend", "csa2_attend_replay", "csa2_attend_static")
 
 _lib = None
 
@@ -68,6 +68,8 @@ def lib() -> C.CDLL:
         L.csa2_index_topk.restype = i32
         L.csa2_attend.argtypes = [p] * 5 + [i64, p, p, p, i32, i32, p, p, sz, p]
         L.csa2_attend.restype = i32
+        L.csa2_attend_replay.argtypes = [p] * 5 + [i64, p, p, p, p, i32, i32, p, p, sz, p]
+        L.csa2_attend_replay.restype = i32
         L.csa2_attend_static.argtypes = [p] * 5 + [i64, p, p, p, i32, i32, p, p]
         L.csa2_attend_static.restype = i32
         _lib = L
@@ -206,3 +208,20 @@ def csa2_attend_static(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, 
         _dev(z_scales, torch.uint8, "z_scales"), cap, _dev(window, torch.uint8, "window"),
         _dev(idx, torch.int32, "idx"), p0a.ctypes.data_as(C.c_void_p), B, T, _dev(out, torch.bfloat16, "out"),
         _stream(stream)))
+
+
+def csa2_attend_replay(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, win_start, out, ws=None,
+                       stream=None) -> None:
+    """csa2_attend after a bounded replay: query t of sequence b sees the window positions
+    max(win_start[b], t-127)..t."""
+    B, T = q.shape[:2]
+    p0a = _host_p0(p0, B)
+    wsa = _host_p0(win_start, B)
+    cap = z_codes.shape[1]
+    if ws is None:
+        ws = workspace(h, OP_ATTEND, B, T, 0, q.device)
+    _check("csa2_attend_replay", lib().csa2_attend_replay(
+        h.ptr, _dev(q, torch.bfloat16, "q"), _dev(sinks, torch.float32, "sinks"), _dev(z_codes, torch.uint8, "z_codes"),
+        _dev(z_scales, torch.uint8, "z_scales"), cap, _dev(window, torch.uint8, "window"),
+        _dev(idx, torch.int32, "idx"), p0a.ctypes.data_as(C.c_void_p), wsa.ctypes.data_as(C.c_void_p), B, T,
+        _dev(out, torch.bfloat16, "out"), _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))

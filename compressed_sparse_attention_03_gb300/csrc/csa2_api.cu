@@ -39,6 +39,12 @@ csa2::SeqPos pack_pos(const int64_t* p0, int b0, int nb) {
 
 csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
 
+csa2::SeqPos no_replay() {
+  csa2::SeqPos s;
+  std::memset(&s, 0, sizeof s);
+  return s;
+}
+
 // Largest visible-entry count over the batch for queries p0..p0+T-1: floor((p0+T)/ratio).
 int64_t max_visible(const int64_t* p0, int B, int T, int rshift) {
   int64_t m = 0;
@@ -211,7 +217,38 @@ csa2_status csa2_attend(csa2_handle* h, const uint16_t* q, const float* sinks, c
   a.cap = cap; a.T = T; a.out = out;
   for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
     const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
-    st = cuda_status(csa2::launch_attend(a, pack_pos(p0, b0, nb), b0, nb, h->rf, ws, ws_bytes, h->num_sms,
+    st = cuda_status(csa2::launch_attend(a, pack_pos(p0, b0, nb), no_replay(), b0, nb, h->rf, ws, ws_bytes, h->num_sms,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+    if (st != CSA2_OK) return st;
+  }
+  return CSA2_OK;
+}
+
+// csa2_attend with per-sequence replay starts (include/csa2.h): the window rows of query t are
+// positions max(win_start[b], t-127)..t.
+csa2_status csa2_attend_replay(csa2_handle* h, const uint16_t* q, const float* sinks, const uint8_t* z_codes,
+                               const uint8_t* z_scales, int64_t cap, const uint8_t* window, const int32_t* idx,
+                               const int64_t* p0, const int64_t* win_start, int B, int T, uint16_t* out, void* ws,
+                               size_t ws_bytes, csa2_stream_t stream) {
+  if (!h || !q || !sinks || !z_codes || !z_scales || !window || !idx || !out) return CSA2_ERR_INVALID_ARG;
+  if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  csa2_status st = check_p0(p0, B, T);
+  if (st != CSA2_OK) return st;
+  if (!win_start) return CSA2_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (win_start[b] < 0 || win_start[b] > p0[b]) return CSA2_ERR_SHAPE;  // 0 <= s <= p0
+  const void* ptrs[] = {q, sinks, z_codes, z_scales, window, idx, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CSA2_ERR_ALIGN;
+  const size_t need = csa2::attend_workspace_bytes(B, T, h->num_sms);
+  if (ws_bytes < need || (need && !ws)) return CSA2_ERR_WORKSPACE;
+  if (need && !aligned16(ws)) return CSA2_ERR_ALIGN;
+  csa2::AttendArgs a{};
+  a.q = q; a.sinks = sinks; a.z_codes = z_codes; a.z_scales = z_scales; a.window = window; a.idx = idx;
+  a.cap = cap; a.T = T; a.out = out;
+  for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
+    const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
+    st = cuda_status(csa2::launch_attend(a, pack_pos(p0, b0, nb), pack_pos(win_start, b0, nb), b0, nb, h->rf, ws, ws_bytes, h->num_sms,
                                          reinterpret_cast<cudaStream_t>(stream)));
     if (st != CSA2_OK) return st;
   }
@@ -245,7 +282,7 @@ csa2_status csa2_attend_static(csa2_handle* h, const uint16_t* q, const float* s
   // Launches of successive groups of sequences reuse the array; they are ordered on `stream`.
   for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
     const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
-    st = cuda_status(csa2::launch_attend(a, pack_pos(p0, b0, nb), b0, nb, h->rf, ws, need, h->num_sms,
+    st = cuda_status(csa2::launch_attend(a, pack_pos(p0, b0, nb), no_replay(), b0, nb, h->rf, ws, need, h->num_sms,
                                          reinterpret_cast<cudaStream_t>(stream)));
     if (st != CSA2_OK) return st;
   }

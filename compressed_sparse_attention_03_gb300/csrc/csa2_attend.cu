@@ -117,9 +117,10 @@ __device__ __forceinline__ float transpose_reduce32(const float (&v)[32], int la
 
 // grid (T, nb, nsplit).  nsplit == 1 writes `out`; otherwise the split's unnormalised O, its
 // reference m (log2 units) and sum l go to the partial buffers for attend_combine_kernel.
-__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, SeqPos pos, int b0, RopeFreq rf,
-                                                                int nsplit, int chunks_per_split, float* part_o,
-                                                                float* part_ml) {
+// wst: per-sequence replay starts s (0 = none); the window rows are positions max(s, t-127)..t.
+__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, SeqPos pos, SeqPos wst, int b0,
+                                                                RopeFreq rf, int nsplit, int chunks_per_split,
+                                                                float* part_o, float* part_ml) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ Bars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   if (warp == 0) {
     // all 512 indices in one round trip (16 per lane); the order of the gathered rows does not
     // matter to the result, so each lane appends its valid entries after a warp prefix sum
-    const int nw = (int)min64(kWin, p + 1);
+    const int nw = (int)min64(kWin, p + 1 - wst.p0[bl]);  // window rows: max(s, p-127) .. p
     const int4* ip = reinterpret_cast<const int4*>(a.idx + qrow * kTopK);
     int32_t jv[16];
 #pragma unroll
@@ -576,7 +577,7 @@ size_t attend_workspace_bytes(int B, int T, int num_sms) {
   return need;
 }
 
-cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf, void* ws,
+cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, const SeqPos& wst, int b0, int nb, const RopeFreq& rf, void* ws,
                           size_t ws_bytes, int num_sms, cudaStream_t st) {
   const int s = choose_splits(nb * a.T, num_sms);
   cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynBytes);
@@ -589,7 +590,7 @@ cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, int b0, int nb
     po = static_cast<float*>(ws);
     pml = po + rows * kH * kD;
   }
-  attend_tc_kernel<<<dim3((unsigned)a.T, (unsigned)nb, (unsigned)s), kThreads, kDynBytes, st>>>(a, pos, b0, rf, s, cps,
+  attend_tc_kernel<<<dim3((unsigned)a.T, (unsigned)nb, (unsigned)s), kThreads, kDynBytes, st>>>(a, pos, wst, b0, rf, s, cps,
                                                                                                  po, pml);
   note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

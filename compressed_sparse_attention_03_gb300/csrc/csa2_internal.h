@@ -73,7 +73,8 @@ cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos,
 void note_launch();
 
 size_t attend_workspace_bytes(int B, int T, int num_sms);
-cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf,
+// wst: per-sequence replay starts of the window (zeros: the plain window of 128 positions).
+cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, const SeqPos& wst, int b0, int nb, const RopeFreq& rf,
                           void* ws, size_t ws_bytes, int num_sms, cudaStream_t st);
 
 // Fixed device scratch of csa2_attend_static: room for this many split-partial rows (one row =

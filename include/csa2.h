@@ -156,6 +156,20 @@ csa2_status csa2_attend(csa2_handle* h, const uint16_t* q, const float* sinks,
                         const uint8_t* window, const int32_t* idx, const int64_t* p0, int B,
                         int T, uint16_t* out, void* ws, size_t ws_bytes, csa2_stream_t stream);
 
+/* (4') csa2_attend after a bounded replay ("Inside DeepSeek V4.1 Flash: Deriving the 890-Byte
+ * KV Cache", section "Bounded replay trades exact state for cheaper resumption"): local
+ * state was rebuilt only from position s on, so query t sees the window positions
+ * max(s, t-127)..t instead of max(0, t-127)..t.
+ *  win_start : HOST int64 [B], the replay start s of each sequence, 0 <= s <= p0[b]
+ *              (CSA2_ERR_SHAPE otherwise).  Window-view rows of positions < s are not read.
+ * Every other argument, the result for s = 0, the workspace and the errors are those of
+ * csa2_attend. */
+csa2_status csa2_attend_replay(csa2_handle* h, const uint16_t* q, const float* sinks,
+                               const uint8_t* z_codes, const uint8_t* z_scales, int64_t cap,
+                               const uint8_t* window, const int32_t* idx, const int64_t* p0,
+                               const int64_t* win_start, int B, int T, uint16_t* out, void* ws,
+                               size_t ws_bytes, csa2_stream_t stream);
+
 /* csa2_attend with no workspace argument.  Not an operation of the pages (they have no
  * counterpart): an interface for callers that cannot allocate device memory at call time,
  * e.g. a serving process that hands all free HBM to its KV-cache pool at start-up, or code

@@ -287,6 +287,33 @@ def test_step_end_to_end(handle, B, T, p0s):
         print(f"step b={b}: swaps={swaps} rows compared={same.sum()} max abs={mx:.3g} rel L2={rl2:.3g}")
 
 
+# ------------------------------------------------------------------------ bounded replay
+@pytest.mark.parametrize("B,T,p0s,starts", [(3, 40, [1000, 5001, 300], [990, 5001, 0]), (2, 1, [8192, 130], [8150, 3])])
+def test_attend_replay(handle, B, T, p0s, starts):
+    x, cap = make_state(B, T, p0s, seed=31 + T)
+    use_oracle_state(x, oracle_write(x, p0s, cap))
+    idx = random_indices(B, T, p0s, seed=6, device=DEV)
+    out = torch.empty(B, T, 64, 512, dtype=torch.bfloat16, device=DEV)
+    csa2.csa2_attend_replay(handle, x["q"], x["sinks"], x["z_codes"], x["z_scales"], x["window"], idx, p0s, starts,
+                            out)
+    errs = []
+    for b, (p0, s0) in enumerate(zip(p0s, starts)):
+        pos = p0 + np.arange(T)
+        ref = oracle.attend(pos, np32(x["q"][b]), np32(x["sinks"]), x["z_codes"][b].cpu().numpy(),
+                            x["z_scales"][b].cpu().numpy(), x["z_codes"].shape[1], x["window"][b].cpu().numpy(),
+                            p0 - 127, idx[b].cpu().numpy(), win_start=s0)
+        errs.append(out_compare(np32(out[b]), ref))
+    print(f"attend replay B={B} T={T}: max abs / rel L2 = {max(e[0] for e in errs)}, {max(e[1] for e in errs)}")
+    # no replay (s = 0) is bit-identical to csa2_attend
+    zero = torch.empty_like(out)
+    csa2.csa2_attend_replay(handle, x["q"], x["sinks"], x["z_codes"], x["z_scales"], x["window"], idx, p0s, [0] * B,
+                            zero)
+    assert torch.equal(zero, run_attend(handle, x, idx, p0s))
+    with pytest.raises(csa2.Csa2Error):  # a start after p0 is not a valid bound
+        csa2.csa2_attend_replay(handle, x["q"], x["sinks"], x["z_codes"], x["z_scales"], x["window"], idx, p0s,
+                                [p + 1 for p in p0s], zero)
+
+
 # ------------------------------------------------------------------------ compression ratio 1
 @pytest.mark.parametrize("B,T,p0s", [(3, 37, [0, 5, 130]), (1, 1, [0]), (2, 1, [7, 4096]), (2, 300, [0, 2001])])
 def test_writer_small_ratio1(handle_r1, B, T, p0s):
