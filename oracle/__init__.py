@@ -70,6 +70,10 @@ def _declare(L: C.CDLL) -> None:
     L.csa2o_index_scores.argtypes = [i32, i32, p, p, p, p, p, i64, p, i64, p, p]
     L.csa2o_topk.restype = i32
     L.csa2o_topk.argtypes = [i32, p, p, i64, i32, p, p, p]
+    L.csa2o_hsi_pool.restype = i32
+    L.csa2o_hsi_pool.argtypes = [i32, p, p, i64, p]
+    L.csa2o_reindex_topk.restype = i32
+    L.csa2o_reindex_topk.argtypes = [i32, p, p, i64, p, i32, p]
     L.csa2o_attend.restype = i32
     L.csa2o_attend.argtypes = [i32, p, p, p, p, p, i64, p, i64, i64, p, f64, i64, p, p, p]
 
@@ -242,3 +246,28 @@ def attend(pos, q, sinks, z_codes, z_scales, n_entries, window, win_p0, idx, bas
     if rc != 0:
         raise ValueError(f"attend: bad arguments ({rc})")
     return (out, mass, nrows) if return_mass else out
+
+
+HSI_BLOCK, HSI_BLOCKS = 8, 2048
+
+
+def hsi_pool(scores, E):
+    """Hierarchical-indexer pool per row: the newest block of 8 entries plus the 2047 best other
+    blocks by their best score (every block when at most 2048), ascending, -1 padded."""
+    scores = _c(scores, np.float64)
+    E = _c(E, np.int64)
+    nq = E.size
+    pool = np.empty((nq, HSI_BLOCKS), np.int32)
+    lib().csa2o_hsi_pool(nq, _ptr(E), _ptr(scores), scores.shape[1], _ptr(pool))
+    return pool
+
+
+def reindex_topk(scores, E, pool, k=TOPK):
+    """Top-k of each row's scores over its pool's visible entries (ties: lower j first)."""
+    scores = _c(scores, np.float64)
+    E = _c(E, np.int64)
+    pool = _c(pool, np.int32)
+    nq = E.size
+    idx = np.empty((nq, k), np.int32)
+    lib().csa2o_reindex_topk(nq, _ptr(E), _ptr(scores), scores.shape[1], _ptr(pool), k, _ptr(idx))
+    return idx

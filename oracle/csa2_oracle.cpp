@@ -347,6 +347,73 @@ int csa2o_topk(int nq, const int64_t* E, const double* scores, int64_t ld, int k
   return 0;
 }
 
+// ---------------------------------------------------------------- hierarchical sparse indexer
+// "Inside DeepSeek V4.1", section "Most layers borrow", and "Deriving the 890-Byte KV Cache",
+// section "Hierarchical indexing bounds the later searches": the first Full layer groups the
+// entries into blocks of 8, scores a block by its best entry score and keeps 2048 blocks
+// (16384 candidates), always including the block that holds the newest entries; later
+// Reindex layers take their own top-512 inside that pool.
+// Reading: block k = entries 8k..8k+7 (visible ones only: j < E); pool = the newest block
+// (E-1)/8 plus the 2047 best other blocks (block score desc, block index asc), or every block
+// when there are at most 2048; ascending block indices, -1 padded.
+constexpr int HSI_BLK = 8, HSI_BLOCKS = 2048;
+
+int csa2o_hsi_pool(int nq, const int64_t* E, const double* scores, int64_t ld, int32_t* pool) {
+#pragma omp parallel for schedule(dynamic)
+  for (int r = 0; r < nq; ++r) {
+    const double* s = scores + (int64_t)r * ld;
+    const int64_t nb = (E[r] + HSI_BLK - 1) / HSI_BLK;
+    std::vector<int64_t> chosen;
+    if (nb <= HSI_BLOCKS) {
+      for (int64_t k = 0; k < nb; ++k) chosen.push_back(k);
+    } else {
+      std::vector<double> bs(nb - 1);
+      for (int64_t k = 0; k + 1 < nb; ++k) {
+        double m = -INFINITY;
+        for (int64_t j = HSI_BLK * k; j < HSI_BLK * (k + 1); ++j) m = std::max(m, s[j]);  // all visible
+        bs[k] = m;
+      }
+      std::vector<int64_t> order(nb - 1);
+      for (int64_t k = 0; k + 1 < nb; ++k) order[k] = k;
+      std::sort(order.begin(), order.end(), [&bs](int64_t a, int64_t b) {
+        if (bs[a] != bs[b]) return bs[a] > bs[b];
+        return a < b;
+      });
+      chosen.assign(order.begin(), order.begin() + (HSI_BLOCKS - 1));
+      chosen.push_back(nb - 1);  // the newest block
+      std::sort(chosen.begin(), chosen.end());
+    }
+    for (int i = 0; i < HSI_BLOCKS; ++i)
+      pool[(int64_t)r * HSI_BLOCKS + i] = i < (int)chosen.size() ? (int32_t)chosen[i] : -1;
+  }
+  return 0;
+}
+
+// Reindex top-k: the k largest of scores[r, j] over the pool's visible entries j (j < E),
+// equal scores -> lower j first; ascending in j, -1 padded.
+int csa2o_reindex_topk(int nq, const int64_t* E, const double* scores, int64_t ld, const int32_t* pool, int k,
+                       int32_t* idx) {
+#pragma omp parallel for schedule(dynamic)
+  for (int r = 0; r < nq; ++r) {
+    const double* s = scores + (int64_t)r * ld;
+    std::vector<int64_t> cand;
+    for (int i = 0; i < HSI_BLOCKS; ++i) {
+      const int32_t blk = pool[(int64_t)r * HSI_BLOCKS + i];
+      if (blk < 0) continue;
+      for (int64_t j = (int64_t)HSI_BLK * blk; j < (int64_t)HSI_BLK * (blk + 1) && j < E[r]; ++j) cand.push_back(j);
+    }
+    std::sort(cand.begin(), cand.end(), [s](int64_t a, int64_t b) {
+      if (s[a] != s[b]) return s[a] > s[b];
+      return a < b;
+    });
+    const int64_t n = std::min<int64_t>(k, (int64_t)cand.size());
+    std::vector<int64_t> chosen(cand.begin(), cand.begin() + n);
+    std::sort(chosen.begin(), chosen.end());
+    for (int i = 0; i < k; ++i) idx[(int64_t)r * k + i] = i < n ? (int32_t)chosen[i] : -1;
+  }
+  return 0;
+}
+
 // ---------------------------------------------------------------- sink-softmax MQA
 // Query rows at absolute positions pos[r] with Q q [nq,64,512] (already rotated), sinks [64].
 // G_t = [window rows for positions max(0,t-127)..t ; Z rows idx[r, i] (>= 0)]   ([PG] J, G_t)

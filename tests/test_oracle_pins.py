@@ -444,6 +444,49 @@ def test_attend_replay_bound():
         oracle.attend(pos, q, sinks, zc, zs, len(zc), win, p - 127, idx, win_start=p + 1)
 
 
+def _brute_pool(s, E):
+    nb = -(-E // 8)
+    if nb <= 2048:
+        return np.arange(nb)
+    bs = s[: 8 * (nb - 1)].reshape(nb - 1, 8).max(axis=1)
+    order = np.lexsort((np.arange(nb - 1), -bs))   # score desc, then block index asc
+    return np.sort(np.concatenate([order[:2047], [nb - 1]]))
+
+
+def test_hsi_pool_brute_force_ties_and_newest_block():
+    # "Hierarchical indexing bounds the later searches": blocks of 8, 2048 blocks, 16384
+    # candidates, the newest block always kept
+    assert oracle.HSI_BLOCK * oracle.HSI_BLOCKS == golden()["hsi_pool"]
+    rng = np.random.default_rng(15)
+    E = np.array([16384 + 8 * 11 + 3, 20000, 100, 16384])
+    ld = int(E.max())
+    s = np.round(rng.standard_normal((4, ld)) * 4) / 4   # coarse values: many exact ties
+    s[1, 8 * ((20000 - 1) // 8):] = -1e9                  # the newest block scores lowest
+    pool = oracle.hsi_pool(s, E)
+    for r in range(4):
+        want = _brute_pool(s[r], int(E[r]))
+        got = pool[r][pool[r] >= 0]
+        assert np.array_equal(got, want)
+        assert np.all(pool[r][len(want):] == -1)
+        assert got[-1] == (E[r] - 1) // 8                 # newest block present
+    assert len(pool[2][pool[2] >= 0]) == 13 and len(pool[3][pool[3] >= 0]) == 2048
+
+
+def test_reindex_topk_brute_force():
+    rng = np.random.default_rng(16)
+    E = np.array([17000, 5000])
+    s = np.round(rng.standard_normal((2, 17000)) * 8) / 8
+    pool = oracle.hsi_pool(rng.standard_normal((2, 17000)), E)   # pool from another layer's scores
+    idx = oracle.reindex_topk(s, E, pool)
+    for r in range(2):
+        blocks = pool[r][pool[r] >= 0]
+        cand = np.concatenate([np.arange(8 * b, min(8 * b + 8, E[r])) for b in blocks])
+        order = cand[np.lexsort((cand, -s[r, cand]))]
+        want = np.sort(order[:512])
+        assert np.array_equal(idx[r][idx[r] >= 0], want)
+        assert set(want) <= set(cand)
+
+
 # ---------------------------------------------------------------- page arithmetic
 def test_kv_bytes_and_work_ratios():
     gd = golden()
