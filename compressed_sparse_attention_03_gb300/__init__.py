@@ -16,7 +16,8 @@ import torch
 _PKG = Path(__file__).resolve().parent
 LIB_PATH = _PKG / "_build" / "libcsa2.so"
 
-OP_WRITE_CACHE, OP_INDEX_TOPK, OP_ATTEND = 0, 1, 2
+OP_WRITE_CACHE, OP_INDEX_TOPK, OP_ATTEND, OP_INDEX_POOL, OP_REINDEX_TOPK = 0, 1, 2, 3, 4
+HSI_BLOCKS = 2048  # pool blocks per query row (blocks of 8 entries)
 HEADS, HEAD_DIM, ROPE_DIMS, IDX_HEADS, IDX_DIM, WINDOW, TOPK = 64, 512, 64, 32, 128, 128, 512
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "inconsistent sizes", 3: "pointer not 16-byte aligned",
@@ -38,7 +39,8 @@ class csa2_config(C.Structure):
 
 EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_string", "csa2_kernel_launches",
            "csa2_workspace_bytes",
-           "csa2_write_cache", "csa2_index_topk", "csa2_attend", "csa2_attend_replay", "csa2_attend_static")
+           "csa2_write_cache", "csa2_index_topk", "csa2_index_pool", "csa2_reindex_topk", "csa2_attend",
+           "csa2_attend_replay", "csa2_attend_static")
 
 _lib = None
 
@@ -66,6 +68,10 @@ def lib() -> C.CDLL:
         L.csa2_write_cache.restype = i32
         L.csa2_index_topk.argtypes = [p] * 5 + [i64, p, i32, i32, p, p, p, sz, p]
         L.csa2_index_topk.restype = i32
+        L.csa2_index_pool.argtypes = [p] * 5 + [i64, p, i32, i32, p, p, p, p, sz, p]
+        L.csa2_index_pool.restype = i32
+        L.csa2_reindex_topk.argtypes = [p] * 5 + [i64, p, i32, i32, p, p, p, p, sz, p]
+        L.csa2_reindex_topk.restype = i32
         L.csa2_attend.argtypes = [p] * 5 + [i64, p, p, p, i32, i32, p, p, sz, p]
         L.csa2_attend.restype = i32
         L.csa2_attend_replay.argtypes = [p] * 5 + [i64, p, p, p, p, i32, i32, p, p, sz, p]
@@ -181,6 +187,36 @@ def csa2_index_topk(h: Handle, qi, wI, ki_codes, ki_scales, p0, idx, top_scores=
         _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
         _dev(idx, torch.int32, "idx"), _dev(top_scores, torch.float32, "top_scores"), _dev(ws, torch.uint8, "ws"),
         ws.numel(), _stream(stream)))
+
+
+def csa2_index_pool(h: Handle, qi, wI, ki_codes, ki_scales, p0, idx, pool, top_scores=None, ws=None,
+                    stream=None) -> None:
+    """csa2_index_topk plus the hierarchical block pool [B, T, 2048] of each query."""
+    B, T = qi.shape[:2]
+    p0a = _host_p0(p0, B)
+    cap = ki_codes.shape[1]
+    if ws is None:
+        ws = workspace(h, OP_INDEX_POOL, B, T, int(((p0a + T) // h.ratio).max()), qi.device)
+    _check("csa2_index_pool", lib().csa2_index_pool(
+        h.ptr, _dev(qi, torch.bfloat16, "qi"), _dev(wI, torch.bfloat16, "wI"), _dev(ki_codes, torch.uint8, "ki_codes"),
+        _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
+        _dev(idx, torch.int32, "idx"), _dev(top_scores, torch.float32, "top_scores"), _dev(pool, torch.int32, "pool"),
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+
+
+def csa2_reindex_topk(h: Handle, qi, wI, ki_codes, ki_scales, p0, pool, idx, top_scores=None, ws=None,
+                      stream=None) -> None:
+    """Top-512 of this layer's indexer scores over the entries of a given block pool."""
+    B, T = qi.shape[:2]
+    p0a = _host_p0(p0, B)
+    cap = ki_codes.shape[1]
+    if ws is None:
+        ws = workspace(h, OP_REINDEX_TOPK, B, T, int(((p0a + T) // h.ratio).max()), qi.device)
+    _check("csa2_reindex_topk", lib().csa2_reindex_topk(
+        h.ptr, _dev(qi, torch.bfloat16, "qi"), _dev(wI, torch.bfloat16, "wI"), _dev(ki_codes, torch.uint8, "ki_codes"),
+        _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
+        _dev(pool, torch.int32, "pool"), _dev(idx, torch.int32, "idx"), _dev(top_scores, torch.float32, "top_scores"),
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
 
 
 def csa2_attend(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, out, ws=None, stream=None) -> None:

@@ -128,6 +128,8 @@ size_t csa2_workspace_bytes(const csa2_handle* h, int op, int B, int T, int64_t 
     case CSA2_OP_WRITE_CACHE: return 0;
     case CSA2_OP_INDEX_TOPK: return csa2::index_workspace_bytes(B, T, max_entries, h->num_sms);
     case CSA2_OP_ATTEND: return csa2::attend_workspace_bytes(B, T, h->num_sms);
+    case CSA2_OP_INDEX_POOL: return csa2::index_workspace_bytes(B, T, max_entries, h->num_sms, csa2::kIndexPool);
+    case CSA2_OP_REINDEX_TOPK: return csa2::index_workspace_bytes(B, T, max_entries, h->num_sms, csa2::kIndexReindex);
   }
   return 0;
 }
@@ -168,10 +170,16 @@ csa2_status csa2_write_cache(csa2_handle* h, const uint16_t* kc, const uint16_t*
   return CSA2_OK;
 }
 
-csa2_status csa2_index_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, const uint8_t* ki_codes,
-                            const uint8_t* ki_scales, int64_t cap, const int64_t* p0, int B, int T, int32_t* idx,
-                            float* top_scores, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+namespace {
+
+// Shared body of the three indexer entry points: mode selects the plain top-512, the top-512
+// plus the hierarchical pool, or the top-512 over a given pool.
+csa2_status index_call(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, const uint8_t* ki_codes,
+                       const uint8_t* ki_scales, int64_t cap, const int64_t* p0, int B, int T, int32_t* idx,
+                       float* top_scores, int32_t* pool_out, const int32_t* pool_in, int mode, void* ws,
+                       size_t ws_bytes, csa2_stream_t stream) {
   if (!h || !qi || !wI || !ki_codes || !ki_scales || !idx) return CSA2_ERR_INVALID_ARG;
+  if ((mode == csa2::kIndexPool && !pool_out) || (mode == csa2::kIndexReindex && !pool_in)) return CSA2_ERR_INVALID_ARG;
   if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
   csa2_status st = check_p0(p0, B, T);
   if (st != CSA2_OK) return st;
@@ -182,20 +190,49 @@ csa2_status csa2_index_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* 
   for (const void* p : ptrs)
     if (!aligned16(p)) return CSA2_ERR_ALIGN;
   if (top_scores && !aligned16(top_scores)) return CSA2_ERR_ALIGN;
-  const size_t need = csa2::index_workspace_bytes(B, T, emax, h->num_sms);
+  if ((pool_out && !aligned16(pool_out)) || (pool_in && !aligned16(pool_in))) return CSA2_ERR_ALIGN;
+  const size_t need = csa2::index_workspace_bytes(B, T, emax, h->num_sms, mode);
   if (ws_bytes < need || (need && !ws)) return CSA2_ERR_WORKSPACE;
   if (!aligned16(ws)) return CSA2_ERR_ALIGN;
   csa2::IndexArgs a{};
   a.qi = qi; a.wI = wI; a.ki_codes = ki_codes; a.ki_scales = ki_scales; a.cap = cap; a.T = T;
   a.rshift = h->rshift;
   a.idx = idx; a.top_scores = top_scores;
+  a.pool_out = mode == csa2::kIndexPool ? pool_out : nullptr;
+  a.pool_in = mode == csa2::kIndexReindex ? pool_in : nullptr;
   for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
     const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
     st = cuda_status(csa2::launch_index_topk(a, pack_pos(p0, b0, nb), b0, nb, emax, ws, ws_bytes, h->num_sms,
-                                             reinterpret_cast<cudaStream_t>(stream)));
+                                             reinterpret_cast<cudaStream_t>(stream), mode));
     if (st != CSA2_OK) return st;
   }
   return CSA2_OK;
+}
+
+}  // namespace
+
+csa2_status csa2_index_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, const uint8_t* ki_codes,
+                            const uint8_t* ki_scales, int64_t cap, const int64_t* p0, int B, int T, int32_t* idx,
+                            float* top_scores, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  return index_call(h, qi, wI, ki_codes, ki_scales, cap, p0, B, T, idx, top_scores, nullptr, nullptr,
+                    csa2::kIndexTopk, ws, ws_bytes, stream);
+}
+
+// Hierarchical Sparse Indexer, owner layer (include/csa2.h): the top-512 plus the block pool.
+csa2_status csa2_index_pool(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, const uint8_t* ki_codes,
+                            const uint8_t* ki_scales, int64_t cap, const int64_t* p0, int B, int T, int32_t* idx,
+                            float* top_scores, int32_t* pool, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  return index_call(h, qi, wI, ki_codes, ki_scales, cap, p0, B, T, idx, top_scores, pool, nullptr, csa2::kIndexPool,
+                    ws, ws_bytes, stream);
+}
+
+// Hierarchical Sparse Indexer, later layer (include/csa2.h): the top-512 over a given pool.
+csa2_status csa2_reindex_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, const uint8_t* ki_codes,
+                              const uint8_t* ki_scales, int64_t cap, const int64_t* p0, int B, int T,
+                              const int32_t* pool, int32_t* idx, float* top_scores, void* ws, size_t ws_bytes,
+                              csa2_stream_t stream) {
+  return index_call(h, qi, wI, ki_codes, ki_scales, cap, p0, B, T, idx, top_scores, nullptr, pool,
+                    csa2::kIndexReindex, ws, ws_bytes, stream);
 }
 
 csa2_status csa2_attend(csa2_handle* h, const uint16_t* q, const float* sinks, const uint8_t* z_codes,

@@ -305,7 +305,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
 //    group's parity; loads its 64 code bytes and 4 scale bytes straight from global memory two
 //    tiles ahead, decodes exactly to fp16 and writes the row into TMEM (kDSlots tiles).
 //  - warp 16 (one thread): the MMAs, A from TMEM, B (Q^I) from shared memory.
-// Each sequence's key tiles are split evenly over gridDim.x / nb persistent blocks.
+// Rows: one query (sequence bl, query t0 + tl) each; a row's key tiles are split evenly over
+// gridDim.x / rows persistent blocks.  With a pool (hierarchical indexer, reindex scan) the
+// row's positions p are its pool's entries 8 * pool[p / 8] + p % 8 instead of 0 .. E-1.
 constexpr int kDSlots = 4, kDThreads = 32 * 17;
 constexpr int kDDec0 = 8, kDMma = 16;
 constexpr uint32_t kDACol = 0;                    // TMEM: A tiles kDSlots x 64 columns
@@ -324,23 +326,50 @@ struct DecBars {
 };
 
 __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs a, SeqPos pos, int b0, int nb,
-                                                                       float* scores, int64_t ld) {
+                                                                       int t0, int tq, int Tq, float* scores,
+                                                                       int64_t ld, int* rowlen) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ DecBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ float wsh[kHI];
+  __shared__ int32_t spool[kHsiBlocks];
+  __shared__ int64_t n_sh;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   unsigned char* sm = smem_raw + (sbase - smem_u32(smem_raw));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int* err = &g_index_error;
-  // this block's sequence and key-tile range
-  const int per_seq = max(1, (int)gridDim.x / nb);
-  const int bl = blockIdx.x / per_seq, part = blockIdx.x % per_seq;
-  const bool active = bl < nb;
-  const int b = b0 + (active ? bl : 0);
-  const int64_t E = active ? (pos.p0[bl] + 1) >> a.rshift : 0;  // visible entries of the one query
-  const int ntile = (int)((E + 127) / 128);
-  const int tpb = (ntile + per_seq - 1) / per_seq;
+  // this block's query row and key-tile range
+  const int nrows = nb * tq;
+  const int per_row = max(1, (int)gridDim.x / nrows);
+  const int rr = blockIdx.x / per_row, part = blockIdx.x % per_row;
+  const bool active = rr < nrows;
+  const int bl = active ? rr / tq : 0, tl = active ? rr % tq : 0;
+  const int b = b0 + bl;
+  const int64_t qrow = (int64_t)b * a.T + t0 + tl;
+  const int64_t E = active ? (pos.p0[bl] + t0 + tl + 1) >> a.rshift : 0;  // visible entries of the query
+  const int32_t* prow = a.pool_in ? a.pool_in + qrow * kHsiBlocks : nullptr;
+  if (active && prow)
+    for (int i = tid; i < kHsiBlocks; i += kDThreads) spool[i] = prow[i];
+  __syncthreads();
+  if (tid == 0) {
+    int64_t n = E;
+    if (prow) {  // ascending blocks, -1 padded; only the last (newest) block can be partial
+      int lo = 0, hi = kHsiBlocks;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (spool[mid] >= 0) lo = mid + 1;
+        else hi = mid;
+      }
+      n = lo == 0 ? 0 : (int64_t)kHsiBlock * (lo - 1) + min64(kHsiBlock, E - (int64_t)kHsiBlock * spool[lo - 1]);
+      n = max64(n, 0);
+    }
+    n_sh = active ? n : 0;
+    if (rowlen && active && part == 0) rowlen[bl * Tq + tl] = (int)n_sh;
+  }
+  __syncthreads();
+  const int64_t n_pos = n_sh;  // positions of the row
+  const int ntile = (int)((n_pos + 127) / 128);
+  const int tpb = (ntile + per_row - 1) / per_row;
   const int t_begin = min(ntile, part * tpb), t_end = min(ntile, t_begin + tpb);
   const int nt = active ? t_end - t_begin : 0;
 
@@ -359,7 +388,7 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   // Q^I -> FP4 -> fp16 image (warps 8-11: warp heads 8(w-8)..+7, lane l values 4l..4l+3), w^I
   if (warp >= kDDec0 && warp < kDDec0 + 4 && active) {
     const int hw = warp - kDDec0;
-    const int64_t src = (int64_t)b * a.T;  // T == 1
+    const int64_t src = qrow;
     for (int h = 8 * hw; h < 8 * hw + 8; ++h) {
       const uint2 raw = *reinterpret_cast<const uint2*>(a.qi + (src * kHI + h) * kDI + 4 * lane);
       float v[4] = {bf16_to_f32(raw.x & 0xffff), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xffff), bf16_to_f32(raw.y >> 16)};
@@ -391,8 +420,9 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
     const uint8_t* codes = a.ki_codes + (int64_t)b * a.cap * 64;
     const uint8_t* scl = a.ki_scales + (int64_t)b * a.cap * 4;
     auto load = [&](int i, uint4 (&c)[4], uint32_t& sc) {
-      const int64_t j = (int64_t)(t_begin + i) * 128 + r;
-      if (i < nt && j < E) {
+      const int64_t pp = (int64_t)(t_begin + i) * 128 + r;
+      const int64_t j = i < nt && pp < n_pos && prow ? (int64_t)kHsiBlock * spool[pp >> 3] + (pp & 7) : pp;
+      if (i < nt && pp < n_pos && j >= 0 && j < E) {  // a pool entry outside 0..E-1 is read as zero
         const uint4* p = reinterpret_cast<const uint4*>(codes + j * 64);
 #pragma unroll
         for (int k = 0; k < 4; ++k) c[k] = __ldg(p + k);
@@ -466,7 +496,7 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
     const int grp = warp >> 2, q4 = warp & 3;  // tile parity, TMEM lane quarter
     const int r = 32 * q4 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16) + kDDCol + 32 * grp;
-    float* out = scores + (int64_t)bl * ld;
+    float* out = scores + ((int64_t)bl * Tq + tl) * ld;  // indexed by position
     float wr[kHI];
 #pragma unroll
     for (int h = 0; h < kHI; ++h) wr[h] = wsh[h];
@@ -482,8 +512,8 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
       float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains of 8
 #pragma unroll
       for (int h = 0; h < 32; ++h) s4[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(u[h]), 0.f), s4[h & 3]);
-      const int64_t j = (int64_t)(t_begin + i) * 128 + r;
-      if (j < E) out[j] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      const int64_t pp = (int64_t)(t_begin + i) * 128 + r;
+      if (pp < n_pos) out[pp] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     }
   }
   tc_fence_before();
@@ -496,12 +526,14 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
 
 }  // namespace
 
-cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, float* scores,
-                                          int64_t ld, int num_sms, cudaStream_t st) {
+cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq,
+                                          int Tq, float* scores, int64_t ld, int* rowlen, int num_sms,
+                                          cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(index_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynDec);
   if (e != cudaSuccess) return e;
-  const int grid = nb >= num_sms ? nb : (num_sms / nb) * nb;
-  index_decode_tc_kernel<<<grid, kDThreads, kDynDec, st>>>(a, pos, b0, nb, scores, ld);
+  const int nrows = nb * tq;
+  const int grid = nrows >= num_sms ? nrows : (num_sms / nrows) * nrows;
+  index_decode_tc_kernel<<<grid, kDThreads, kDynDec, st>>>(a, pos, b0, nb, t0, tq, Tq, scores, ld, rowlen);
   note_launch();
   return cudaGetLastError();
 }

@@ -32,13 +32,19 @@ struct IndexPlan {
   int chunk;        // top-k stage-1 chunk
   int nchunks;
   bool tc;          // prefill: tensor-core score GEMM (queries per pass >= kMinTcQueries)
-  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, off_img, total;
+  int pnch;         // hierarchical pool: chunks of kPoolChunk blocks (pool mode)
+  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, off_img, off_rl, off_pk, off_pj, off_pn, total;
 };
+
+constexpr int kPoolChunk = 16384;             // blocks per chunk of the pool select
+constexpr int kPoolSel = kHsiBlocks - 1;      // best other blocks; the newest is always added
 
 constexpr int kMinTcQueries = 8;
 
-IndexPlan make_plan(int nb, int T, int64_t max_entries) {
+IndexPlan make_plan(int nb, int T, int64_t max_entries, int mode = kIndexTopk) {
   IndexPlan p;
+  // a reindex row holds the pool's positions (at most 2048 blocks of 8), not all entries
+  if (mode == kIndexReindex) max_entries = min64(max_entries, (int64_t)kHsiBlock * kHsiBlocks);
   p.ld = ((max(max_entries, (int64_t)1) + 31) / 32) * 32;
   int64_t per_q = (int64_t)nb * p.ld * 4;
   int64_t tq = (int64_t)(kScoreBudget / (size_t)per_q);
@@ -48,7 +54,9 @@ IndexPlan make_plan(int nb, int T, int64_t max_entries) {
   p.chunk = (int)c;
   p.nchunks = (int)((p.ld + c - 1) / c);
   size_t rows = (size_t)nb * p.Tq;
-  p.tc = T >= kMinTcQueries;
+  p.tc = T >= kMinTcQueries && mode != kIndexReindex;  // a pool scan gathers rows per query
+  const int64_t nblk = (max_entries + kHsiBlock - 1) / kHsiBlock;
+  p.pnch = mode == kIndexPool && nblk > kHsiBlocks ? (int)((nblk + kPoolChunk - 1) / kPoolChunk) : 0;
   size_t off = 0;
   p.off_q = off; off += p.tc ? 0 : align256(rows * kHI * kDI * 4);
   p.off_w = off; off += align256(rows * kHI * 4);
@@ -57,6 +65,10 @@ IndexPlan make_plan(int nb, int T, int64_t max_entries) {
   p.off_cj = off; off += align256(rows * p.nchunks * kTopK * 4);
   p.off_cn = off; off += align256(rows * p.nchunks * 4);
   p.off_img = off; off += p.tc ? align256(index_tc_image_bytes(nb, p.Tq, p.ld)) : 0;
+  p.off_rl = off; off += mode == kIndexReindex ? align256(rows * 4) : 0;
+  p.off_pk = off; off += align256(rows * p.pnch * kPoolSel * 4);
+  p.off_pj = off; off += align256(rows * p.pnch * kPoolSel * 4);
+  p.off_pn = off; off += align256(rows * p.pnch * 4);
   p.total = off;
   return p;
 }
@@ -328,9 +340,15 @@ __device__ void compact_selected(const uint32_t* keys, const int32_t* js, int64_
 
 // Stage 1: grid (nchunks, rows, nb).  Local top-512 of one chunk of one query's scores.
 // With a single chunk the result is final and goes straight to idx / top_scores.
+// With a pool (reindex), a row's positions map to entries 8 * pool[p / 8] + p % 8 and rowlen
+// holds the number of visible positions.
+__device__ __forceinline__ int32_t pool_entry(const int32_t* prow, int32_t p) {
+  return prow ? kHsiBlock * prow[p >> 3] + (p & (kHsiBlock - 1)) : p;
+}
+
 __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, SeqPos pos, int b0, int t0, int Tq,
                                                                   const float* scores, int64_t ld, int chunk, int nchunks,
-                                                                  uint32_t* ck, int32_t* cj, int* cn) {
+                                                                  uint32_t* ck, int32_t* cj, int* cn, const int* rowlen) {
   extern __shared__ uint32_t skeys[];
   __shared__ SelectShared sh;
   __shared__ uint32_t okey[kTopK];
@@ -339,10 +357,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, S
   const int t = t0 + tl;
   if (t >= a.T || tl >= Tq) return;
   const int b = b0 + bl;
-  const int64_t E = (pos.p0[bl] + t + 1) >> a.rshift;
+  const int64_t row = (int64_t)bl * Tq + tl;
+  const int64_t E = rowlen ? rowlen[row] : (pos.p0[bl] + t + 1) >> a.rshift;
   const int64_t cs = (int64_t)c * chunk;
   const int n = (int)max64(0, min64(chunk, E - cs));
-  const int64_t row = (int64_t)bl * Tq + tl;
   const float* src = scores + row * ld + cs;  // 16-byte aligned: ld and the chunk are multiples of 32
   const int n4 = n >> 2;
   constexpr int kLB = 4;  // 16-byte loads in flight per thread
@@ -375,8 +393,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, S
   if (nchunks == 1) {
     int32_t* idx = a.idx + ((int64_t)b * a.T + t) * kTopK;
     float* ts = a.top_scores ? a.top_scores + ((int64_t)b * a.T + t) * kTopK : nullptr;
+    const int32_t* prow = a.pool_in ? a.pool_in + ((int64_t)b * a.T + t) * kHsiBlocks : nullptr;
     for (int i = threadIdx.x; i < kTopK; i += kTopkThreads) {
-      idx[i] = i < K ? oj[i] : -1;
+      idx[i] = i < K ? pool_entry(prow, oj[i]) : -1;
       if (ts) ts[i] = i < K ? key_score(okey[i]) : __int_as_float(0x7fc00000);
     }
   } else {
@@ -450,26 +469,138 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(IndexArgs a, i
   __syncthreads();
   int32_t* idx = a.idx + ((int64_t)b * a.T + t) * kTopK;
   float* ts = a.top_scores ? a.top_scores + ((int64_t)b * a.T + t) * kTopK : nullptr;
+  const int32_t* prow = a.pool_in ? a.pool_in + ((int64_t)b * a.T + t) * kHsiBlocks : nullptr;
   for (int i = threadIdx.x; i < kTopK; i += kTopkThreads) {
-    idx[i] = i < K ? oj[i] : -1;
+    idx[i] = i < K ? pool_entry(prow, oj[i]) : -1;
     if (ts) ts[i] = i < K ? key_score(okey[i]) : __int_as_float(0x7fc00000);
   }
+}
+
+// ------------------------------------------------------------------ hierarchical pool
+// "Inside DeepSeek V4.1", section "Most layers borrow": blocks of 8 entries scored by their
+// best entry, 2048 blocks kept, the block holding the newest entries always among them.
+// Pool = the newest block + the kPoolSel best other blocks (block score desc, block asc), or
+// every block when there are at most 2048; ascending, -1 padded.  The newest block's key is 0
+// (below every finite score) so that the select skips it; it is appended last.
+// Stage 1: grid (pool chunks, rows, nb).  A row with a single chunk writes its pool directly.
+__global__ void __launch_bounds__(kTopkThreads) pool_chunk_kernel(IndexArgs a, SeqPos pos, int b0, int t0, int Tq,
+                                                                  const float* scores, int64_t ld, int pnch,
+                                                                  uint32_t* pk, int32_t* pj, int* pn) {
+  extern __shared__ uint32_t pkeys[];  // [kPoolChunk] block keys, then okey / oj [kPoolSel]
+  uint32_t* okey = pkeys + kPoolChunk;
+  int32_t* oj = reinterpret_cast<int32_t*>(okey + kPoolSel);
+  __shared__ SelectShared sh;
+  const int c = blockIdx.x, tl = blockIdx.y, bl = blockIdx.z;
+  const int t = t0 + tl;
+  if (t >= a.T || tl >= Tq) return;
+  const int b = b0 + bl;
+  const int64_t E = (pos.p0[bl] + t + 1) >> a.rshift;
+  const int64_t nblk = (E + kHsiBlock - 1) / kHsiBlock;
+  int32_t* pool = a.pool_out + ((int64_t)b * a.T + t) * kHsiBlocks;
+  if (nblk <= kHsiBlocks) {  // every block
+    if (c == 0)
+      for (int i = threadIdx.x; i < kHsiBlocks; i += kTopkThreads) pool[i] = i < nblk ? i : -1;
+    return;
+  }
+  const int rnch = (int)((nblk + kPoolChunk - 1) / kPoolChunk);
+  if (c >= rnch) return;
+  const int64_t row = (int64_t)bl * Tq + tl;
+  const int64_t cb = (int64_t)c * kPoolChunk;
+  const int n = (int)min64(kPoolChunk, nblk - cb);
+  const float4* src = reinterpret_cast<const float4*>(scores + row * ld);  // 32-byte aligned blocks
+  for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+    const int64_t k = cb + i;
+    uint32_t key = 0u;
+    if (k != nblk - 1) {  // all 8 entries of an older block are visible
+      const float4 u = __ldg(src + 2 * k), v = __ldg(src + 2 * k + 1);
+      key = score_key(fmaxf(fmaxf(fmaxf(u.x, u.y), fmaxf(u.z, u.w)), fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w))));
+    }
+    pkeys[i] = key;
+  }
+  __syncthreads();
+  const int K = min(kPoolSel, n);
+  if (n <= kPoolSel) {
+    for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+      okey[i] = pkeys[i];
+      oj[i] = (int32_t)(cb + i);
+    }
+  } else {
+    uint32_t thr;
+    int need_eq;
+    radix_select(pkeys, n, K, sh, &thr, &need_eq);
+    compact_selected(pkeys, nullptr, cb, n, thr, need_eq, sh, okey, oj);
+  }
+  __syncthreads();
+  if (rnch == 1) {  // n = nblk > kPoolSel: the kPoolSel best older blocks, ascending, then the newest
+    for (int i = threadIdx.x; i < kHsiBlocks; i += kTopkThreads) pool[i] = i < kPoolSel ? oj[i] : (int32_t)(nblk - 1);
+  } else {
+    const int64_t base = (row * pnch + c) * kPoolSel;
+    for (int i = threadIdx.x; i < K; i += kTopkThreads) {
+      pk[base + i] = okey[i];
+      pj[base + i] = oj[i];
+    }
+    if (threadIdx.x == 0) pn[row * pnch + c] = K;
+  }
+}
+
+// Stage 2: grid (rows, nb).  Rows with more than one pool chunk: select from the chunk lists.
+__global__ void __launch_bounds__(kTopkThreads) pool_merge_kernel(IndexArgs a, SeqPos pos, int b0, int t0, int Tq,
+                                                                  int pnch, const uint32_t* pk, const int32_t* pj,
+                                                                  const int* pn) {
+  extern __shared__ uint32_t msm[];
+  uint32_t* keys = msm;                                                 // [pnch * kPoolSel]
+  int32_t* js = reinterpret_cast<int32_t*>(keys + pnch * kPoolSel);     // [pnch * kPoolSel]
+  uint32_t* okey = reinterpret_cast<uint32_t*>(js + pnch * kPoolSel);   // [kPoolSel]
+  int32_t* oj = reinterpret_cast<int32_t*>(okey + kPoolSel);            // [kPoolSel]
+  __shared__ SelectShared sh;
+  __shared__ int offs[kMaxChunks + 1];
+  const int tl = blockIdx.x, bl = blockIdx.y;
+  const int t = t0 + tl;
+  if (t >= a.T || tl >= Tq) return;
+  const int b = b0 + bl;
+  const int64_t E = (pos.p0[bl] + t + 1) >> a.rshift;
+  const int64_t nblk = (E + kHsiBlock - 1) / kHsiBlock;
+  const int rnch = (int)((nblk + kPoolChunk - 1) / kPoolChunk);
+  if (nblk <= kHsiBlocks || rnch <= 1) return;  // written by stage 1
+  const int64_t row = (int64_t)bl * Tq + tl;
+  if (threadIdx.x == 0) {
+    offs[0] = 0;
+    for (int c = 0; c < rnch; ++c) offs[c + 1] = offs[c] + pn[row * pnch + c];
+  }
+  __syncthreads();
+  const int n = offs[rnch];
+  for (int q = threadIdx.x; q < rnch * kPoolSel; q += kTopkThreads) {
+    const int c = q / kPoolSel, i = q % kPoolSel;
+    if (i < offs[c + 1] - offs[c]) {
+      const int64_t src = (row * pnch + c) * kPoolSel + i;
+      keys[offs[c] + i] = pk[src];
+      js[offs[c] + i] = pj[src];
+    }
+  }
+  __syncthreads();
+  uint32_t thr;
+  int need_eq;
+  radix_select(keys, n, kPoolSel, sh, &thr, &need_eq);  // n >= kPoolSel older blocks
+  compact_selected(keys, js, 0, n, thr, need_eq, sh, okey, oj);
+  __syncthreads();
+  int32_t* pool = a.pool_out + ((int64_t)b * a.T + t) * kHsiBlocks;
+  for (int i = threadIdx.x; i < kHsiBlocks; i += kTopkThreads) pool[i] = i < kPoolSel ? oj[i] : (int32_t)(nblk - 1);
 }
 
 }  // namespace
 
 // Launches take groups of kMaxSeqPerLaunch sequences; a smaller tail group may take more queries
 // per pass, so the need is the larger of the two group plans.
-size_t index_workspace_bytes(int B, int T, int64_t max_entries, int /*num_sms*/) {
-  size_t need = make_plan(min(B, kMaxSeqPerLaunch), T, max_entries).total;
+size_t index_workspace_bytes(int B, int T, int64_t max_entries, int /*num_sms*/, int mode) {
+  size_t need = make_plan(min(B, kMaxSeqPerLaunch), T, max_entries, mode).total;
   if (B > kMaxSeqPerLaunch && B % kMaxSeqPerLaunch)
-    need = std::max(need, make_plan(B % kMaxSeqPerLaunch, T, max_entries).total);
+    need = std::max(need, make_plan(B % kMaxSeqPerLaunch, T, max_entries, mode).total);
   return need;
 }
 
 cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int64_t max_entries, void* ws,
-                              size_t ws_bytes, int num_sms, cudaStream_t st) {
-  const IndexPlan p = make_plan(min(nb, kMaxSeqPerLaunch), a.T, max_entries);
+                              size_t ws_bytes, int num_sms, cudaStream_t st, int mode) {
+  const IndexPlan p = make_plan(min(nb, kMaxSeqPerLaunch), a.T, max_entries, mode);
   if (ws_bytes < p.total) return cudaErrorInvalidValue;
   char* base = static_cast<char*>(ws);
   float* qdq = reinterpret_cast<float*>(base + p.off_q);
@@ -478,6 +609,12 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
   uint32_t* ck = reinterpret_cast<uint32_t*>(base + p.off_ck);
   int32_t* cj = reinterpret_cast<int32_t*>(base + p.off_cj);
   int* cn = reinterpret_cast<int*>(base + p.off_cn);
+  int* rowlen = mode == kIndexReindex ? reinterpret_cast<int*>(base + p.off_rl) : nullptr;
+  uint32_t* pk = reinterpret_cast<uint32_t*>(base + p.off_pk);
+  int32_t* pj = reinterpret_cast<int32_t*>(base + p.off_pj);
+  int* pn = reinterpret_cast<int*>(base + p.off_pn);
+  const size_t pool_chunk_smem = (size_t)kPoolChunk * 4 + (size_t)kPoolSel * 8;
+  const size_t pool_merge_smem = (size_t)max(p.pnch, 1) * kPoolSel * 8 + (size_t)kPoolSel * 8;
   const size_t score_smem = (size_t)kQT * kHI * kDI * 4;
   const size_t chunk_smem = (size_t)p.chunk * 4;
   const size_t merge_smem = (size_t)p.nchunks * kTopK * 8;
@@ -488,17 +625,27 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)merge_smem);
   if (e != cudaSuccess) return e;
+  if (mode == kIndexPool) {
+    e = cudaFuncSetAttribute(pool_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pool_chunk_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(pool_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pool_merge_smem);
+    if (e != cudaSuccess) return e;
+  }
   for (int t0 = 0; t0 < a.T; t0 += p.Tq) {
     const int tq = min(p.Tq, a.T - t0);
     int64_t emax = 0;
     for (int i = 0; i < nb; ++i) emax = max(emax, (pos.p0[i] + t0 + tq) >> a.rshift);
-    if (p.tc) {
+    if (mode == kIndexReindex) {  // every query row scans its own pool
+      e = launch_index_scores_decode_tc(a, pos, b0, nb, t0, tq, p.Tq, sc, p.ld, rowlen, num_sms, st);
+      if (e != cudaSuccess) return e;
+      emax = min64(emax, (int64_t)kHsiBlock * kHsiBlocks);
+    } else if (p.tc) {
       e = launch_index_scores_tc(a, pos, b0, nb, t0, tq, p.Tq, emax, reinterpret_cast<uint8_t*>(base + p.off_img), wq, sc,
                                  p.ld, num_sms, st);
       if (e != cudaSuccess) return e;
     } else if (a.T == 1) {
       if (emax > 0) {
-        e = launch_index_scores_decode_tc(a, pos, b0, nb, sc, p.ld, num_sms, st);
+        e = launch_index_scores_decode_tc(a, pos, b0, nb, 0, 1, 1, sc, p.ld, nullptr, num_sms, st);
         if (e != cudaSuccess) return e;
       }
     } else {
@@ -506,7 +653,7 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
       note_launch();
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (!p.tc && a.T > 1 && emax > 0) {
+    if (mode != kIndexReindex && !p.tc && a.T > 1 && emax > 0) {
       dim3 g((unsigned)((emax + kScoreThreads - 1) / kScoreThreads), (unsigned)((tq + kQT - 1) / kQT), (unsigned)nb);
       score_kernel<<<g, kScoreThreads, score_smem, st>>>(a, pos, b0, t0, p.Tq, qdq, wq, sc, p.ld);
       note_launch();
@@ -514,13 +661,26 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
     }
     const int nch = (int)max64(1, (emax + p.chunk - 1) / p.chunk);
     topk_chunk_kernel<<<dim3(nch, tq, nb), kTopkThreads, chunk_smem, st>>>(a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch,
-                                                                            ck, cj, cn);
+                                                                            ck, cj, cn, rowlen);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (nch > 1) {
       topk_merge_kernel<<<dim3(tq, nb), kTopkThreads, (size_t)nch * kTopK * 8, st>>>(a, b0, t0, p.Tq, nch, ck, cj, cn);
       note_launch();
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (mode == kIndexPool) {  // the block pool from this pass's score rows
+      const int64_t nblk = (emax + kHsiBlock - 1) / kHsiBlock;
+      const int pn_launch = nblk > kHsiBlocks ? (int)((nblk + kPoolChunk - 1) / kPoolChunk) : 1;
+      pool_chunk_kernel<<<dim3(pn_launch, tq, nb), kTopkThreads, pool_chunk_smem, st>>>(a, pos, b0, t0, p.Tq, sc, p.ld,
+                                                                                      p.pnch, pk, pj, pn);
+      note_launch();
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if (pn_launch > 1) {
+        pool_merge_kernel<<<dim3(tq, nb), kTopkThreads, pool_merge_smem, st>>>(a, pos, b0, t0, p.Tq, p.pnch, pk, pj, pn);
+        note_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      }
     }
   }
   return cudaSuccess;

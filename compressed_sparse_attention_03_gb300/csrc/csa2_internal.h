@@ -44,7 +44,14 @@ struct IndexArgs {
   int rshift;  // log2 of the compression ratio: query t sees entries j < (t+1) >> rshift
   int32_t* idx;
   float* top_scores;
+  // hierarchical indexer: pool_out [B, T, 2048] receives the block pool (csa2_index_pool);
+  // pool_in [B, T, 2048] restricts the scan to a pool (csa2_reindex_topk)
+  int32_t* pool_out;
+  const int32_t* pool_in;
 };
+
+constexpr int kHsiBlock = 8, kHsiBlocks = 2048;  // blocks of 8 entries, 2048 blocks per pool
+enum IndexMode { kIndexTopk = 0, kIndexPool = 1, kIndexReindex = 2 };
 
 struct AttendArgs {
   const uint16_t* q;
@@ -60,15 +67,19 @@ struct AttendArgs {
 // `b0` is the batch index of the first sequence in `pos`, `nb` how many follow.
 cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf,
                           cudaStream_t st);
-size_t index_workspace_bytes(int B, int T, int64_t max_entries, int num_sms);
+size_t index_workspace_bytes(int B, int T, int64_t max_entries, int num_sms, int mode = kIndexTopk);
 cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int64_t max_entries,
-                              void* ws, size_t ws_bytes, int num_sms, cudaStream_t st);
+                              void* ws, size_t ws_bytes, int num_sms, cudaStream_t st, int mode = kIndexTopk);
 size_t index_tc_image_bytes(int nb, int Tq, int64_t max_entries);
 cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq, int Tq,
                                    int64_t emax, uint8_t* img, float* wq, float* scores, int64_t ld, int num_sms,
                                    cudaStream_t st);
-cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, float* scores,
-                                          int64_t ld, int num_sms, cudaStream_t st);
+// One query row per (sequence, t) of the pass t0 .. t0+tq-1 (T == 1, or a pool scan); row r =
+// bl * Tq + tl.  With a.pool_in, row r's positions are its pool's entries and rowlen[r]
+// receives the number of visible ones.
+cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq,
+                                          int Tq, float* scores, int64_t ld, int* rowlen, int num_sms,
+                                          cudaStream_t st);
 // Counts one kernel enqueued by this library (read back by csa2_kernel_launches).
 void note_launch();
 

@@ -91,7 +91,13 @@ const char* csa2_status_string(csa2_status s);
  * device; a launch that failed is counted too).  Host-side counter; never synchronises. */
 uint64_t csa2_kernel_launches(void);
 
-enum { CSA2_OP_WRITE_CACHE = 0, CSA2_OP_INDEX_TOPK = 1, CSA2_OP_ATTEND = 2 };
+enum {
+  CSA2_OP_WRITE_CACHE = 0,
+  CSA2_OP_INDEX_TOPK = 1,
+  CSA2_OP_ATTEND = 2,
+  CSA2_OP_INDEX_POOL = 3,
+  CSA2_OP_REINDEX_TOPK = 4
+};
 
 /* Bytes of workspace the call `op` needs for B sequences of T new tokens whose largest
  * visible entry count is at most max_entries (for decode: the cached entries).  Returns 0
@@ -139,6 +145,34 @@ csa2_status csa2_index_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* 
                             const uint8_t* ki_codes, const uint8_t* ki_scales, int64_t cap,
                             const int64_t* p0, int B, int T, int32_t* idx, float* top_scores,
                             void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* (2)+(3) Hierarchical Sparse Indexer, owner layer ("Inside DeepSeek V4.1", section "Most
+ * layers borrow"; "Deriving the 890-Byte KV Cache", section "Hierarchical indexing bounds the
+ * later searches").  Arguments and idx / top_scores as csa2_index_topk, plus
+ *  pool : int32 [B, T, 2048] per query the entry blocks (block k = entries 8k..8k+7) that
+ *         later layers search: the newest block (the one holding entry E-1, E the visible
+ *         entries) and the 2047 other blocks with the largest block score (the maximum of
+ *         S^I over its 8 entries; equal scores: lower block first).  With at most 2048 blocks
+ *         every block is kept.  Ascending, -1 padded.
+ * Workspace: csa2_workspace_bytes(h, CSA2_OP_INDEX_POOL, B, T, max_entries). */
+csa2_status csa2_index_pool(csa2_handle* h, const uint16_t* qi, const uint16_t* wI,
+                            const uint8_t* ki_codes, const uint8_t* ki_scales, int64_t cap,
+                            const int64_t* p0, int B, int T, int32_t* idx, float* top_scores,
+                            int32_t* pool, void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* (2)+(3) Hierarchical Sparse Indexer, later layer: S^I of this layer's queries over the
+ * entries of `pool` only (same pages and sections as csa2_index_pool), and their top-512.
+ *  pool : int32 [B, T, 2048] as written by csa2_index_pool for the same p0 and T: ascending
+ *         blocks, -1 padded, every block but the last fully visible.  A block outside that
+ *         rule gives unspecified idx (entries it names beyond E-1 are scored as zero keys)
+ *         but no access outside the caches.
+ *  idx / top_scores : as csa2_index_topk, over the pool's visible entries (at most 16384).
+ * Workspace: csa2_workspace_bytes(h, CSA2_OP_REINDEX_TOPK, B, T, max_entries). */
+csa2_status csa2_reindex_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* wI,
+                              const uint8_t* ki_codes, const uint8_t* ki_scales, int64_t cap,
+                              const int64_t* p0, int B, int T, const int32_t* pool,
+                              int32_t* idx, float* top_scores, void* ws, size_t ws_bytes,
+                              csa2_stream_t stream);
 
 /* (4) Sink-softmax MQA, [PG] equations for J^w_t, Y, J, G_t, S, A, O and O-bar.
  *  q      : bf16 [B, T, 64, 512] queries, RoPE already applied to dims 448..511.

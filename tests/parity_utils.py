@@ -88,14 +88,15 @@ def e4m3_compare(g, o, pre):
     return int(bad.sum())
 
 
-def topk_compare(g_idx, o_idx, o_scores, kth, E):
+def topk_compare(g_idx, o_idx, o_scores, kth, E, n_cand=None):
     """Rows of GPU vs oracle top-512 indices.  o_scores [nq, >=E]: oracle fp64 scores;
-    kth [nq, 2]: oracle 512th / 513th scores.  Returns the number of swapped entries."""
+    kth [nq, 2]: oracle 512th / 513th scores; entries lie in 0..E-1 and n_cand (default E)
+    are candidates.  Returns the number of swapped entries."""
     g_idx, o_idx = np.asarray(g_idx), np.asarray(o_idx)
     swaps = 0
     for r in range(g_idx.shape[0]):
         g = g_idx[r]
-        k = min(512, int(E[r]))
+        k = min(512, int(E[r] if n_cand is None else n_cand[r]))
         assert np.all(g[k:] == -1), f"row {r}: expected {512 - k} trailing -1"
         gv = g[:k]
         assert np.all(np.diff(gv) > 0) and (k == 0 or (gv[0] >= 0 and gv[-1] < E[r])), f"row {r}: not ascending / out of range"
@@ -135,3 +136,43 @@ def random_indices(B, T, p0s, seed, device="cpu"):
                 sel = torch.randperm(E, generator=g)[:k].sort().values
                 idx[b, t, :k] = sel.to(torch.int32)
     return idx.to(device)
+
+
+def pool_compare(g_pool, o_pool, scores, E, nsel=2047, nblocks=2048, block=8):
+    """Rows of GPU vs oracle hierarchical pools.  A row must be ascending, -1 padded, hold
+    min(blocks, nblocks) blocks and the newest block; a block present on one side only is
+    allowed where its oracle block score lies within REL_TIE of the oracle's nsel-th best
+    older block.  Returns the number of swapped blocks."""
+    g_pool, o_pool = np.asarray(g_pool), np.asarray(o_pool)
+    swaps = 0
+    for r in range(g_pool.shape[0]):
+        nb = (int(E[r]) + block - 1) // block
+        k = min(nb, nblocks)
+        g = g_pool[r]
+        assert np.all(g[k:] == -1), f"row {r}: expected {nblocks - k} trailing -1"
+        gv = g[:k]
+        assert np.all(np.diff(gv) > 0) and (k == 0 or (gv[0] >= 0 and gv[-1] == nb - 1)), f"row {r}: pool order"
+        if np.array_equal(gv, o_pool[r, :k]):
+            continue
+        bs = scores[r, : (nb - 1) * block].reshape(nb - 1, block).max(axis=1)
+        bound = np.sort(bs)[::-1][nsel - 1]
+        a, b = np.setdiff1d(gv, o_pool[r, :k]), np.setdiff1d(o_pool[r, :k], gv)
+        for j in np.concatenate([a, b]):
+            assert abs(bs[j] - bound) <= REL_TIE * abs(bound), (
+                f"row {r}: block {j} swapped with oracle block score {bs[j]!r} vs boundary {bound!r}")
+        swaps += len(a)
+    return swaps
+
+
+def pool_kth(scores, E, pool, k=512, block=8):
+    """Oracle k-th and (k+1)-th largest scores over each row's pool entries (-inf if none)."""
+    kth = np.full((scores.shape[0], 2), -np.inf)
+    for r in range(scores.shape[0]):
+        blks = pool[r][pool[r] >= 0].astype(np.int64)
+        j = (block * blks[:, None] + np.arange(block)[None, :]).ravel()
+        j = j[j < E[r]]
+        v = np.sort(scores[r, j])[::-1]
+        for c in range(2):
+            if len(v) > k - 1 + c:
+                kth[r, c] = v[k - 1 + c]
+    return kth
