@@ -91,6 +91,16 @@ def indexer_pairs(B: int, p0: int, T: int, ratio: int = 2) -> int:
     return int(B * ((t + 1) // ratio).sum())
 
 
+def hsi_bytes(B: int, p0: int, ratio: int = 2) -> dict:
+    """Algorithmic HBM bytes of the hierarchical indexer at decode (T=1): the owner layer reads
+    every visible key (68 B) and writes the top-512 and the 2048-block pool; a later layer reads
+    its pool and the keys of at most 2048 blocks of 8 and writes its top-512."""
+    E = (p0 + 1) // ratio
+    q = HI * DI * 2 + HI * 2
+    n_re = min(E, 8 * 2048)
+    return dict(owner=B * (E * 68 + q + 512 * 4 + 2048 * 4), reindex=B * (2048 * 4 + n_re * 68 + q + 512 * 4))
+
+
 def decode_bytes(B: int, p0: int, ratio: int = 2) -> dict:
     """Algorithmic HBM bytes of one decode step (T=1): indexer keys over all visible entries,
     the 512 selected Z rows, 128 window rows, Q, Q^I, w^I, the output, the step's writes."""
@@ -240,6 +250,46 @@ def time_workload(step: Step, steps: int, warmup: int, ws: int, flush: torch.Ten
     return statistics.mean(total), {n: statistics.mean(v) for n, v in per.items()}, launches
 
 
+def time_hsi(csa2, step: Step, steps: int, warmup: int, ws: int, flush: torch.Tensor):
+    """Owner layer (csa2_index_pool) and a later layer (csa2_reindex_topk over that pool), one
+    after the other on the step's resident queries and keys; per-call device times."""
+    wl, x, dev = step.wl, step.x, step.idx.device
+    pool = torch.empty(wl.B, wl.T, csa2.HSI_BLOCKS, dtype=torch.int32, device=dev)
+    idx2 = torch.empty_like(step.idx)
+    ws_p = csa2.workspace(step.h, csa2.OP_INDEX_POOL, wl.B, wl.T, wl.cap, dev)
+    ws_r = csa2.workspace(step.h, csa2.OP_REINDEX_TOPK, wl.B, wl.T, wl.cap, dev)
+    s = torch.cuda.current_stream()
+
+    def owner():
+        csa2.csa2_index_pool(step.h, x["qi"], x["wI"], x["ki_codes"], x["ki_scales"], step.p0, step.idx, pool,
+                             ws=ws_p, stream=s)
+
+    def later():
+        csa2.csa2_reindex_topk(step.h, x["qi"], x["wI"], x["ki_codes"], x["ki_scales"], step.p0, pool, idx2,
+                               ws=ws_r, stream=s)
+
+    for _ in range(warmup):
+        owner(); later()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    launches0 = csa2.csa2_kernel_launches()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(s)
+        owner()
+        ev[i][1].record(s)
+        later()
+        ev[i][2].record(s)
+    torch.cuda.synchronize()
+    launches = csa2.csa2_kernel_launches() - launches0
+    barrier(ws)
+    own = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(steps))
+    re = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(steps))
+    return own, re, launches
+
+
 class _Null:
     def __enter__(self):
         return self
@@ -364,6 +414,23 @@ def run_ours(args, rank, ws):
             "gpu_launches": dlaunches,
         }
         del dstep
+    if not args.no_decode and args.hsi_workload:
+        hw = inputs.WORKLOADS[args.hsi_workload]
+        hstep = Step(csa2, inputs, hw, seed_for_rank(hw.seed, rank), dev)
+        own_ms, re_ms, hl = time_hsi(csa2, hstep, args.steps, args.warmup, ws, flush)
+        own_ms, re_ms = max_over_ranks(own_ms, ws), max_over_ranks(re_ms, ws)
+        hb = hsi_bytes(hw.B, hw.p0, hw.ratio)
+        line["hsi"] = {
+            "workload": hw.name, "B": hw.B, "p0": hw.p0, "ratio": hw.ratio,
+            "owner_ms": own_ms, "reindex_ms": re_ms,
+            "roofline_owner": {"bound": "hbm", "achieved": hb["owner"] / (own_ms / 1e3) / 1e9, "peak": hbm,
+                               "unit": "GB/s", "frac": hb["owner"] / (own_ms / 1e3) / 1e9 / hbm, "bytes": hb["owner"]},
+            "roofline_reindex": {"bound": "hbm", "achieved": hb["reindex"] / (re_ms / 1e3) / 1e9, "peak": hbm,
+                                 "unit": "GB/s", "frac": hb["reindex"] / (re_ms / 1e3) / 1e9 / hbm,
+                                 "bytes": hb["reindex"]},
+            "gpu_launches": hl,
+        }
+        del hstep
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     return line
@@ -446,6 +513,7 @@ def main():
     ap.add_argument("--workload", default="prefill_4k")
     ap.add_argument("--decode-workload", default="decode_1m")
     ap.add_argument("--ratio1-workload", default="decode_512k_r1", help="empty: skip the ratio-1 decode object")
+    ap.add_argument("--hsi-workload", default="decode_1m", help="empty: skip the hierarchical-indexer object")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

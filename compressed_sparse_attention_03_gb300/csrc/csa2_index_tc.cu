@@ -35,10 +35,12 @@ constexpr uint32_t kBOff = 0, kAOff = 131072, kWOff = 196608, kDynTC = 196608 + 
 
 __device__ int g_index_error;
 
-__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n}\n" : "=r"(r) : "r"(byte));
-  return r;
+// Four code bytes (8 values, element 2k in the low nibble of byte k) -> four f16x2.
+__device__ __forceinline__ void cvt_e2m1x8_f16x8(uint32_t w, uint32_t* o) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      " cvt.rn.f16x2.e2m1x2 %1, b1;\n cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
 }
 __device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t y) {
   uint32_t r;
@@ -299,37 +301,56 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
 // would cost 4x the key bytes in extra HBM traffic) and the decoded tile goes to tensor
 // memory, where the MMA reads its A operand: staging it in shared memory made the 32 KB
 // store + 32 KB operand read per tile the bottleneck of the shared-memory port.
-//  - warps 0-7 (epilogue, group = warp / 4, TMEM lane quarter = warp % 4): ReLU, the w^I
-//    weighting and the fp32 score stores for the tiles of their parity (accumulator = parity).
-//  - warps 8-15 (decoders, group = (warp - 8) / 4): thread = key row of the tiles of the
-//    group's parity; loads its 64 code bytes and 4 scale bytes straight from global memory two
-//    tiles ahead, decodes exactly to fp16 and writes the row into TMEM (kDSlots tiles).
-//  - warp 16 (one thread): the MMAs, A from TMEM, B (Q^I) from shared memory.
+//  - warps 0-3 (epilogue, TMEM lane quarter = warp): ReLU, the w^I weighting and the fp32
+//    score stores of every tile (accumulator = tile % 4).
+//  - warp 22 (producer): bulk copies of the code bytes (64 per key) of kDGroup tiles at a
+//    time (one copy of their contiguous keys, or one per pool block of 8) into a ring of
+//    kDStages groups in shared memory.  Per-thread loads could not keep enough bytes in
+//    flight (the load queue filled long before HBM did), and one bulk copy per 8 KB tile ran
+//    at well under the copy bandwidth that 16 KB copies reach.
+//  - warps 4-19 (decoders, group = (warp - 4) / 4, rows 32 * (warp % 4) ..): the tiles
+//    i = group mod kDGroups, lane = key row; four groups, so that each warp has four tiles'
+//    time for the latency of its decode chain.  The 4 scale bytes of a row come by a plain
+//    load issued two group tiles ahead; the codes from the stage.  Exact decode to fp16 into TMEM
+//    (kDSlots tiles); rows past the last key (or naming an entry outside 0..E-1) are zero.
+//  - warps 20 and 21 (one thread each): the MMAs of the even / odd tiles, A from TMEM, B
+//    (Q^I) from shared memory.  A thread that waits stalls until its own MMAs in flight have
+//    finished; with two issuers one of them keeps the tensor pipe busy meanwhile.
 // Rows: one query (sequence bl, query t0 + tl) each; a row's key tiles are split evenly over
-// gridDim.x / rows persistent blocks.  With a pool (hierarchical indexer, reindex scan) the
-// row's positions p are its pool's entries 8 * pool[p / 8] + p % 8 instead of 0 .. E-1.
-constexpr int kDSlots = 4, kDThreads = 32 * 17;
-constexpr int kDDec0 = 8, kDMma = 16;
+// gridDim.x / rows persistent blocks.  With hist, each row also gets the histogram of its
+// score keys (kHistBins bins, added up over its blocks) that lets the top-k skip most keys.
+// With a pool (hierarchical indexer, reindex scan) the row's positions p are its pool's
+// entries 8 * pool[p / 8] + p % 8 instead of 0 .. E-1.
+constexpr int kDSlots = 6, kDAcc = 4, kDGroups = 4, kDThreads = 32 * 23;
+constexpr int kDDec0 = 4, kDMma = 20, kDProd = 22;  // MMA issuers: warps 20 (even tiles) and 21 (odd)
 constexpr uint32_t kDACol = 0;                    // TMEM: A tiles kDSlots x 64 columns
-constexpr uint32_t kDDCol = kDSlots * 64;          // TMEM: two 32-column accumulators
+constexpr uint32_t kDDCol = kDSlots * 64;          // TMEM: kDAcc 32-column accumulators
 constexpr uint32_t kDTmemCols = 512;
 constexpr uint32_t kDQOff = 0;                     // smem: Q^I image, 2 atoms x [32 heads x 128 B]
-constexpr uint32_t kDynDec = kDQOff + 8192 + 1024;
+constexpr int kDGroup = 2;                         // tiles per stage (one copy)
+constexpr int kDStages = 6;                        // stages in the ring
+constexpr uint32_t kDStageOff = kDQOff + 8192;     // smem: codes [kDStages][kDGroup x 128 rows x 64 B]
+constexpr uint32_t kDynDec = kDStageOff + kDStages * kDGroup * 8192 + 1024;
+static_assert(kDGroup == 2, "a stage holds two tiles (of two decoder groups)");
 static_assert(kDSlots % 2 == 0, "a decoder group keeps the parity of its tiles");
-static_assert(kDDCol + 64 <= kDTmemCols, "TMEM columns");
+static_assert(kDDCol + 32 * kDAcc <= kDTmemCols, "TMEM columns");
+static_assert(kDAcc == 4, "accumulator = tile & 3");
 
 // a_full[slot]: the tile in a slot is decoded (4 decoder warps).  done[slot]: the MMAs of the
 // tile in a slot completed (one commit): the slot is free and accumulator slot & 1 holds its
-// scores.  d_free[k]: the epilogue group of parity k has read accumulator k (4 warps).
+// scores.  d_free[k]: the epilogue group of tile parity k & 1 has read accumulator k (4 warps).
+// s_full[s] / s_empty[s]: stage s holds its tiles' codes (transaction count) / the decoder
+// warps of its tiles (four per tile) have read it.
 struct DecBars {
-  uint64_t a_full[kDSlots], done[kDSlots], d_free[2];
+  uint64_t a_full[kDSlots], done[kDSlots], d_free[kDAcc], s_full[kDStages], s_empty[kDStages];
 };
 
 __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs a, SeqPos pos, int b0, int nb,
                                                                        int t0, int tq, int Tq, float* scores,
-                                                                       int64_t ld, int* rowlen) {
+                                                                       int64_t ld, int* rowlen, uint32_t* hist) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ DecBars bars;
+  __shared__ uint32_t shist[kHistBins];
   __shared__ uint32_t tmem_base_sh;
   __shared__ float wsh[kHI];
   __shared__ int32_t spool[kHsiBlocks];
@@ -350,6 +371,8 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   const int32_t* prow = a.pool_in ? a.pool_in + qrow * kHsiBlocks : nullptr;
   if (active && prow)
     for (int i = tid; i < kHsiBlocks; i += kDThreads) spool[i] = prow[i];
+  if (hist)
+    for (int i = tid; i < kHistBins; i += kDThreads) shist[i] = 0u;
   __syncthreads();
   if (tid == 0) {
     int64_t n = E;
@@ -378,7 +401,11 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
       mbar_init(&bars.a_full[i], 4);  // the four warps of one decoder group
       mbar_init(&bars.done[i], 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&bars.d_free[i], 4);  // the four warps of one epilogue group
+    for (int i = 0; i < kDAcc; ++i) mbar_init(&bars.d_free[i], 4);  // the four warps of one epilogue group
+    for (int i = 0; i < kDStages; ++i) {
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.s_empty[i], 4 * kDGroup);
+    }
     mbar_fence_init();
   }
   if (warp == kDMma) {
@@ -412,78 +439,107 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp >= kDDec0 && warp < kDDec0 + 8) {
+  if (warp >= kDDec0 && warp < kDDec0 + 4 * kDGroups) {
     // ============================================================ decoders: thread = key row
     const int grp = (warp - kDDec0) >> 2, q4 = warp & 3;
-    const int r = 32 * q4 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint8_t* codes = a.ki_codes + (int64_t)b * a.cap * 64;
     const uint8_t* scl = a.ki_scales + (int64_t)b * a.cap * 4;
-    auto load = [&](int i, uint4 (&c)[4], uint32_t& sc) {
-      const int64_t pp = (int64_t)(t_begin + i) * 128 + r;
-      const int64_t j = i < nt && pp < n_pos && prow ? (int64_t)kHsiBlock * spool[pp >> 3] + (pp & 7) : pp;
-      if (i < nt && pp < n_pos && j >= 0 && j < E) {  // a pool entry outside 0..E-1 is read as zero
-        const uint4* p = reinterpret_cast<const uint4*>(codes + j * 64);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) c[k] = __ldg(p + k);
-        sc = __ldg(reinterpret_cast<const uint32_t*>(scl + j * 4));
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) c[k] = make_uint4(0u, 0u, 0u, 0u);  // rows past the last key: zero
-        sc = 0x7f7f7f7fu;
-      }
+    // the entry at this lane's row of tile i, or -1 (past the last key, or a pool entry
+    // outside 0..E-1)
+    auto entry = [&](int i) -> int64_t {
+      const int64_t pp = (int64_t)(t_begin + i) * 128 + 32 * q4 + lane;
+      if (i >= nt || pp >= n_pos) return -1;
+      const int64_t j = prow ? (int64_t)kHsiBlock * spool[pp >> 3] + (pp & 7) : pp;
+      return j >= 0 && j < E ? j : -1;
     };
-    uint4 ca[4], cb[4];
-    uint32_t sa, sb;
-    load(grp, ca, sa);
-    load(grp + 2, cb, sb);
+    auto scale = [&](int i) -> uint32_t {
+      const int64_t j = entry(i);
+      return j >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(scl + j * 4)) : 0u;
+    };
+    uint32_t sa = scale(grp), sb = scale(grp + kDGroups);
 #pragma unroll 1
-    for (int i = grp; i < nt; i += 2) {
-      uint4 cc[4];
-      uint32_t scc;
-      load(i + 4, cc, scc);  // two tiles of this group ahead
+    for (int i = grp; i < nt; i += kDGroups) {
+      const uint32_t sc_next = scale(i + 2 * kDGroups);  // two group tiles ahead
+      const int gi = i / kDGroup, s = gi % kDStages;
+      const bool valid = entry(i) >= 0;
+      mbar_wait(&bars.s_full[s], (gi / kDStages) & 1, err, 35);
+      uint4 cw[4];
+      const uint4* rc = reinterpret_cast<const uint4*>(sm + kDStageOff + (s * kDGroup + i % kDGroup) * 8192 +
+                                                       (32 * q4 + lane) * 64);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cw[k] = valid ? rc[k] : make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.s_empty[s]);  // the codes are in registers
       const int slot = i % kDSlots;
       if (i >= kDSlots) mbar_wait(&bars.done[slot], ((i / kDSlots) - 1) & 1, err, 34);  // slot's last tile done
       tc_fence_after();
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {  // 32 values: 16 code bytes, one scale byte
         const uint32_t s2 = pow2_h2((int)((sa >> (8 * blk)) & 255u) - 127);
-        const uint32_t wd[4] = {ca[blk].x, ca[blk].y, ca[blk].z, ca[blk].w};
+        const uint32_t wd[4] = {cw[blk].x, cw[blk].y, cw[blk].z, cw[blk].w};
         uint32_t o[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 4; ++q) {
+          cvt_e2m1x8_f16x8(wd[q], o + 4 * q);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) o[4 * q + k] = hmul2(cvt_e2m1x2_f16x2((wd[q] >> (8 * k)) & 255u), s2);
+          for (int k = 0; k < 4; ++k) o[4 * q + k] = hmul2(o[4 * q + k], s2);
+        }
         tmem_st16(lane_addr + kDACol + slot * 64 + 16 * blk, o);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.a_full[slot]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        ca[k] = cb[k];
-        cb[k] = cc[k];
-      }
       sa = sb;
-      sb = scc;
+      sb = sc_next;
     }
-  } else if (warp == kDMma) {
-    // ============================================================ MMA issuer
+  } else if (warp == kDProd) {
+    // ============================================================ producer: code stages
+    const uint8_t* codes = a.ki_codes + (int64_t)b * a.cap * 64;
+    const int64_t p_end = min64(n_pos, (int64_t)(t_begin + nt) * 128);  // this block's positions end here
+    const int ng = (nt + kDGroup - 1) / kDGroup;
+#pragma unroll 1
+    for (int gi = 0; gi < ng; ++gi) {
+      const int s = gi % kDStages;
+      if (gi >= kDStages) mbar_wait(&bars.s_empty[s], ((gi / kDStages) - 1) & 1, err, 36);
+      const int64_t p0g = (int64_t)(t_begin + gi * kDGroup) * 128;  // first position of the group
+      // lane k: the positions 8k .. 8k+7 of the group (one pool block; without a pool the
+      // group's keys are contiguous and lane 0 copies them all)
+      int64_t j0 = -1;
+      uint32_t bytes = 0;
+      const int64_t pp = p0g + 8 * lane;
+      if (pp < p_end) {
+        if (prow) {
+          j0 = (int64_t)kHsiBlock * spool[pp >> 3];
+          const int64_t nv = min64(8, p_end - pp);
+          const int64_t m = j0 >= 0 && j0 < E ? min64(nv, E - j0) : 0;
+          bytes = (uint32_t)(64 * m);
+        } else if (lane == 0) {
+          j0 = pp;
+          bytes = (uint32_t)(64 * min64(kDGroup * 128, p_end - pp));
+        }
+      }
+      const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
+      if (lane == 0) mbar_arrive_expect_tx(&bars.s_full[s], total);
+      __syncwarp();
+      if (bytes) bulk_g2s(sm + kDStageOff + s * kDGroup * 8192 + 8 * lane * 64, codes + j0 * 64, bytes, &bars.s_full[s]);
+    }
+  } else if (warp == kDMma || warp == kDMma + 1) {
+    // ============================================================ MMA issuers
     if (lane == 0) {
-      // The MMA thread shares its sub-partition with four busy warps: keep its instruction
+      // An MMA thread shares its sub-partition with four busy warps: keep its instruction
       // stream short (the Q^I descriptors never change; A and D are plain TMEM offsets).
       const uint32_t idesc = idesc_f16(false, false, 128, 32);
       uint64_t bdesc[8];
 #pragma unroll
       for (int k16 = 0; k16 < 8; ++k16)
         bdesc[k16] = sw128_desc(sbase + kDQOff + (k16 >> 2) * 4096 + (k16 & 3) * 32, 16, 1024);
-      for (int i = 0; i < nt; ++i) {
-        const int slot = i % kDSlots, sD = i & 1;
+      for (int i = warp - kDMma; i < nt; i += 2) {
+        const int slot = i % kDSlots, acc = i & 3;
         mbar_wait(&bars.a_full[slot], (i / kDSlots) & 1, err, 22);
-        if (i >= 2) mbar_wait(&bars.d_free[sD], ((i >> 1) - 1) & 1, err, 23);
+        if (i >= kDAcc) mbar_wait(&bars.d_free[acc], ((i >> 2) - 1) & 1, err, 23);
         tc_fence_after();
-        const uint32_t ta = tmem + kDACol + slot * 64, td = tmem + kDDCol + 32 * sD;
+        const uint32_t ta = tmem + kDACol + slot * 64, td = tmem + kDDCol + 32 * acc;
         mma_f16_ts(td, ta, bdesc[0], idesc, 0u);
 #pragma unroll
         for (int k16 = 1; k16 < 8; ++k16) mma_f16_ts(td, ta + 8 * k16, bdesc[k16], idesc, 1u);
@@ -493,27 +549,31 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
     __syncwarp();
   } else {
     // ============================================================ epilogue: thread = key lane
-    const int grp = warp >> 2, q4 = warp & 3;  // tile parity, TMEM lane quarter
+    const int q4 = warp & 3;  // TMEM lane quarter
     const int r = 32 * q4 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16) + kDDCol + 32 * grp;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16) + kDDCol;
     float* out = scores + ((int64_t)bl * Tq + tl) * ld;  // indexed by position
     float wr[kHI];
 #pragma unroll
     for (int h = 0; h < kHI; ++h) wr[h] = wsh[h];
-    for (int i = grp; i < nt; i += 2) {
+    for (int i = 0; i < nt; ++i) {
       mbar_wait(&bars.done[i % kDSlots], (i / kDSlots) & 1, err, 24);
       tc_fence_after();
       uint32_t u[32];
-      tmem_ld32(lane_addr, u);
+      tmem_ld32(lane_addr + 32 * (i & 3), u);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.d_free[grp]);
+      if (lane == 0) mbar_arrive(&bars.d_free[i & 3]);
       float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains of 8
 #pragma unroll
       for (int h = 0; h < 32; ++h) s4[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(u[h]), 0.f), s4[h & 3]);
       const int64_t pp = (int64_t)(t_begin + i) * 128 + r;
-      if (pp < n_pos) out[pp] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      if (pp < n_pos) {
+        const float sc = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        out[pp] = sc;
+        if (hist) atomicAdd(&shist[score_key(sc) >> kHistShift], 1u);
+      }
     }
   }
   tc_fence_before();
@@ -522,18 +582,27 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
     tc_fence_after();
     tmem_dealloc(tmem, kDTmemCols);
   }
+  if (hist && nt > 0) {  // this block's counts into the row's histogram
+    uint32_t* hrow = hist + ((int64_t)bl * Tq + tl) * kHistBins;
+    for (int i = tid; i < kHistBins; i += kDThreads)
+      if (shist[i]) atomicAdd(hrow + i, shist[i]);
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq,
-                                          int Tq, float* scores, int64_t ld, int* rowlen, int num_sms,
-                                          cudaStream_t st) {
+                                          int Tq, float* scores, int64_t ld, int* rowlen, uint32_t* hist,
+                                          int num_sms, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(index_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynDec);
   if (e != cudaSuccess) return e;
   const int nrows = nb * tq;
   const int grid = nrows >= num_sms ? nrows : (num_sms / nrows) * nrows;
-  index_decode_tc_kernel<<<grid, kDThreads, kDynDec, st>>>(a, pos, b0, nb, t0, tq, Tq, scores, ld, rowlen);
+  if (hist) {  // the blocks add their counts
+    e = cudaMemsetAsync(hist, 0, (size_t)nb * Tq * kHistBins * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+  }
+  index_decode_tc_kernel<<<grid, kDThreads, kDynDec, st>>>(a, pos, b0, nb, t0, tq, Tq, scores, ld, rowlen, hist);
   note_launch();
   return cudaGetLastError();
 }

@@ -33,7 +33,8 @@ struct IndexPlan {
   int nchunks;
   bool tc;          // prefill: tensor-core score GEMM (queries per pass >= kMinTcQueries)
   int pnch;         // hierarchical pool: chunks of kPoolChunk blocks (pool mode)
-  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, off_img, off_rl, off_pk, off_pj, off_pn, total;
+  bool dec;         // scores from the per-query scan (one query, or a pool), with histograms
+  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, off_img, off_rl, off_pk, off_pj, off_pn, off_h, total;
 };
 
 constexpr int kPoolChunk = 16384;             // blocks per chunk of the pool select
@@ -55,6 +56,7 @@ IndexPlan make_plan(int nb, int T, int64_t max_entries, int mode = kIndexTopk) {
   p.nchunks = (int)((p.ld + c - 1) / c);
   size_t rows = (size_t)nb * p.Tq;
   p.tc = T >= kMinTcQueries && mode != kIndexReindex;  // a pool scan gathers rows per query
+  p.dec = T == 1 || mode == kIndexReindex;
   const int64_t nblk = (max_entries + kHsiBlock - 1) / kHsiBlock;
   p.pnch = mode == kIndexPool && nblk > kHsiBlocks ? (int)((nblk + kPoolChunk - 1) / kPoolChunk) : 0;
   size_t off = 0;
@@ -69,6 +71,7 @@ IndexPlan make_plan(int nb, int T, int64_t max_entries, int mode = kIndexTopk) {
   p.off_pk = off; off += align256(rows * p.pnch * kPoolSel * 4);
   p.off_pj = off; off += align256(rows * p.pnch * kPoolSel * 4);
   p.off_pn = off; off += align256(rows * p.pnch * 4);
+  p.off_h = off; off += p.dec ? align256(rows * kHistBins * 4) : 0;
   p.total = off;
   return p;
 }
@@ -171,15 +174,6 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(IndexArgs a, SeqPo
 }
 
 // ------------------------------------------------------------------ top-k
-// Order-preserving map of a float score to uint32 (larger score -> larger key, -0 == +0).
-__device__ __forceinline__ uint32_t score_key(float x) {
-  uint32_t u = __float_as_uint(x);
-  if ((u << 1) == 0) u = 0;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_score(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
 
 constexpr int kTopkWarps = kTopkThreads / 32;
 
@@ -346,13 +340,64 @@ __device__ __forceinline__ int32_t pool_entry(const int32_t* prow, int32_t p) {
   return prow ? kHsiBlock * prow[p >> 3] + (p & (kHsiBlock - 1)) : p;
 }
 
+// Lower edge (a key) of the histogram bin holding the K-th largest key of a row, so that all
+// of the row's K largest keys are >= it (0 if the histogram holds fewer than K keys).
+__device__ uint32_t hist_lower(const uint32_t* hist, int K, SelectShared& sh) {
+  static_assert(kTopkThreads * 4 == kHistBins, "four bins per thread");
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+  const int top = kHistBins - 1 - 4 * tid;  // this thread's bins top .. top-3, from the largest keys down
+  const uint4 v4 = __ldg(reinterpret_cast<const uint4*>(hist + top - 3));
+  const uint32_t v[4] = {v4.w, v4.z, v4.y, v4.x};
+  const uint32_t s = v[0] + v[1] + v[2] + v[3];
+  uint32_t x = s;  // inclusive scan over the threads (bins in descending order)
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (l >= o) x += y;
+  }
+  if (l == 31) sh.red[0][w] = x;
+  if (tid == 0) sh.bucket = 0u;
+  __syncthreads();
+  if (w == 0) {
+    uint32_t y = l < kTopkWarps ? sh.red[0][l] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t z = __shfl_up_sync(0xffffffffu, y, o);
+      if (l >= o) y += z;
+    }
+    if (l < kTopkWarps) sh.red[1][l] = y;
+  }
+  __syncthreads();
+  const uint32_t excl = x - s + (w ? sh.red[1][w - 1] : 0u);
+  if (excl < (uint32_t)K && excl + s >= (uint32_t)K) {
+    uint32_t c = excl;
+    int b = top;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      c += v[u];
+      if (c >= (uint32_t)K) {
+        b = top - u;
+        break;
+      }
+    }
+    sh.bucket = (uint32_t)b << kHistShift;
+  }
+  __syncthreads();
+  return sh.bucket;
+}
+
+// With hist (the row's score histogram), a chunk whose keys at or above the K-th largest
+// key's bin number at most 512 passes exactly those on (a superset of its part of the row's
+// top-512, in position order) and skips the radix select.
 __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, SeqPos pos, int b0, int t0, int Tq,
                                                                   const float* scores, int64_t ld, int chunk, int nchunks,
-                                                                  uint32_t* ck, int32_t* cj, int* cn, const int* rowlen) {
+                                                                  uint32_t* ck, int32_t* cj, int* cn, const int* rowlen,
+                                                                  const uint32_t* hist) {
   extern __shared__ uint32_t skeys[];
   __shared__ SelectShared sh;
   __shared__ uint32_t okey[kTopK];
   __shared__ int32_t oj[kTopK];
+  __shared__ int cnt_sh;
   const int c = blockIdx.x, tl = blockIdx.y, bl = blockIdx.z;
   const int t = t0 + tl;
   if (t >= a.T || tl >= Tq) return;
@@ -361,6 +406,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, S
   const int64_t E = rowlen ? rowlen[row] : (pos.p0[bl] + t + 1) >> a.rshift;
   const int64_t cs = (int64_t)c * chunk;
   const int n = (int)max64(0, min64(chunk, E - cs));
+  // the candidates' lower bound, before the loads (the histogram is complete)
+  const uint32_t lower = hist && n > kTopK ? hist_lower(hist + row * kHistBins, (int)min64(kTopK, E), sh) : 0u;
   const float* src = scores + row * ld + cs;  // 16-byte aligned: ld and the chunk are multiples of 32
   const int n4 = n >> 2;
   constexpr int kLB = 4;  // 16-byte loads in flight per thread
@@ -376,18 +423,33 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, S
             make_uint4(score_key(f[u].x), score_key(f[u].y), score_key(f[u].z), score_key(f[u].w));
   }
   for (int i = 4 * n4 + threadIdx.x; i < n; i += kTopkThreads) skeys[i] = score_key(src[i]);
+  if (threadIdx.x == 0) cnt_sh = 0;
   __syncthreads();
-  const int K = min(kTopK, n);
+  int K = min(kTopK, n);  // entries in okey / oj
   if (n <= kTopK) {  // every candidate is kept, already in position order
     for (int i = threadIdx.x; i < n; i += kTopkThreads) {
       okey[i] = skeys[i];
       oj[i] = (int32_t)(cs + i);
     }
   } else {
-    uint32_t thr;
-    int need_eq;
-    radix_select(skeys, n, K, sh, &thr, &need_eq);
-    compact_selected(skeys, nullptr, cs, n, thr, need_eq, sh, okey, oj);
+    int cnt = kTopK + 1;
+    if (lower > 0u) {
+      int m = 0;
+      for (int i = threadIdx.x; i < n; i += kTopkThreads) m += skeys[i] >= lower;
+      m = __reduce_add_sync(0xffffffffu, m);
+      if ((threadIdx.x & 31) == 0) atomicAdd(&cnt_sh, m);
+      __syncthreads();
+      cnt = cnt_sh;
+    }
+    if (cnt <= kTopK) {  // keys >= lower, position order (a single chunk: exactly its top 512)
+      compact_selected(skeys, nullptr, cs, n, lower - 1u, 0, sh, okey, oj);
+      K = cnt;
+    } else {
+      uint32_t thr;
+      int need_eq;
+      radix_select(skeys, n, K, sh, &thr, &need_eq);
+      compact_selected(skeys, nullptr, cs, n, thr, need_eq, sh, okey, oj);
+    }
   }
   __syncthreads();
   if (nchunks == 1) {
@@ -610,6 +672,7 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
   int32_t* cj = reinterpret_cast<int32_t*>(base + p.off_cj);
   int* cn = reinterpret_cast<int*>(base + p.off_cn);
   int* rowlen = mode == kIndexReindex ? reinterpret_cast<int*>(base + p.off_rl) : nullptr;
+  uint32_t* hist = p.dec ? reinterpret_cast<uint32_t*>(base + p.off_h) : nullptr;
   uint32_t* pk = reinterpret_cast<uint32_t*>(base + p.off_pk);
   int32_t* pj = reinterpret_cast<int32_t*>(base + p.off_pj);
   int* pn = reinterpret_cast<int*>(base + p.off_pn);
@@ -636,7 +699,7 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
     int64_t emax = 0;
     for (int i = 0; i < nb; ++i) emax = max(emax, (pos.p0[i] + t0 + tq) >> a.rshift);
     if (mode == kIndexReindex) {  // every query row scans its own pool
-      e = launch_index_scores_decode_tc(a, pos, b0, nb, t0, tq, p.Tq, sc, p.ld, rowlen, num_sms, st);
+      e = launch_index_scores_decode_tc(a, pos, b0, nb, t0, tq, p.Tq, sc, p.ld, rowlen, hist, num_sms, st);
       if (e != cudaSuccess) return e;
       emax = min64(emax, (int64_t)kHsiBlock * kHsiBlocks);
     } else if (p.tc) {
@@ -645,7 +708,7 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
       if (e != cudaSuccess) return e;
     } else if (a.T == 1) {
       if (emax > 0) {
-        e = launch_index_scores_decode_tc(a, pos, b0, nb, 0, 1, 1, sc, p.ld, nullptr, num_sms, st);
+        e = launch_index_scores_decode_tc(a, pos, b0, nb, 0, 1, 1, sc, p.ld, nullptr, hist, num_sms, st);
         if (e != cudaSuccess) return e;
       }
     } else {
@@ -661,7 +724,7 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
     }
     const int nch = (int)max64(1, (emax + p.chunk - 1) / p.chunk);
     topk_chunk_kernel<<<dim3(nch, tq, nb), kTopkThreads, chunk_smem, st>>>(a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch,
-                                                                            ck, cj, cn, rowlen);
+                                                                            ck, cj, cn, rowlen, hist);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (nch > 1) {

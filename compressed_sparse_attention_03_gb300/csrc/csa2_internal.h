@@ -78,7 +78,7 @@ cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0
 // bl * Tq + tl.  With a.pool_in, row r's positions are its pool's entries and rowlen[r]
 // receives the number of visible ones.
 cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq,
-                                          int Tq, float* scores, int64_t ld, int* rowlen, int num_sms,
+                                          int Tq, float* scores, int64_t ld, int* rowlen, uint32_t* hist, int num_sms,
                                           cudaStream_t st);
 // Counts one kernel enqueued by this library (read back by csa2_kernel_launches).
 void note_launch();

@@ -14,9 +14,9 @@ namespace sm100 {
 
 // Each poll may suspend the thread for up to kSuspendNs (it resumes as soon as the phase
 // completes), so a waiting warp does not take issue slots from the working ones; kSpinLimit
-// polls bound a wait to a few seconds.
+// polls bound a wait to about 80 ms, far above any wait of a working pipeline (microseconds).
 constexpr uint32_t kSuspendNs = 20000;
-constexpr uint32_t kSpinLimit = 1u << 18;
+constexpr uint32_t kSpinLimit = 1u << 12;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -41,10 +41,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Returns false (and records
-// `code` in *err) if it did not within the spin limit.
+// `code` in *err) if it did not within the spin limit.  Once an error is recorded, a wait
+// that is still pending after 64 polls gives up too, so that a broken pipeline ends after
+// one spin limit rather than one per wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (err && (i & 63u) == 63u && *reinterpret_cast<volatile int*>(err) != 0) return false;
+  }
   if (err) atomicCAS(err, 0, code);
   return false;
 }
@@ -73,6 +77,16 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// The same with a source size: src_bytes (0 or the full size) are read, the rest of the
+// destination is zero-filled (src_bytes = 0 reads nothing).
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4_zfill(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
 }
 // The mbarrier receives one arrival once every cp.async this thread issued so far has landed
 // (.noinc: that arrival is part of the count the barrier was initialised with).
