@@ -22,8 +22,10 @@
 // Warp roles (416 threads):
 //   warps 0-3   softmax + epilogue; thread = TMEM lane = row of S^T / dim of O^T
 //   warps 4-11  producers: Q -> smem once, then gather + decode 128 rows per chunk, two
-//               threads per row; the raw rows of chunk c+1 wait in registers while chunk c
-//               is consumed and are written as soon as the O MMAs free each 128-dim tile
+//               threads per row (atoms 2a and 2a+1 of tile a); the raw rows of chunk c+1
+//               wait in registers while chunk c is consumed and are written as soon as the
+//               O MMAs free each 128-dim tile.  Both threads of a row sit in one warp and
+//               work on the same tile at each step, so no lane waits for a later tile.
 //   warp 12     TMEM allocation and the single MMA-issuing thread
 // Online softmax with a lazy reference: a head's reference m only moves when a chunk's
 // maximum exceeds it by more than kTau (log2 units), so P <= 2^kTau and O is rescaled in
@@ -33,6 +35,7 @@
 #include <algorithm>
 
 #include "csa2_common.cuh"
+#include "csa2_fp16.cuh"
 #include "csa2_sm100.cuh"
 
 namespace csa2 {
@@ -55,30 +58,10 @@ constexpr uint32_t kTmemCols = 512, kLCol = 256, kSCol = 320;
 __device__ int g_attend_error;
 
 struct Bars {
-  uint64_t q_full, s_full, p_full, l_done;
+  uint64_t q_raw, q_full, s_full, p_full, l_done;
   uint64_t atom_full[8];
   uint64_t tile_free[4];
 };
-
-__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n}\n" : "=r"(r) : "r"(byte));
-  return r;
-}
-__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two) {
-  uint32_t r;
-  asm("{\n .reg .b16 h0, h1;\n mov.b32 {h0, h1}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h0;\n}\n" : "=r"(r) : "r"(two));
-  return r;
-}
-__device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t y) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(x), "r"(y));
-  return r;
-}
-__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 
 // Reduce v[32] over the 32 lanes of the warp; lane l receives the result for entry l.
 // Each round a lane keeps half of its entries and exchanges the other half.
@@ -172,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     }
   }
   if (tid == 32) {
+    mbar_init(&bars.q_raw, 1);
     mbar_init(&bars.q_full, 8);
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.p_full, 4);
@@ -179,6 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     for (int i = 0; i < 8; ++i) mbar_init(&bars.atom_full[i], 8);
     for (int i = 0; i < 4; ++i) mbar_init(&bars.tile_free[i], 1);
     mbar_fence_init();
+    // Q (bf16 [64][512], 64 KB) into the G area with one bulk copy, while warp 0 reads the
+    // indices; the producers convert it after the setup barrier
+    mbar_arrive_expect_tx(&bars.q_raw, kH * kD * 2);
+    bulk_g2s(sm + kGOff, a.q + qrow * kH * kD, kH * kD * 2, &bars.q_raw);
   }
   if (warp == 12) {
     tmem_alloc(&tmem_base_sh, kTmemCols);
@@ -207,55 +195,55 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       const int ri = (c_begin + i) * kRows + row;
       kind = 0;
       if (ri < n) {
+        // atom k = 2 * at + half covers dims 64k .. 64k+63
         if (ri < nw) {
           kind = 1;
-          const uint4* src = reinterpret_cast<const uint4*>(a.window + ((int64_t)b * (127 + T) + rows[ri]) * kD + 256 * half);
+          const uint4* src = reinterpret_cast<const uint4*>(a.window + ((int64_t)b * (127 + T) + rows[ri]) * kD);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) raw[k] = src[k];
+          for (int at = 0; at < 4; ++at)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) raw[4 * at + q] = src[4 * (2 * at + half) + q];  // 64 FP8 bytes
         } else {
           kind = 2;
           const int64_t j = rows[ri];
-          const uint4* src = reinterpret_cast<const uint4*>(a.z_codes + ((int64_t)b * a.cap + j) * 256 + 128 * half);
+          const uint4* src = reinterpret_cast<const uint4*>(a.z_codes + ((int64_t)b * a.cap + j) * 256);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) raw[k] = src[k];
-          const uint2 s = *reinterpret_cast<const uint2*>(a.z_scales + ((int64_t)b * a.cap + j) * 16 + 8 * half);
-          raw[8] = make_uint4(s.x, s.y, 0u, 0u);
+          for (int at = 0; at < 4; ++at)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) raw[2 * at + q] = src[2 * (2 * at + half) + q];  // 32 FP4 code bytes
+          raw[8] = *reinterpret_cast<const uint4*>(a.z_scales + ((int64_t)b * a.cap + j) * 16);  // all 16 scales
         }
       }
     };
+    mbar_wait(&bars.q_raw, 0, err, 8);  // the staged Q has landed (waited for even without chunks)
     if (nloc > 0) {
-      // Q (bf16 [64][512]) -> fp16, 8 K-major atoms of [64 heads x 64 dims].  A thread's 16
-      // loads are in flight together, and the first chunk's rows are requested before the
-      // conversion so that both latencies overlap.
-      const uint4* qs = reinterpret_cast<const uint4*>(a.q + qrow * kH * kD);
+      // Q (bf16, staged in the G area) -> fp16, 8 K-major atoms of [64 heads x 64 dims]; the
+      // first chunk's rows are requested before the conversion so that their latency overlaps.
+      load(0);
+      const uint4* qs = reinterpret_cast<const uint4*>(sm + kGOff);
+#pragma unroll 4
+      for (int k = 0; k < 16; ++k) {
+        const int i = pidx + 256 * k;
+        const uint4 qv = qs[i];
+        const int h = i >> 6, d0 = (i & 63) * 8;
+        const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+        uint32_t o[4];
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        uint4 qv[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) qv[k] = qs[pidx + 256 * (8 * part + k)];
-        if (part == 0) load(0);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int i = pidx + 256 * (8 * part + k);
-          const int h = i >> 6, d0 = (i & 63) * 8;
-          const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
-          uint32_t o[4];
-#pragma unroll
-          for (int m = 0; m < 4; ++m) o[m] = f2_to_h2(bf16_to_f32(w[m] & 0xffffu), bf16_to_f32(w[m] >> 16));
-          *reinterpret_cast<uint4*>(sm + kQOff + (d0 >> 6) * 8192 + sw128_off(h, (d0 & 63) >> 3)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-        }
+        for (int m = 0; m < 4; ++m) o[m] = f2_to_h2(bf16_to_f32(w[m] & 0xffffu), bf16_to_f32(w[m] >> 16));
+        *reinterpret_cast<uint4*>(sm + kQOff + (d0 >> 6) * 8192 + sw128_off(h, (d0 & 63) >> 3)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
       }
       if (pidx < 64) *reinterpret_cast<uint4*>(sm + kOnesOff + 16 * pidx) = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.q_full);
+      named_bar_sync(2, 256);  // every producer has read its staged Q before G is written
     }
     for (int i = 0; i < nloc; ++i) {
 #pragma unroll
       for (int at = 0; at < 4; ++at) {
-        const int k = 4 * half + at;  // atom: 64 dims
-        if (i > 0 && (at & 1) == 0) mbar_wait(&bars.tile_free[k >> 1], (i - 1) & 1, err, 1);
+        const int k = 2 * at + half;  // atom: 64 dims, in tile at
+        if (i > 0) mbar_wait(&bars.tile_free[at], (i - 1) & 1, err, 1);
         uint32_t o[32];
         if (kind == 1) {
 #pragma unroll
@@ -269,19 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
             }
           }
         } else if (kind == 2) {
-          const uint32_t sw = at < 2 ? raw[8].x : raw[8].y;
+          const uint32_t sw = k < 2 ? raw[8].x : k < 4 ? raw[8].y : k < 6 ? raw[8].z : raw[8].w;  // bytes 2k, 2k+1
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk) {  // 32 dims per scale byte
-            const int e = (int)((sw >> (16 * (at & 1) + 8 * blk)) & 255u) - 127;
-            const float sf = ldexpf(1.0f, e);
-            const uint32_t s2 = f2_to_h2(sf, sf);
+            const uint32_t s2 = pow2_h2((int)((sw >> (16 * (k & 1) + 8 * blk)) & 255u) - 127);
             const uint4 v = raw[2 * at + blk];
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int m = 0; m < 4; ++m) {
+              cvt_e2m1x8_f16x8(w[m], o + 16 * blk + 4 * m);
 #pragma unroll
-              for (int by = 0; by < 4; ++by)
-                o[16 * blk + 4 * m + by] = hmul2(cvt_e2m1x2_f16x2((w[m] >> (8 * by)) & 255u), s2);
+              for (int by = 0; by < 4; ++by) o[16 * blk + 4 * m + by] = hmul2(o[16 * blk + 4 * m + by], s2);
+            }
           }
         } else {
 #pragma unroll
@@ -293,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
           *reinterpret_cast<uint4*>(dst + sw128_off(row, q)) = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
         fence_proxy_async();
         __syncwarp();
-        if (lane < 2) mbar_arrive(&bars.atom_full[4 * lane + at]);
+        if (lane < 2) mbar_arrive(&bars.atom_full[2 * at + lane]);
       }
       if (i + 1 < nloc) load(i + 1);
     }
@@ -308,15 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       const uint64_t ones_desc = sw128_desc(sbase + kOnesOff, 16, 0);  // every row group reads the same atom
       for (int i = 0; i < nloc; ++i) {
         // S^T = G_c Q^T into one accumulator.  Every wait of this thread stalls until its MMAs in
-        // flight drain, so it waits for atoms k and k+4 together (the two producer halves write
-        // them at the same time).
+        // flight drain, so it waits for atoms 2 k2 and 2 k2 + 1 together (the two producer halves
+        // write them at the same time).
         for (int k2 = 0; k2 < 4; ++k2) {
-          mbar_wait(&bars.atom_full[k2], i & 1, err, 3);
-          mbar_wait(&bars.atom_full[k2 + 4], i & 1, err, 3);
+          mbar_wait(&bars.atom_full[2 * k2], i & 1, err, 3);
+          mbar_wait(&bars.atom_full[2 * k2 + 1], i & 1, err, 3);
           tc_fence_after();
 #pragma unroll
           for (int hk = 0; hk < 2; ++hk) {
-            const int k = k2 + 4 * hk;
+            const int k = 2 * k2 + hk;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_f16_ss(tmem + kSCol, sw128_desc(gg + k * 16384 + kk * 32, 16, 1024),
@@ -326,11 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         mma_commit(&bars.s_full);
         mbar_wait(&bars.p_full, i & 1, err, 4);
         tc_fence_after();
-        // O^T tiles one after the other (each frees its two atoms for the next chunk), then the
-        // row sums.  Order 0, 2, 1, 3: the two producer halves refill tiles {0,1} and {2,3}, so
-        // both get a free tile early and the paired atom waits above are met sooner.
-        for (int mi = 0; mi < 4; ++mi) {
-          const int m = ((mi & 1) << 1) | (mi >> 1);
+        // O^T tiles one after the other in the order the producers refill them (each frees its
+        // two atoms for the next chunk), then the row sums.
+        for (int m = 0; m < 4; ++m) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_f16_ss(tmem + 64 * m, sw128_desc(gg + 2 * m * 16384 + kk * 2048, 16384, 1024),
@@ -450,7 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     }
     named_bar_sync(1, 128);
     if (nsplit == 1) {
-      uint16_t* outq = a.out + qrow * kH * kD;
+      // the output row [64 heads][512 dims] is assembled in the G area (free: the last MMAs
+      // are done) and written with one bulk copy
+      uint16_t* ost = reinterpret_cast<uint16_t*>(sm + kGOff);
       for (int m = 0; m < 4; ++m) {
         const int d = 128 * m + r;
         float cs = 1.f, sn = 0.f;
@@ -473,9 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
 #pragma unroll
           for (int h = 0; h < 32; ++h) {
             const __nv_bfloat16 v = __float2bfloat16_rn(o[h]);
-            outq[(32 * hh + h) * kD + d] = *reinterpret_cast<const uint16_t*>(&v);
+            ost[(32 * hh + h) * kD + d] = *reinterpret_cast<const uint16_t*>(&v);
           }
         }
+      }
+      fence_proxy_async();
+      named_bar_sync(1, 128);
+      if (tid == 0) {
+        bulk_s2g(a.out + qrow * kH * kD, ost, kH * kD * 2);
+        bulk_commit();
+        bulk_wait_all();  // the copy has read the shared memory (and written) before exit
       }
     } else {
       const int64_t pr_row = ((int64_t)bl * T + t) * nsplit + split;

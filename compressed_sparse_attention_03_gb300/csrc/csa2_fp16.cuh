@@ -1,0 +1,45 @@
+// Exact FP4 (E2M1) / FP8 (E4M3) -> fp16 conversions for building tensor-core operands, with
+// power-of-two scales applied in fp16 (E2M1 x 2^e is exact in fp16 for -22 <= e <= 12; E4M3
+// values are always exact).
+#pragma once
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace csa2 {
+
+// Four code bytes (8 values, element 2k in the low nibble of byte k) -> four f16x2.
+__device__ __forceinline__ void cvt_e2m1x8_f16x8(uint32_t w, uint32_t* o) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      " cvt.rn.f16x2.e2m1x2 %1, b1;\n cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t y) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(x), "r"(y));
+  return r;
+}
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Both halves = 2^e as fp16 bits, built without arithmetic: normal for -14 <= e <= 15,
+// subnormal down to 2^-24, 0 below, +inf above (the values an fp32 2^e rounds to in fp16).
+__device__ __forceinline__ uint32_t pow2_h2(int e) {
+  uint32_t h;
+  if (e > 15) h = 0x7C00u;
+  else if (e >= -14) h = (uint32_t)(e + 15) << 10;
+  else if (e >= -24) h = 1u << (e + 24);
+  else h = 0u;
+  return h | (h << 16);
+}
+
+// Two E4M3 codes (low 16 bits) -> f16x2.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{\n .reg .b16 h0, h1;\n mov.b32 {h0, h1}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h0;\n}\n" : "=r"(r) : "r"(two));
+  return r;
+}
+
+}  // namespace csa2

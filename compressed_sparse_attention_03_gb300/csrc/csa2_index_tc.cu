@@ -20,6 +20,7 @@
 #include <cuda_fp16.h>
 
 #include "csa2_common.cuh"
+#include "csa2_fp16.cuh"
 #include "csa2_sm100.cuh"
 
 namespace csa2 {
@@ -35,33 +36,6 @@ constexpr uint32_t kBOff = 0, kAOff = 131072, kWOff = 196608, kDynTC = 196608 + 
 
 __device__ int g_index_error;
 
-// Four code bytes (8 values, element 2k in the low nibble of byte k) -> four f16x2.
-__device__ __forceinline__ void cvt_e2m1x8_f16x8(uint32_t w, uint32_t* o) {
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n"
-      " cvt.rn.f16x2.e2m1x2 %1, b1;\n cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(w));
-}
-__device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t y) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(x), "r"(y));
-  return r;
-}
-__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Both halves = 2^e as fp16 bits, built without arithmetic: normal for -14 <= e <= 15,
-// subnormal down to 2^-24, 0 below, +inf above (the values an fp32 2^e rounds to in fp16).
-__device__ __forceinline__ uint32_t pow2_h2(int e) {
-  uint32_t h;
-  if (e > 15) h = 0x7C00u;
-  else if (e >= -14) h = (uint32_t)(e + 15) << 10;
-  else if (e >= -24) h = 1u << (e + 24);
-  else h = 0u;
-  return h | (h << 16);
-}
 
 // Q^I (bf16) -> FP4 (E2M1, UE8M0 per 32) -> fp16 image.  grid (Tq, nb), 128 threads: warp w
 // handles heads 8w..8w+7, lane l values 4l..4l+3.  Query t of the chunk lives in tile t/8,
