@@ -345,6 +345,10 @@ def profiled_traffic(profile: str, sources) -> int | None:
 
 
 CSRC = "compressed_sparse_attention_03_gb300/csrc/"
+# sources a profiled kernel is built from (a change to any of them makes its ncu traffic stale)
+_HDRS = [CSRC + "csa2_common.cuh", CSRC + "csa2_fp16.cuh", CSRC + "csa2_sm100.cuh", CSRC + "csa2_internal.h"]
+ATTEND_SOURCES = [CSRC + "csa2_attend.cu"] + _HDRS
+INDEX_SOURCES = [CSRC + "csa2_index_tc.cu", CSRC + "csa2_indexer.cu"] + _HDRS
 
 
 def peaks():
@@ -382,7 +386,7 @@ def run_ours(args, rank, ws):
         "roofline": {"kernel": "attend_kernel", "bound": "tensor", "achieved": achieved, "peak": bf16,
                      "unit": "TFLOP/s", "frac": achieved / bf16, "peak_source": f"{src} bf16 burst",
                      "flops_per_launch": flops,
-                     "traffic": profiled_traffic("attend_tc_kernel_prefill_4k.md", [CSRC + "csa2_attend.cu"]),
+                     "traffic": profiled_traffic("attend_tc_kernel_prefill_4k.md", ATTEND_SOURCES),
                      "traffic_source": "profiles/attend_tc_kernel_prefill_4k.md (null once the kernel changed)"},
         "e2e": e2e,
         "gpu_launches": launches,
@@ -408,8 +412,7 @@ def run_ours(args, rank, ws):
             "roofline_index": {"bound": "hbm", "achieved": by["indexer"] / (idx_ms / 1e3) / 1e9, "peak": hbm,
                                "unit": "GB/s", "frac": by["indexer"] / (idx_ms / 1e3) / 1e9 / hbm,
                                "bytes": by["indexer"], "peak_source": f"{src} copy bandwidth",
-                               "traffic": profiled_traffic("index_decode_decode_1m.md",
-                                                           [CSRC + "csa2_index_tc.cu", CSRC + "csa2_indexer.cu"])
+                               "traffic": profiled_traffic("index_decode_decode_1m.md", INDEX_SOURCES)
                                if name == "decode_1m" else None},
             "gpu_launches": dlaunches,
         }

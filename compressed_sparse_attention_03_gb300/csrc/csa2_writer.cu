@@ -4,8 +4,8 @@
 // K^I (RoPE by 2j on dims 64..127, FP4) and the window W (RMSNorm of w^a, RoPE by t, FP8).
 // RMSNorm as on "DeepSeek V4.1 - Window layer / Attention RMSNorm" (eps 1e-20).
 //
-// Precision: fp32 elementwise work, fp64 sums of squares, and a compensated (double-float)
-// dot product for c W_IK, so that the values reaching the FP4/FP8 rounding differ from an
+// Precision: fp32 elementwise work, compensated (double-float fp32) sums of squares and a
+// compensated dot product for c W_IK, so that the values reaching the FP4/FP8 rounding differ from an
 // fp64 evaluation by a few fp32 ulps and the codes match except at rounding midpoints.
 #include "csa2_common.cuh"
 #include "csa2_sm100.cuh"
