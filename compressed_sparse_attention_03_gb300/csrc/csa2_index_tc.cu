@@ -289,7 +289,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
 //    (kDSlots tiles); rows past the last key (or naming an entry outside 0..E-1) are zero.
 //  - warps 20 and 21 (one thread each): the MMAs of the even / odd tiles, A from TMEM, B
 //    (Q^I) from shared memory.  A thread that waits stalls until its own MMAs in flight have
-//    finished; with two issuers one of them keeps the tensor pipe busy meanwhile.
+//    finished; with two issuers one of them keeps the tensor pipe busy meanwhile.  Each A slot
+//    and accumulator stays with one issuer (kDSlots and kDAcc are even), so no slot passes
+//    from one issuing thread's MMAs to another's: a four-issuer variant that did hand slots
+//    over gave an intermittent wrong score and no speedup.
 // Rows: one query (sequence bl, query t0 + tl) each; a row's key tiles are split evenly over
 // gridDim.x / rows persistent blocks.  With hist, each row also gets the histogram of its
 // score keys (kHistBins bins, added up over its blocks) that lets the top-k skip most keys.
@@ -309,6 +312,7 @@ static_assert(kDGroup == 2, "a stage holds two tiles (of two decoder groups)");
 static_assert(kDSlots % 2 == 0, "a decoder group keeps the parity of its tiles");
 static_assert(kDDCol + 32 * kDAcc <= kDTmemCols, "TMEM columns");
 static_assert(kDAcc == 4, "accumulator = tile & 3");
+static_assert(kDSlots % 2 == 0 && kDAcc % 2 == 0, "slots and accumulators keep the issuer (tile parity)");
 
 // a_full[slot]: the tile in a slot is decoded (4 decoder warps).  done[slot]: the MMAs of the
 // tile in a slot completed (one commit): the slot is free and accumulator slot & 1 holds its
