@@ -22,7 +22,7 @@ HEADS, HEAD_DIM, ROPE_DIMS, IDX_HEADS, IDX_DIM, WINDOW, TOPK = 64, 512, 64, 32, 
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "inconsistent sizes", 3: "pointer not 16-byte aligned",
            4: "workspace too small", 5: "unsupported configuration", 6: "CUDA error",
-           7: "batch exceeds the fixed scratch of csa2_attend_static"}
+           7: "batch exceeds the fixed scratch of csa2_attend_static", 8: "a bounded wait inside a kernel gave up"}
 
 
 class Csa2Error(RuntimeError):
@@ -40,7 +40,7 @@ class csa2_config(C.Structure):
 EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_string", "csa2_kernel_launches",
            "csa2_workspace_bytes",
            "csa2_write_cache", "csa2_index_topk", "csa2_index_pool", "csa2_reindex_topk", "csa2_attend",
-           "csa2_attend_replay", "csa2_attend_static")
+           "csa2_attend_replay", "csa2_attend_static", "csa2_check", "csa2_selftest_timeout")
 
 _lib = None
 
@@ -68,6 +68,10 @@ def lib() -> C.CDLL:
         L.csa2_write_cache.restype = i32
         L.csa2_index_topk.argtypes = [p] * 5 + [i64, p, i32, i32, p, p, p, sz, p]
         L.csa2_index_topk.restype = i32
+        L.csa2_check.argtypes = [p, p]
+        L.csa2_check.restype = i32
+        L.csa2_selftest_timeout.argtypes = [p, p]
+        L.csa2_selftest_timeout.restype = i32
         L.csa2_index_pool.argtypes = [p] * 5 + [i64, p, i32, i32, p, p, p, p, sz, p]
         L.csa2_index_pool.restype = i32
         L.csa2_reindex_topk.argtypes = [p] * 5 + [i64, p, i32, i32, p, p, p, p, sz, p]
@@ -217,6 +221,20 @@ def csa2_reindex_topk(h: Handle, qi, wI, ki_codes, ki_scales, p0, pool, idx, top
         _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
         _dev(pool, torch.int32, "pool"), _dev(idx, torch.int32, "idx"), _dev(top_scores, torch.float32, "top_scores"),
         _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+
+
+def csa2_check(h: Handle, stream=None) -> int:
+    """Synchronises the stream and returns the status of the bounded waits since the last
+    check (0, or 8 = a wait gave up).  Does not raise on 8: the caller decides."""
+    st = lib().csa2_check(h.ptr, _stream(stream))
+    if st not in (0, 8):
+        _check("csa2_check", st)
+    return st
+
+
+def csa2_selftest_timeout(h: Handle, stream=None) -> None:
+    """Enqueues a kernel whose one bounded wait can never complete (a test of csa2_check)."""
+    _check("csa2_selftest_timeout", lib().csa2_selftest_timeout(h.ptr, _stream(stream)))
 
 
 def csa2_attend(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, out, ws=None, stream=None) -> None:

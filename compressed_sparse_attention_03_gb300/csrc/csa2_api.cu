@@ -118,6 +118,7 @@ const char* csa2_status_string(csa2_status s) {
     case CSA2_ERR_UNSUPPORTED: return "unsupported configuration";
     case CSA2_ERR_CUDA: return "CUDA error";
     case CSA2_ERR_TOO_LARGE: return "batch exceeds the fixed scratch of csa2_attend_static";
+    case CSA2_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
   }
   return "unknown status";
 }
@@ -327,3 +328,24 @@ csa2_status csa2_attend_static(csa2_handle* h, const uint16_t* q, const float* s
 }
 
 }  // extern "C"
+
+// Reports what the bounded waits of earlier kernels recorded (include/csa2.h).
+csa2_status csa2_check(csa2_handle* h, csa2_stream_t stream) {
+  if (!h) return CSA2_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (dev != h->device) return CSA2_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
+  int ea = 0, ei = 0;
+  if (csa2::take_attend_error(&ea) != cudaSuccess || csa2::take_index_error(&ei) != cudaSuccess) return CSA2_ERR_CUDA;
+  return (ea || ei) ? CSA2_ERR_TIMEOUT : CSA2_OK;
+}
+
+// Test hook for the timeout report (include/csa2.h).
+csa2_status csa2_selftest_timeout(csa2_handle* h, csa2_stream_t stream) {
+  if (!h) return CSA2_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (dev != h->device) return CSA2_ERR_INVALID_ARG;
+  return cuda_status(csa2::launch_wait_probe(reinterpret_cast<cudaStream_t>(stream)));
+}

@@ -596,4 +596,12 @@ cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, const SeqPos& 
   return e;
 }
 
+// Reads and clears the attention kernels' device error word (0 = no bounded wait gave up).
+cudaError_t take_attend_error(int* code) {
+  const int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_attend_error, sizeof(int));
+  if (e == cudaSuccess && *code != 0) e = cudaMemcpyToSymbol(g_attend_error, &zero, sizeof(int));
+  return e;
+}
+
 }  // namespace csa2

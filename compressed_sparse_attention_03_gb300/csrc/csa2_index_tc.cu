@@ -616,4 +616,31 @@ cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0
   return cudaGetLastError();
 }
 
+// Reads and clears the indexer kernels' device error word (0 = no bounded wait gave up).
+cudaError_t take_index_error(int* code) {
+  const int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_index_error, sizeof(int));
+  if (e == cudaSuccess && *code != 0) e = cudaMemcpyToSymbol(g_index_error, &zero, sizeof(int));
+  return e;
+}
+
+namespace {
+// One thread waits on a barrier that nothing arrives at: the bounded wait gives up after its
+// spin limit (about 80 ms), records code 99 in the error word and the kernel returns.
+__global__ void wait_probe_kernel() {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    mbar_wait(&bar, 0, &g_index_error, 99);
+  }
+}
+}  // namespace
+
+cudaError_t launch_wait_probe(cudaStream_t st) {
+  wait_probe_kernel<<<1, 32, 0, st>>>();
+  note_launch();
+  return cudaGetLastError();
+}
+
 }  // namespace csa2

@@ -80,6 +80,12 @@ cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0
 cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq,
                                           int Tq, float* scores, int64_t ld, int* rowlen, uint32_t* hist, int num_sms,
                                           cudaStream_t st);
+// Device error words of the bounded waits: read and cleared (synchronous; the caller has
+// synchronised the work it checks).
+cudaError_t take_attend_error(int* code);
+cudaError_t take_index_error(int* code);
+// A kernel whose one bounded wait can never complete (a test of the timeout report).
+cudaError_t launch_wait_probe(cudaStream_t st);
 // Counts one kernel enqueued by this library (read back by csa2_kernel_launches).
 void note_launch();
 

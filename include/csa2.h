@@ -26,6 +26,8 @@
  *    tokens of each sequence (its cached length before the call).
  *  - Every call is asynchronous on `stream` and never synchronises.  Argument errors are
  *    returned before anything is launched; launch errors come back as CSA2_ERR_CUDA.
+ *  - Every wait inside a kernel is bounded (about 80 ms).  A wait that gives up records a
+ *    code in a device error word and lets its kernel finish; csa2_check reports it.
  *
  * Storage formats (fixed by this library)
  *  - FP4 cache row of n values: n/2 code bytes (E2M1, element 2i in the low nibble of byte
@@ -59,7 +61,8 @@ typedef enum {
   CSA2_ERR_WORKSPACE = 4,   /* workspace smaller than csa2_workspace_bytes() */
   CSA2_ERR_UNSUPPORTED = 5, /* configuration outside what the kernels implement */
   CSA2_ERR_CUDA = 6,        /* a CUDA launch or device query failed */
-  CSA2_ERR_TOO_LARGE = 7    /* batch needs more than csa2_attend_static's fixed scratch */
+  CSA2_ERR_TOO_LARGE = 7,   /* batch needs more than csa2_attend_static's fixed scratch */
+  CSA2_ERR_TIMEOUT = 8      /* a bounded wait inside a kernel gave up (csa2_check) */
 } csa2_status;
 
 /* Layer configuration.  The integer fields must equal the defaults shown. */
@@ -173,6 +176,21 @@ csa2_status csa2_reindex_topk(csa2_handle* h, const uint16_t* qi, const uint16_t
                               const int64_t* p0, int B, int T, const int32_t* pool,
                               int32_t* idx, float* top_scores, void* ws, size_t ws_bytes,
                               csa2_stream_t stream);
+
+/* Failure report (no counterpart on the pages).  Synchronises `stream`, then reports whether
+ * a bounded wait inside any kernel of this library gave up since the last check:
+ * CSA2_ERR_TIMEOUT (the outputs of the calls since then are not to be trusted), CSA2_ERR_CUDA
+ * if synchronising or reading the error words failed, CSA2_OK otherwise.  Clears the error
+ * words.  Call with the handle's device current; while an error word is set, later waits
+ * that stay pending give up early, so check before trusting further results.  Not for use
+ * inside stream capture (it synchronises). */
+csa2_status csa2_check(csa2_handle* h, csa2_stream_t stream);
+
+/* Test hook for csa2_check (no counterpart on the pages): enqueues one kernel whose single
+ * bounded wait can never complete (nothing arrives at its barrier), so that the next
+ * csa2_check returns CSA2_ERR_TIMEOUT.  The kernel ends by itself after the wait's bound
+ * (about 80 ms); it faults nothing and the device stays usable. */
+csa2_status csa2_selftest_timeout(csa2_handle* h, csa2_stream_t stream);
 
 /* (4) Sink-softmax MQA, [PG] equations for J^w_t, Y, J, G_t, S, A, O and O-bar.
  *  q      : bf16 [B, T, 64, 512] queries, RoPE already applied to dims 448..511.

@@ -40,6 +40,7 @@ def test_status_strings_and_config_checks(lib):
     assert lib.csa2_status_string(0) == b"ok"
     assert lib.csa2_status_string(4) == b"workspace too small"
     assert lib.csa2_status_string(7) == b"batch exceeds the fixed scratch of csa2_attend_static"
+    assert lib.csa2_status_string(8) == b"a bounded wait inside a kernel gave up"
     cfg = csa2.csa2_config()
     lib.csa2_default_config(C.byref(cfg))
     assert (cfg.heads, cfg.head_dim, cfg.rope_dims, cfg.idx_heads, cfg.idx_dim, cfg.window, cfg.topk, cfg.ratio) == \
@@ -60,4 +61,8 @@ def test_status_strings_and_config_checks(lib):
     assert lib.csa2_workspace_bytes(None, 1, 1, 1, 10) == 0
     assert lib.csa2_index_topk(*([None] * 5), 0, None, 1, 1, None, None, None, 0, None) == 1
     assert lib.csa2_attend_static(*([None] * 5), 0, None, None, None, 1, 1, None, None) == 1
+    assert lib.csa2_index_pool(*([None] * 5), 0, None, 1, 1, None, None, None, None, 0, None) == 1
+    assert lib.csa2_reindex_topk(*([None] * 5), 0, None, 1, 1, None, None, None, None, 0, None) == 1
+    assert lib.csa2_check(None, None) == 1
+    assert lib.csa2_selftest_timeout(None, None) == 1
     assert lib.csa2_kernel_launches() == launches
