@@ -52,6 +52,7 @@ constexpr float kTau = 8.0f;                // lazy-rescale threshold (log2 unit
 // dynamic shared memory (1024-aligned): Q 8 atoms x [64 x 128 B], G 8 atoms x [128 x 128 B],
 // P [128 rows x 128 B], one 1 KB swizzle atom of fp16 ones
 constexpr uint32_t kQOff = 0, kGOff = 65536, kPOff = 196608, kOnesOff = 212992, kDynBytes = 214016 + 1024;
+static_assert(kPOff - kGOff == kH * kD * 4, "the G area holds one fp32 output row (split partials)");
 // TMEM columns: O^T tiles at 0, 64, 128, 192; row sums at 256; S^T at 320
 constexpr uint32_t kTmemCols = 512, kLCol = 256, kSCol = 320;
 
@@ -474,6 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     } else {
       const int64_t pr_row = ((int64_t)bl * T + t) * nsplit + split;
       float* po = part_o + pr_row * kH * kD;
+      // the split's O [64 heads][512 dims] fp32 (128 KB, the whole G area) in shared memory,
+      // then one bulk copy; a split without chunks first lets the staged Q copy land
+      float* ost = reinterpret_cast<float*>(sm + kGOff);
+      if (nloc == 0) mbar_wait(&bars.q_raw, 0, err, 9);
       for (int m = 0; m < 4; ++m) {
         const int d = 128 * m + r;
         for (int hh = 0; hh < 2; ++hh) {
@@ -486,8 +491,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
             for (int h = 0; h < 32; ++h) u[h] = 0u;
           }
 #pragma unroll
-          for (int h = 0; h < 32; ++h) po[(32 * hh + h) * kD + d] = __uint_as_float(u[h]);
+          for (int h = 0; h < 32; ++h) ost[(32 * hh + h) * kD + d] = __uint_as_float(u[h]);
         }
+      }
+      fence_proxy_async();
+      named_bar_sync(1, 128);
+      if (tid == 0) {
+        bulk_s2g(po, ost, kH * kD * 4);
+        bulk_commit();
+        bulk_wait_all();
       }
       if (tid < 64) {
         part_ml[(pr_row * kH + tid) * 2] = m_ref[tid];
