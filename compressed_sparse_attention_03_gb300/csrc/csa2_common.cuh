@@ -35,9 +35,6 @@ __device__ __forceinline__ uint32_t f32_to_e2m1(float x) {
   return s | m;
 }
 
-// UE8M0 exponent for a block with absolute maximum amax: floor(log2 amax) - 2, clamped to
-// [-127, 127]; amax == 0 (or subnormal) gives -127.
-// 2^k as a float built from its bits: exact for -149 <= k <= 127 (subnormal below -126).
 // Order-preserving map of a float score to uint32 (larger score -> larger key, -0 == +0).
 __device__ __forceinline__ uint32_t score_key(float x) {
   uint32_t u = __float_as_uint(x);
@@ -52,6 +49,7 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // exponent bits and 2 mantissa bits), so a bin spans at most a factor 1.25 of |score|.
 constexpr int kHistBits = 11, kHistBins = 1 << kHistBits, kHistShift = 32 - kHistBits;
 
+// 2^k as a float built from its bits: exact for -149 <= k <= 127 (subnormal below -126).
 __device__ __forceinline__ float pow2f(int k) {
   if (k > 127) return __uint_as_float(0x7f800000u);
   if (k >= -126) return __uint_as_float((uint32_t)(k + 127) << 23);
@@ -59,6 +57,8 @@ __device__ __forceinline__ float pow2f(int k) {
   return 0.f;
 }
 
+// UE8M0 exponent for a block with absolute maximum amax: floor(log2 amax) - 2, clamped to
+// [-127, 127]; amax == 0 (or subnormal) gives -127.
 __device__ __forceinline__ int mx_scale_exp(float amax) {
   int E = (int)((__float_as_uint(amax) >> 23) & 255u);
   if (E == 0) return -127;

@@ -35,6 +35,20 @@ __device__ __forceinline__ uint32_t pow2_h2(int e) {
   return h | (h << 16);
 }
 
+// Two fp32 values (already divided by their block scale) -> two E2M1 codes in one byte, `lo`
+// in the low nibble: round to nearest with ties to the even code, saturating at +-6.
+__device__ __forceinline__ uint32_t cvt_f32x2_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n cvt.u32.u8 %0, t;\n}\n" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+// One code byte (two E2M1 values) -> f16x2.
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n}\n" : "=r"(r) : "r"(byte));
+  return r;
+}
+
 // Two E4M3 codes (low 16 bits) -> f16x2.
 __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two) {
   uint32_t r;

@@ -61,13 +61,21 @@ __global__ void __launch_bounds__(128) qimage_kernel(IndexArgs a, int b0, int t0
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     const int e = mx_scale_exp(amax);
-    float q[4];
-    const float down = pow2f(-e), up = pow2f(e);  // exact powers of two
+    const float down = pow2f(-e);  // exact power of two
+    uint2 img;
+    if (e >= -24 && e <= 15) {  // 2^e is an fp16 number: code x 2^e rounds exactly as via fp32
+      const uint32_t s2 = pow2_h2(e);
+      img.x = hmul2(cvt_e2m1x2_f16x2(cvt_f32x2_e2m1x2(v[0] * down, v[1] * down)), s2);
+      img.y = hmul2(cvt_e2m1x2_f16x2(cvt_f32x2_e2m1x2(v[2] * down, v[3] * down)), s2);
+    } else {
+      const float up = pow2f(e);
+      float q[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = e2m1_to_f32(f32_to_e2m1(v[i] * down)) * up;
+      for (int i = 0; i < 4; ++i) q[i] = e2m1_to_f32(f32_to_e2m1(v[i] * down)) * up;
+      img = make_uint2(f2_to_h2(q[0], q[1]), f2_to_h2(q[2], q[3]));
+    }
     const int n = (tl % kQPerTile) * kHI + h, d = 4 * l;
-    *reinterpret_cast<uint2*>(tile + (d >> 6) * 32768 + sw128_off(n, (d & 63) >> 3) + (d & 7) * 2) =
-        make_uint2(f2_to_h2(q[0], q[1]), f2_to_h2(q[2], q[3]));
+    *reinterpret_cast<uint2*>(tile + (d >> 6) * 32768 + sw128_off(n, (d & 63) >> 3) + (d & 7) * 2) = img;
   }
   if (threadIdx.x < kHI) wq[((int64_t)bl * Tq + tl) * kHI + threadIdx.x] = bf16_to_f32(a.wI[src * kHI + threadIdx.x]);
 }
