@@ -188,9 +188,16 @@ struct SelectShared {
 // Radix select over keys[0..n): on return *thr is the K-th largest key and *need_eq the
 // number of keys equal to *thr that belong to the top K (the lowest-index ones).  The digits
 // start at the highest bit in which the smallest and largest key differ (the bits above are
-// common to every key and would put all keys into one bin).
+// common to every key and would put all keys into one bin).  Up to kSmallSelect keys share one
+// histogram (clearing and folding one per warp would cost more than the few collisions);
+// longer rows count into one histogram per warp.
+constexpr int kSmallSelect = 4096;
+
 __device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared& sh, uint32_t* thr, int* need_eq) {
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+  const bool one_hist = n <= kSmallSelect;
+  const int hw = one_hist ? 0 : w;                       // this thread's histogram
+  const int nclear = (one_hist ? 1 : kTopkWarps) * 256;  // words to clear per pass
   uint32_t mn = 0xffffffffu, mx = 0u;
   for (int i = tid; i < n; i += kTopkThreads) {
     const uint32_t k = keys[i];
@@ -223,20 +230,22 @@ __device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared& s
   for (int hi = top; hi >= 0; hi -= 8) {
     const int lo = max(hi - 7, 0);
     const uint32_t dmask = (2u << (hi - lo)) - 1u;
-    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&sh.hist[0][0])[i] = 0;
+    for (int i = tid; i < nclear; i += kTopkThreads) (&sh.hist[0][0])[i] = 0;
     __syncthreads();
     for (int i = tid; i < n; i += kTopkThreads) {
       const uint32_t k = keys[i];
-      if ((k & mask) == prefix) atomicAdd(&sh.hist[w][(k >> lo) & dmask], 1u);
+      if ((k & mask) == prefix) atomicAdd(&sh.hist[hw][(k >> lo) & dmask], 1u);
     }
     __syncthreads();
-    for (int b = tid; b < 256; b += kTopkThreads) {  // fold the per-warp histograms into warp 0's
-      uint32_t c = 0;
+    if (!one_hist) {
+      for (int b = tid; b < 256; b += kTopkThreads) {  // fold the per-warp histograms into warp 0's
+        uint32_t c = 0;
 #pragma unroll
-      for (int x = 0; x < kTopkWarps; ++x) c += sh.hist[x][b];
-      sh.hist[0][b] = c;
+        for (int x = 0; x < kTopkWarps; ++x) c += sh.hist[x][b];
+        sh.hist[0][b] = c;
+      }
+      __syncthreads();
     }
-    __syncthreads();
     if (tid < 32) {
       // lane l owns bins 255-8l .. 248-8l (descending)
       uint32_t c[8], tot = 0;
