@@ -271,3 +271,21 @@ def reindex_topk(scores, E, pool, k=TOPK):
     idx = np.empty((nq, k), np.int32)
     lib().csa2o_reindex_topk(nq, _ptr(E), _ptr(scores), scores.shape[1], _ptr(pool), k, _ptr(idx))
     return idx
+
+
+# ------------------------------------------------------------------ grouped output projection
+# "Inside DeepSeek V4.1", section "Attention that looks at 640 places": the outputs go back
+# through 8 groups of a 1,024-wide bottleneck; [PG] o^g_{t,r} = [O-bar_{h,t}]_{h in r} W_OA,r.
+# Group r holds heads 8r .. 8r+7, concatenated head after head (input k = 512 (h - 8r) + d).
+OUT_GROUPS, OUT_GROUP_HEADS, OUT_GROUP_WIDTH = 8, 8, 1024
+
+
+def out_group_proj(o_bar, w_oa):
+    """o_bar [n, 64, 512] (the attention output), w_oa [8, 1024, 4096] (group r, output i,
+    input k) -> o^g [n, 8, 1024] in fp64: o^g[:, r, i] = sum_k o_bar_r[:, k] w_oa[r, i, k]."""
+    o = np.asarray(o_bar, np.float64)
+    n = o.shape[0]
+    o = o.reshape(n, OUT_GROUPS, OUT_GROUP_HEADS * 512)
+    w = np.asarray(w_oa, np.float64)
+    return np.einsum("nrk,rik->nri", o, w)
+

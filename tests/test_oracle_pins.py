@@ -504,3 +504,38 @@ def test_kv_bytes_and_work_ratios():
     assert abs((0.5 + 128 / (2 * 1e6)) - gd["ced_ratio_1e6_w128"]) < 1e-12
     assert 2048 * 8 == gd["hsi_pool"] and round(1e6 / 16384) == gd["hsi_reduction_1m"]
     assert gd["window_rows"] + gd["selected_rows"] == gd["attended_rows"]
+
+
+def test_out_group_proj_selection_weights_pick_the_group_heads():
+    # W_OA,r = [I_1024 | 0]: group r's output i is input k = i of the group, i.e. head
+    # 8r + i // 512, dim i % 512 (heads concatenated one after another inside a group)
+    rng = np.random.default_rng(3)
+    o = rng.standard_normal((5, 64, 512))
+    w = np.zeros((8, 1024, 4096))
+    w[:, np.arange(1024), np.arange(1024)] = 1.0
+    out = oracle.out_group_proj(o, w)
+    for r in range(8):
+        assert np.array_equal(out[:, r, :512], o[:, 8 * r])
+        assert np.array_equal(out[:, r, 512:], o[:, 8 * r + 1])
+    # a weight on input k of group r reads head 8r + k // 512, dim k % 512
+    w2 = np.zeros((8, 1024, 4096))
+    w2[5, 7, 3 * 512 + 11] = 2.0
+    out2 = oracle.out_group_proj(o, w2)
+    assert np.allclose(out2[:, 5, 7], 2.0 * o[:, 8 * 5 + 3, 11], rtol=0, atol=0)
+    assert np.count_nonzero(out2) == np.count_nonzero(o[:, 43, 11])
+
+
+def test_out_group_proj_group_locality_and_linearity():
+    rng = np.random.default_rng(4)
+    o = rng.standard_normal((3, 64, 512))
+    w = rng.standard_normal((8, 1024, 4096)) / 64
+    base = oracle.out_group_proj(o, w)
+    o2 = o.copy()
+    o2[:, 8 * 6 + 2] += rng.standard_normal((3, 512))  # a head of group 6 only
+    moved = oracle.out_group_proj(o2, w)
+    assert np.array_equal(np.delete(moved, 6, axis=1), np.delete(base, 6, axis=1))
+    assert not np.allclose(moved[:, 6], base[:, 6])
+    # brute force of one output against the definition's sum, element by element
+    r, i, n = 2, 900, 1
+    ref = sum(o[n, 8 * r + k // 512, k % 512] * w[r, i, k] for k in range(4096))
+    assert abs(base[n, r, i] - ref) <= 1e-12 * max(1.0, abs(ref))
