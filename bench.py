@@ -290,6 +290,35 @@ def time_hsi(csa2, step: Step, steps: int, warmup: int, ws: int, flush: torch.Te
     return own, re, launches
 
 
+def time_out_proj(csa2, inputs, M, steps, warmup, ws, flush, bf16, src, rank):
+    """The grouped output projection W_OA on M attention-output rows (prefill_4k: M = 4096)."""
+    x = inputs.out_proj_inputs(M, seed_for_rank(1, rank), "cuda")
+    h = csa2.csa2_create()
+    out = torch.empty(M, 8, 1024, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        csa2.csa2_out_group_proj(h, x["o"], x["w_oa"], out, stream=s)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(ws)
+    launches0 = csa2.csa2_kernel_launches()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(s)
+        csa2.csa2_out_group_proj(h, x["o"], x["w_oa"], out, stream=s)
+        ev[i][1].record(s)
+    torch.cuda.synchronize()
+    launches = csa2.csa2_kernel_launches() - launches0
+    barrier(ws)
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), ws)
+    flops = 2.0 * M * 8 * 1024 * 4096
+    tf = flops / (ms / 1e3) / 1e12
+    return {"rows": M, "ms": ms, "gpu_launches": launches,
+            "roofline": {"kernel": "outproj_kernel", "bound": "tensor", "achieved": tf, "peak": bf16,
+                         "unit": "TFLOP/s", "frac": tf / bf16, "flops_per_launch": flops,
+                         "peak_source": f"{src} bf16 burst"}}
+
+
 class _Null:
     def __enter__(self):
         return self
@@ -434,6 +463,9 @@ def run_ours(args, rank, ws):
             "gpu_launches": hl,
         }
         del hstep
+    if not args.no_decode and args.out_proj_rows:
+        line["out_proj"] = time_out_proj(csa2, inputs, args.out_proj_rows, args.steps, args.warmup, ws, flush, bf16,
+                                         src, rank)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     return line
@@ -516,6 +548,7 @@ def main():
     ap.add_argument("--workload", default="prefill_4k")
     ap.add_argument("--decode-workload", default="decode_1m")
     ap.add_argument("--ratio1-workload", default="decode_512k_r1", help="empty: skip the ratio-1 decode object")
+    ap.add_argument("--out-proj-rows", type=int, default=4096, help="0: skip the output-projection object")
     ap.add_argument("--hsi-workload", default="decode_1m", help="empty: skip the hierarchical-indexer object")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

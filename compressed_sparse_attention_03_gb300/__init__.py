@@ -40,7 +40,8 @@ class csa2_config(C.Structure):
 EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_string", "csa2_kernel_launches",
            "csa2_workspace_bytes",
            "csa2_write_cache", "csa2_index_topk", "csa2_index_pool", "csa2_reindex_topk", "csa2_attend",
-           "csa2_attend_replay", "csa2_attend_static", "csa2_check", "csa2_selftest_timeout")
+           "csa2_attend_replay", "csa2_attend_static", "csa2_check", "csa2_selftest_timeout",
+           "csa2_out_group_proj")
 
 _lib = None
 
@@ -68,6 +69,8 @@ def lib() -> C.CDLL:
         L.csa2_write_cache.restype = i32
         L.csa2_index_topk.argtypes = [p] * 5 + [i64, p, i32, i32, p, p, p, sz, p]
         L.csa2_index_topk.restype = i32
+        L.csa2_out_group_proj.argtypes = [p, p, p, i64, p, p]
+        L.csa2_out_group_proj.restype = i32
         L.csa2_check.argtypes = [p, p]
         L.csa2_check.restype = i32
         L.csa2_selftest_timeout.argtypes = [p, p]
@@ -221,6 +224,16 @@ def csa2_reindex_topk(h: Handle, qi, wI, ki_codes, ki_scales, p0, pool, idx, top
         _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
         _dev(pool, torch.int32, "pool"), _dev(idx, torch.int32, "idx"), _dev(top_scores, torch.float32, "top_scores"),
         _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+
+
+def csa2_out_group_proj(h: Handle, o, w_oa, out, stream=None) -> None:
+    """o [.., 64, 512] bf16 -> out [.., 8, 1024] bf16 through the 8 grouped W_OA [8, 1024, 4096]."""
+    M = o.numel() // (64 * 512)
+    if out.numel() != M * 8 * 1024 or w_oa.numel() != 8 * 1024 * 4096:
+        raise ValueError("csa2_out_group_proj: shapes")
+    _check("csa2_out_group_proj", lib().csa2_out_group_proj(
+        h.ptr, _dev(o, torch.bfloat16, "o"), _dev(w_oa, torch.bfloat16, "w_oa"), M,
+        _dev(out, torch.bfloat16, "out"), _stream(stream)))
 
 
 def csa2_check(h: Handle, stream=None) -> int:

@@ -336,9 +336,11 @@ csa2_status csa2_check(csa2_handle* h, csa2_stream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
   if (dev != h->device) return CSA2_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
-  int ea = 0, ei = 0;
-  if (csa2::take_attend_error(&ea) != cudaSuccess || csa2::take_index_error(&ei) != cudaSuccess) return CSA2_ERR_CUDA;
-  return (ea || ei) ? CSA2_ERR_TIMEOUT : CSA2_OK;
+  int ea = 0, ei = 0, eo = 0;
+  if (csa2::take_attend_error(&ea) != cudaSuccess || csa2::take_index_error(&ei) != cudaSuccess ||
+      csa2::take_outproj_error(&eo) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  return (ea || ei || eo) ? CSA2_ERR_TIMEOUT : CSA2_OK;
 }
 
 // Test hook for the timeout report (include/csa2.h).
@@ -348,4 +350,16 @@ csa2_status csa2_selftest_timeout(csa2_handle* h, csa2_stream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
   if (dev != h->device) return CSA2_ERR_INVALID_ARG;
   return cuda_status(csa2::launch_wait_probe(reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Grouped output projection W_OA (include/csa2.h).
+csa2_status csa2_out_group_proj(csa2_handle* h, const uint16_t* o, const uint16_t* w_oa, int64_t M, uint16_t* out,
+                                csa2_stream_t stream) {
+  if (!h || !o || !w_oa || !out) return CSA2_ERR_INVALID_ARG;
+  if (M <= 0 || M > (int64_t(1) << 31)) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(w_oa) || !aligned16(out)) return CSA2_ERR_ALIGN;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (dev != h->device) return CSA2_ERR_INVALID_ARG;
+  return cuda_status(csa2::launch_out_group_proj(o, w_oa, M, out, h->num_sms, reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -84,6 +84,11 @@ cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos,
 // synchronised the work it checks).
 cudaError_t take_attend_error(int* code);
 cudaError_t take_index_error(int* code);
+cudaError_t take_outproj_error(int* code);
+// Grouped output projection: o [M, 64, 512] bf16, w [8, 1024, 4096] bf16 (group, output,
+// input), out [M, 8, 1024] bf16.
+cudaError_t launch_out_group_proj(const uint16_t* o, const uint16_t* w, int64_t M, uint16_t* out, int num_sms,
+                                  cudaStream_t st);
 // A kernel whose one bounded wait can never complete (a test of the timeout report).
 cudaError_t launch_wait_probe(cudaStream_t st);
 // Counts one kernel enqueued by this library (read back by csa2_kernel_launches).

@@ -115,6 +115,17 @@ def layer_params(seed: int, device="cpu"):
     return dict(gamma_c=gamma_c, w_ik=w_ik, gamma_ik=gamma_ik, gamma_w=gamma_w, sinks=sinks)
 
 
+def out_proj_inputs(M: int, seed: int, device="cpu"):
+    """Grouped output projection: attention outputs O-bar [M,64,512] bf16 ~ 0.5 N(0,1) (the
+    scale of a softmax-weighted mean of unit rows) and W_OA [8,1024,4096] bf16 ~
+    N(0,1)/sqrt(4096) (group, output, input)."""
+    g = _gen(40_000 + seed, device)
+    f32 = dict(device=device, dtype=torch.float32, generator=g)
+    o = (0.5 * torch.randn(M, H, D, **f32)).to(torch.bfloat16)
+    w = (torch.randn(8, 1024, 8 * D, **f32) / (8 * D) ** 0.5).to(torch.bfloat16)
+    return dict(o=o, w_oa=w)
+
+
 def step_inputs(B: int, T: int, seed: int, device="cpu"):
     """Per-token inputs of one step, all bf16: k^c, g^c, w^a [B,T,512] ~N(0,1);
     Q [B,T,64,512] ~N(0,1); Q^I [B,T,32,128] ~N(0,1); w^I [B,T,32] ~N(0,1)/sqrt(128*32)."""

@@ -177,6 +177,17 @@ csa2_status csa2_reindex_topk(csa2_handle* h, const uint16_t* qi, const uint16_t
                               int32_t* idx, float* top_scores, void* ws, size_t ws_bytes,
                               csa2_stream_t stream);
 
+/* Grouped output projection W_OA ("Inside DeepSeek V4.1", section "Attention that looks at
+ * 640 places": 8 groups of a 1,024-wide bottleneck; [PG] o^g_{t,r} = [O-bar_{h,t}]_{h in r} W_OA,r).
+ *  o    : bf16 [M, 64, 512]  attention outputs (M = B*T rows, e.g. csa2_attend's `out`).
+ *  w_oa : bf16 [8, 1024, 4096]  per group r the weights as [output i][input k], input
+ *         k = 512 (h - 8r) + d for head h of group r (heads 8r .. 8r+7, one after another).
+ *  out  : bf16 [M, 8, 1024]  o^g; fp32 accumulation, rounded to bf16 once.
+ * The model width that W_OB maps o^g back to is not on the pages, so W_OB is not provided.
+ * Workspace: none. */
+csa2_status csa2_out_group_proj(csa2_handle* h, const uint16_t* o, const uint16_t* w_oa,
+                                int64_t M, uint16_t* out, csa2_stream_t stream);
+
 /* Failure report (no counterpart on the pages).  Synchronises `stream`, then reports whether
  * a bounded wait inside any kernel of this library gave up since the last check:
  * CSA2_ERR_TIMEOUT (the outputs of the calls since then are not to be trusted), CSA2_ERR_CUDA
