@@ -316,7 +316,9 @@ def time_out_proj(csa2, inputs, M, steps, warmup, ws, flush, bf16, src, rank):
     return {"rows": M, "ms": ms, "gpu_launches": launches,
             "roofline": {"kernel": "outproj_kernel", "bound": "tensor", "achieved": tf, "peak": bf16,
                          "unit": "TFLOP/s", "frac": tf / bf16, "flops_per_launch": flops,
-                         "peak_source": f"{src} bf16 burst"}}
+                         "peak_source": f"{src} bf16 burst",
+                         "traffic": profiled_traffic("outproj_kernel_prefill_4k.md", OUTPROJ_SOURCES) if M == 4096
+                         else None}}
 
 
 class _Null:
@@ -378,6 +380,7 @@ CSRC = "compressed_sparse_attention_03_gb300/csrc/"
 _HDRS = [CSRC + "csa2_common.cuh", CSRC + "csa2_fp16.cuh", CSRC + "csa2_sm100.cuh", CSRC + "csa2_internal.h"]
 ATTEND_SOURCES = [CSRC + "csa2_attend.cu"] + _HDRS
 INDEX_SOURCES = [CSRC + "csa2_index_tc.cu", CSRC + "csa2_indexer.cu"] + _HDRS
+OUTPROJ_SOURCES = [CSRC + "csa2_outproj.cu"] + _HDRS
 
 
 def peaks():
