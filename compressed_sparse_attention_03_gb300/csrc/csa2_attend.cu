@@ -168,6 +168,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     // indices; the producers convert it after the setup barrier
     mbar_arrive_expect_tx(&bars.q_raw, kH * kD * 2);
     bulk_g2s(sm + kGOff, a.q + qrow * kH * kD, kH * kD * 2, &bars.q_raw);
+    // the query one wave of blocks ahead (it will most likely run on some SM when this block
+    // ends): its Q and index row into L2, so that its prologue starts from L2
+    uint32_t nsm;
+    asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));  // SMs of the device: one block each at a time
+    const int ahead = (int)nsm;
+    if (split == 0 && t + ahead < T) {
+      bulk_prefetch_l2(a.q + (qrow + ahead) * kH * kD, kH * kD * 2);
+      bulk_prefetch_l2(a.idx + (qrow + ahead) * kTopK, kTopK * 4);
+    }
   }
   if (warp == 12) {
     tmem_alloc(&tmem_base_sh, kTmemCols);
@@ -216,11 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         }
       }
     };
+    // the first chunk's rows are requested before waiting for the staged Q, so that the two
+    // latencies overlap (the row list is complete at the setup barrier)
+    if (nloc > 0) load(0);
     mbar_wait(&bars.q_raw, 0, err, 8);  // the staged Q has landed (waited for even without chunks)
     if (nloc > 0) {
-      // Q (bf16, staged in the G area) -> fp16, 8 K-major atoms of [64 heads x 64 dims]; the
-      // first chunk's rows are requested before the conversion so that their latency overlaps.
-      load(0);
+      // Q (bf16, staged in the G area) -> fp16, 8 K-major atoms of [64 heads x 64 dims]
       const uint4* qs = reinterpret_cast<const uint4*>(sm + kGOff);
 #pragma unroll 4
       for (int k = 0; k < 16; ++k) {
