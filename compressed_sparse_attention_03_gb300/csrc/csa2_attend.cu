@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       if (tid == 0) {
         bulk_s2g(a.out + qrow * kH * kD, ost, kH * kD * 2);
         bulk_commit();
-        bulk_wait_all();  // the copy has read the shared memory (and written) before exit
+        bulk_wait_read();  // the copy has read the shared memory before the block exits
       }
     } else {
       const int64_t pr_row = ((int64_t)bl * T + t) * nsplit + split;
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       if (tid == 0) {
         bulk_s2g(po, ost, kH * kD * 4);
         bulk_commit();
-        bulk_wait_all();
+        bulk_wait_read();
       }
       if (tid < 64) {
         part_ml[(pr_row * kH + tid) * 2] = m_ref[tid];
