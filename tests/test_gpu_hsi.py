@@ -157,3 +157,20 @@ def test_hsi_argument_errors(handle):
         csa2.csa2_index_pool(handle, x["qi"], x["wI"], x["ki_codes"], x["ki_scales"], [100], idx, None)
     with pytest.raises(RuntimeError):
         csa2.csa2_reindex_topk(handle, x["qi"], x["wI"], x["ki_codes"], x["ki_scales"], [100], None, idx)
+
+
+def test_hsi_two_launch_groups(handle):
+    # 130 sequences run as a group of 128 and a tail of 2 (its workspace and its pool rows at
+    # sequence offset 128); contexts from a few blocks to more than 2048 blocks
+    rng = np.random.default_rng(12)
+    B = 130
+    p0s = rng.integers(0, 40000, B)
+    p0s[-1] = 36001  # the tail holds a row with more than 2048 blocks
+    x, cap = make_state(B, 1, p0s, seed=31)
+    rows = [0, 1, 64, 127, 128, 129]
+    idx, pool = run_pool(handle, x, p0s)
+    for b in rows:
+        sc, E = oracle_scores(x, x["qi"], x["wI"], b, int(p0s[b]), np.arange(1), 2)
+        oidx, _, kth = oracle.topk(sc, E)
+        topk_compare(idx[b].cpu().numpy(), oidx, sc, kth, E)
+        pool_compare(pool[b].cpu().numpy(), oracle.hsi_pool(sc, E), sc, E)
