@@ -18,7 +18,8 @@ namespace {
 constexpr int kQprepThreads = 128;
 constexpr int kScoreThreads = 256;  // one key per thread
 constexpr int kQT = 4;              // queries per score block
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 512;  // select blocks that read a score histogram, merges, pools
+constexpr int kTopkSmall = 128;    // select blocks of rows without a histogram (several per SM)
 constexpr int kMaxChunks = 32;
 constexpr int kMinChunk = 4096;
 constexpr int kMaxChunk = 32768;
@@ -175,12 +176,12 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(IndexArgs a, SeqPo
 
 // ------------------------------------------------------------------ top-k
 
-constexpr int kTopkWarps = kTopkThreads / 32;
-
+template <int NT>
 struct SelectShared {
-  uint32_t hist[kTopkWarps][256];  // one histogram per warp: fewer same-address atomics
-  uint32_t red[2][kTopkWarps];
-  int warp_tot[2][kTopkWarps];
+  static constexpr int kWarps = NT / 32;
+  uint32_t hist[kWarps][256];  // one histogram per warp: fewer same-address atomics
+  uint32_t red[2][kWarps];
+  int warp_tot[2][kWarps];
   uint32_t bucket;
   int krem;
 };
@@ -193,13 +194,15 @@ struct SelectShared {
 // longer rows count into one histogram per warp.
 constexpr int kSmallSelect = 4096;
 
-__device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared& sh, uint32_t* thr, int* need_eq) {
+template <int NT>
+__device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared<NT>& sh, uint32_t* thr, int* need_eq) {
+  constexpr int kWarps = NT / 32;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
   const bool one_hist = n <= kSmallSelect;
-  const int hw = one_hist ? 0 : w;                       // this thread's histogram
-  const int nclear = (one_hist ? 1 : kTopkWarps) * 256;  // words to clear per pass
+  const int hw = one_hist ? 0 : w;                   // this thread's histogram
+  const int nclear = (one_hist ? 1 : kWarps) * 256;  // words to clear per pass
   uint32_t mn = 0xffffffffu, mx = 0u;
-  for (int i = tid; i < n; i += kTopkThreads) {
+  for (int i = tid; i < n; i += NT) {
     const uint32_t k = keys[i];
     mn = min(mn, k);
     mx = max(mx, k);
@@ -213,7 +216,7 @@ __device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared& s
   __syncthreads();
   mn = 0xffffffffu;
   mx = 0u;
-  for (int x = 0; x < kTopkWarps; ++x) {
+  for (int x = 0; x < kWarps; ++x) {
     mn = min(mn, sh.red[0][x]);
     mx = max(mx, sh.red[1][x]);
   }
@@ -230,18 +233,18 @@ __device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared& s
   for (int hi = top; hi >= 0; hi -= 8) {
     const int lo = max(hi - 7, 0);
     const uint32_t dmask = (2u << (hi - lo)) - 1u;
-    for (int i = tid; i < nclear; i += kTopkThreads) (&sh.hist[0][0])[i] = 0;
+    for (int i = tid; i < nclear; i += NT) (&sh.hist[0][0])[i] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kTopkThreads) {
+    for (int i = tid; i < n; i += NT) {
       const uint32_t k = keys[i];
       if ((k & mask) == prefix) atomicAdd(&sh.hist[hw][(k >> lo) & dmask], 1u);
     }
     __syncthreads();
     if (!one_hist) {
-      for (int b = tid; b < 256; b += kTopkThreads) {  // fold the per-warp histograms into warp 0's
+      for (int b = tid; b < 256; b += NT) {  // fold the per-warp histograms into warp 0's
         uint32_t c = 0;
 #pragma unroll
-        for (int x = 0; x < kTopkWarps; ++x) c += sh.hist[x][b];
+        for (int x = 0; x < kWarps; ++x) c += sh.hist[x][b];
         sh.hist[0][b] = c;
       }
       __syncthreads();
@@ -285,11 +288,13 @@ __device__ void radix_select(const uint32_t* keys, int n, int K, SelectShared& s
 // taken; of the keys == thr only the first need_eq (in position order).  js == nullptr
 // means j = j0 + position.  Each warp owns one contiguous segment: a counting pass, one scan
 // of the per-warp counts, then an ordered writing pass.
+template <int NT>
 __device__ void compact_selected(const uint32_t* keys, const int32_t* js, int64_t j0, int n, uint32_t thr, int need_eq,
-                                 SelectShared& sh, uint32_t* out_key, int32_t* out_j) {
+                                 SelectShared<NT>& sh, uint32_t* out_key, int32_t* out_j) {
+  constexpr int kWarps = NT / 32;
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const uint32_t lt = (1u << l) - 1u;
-  const int seg = (((n + kTopkWarps - 1) / kTopkWarps) + 31) & ~31;
+  const int seg = (((n + kWarps - 1) / kWarps) + 31) & ~31;
   const int s0 = min(n, w * seg), s1 = min(n, s0 + seg);
   int gt = 0, eq = 0;
   for (int i0 = s0; i0 < s1; i0 += 32) {
@@ -305,7 +310,7 @@ __device__ void compact_selected(const uint32_t* keys, const int32_t* js, int64_
   }
   __syncthreads();
   // lane x holds warp x's counts; exclusive scans give this warp's equal-key rank and output base
-  const int g = l < kTopkWarps ? sh.warp_tot[0][l] : 0, e = l < kTopkWarps ? sh.warp_tot[1][l] : 0;
+  const int g = l < kWarps ? sh.warp_tot[0][l] : 0, e = l < kWarps ? sh.warp_tot[1][l] : 0;
   int e_inc = e;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -351,7 +356,7 @@ __device__ __forceinline__ int32_t pool_entry(const int32_t* prow, int32_t p) {
 
 // Lower edge (a key) of the histogram bin holding the K-th largest key of a row, so that all
 // of the row's K largest keys are >= it (0 if the histogram holds fewer than K keys).
-__device__ uint32_t hist_lower(const uint32_t* hist, int K, SelectShared& sh) {
+__device__ uint32_t hist_lower(const uint32_t* hist, int K, SelectShared<kTopkThreads>& sh) {
   static_assert(kTopkThreads * 4 == kHistBins, "four bins per thread");
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
   const int top = kHistBins - 1 - 4 * tid;  // this thread's bins top .. top-3, from the largest keys down
@@ -368,13 +373,13 @@ __device__ uint32_t hist_lower(const uint32_t* hist, int K, SelectShared& sh) {
   if (tid == 0) sh.bucket = 0u;
   __syncthreads();
   if (w == 0) {
-    uint32_t y = l < kTopkWarps ? sh.red[0][l] : 0u;
+    uint32_t y = l < SelectShared<kTopkThreads>::kWarps ? sh.red[0][l] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t z = __shfl_up_sync(0xffffffffu, y, o);
       if (l >= o) y += z;
     }
-    if (l < kTopkWarps) sh.red[1][l] = y;
+    if (l < SelectShared<kTopkThreads>::kWarps) sh.red[1][l] = y;
   }
   __syncthreads();
   const uint32_t excl = x - s + (w ? sh.red[1][w - 1] : 0u);
@@ -397,13 +402,16 @@ __device__ uint32_t hist_lower(const uint32_t* hist, int K, SelectShared& sh) {
 
 // With hist (the row's score histogram), a chunk whose keys at or above the K-th largest
 // key's bin number at most 512 passes exactly those on (a superset of its part of the row's
-// top-512, in position order) and skips the radix select.
-__global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, SeqPos pos, int b0, int t0, int Tq,
-                                                                  const float* scores, int64_t ld, int chunk, int nchunks,
-                                                                  uint32_t* ck, int32_t* cj, int* cn, const int* rowlen,
-                                                                  const uint32_t* hist) {
+// top-512, in position order) and skips the radix select.  NT threads per block: rows with a
+// histogram take kTopkThreads (hist_lower reads four bins per thread); the others take
+// kTopkSmall, so that several rows share an SM and hide one another's barrier latency.
+template <int NT>
+__global__ void __launch_bounds__(NT) topk_chunk_kernel(IndexArgs a, SeqPos pos, int b0, int t0, int Tq,
+                                                        const float* scores, int64_t ld, int chunk, int nchunks,
+                                                        uint32_t* ck, int32_t* cj, int* cn, const int* rowlen,
+                                                        const uint32_t* hist) {
   extern __shared__ uint32_t skeys[];
-  __shared__ SelectShared sh;
+  __shared__ SelectShared<NT> sh;
   __shared__ uint32_t okey[kTopK];
   __shared__ int32_t oj[kTopK];
   __shared__ int cnt_sh;
@@ -416,27 +424,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, S
   const int64_t cs = (int64_t)c * chunk;
   const int n = (int)max64(0, min64(chunk, E - cs));
   // the candidates' lower bound, before the loads (the histogram is complete)
-  const uint32_t lower = hist && n > kTopK ? hist_lower(hist + row * kHistBins, (int)min64(kTopK, E), sh) : 0u;
+  uint32_t lower = 0u;
+  if constexpr (NT == kTopkThreads)
+    if (hist && n > kTopK) lower = hist_lower(hist + row * kHistBins, (int)min64(kTopK, E), sh);
   const float* src = scores + row * ld + cs;  // 16-byte aligned: ld and the chunk are multiples of 32
   const int n4 = n >> 2;
   constexpr int kLB = 4;  // 16-byte loads in flight per thread
-  for (int v0 = threadIdx.x; v0 < n4; v0 += kLB * kTopkThreads) {
+  for (int v0 = threadIdx.x; v0 < n4; v0 += kLB * NT) {
     float4 f[kLB];
 #pragma unroll
     for (int u = 0; u < kLB; ++u)
-      if (v0 + u * kTopkThreads < n4) f[u] = __ldg(reinterpret_cast<const float4*>(src) + v0 + u * kTopkThreads);
+      if (v0 + u * NT < n4) f[u] = __ldg(reinterpret_cast<const float4*>(src) + v0 + u * NT);
 #pragma unroll
     for (int u = 0; u < kLB; ++u)
-      if (v0 + u * kTopkThreads < n4)
-        reinterpret_cast<uint4*>(skeys)[v0 + u * kTopkThreads] =
+      if (v0 + u * NT < n4)
+        reinterpret_cast<uint4*>(skeys)[v0 + u * NT] =
             make_uint4(score_key(f[u].x), score_key(f[u].y), score_key(f[u].z), score_key(f[u].w));
   }
-  for (int i = 4 * n4 + threadIdx.x; i < n; i += kTopkThreads) skeys[i] = score_key(src[i]);
+  for (int i = 4 * n4 + threadIdx.x; i < n; i += NT) skeys[i] = score_key(src[i]);
   if (threadIdx.x == 0) cnt_sh = 0;
   __syncthreads();
   int K = min(kTopK, n);  // entries in okey / oj
   if (n <= kTopK) {  // every candidate is kept, already in position order
-    for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+    for (int i = threadIdx.x; i < n; i += NT) {
       okey[i] = skeys[i];
       oj[i] = (int32_t)(cs + i);
     }
@@ -444,7 +454,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, S
     int cnt = kTopK + 1;
     if (lower > 0u) {
       int m = 0;
-      for (int i = threadIdx.x; i < n; i += kTopkThreads) m += skeys[i] >= lower;
+      for (int i = threadIdx.x; i < n; i += NT) m += skeys[i] >= lower;
       m = __reduce_add_sync(0xffffffffu, m);
       if ((threadIdx.x & 31) == 0) atomicAdd(&cnt_sh, m);
       __syncthreads();
@@ -465,13 +475,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(IndexArgs a, S
     int32_t* idx = a.idx + ((int64_t)b * a.T + t) * kTopK;
     float* ts = a.top_scores ? a.top_scores + ((int64_t)b * a.T + t) * kTopK : nullptr;
     const int32_t* prow = a.pool_in ? a.pool_in + ((int64_t)b * a.T + t) * kHsiBlocks : nullptr;
-    for (int i = threadIdx.x; i < kTopK; i += kTopkThreads) {
+    for (int i = threadIdx.x; i < kTopK; i += NT) {
       idx[i] = i < K ? pool_entry(prow, oj[i]) : -1;
       if (ts) ts[i] = i < K ? key_score(okey[i]) : __int_as_float(0x7fc00000);
     }
   } else {
     const int64_t base = (row * nchunks + c) * kTopK;
-    for (int i = threadIdx.x; i < K; i += kTopkThreads) {
+    for (int i = threadIdx.x; i < K; i += NT) {
       ck[base + i] = okey[i];
       cj[base + i] = oj[i];
     }
@@ -485,7 +495,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(IndexArgs a, i
   extern __shared__ uint32_t smem[];
   uint32_t* skeys = smem;                                                // [nchunks*512]
   int32_t* sjs = reinterpret_cast<int32_t*>(smem + nchunks * kTopK);    // [nchunks*512]
-  __shared__ SelectShared sh;
+  __shared__ SelectShared<kTopkThreads> sh;
   __shared__ uint32_t okey[kTopK];
   __shared__ int32_t oj[kTopK];
   __shared__ int offs[kMaxChunks + 1];
@@ -560,7 +570,7 @@ __global__ void __launch_bounds__(kTopkThreads) pool_chunk_kernel(IndexArgs a, S
   extern __shared__ uint32_t pkeys[];  // [kPoolChunk] block keys, then okey / oj [kPoolSel]
   uint32_t* okey = pkeys + kPoolChunk;
   int32_t* oj = reinterpret_cast<int32_t*>(okey + kPoolSel);
-  __shared__ SelectShared sh;
+  __shared__ SelectShared<kTopkThreads> sh;
   const int c = blockIdx.x, tl = blockIdx.y, bl = blockIdx.z;
   const int t = t0 + tl;
   if (t >= a.T || tl >= Tq) return;
@@ -623,7 +633,7 @@ __global__ void __launch_bounds__(kTopkThreads) pool_merge_kernel(IndexArgs a, S
   int32_t* js = reinterpret_cast<int32_t*>(keys + pnch * kPoolSel);     // [pnch * kPoolSel]
   uint32_t* okey = reinterpret_cast<uint32_t*>(js + pnch * kPoolSel);   // [kPoolSel]
   int32_t* oj = reinterpret_cast<int32_t*>(okey + kPoolSel);            // [kPoolSel]
-  __shared__ SelectShared sh;
+  __shared__ SelectShared<kTopkThreads> sh;
   __shared__ int offs[kMaxChunks + 1];
   const int tl = blockIdx.x, bl = blockIdx.y;
   const int t = t0 + tl;
@@ -688,12 +698,14 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
   const size_t pool_chunk_smem = (size_t)kPoolChunk * 4 + (size_t)kPoolSel * 8;
   const size_t pool_merge_smem = (size_t)max(p.pnch, 1) * kPoolSel * 8 + (size_t)kPoolSel * 8;
   const size_t score_smem = (size_t)kQT * kHI * kDI * 4;
-  const size_t chunk_smem = (size_t)p.chunk * 4;
+  const size_t chunk_smem = (size_t)min64(p.chunk, p.ld) * 4;  // a chunk holds at most ld keys
   const size_t merge_smem = (size_t)p.nchunks * kTopK * 8;
   cudaError_t e;
   e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)score_smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chunk_smem);
+  e = cudaFuncSetAttribute(topk_chunk_kernel<kTopkThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chunk_smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(topk_chunk_kernel<kTopkSmall>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chunk_smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)merge_smem);
   if (e != cudaSuccess) return e;
@@ -732,8 +744,12 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const int nch = (int)max64(1, (emax + p.chunk - 1) / p.chunk);
-    topk_chunk_kernel<<<dim3(nch, tq, nb), kTopkThreads, chunk_smem, st>>>(a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch,
-                                                                            ck, cj, cn, rowlen, hist);
+    if (hist)
+      topk_chunk_kernel<kTopkThreads><<<dim3(nch, tq, nb), kTopkThreads, chunk_smem, st>>>(
+          a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch, ck, cj, cn, rowlen, hist);
+    else
+      topk_chunk_kernel<kTopkSmall><<<dim3(nch, tq, nb), kTopkSmall, chunk_smem, st>>>(
+          a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch, ck, cj, cn, rowlen, nullptr);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (nch > 1) {

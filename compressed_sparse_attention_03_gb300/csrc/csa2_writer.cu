@@ -5,8 +5,9 @@
 // RMSNorm as on "DeepSeek V4.1 - Window layer / Attention RMSNorm" (eps 1e-20).
 //
 // Precision: fp32 elementwise work, compensated (double-float fp32) sums of squares and a
-// compensated dot product for c W_IK, so that the values reaching the FP4/FP8 rounding differ from an
-// fp64 evaluation by a few fp32 ulps and the codes match except at rounding midpoints.
+// compensated dot product for c W_IK (fp32 FMA chains of kChain terms, each folded into a
+// double-float sum), so that the values reaching the FP4/FP8 rounding differ from an fp64
+// evaluation by about 1e-7 of the row's rms and the codes match except at rounding midpoints.
 #include "csa2_common.cuh"
 #include "csa2_sm100.cuh"
 
@@ -16,6 +17,9 @@ namespace {
 constexpr int kWriterThreads = 128;       // window kernel: one token per block
 constexpr int kEntryThreads = 512;        // entries kernel: four groups of 128
 constexpr int kEntriesPerBlock = 4;       // one per group
+// Products of c W_IK summed in plain fp32 before joining the double-float sum: a chain of 16
+// terms of size ~|c||w| carries a rounding error of a few 1e-8 of the result's rms.
+constexpr int kChain = 16;
 
 // Pack the four 4-bit codes of one thread (4 consecutive values) into two bytes.
 __device__ __forceinline__ uint16_t pack4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
@@ -38,6 +42,12 @@ __device__ __forceinline__ uint16_t fp4_quant4(const float v[4], uint8_t* scale_
 // Double-float accumulation of sum(x*w): error-free product (fma) and two-sum.
 struct DF {
   float s, c;
+  __device__ __forceinline__ void add(float p) {  // two-sum
+    float t = s + p;
+    float bb = t - s;
+    c += (s - (t - bb)) + (p - bb);
+    s = t;
+  }
   __device__ __forceinline__ void add_prod(float x, float w) {
     float p = x * w;
     float pe = fmaf(x, w, -p);
@@ -158,35 +168,35 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
   __syncthreads();
 
   // ---- phase 2: quarter g of k^i = c W_IK for the block's entries (thread = output column)
-  if (ne == 1) {  // one entry (decode): accumulate it alone, in two chains (even / odd K)
-    DF acc0{0.f, 0.f}, acc1{0.f, 0.f};
+  {
     const int o = gt;
-    for (int d0 = 128 * g; d0 < 128 * g + 128; d0 += 16) {
-      uint32_t wv[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) wv[u] = __ldg(a.w_ik + (d0 + u) * kDI + o);
-#pragma unroll
-      for (int u = 0; u < 16; u += 2) {
-        acc0.add_prod(sc[0][d0 + u], __uint_as_float(wv[u] << 16));
-        acc1.add_prod(sc[0][d0 + u + 1], __uint_as_float(wv[u + 1] << 16));
-      }
-    }
-    acc0.add_prod(acc1.s, 1.f);
-    acc0.c += acc1.c;
-    part[g][0][o] = make_float2(acc0.s, acc0.c);
-  } else {
+    const int nacc = ne == 1 ? 1 : kEntriesPerBlock;  // one entry (decode) skips the empty rows
     DF acc[kEntriesPerBlock];
 #pragma unroll
     for (int e = 0; e < kEntriesPerBlock; ++e) acc[e] = DF{0.f, 0.f};
-    const int o = gt;
-#pragma unroll 4
-    for (int d = 128 * g; d < 128 * g + 128; ++d) {
-      const float w = bf16_to_f32(a.w_ik[d * kDI + o]);
+    for (int d0 = 128 * g; d0 < 128 * g + 128; d0 += kChain) {
+      float w[kChain];
 #pragma unroll
-      for (int e = 0; e < kEntriesPerBlock; ++e) acc[e].add_prod(sc[e][d], w);
+      for (int u = 0; u < kChain; ++u) w[u] = bf16_to_f32(__ldg(a.w_ik + (d0 + u) * kDI + o));
+#pragma unroll
+      for (int e = 0; e < kEntriesPerBlock; ++e) {
+        if (e < nacc) {
+          float s = 0.f;
+#pragma unroll
+          for (int u = 0; u < kChain; u += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(&sc[e][d0 + u]);
+            s = fmaf(x.x, w[u], s);
+            s = fmaf(x.y, w[u + 1], s);
+            s = fmaf(x.z, w[u + 2], s);
+            s = fmaf(x.w, w[u + 3], s);
+          }
+          acc[e].add(s);
+        }
+      }
     }
 #pragma unroll
-    for (int e = 0; e < kEntriesPerBlock; ++e) part[g][e][o] = make_float2(acc[e].s, acc[e].c);
+    for (int e = 0; e < kEntriesPerBlock; ++e)
+      if (e < nacc) part[g][e][o] = make_float2(acc[e].s, acc[e].c);
   }
   __syncthreads();
 
