@@ -29,6 +29,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kQPerTile = 8;                       // queries per query tile (N = 256)
+static_assert(kQPerTile % 2 == 0, "the epilogue reads two queries per TMEM wait");
 constexpr uint32_t kQImg = 65536, kKImg = 32768;   // bytes per image
 constexpr int kThreadsTC = 256;
 // dynamic smem: B (query images) 2 x 64 KB, A (key images) 2 x 32 KB, w^I 2 x [8][32] floats
@@ -251,16 +252,30 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
         mbar_wait(&bars.d_full[sD], (dc >> 1) & 1, err, 16);
         tc_fence_after();
         const int64_t j = (int64_t)kt * 128 + r;
+        // two queries per TMEM wait, and four independent partial sums per query (heads h mod 4),
+        // so that one warp per sub-partition is not held by load waits and one long FMA chain
 #pragma unroll 1
-        for (int q = 0; q < kQPerTile; ++q) {
-          const int tl = qt * kQPerTile + q;
-          uint32_t u[32];
-          tmem_ld32(lane_addr + 256 * sD + 32 * q, u);
+        for (int q = 0; q < kQPerTile; q += 2) {
+          uint32_t u[2][32];
+          tmem_ld32(lane_addr + 256 * sD + 32 * q, u[0]);
+          tmem_ld32(lane_addr + 256 * sD + 32 * (q + 1), u[1]);
           tmem_wait_ld();
-          float s = 0.f;
 #pragma unroll
-          for (int h = 0; h < 32; ++h) s = fmaf(wsm[32 * q + h], fmaxf(__uint_as_float(u[h]), 0.f), s);
-          if (tl < tq && j < ((p0 + tl + 1) >> a.rshift)) scores[((int64_t)bl * Tq + tl) * ld + j] = s;
+          for (int e = 0; e < 2; ++e) {
+            const int tl = qt * kQPerTile + q + e;
+            const float4* w4 = reinterpret_cast<const float4*>(wsm + 32 * (q + e));
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+              const float4 w = w4[h4];
+              s[0] = fmaf(w.x, fmaxf(__uint_as_float(u[e][4 * h4]), 0.f), s[0]);
+              s[1] = fmaf(w.y, fmaxf(__uint_as_float(u[e][4 * h4 + 1]), 0.f), s[1]);
+              s[2] = fmaf(w.z, fmaxf(__uint_as_float(u[e][4 * h4 + 2]), 0.f), s[2]);
+              s[3] = fmaf(w.w, fmaxf(__uint_as_float(u[e][4 * h4 + 3]), 0.f), s[3]);
+            }
+            if (tl < tq && j < ((p0 + tl + 1) >> a.rshift))
+              scores[((int64_t)bl * Tq + tl) * ld + j] = (s[0] + s[1]) + (s[2] + s[3]);
+          }
         }
         tc_fence_before();
         __syncwarp();
