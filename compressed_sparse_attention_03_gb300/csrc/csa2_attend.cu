@@ -20,7 +20,8 @@
 // accumulators costs more, so each accumulator receives its MMAs consecutively.
 //
 // Warp roles (416 threads):
-//   warps 0-3   softmax + epilogue; thread = TMEM lane = row of S^T / dim of O^T
+//   warps 0-3   softmax (thread = TMEM lane = row of S^T), then the row sums and 1/denominator;
+//               with the producers, the output epilogue (thread = TMEM lane = dim of O^T)
 //   warps 4-11  producers: Q -> smem once, then gather + decode 128 rows per chunk, two
 //               threads per row (atoms 2a and 2a+1 of tile a); the raw rows of chunk c+1
 //               wait in registers while chunk c is consumed and are written as soon as the
@@ -444,45 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       l_run[tid] = l;
       den_s[tid] = nsplit == 1 ? 1.f / (l + exp2f(a.sinks[tid] * kLog2e - m_ref[tid])) : 1.f;
     }
-    named_bar_sync(1, 128);
-    if (nsplit == 1) {
-      // the output row [64 heads][512 dims] is assembled in the G area (free: the last MMAs
-      // are done) and written with one bulk copy
-      uint16_t* ost = reinterpret_cast<uint16_t*>(sm + kGOff);
-      for (int m = 0; m < 4; ++m) {
-        const int d = 128 * m + r;
-        float cs = 1.f, sn = 0.f;
-        if (m == 3 && r >= 64) rope_cs(p, rf.inv_freq[(d - (kD - kDR)) >> 1], -1.0f, cs, sn);
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t u[32];
-          tmem_ld32(lane_addr + 64 * m + 32 * hh, u);
-          tmem_wait_ld();
-          float o[32];
-#pragma unroll
-          for (int h = 0; h < 32; ++h) o[h] = __uint_as_float(u[h]) * den_s[32 * hh + h];
-          if (m == 3 && warp >= 2) {  // dims 448..511: rotate each (even, odd) pair back by -t
-            const bool odd = d & 1;
-#pragma unroll
-            for (int h = 0; h < 32; ++h) {
-              const float partner = __shfl_xor_sync(0xffffffffu, o[h], 1);
-              o[h] = odd ? fmaf(partner, sn, o[h] * cs) : fmaf(-partner, sn, o[h] * cs);
-            }
-          }
-#pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            const __nv_bfloat16 v = __float2bfloat16_rn(o[h]);
-            ost[(32 * hh + h) * kD + d] = *reinterpret_cast<const uint16_t*>(&v);
-          }
-        }
-      }
-      fence_proxy_async();
+    if (nsplit != 1) {
       named_bar_sync(1, 128);
-      if (tid == 0) {
-        bulk_s2g(a.out + qrow * kH * kD, ost, kH * kD * 2);
-        bulk_commit();
-        bulk_wait_read();  // the copy has read the shared memory before the block exits
-      }
-    } else {
       const int64_t pr_row = ((int64_t)bl * T + t) * nsplit + split;
       float* po = part_o + pr_row * kH * kD;
       // the split's O [64 heads][512 dims] fp32 (128 KB, the whole G area) in shared memory,
@@ -514,6 +478,47 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       if (tid < 64) {
         part_ml[(pr_row * kH + tid) * 2] = m_ref[tid];
         part_ml[(pr_row * kH + tid) * 2 + 1] = l_run[tid];
+      }
+    }
+  }
+  if (nsplit == 1 && warp < 12) {
+    // ------------------------------------------------------------ output (warps 0-11)
+    // O^T tile m, heads 32hh..32hh+31 -> bf16, straight to global: lane = dim, so a warp writes
+    // 64 contiguous bytes per head.  The producers are idle by now and reach the same TMEM lane
+    // quarters (warp % 4), so each quarter's eight (tile, head half) units go to three warps.
+    named_bar_sync(3, 384);  // warps 0-3 have seen the last MMAs complete and written den_s
+    tc_fence_after();
+    const int q4 = warp & 3, slot = warp >> 2;
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
+    uint16_t* orow = a.out + qrow * kH * kD;
+    for (int u = slot; u < 8; u += 3) {
+      const int m = u >> 1, hh = u & 1, d = 128 * m + r;
+      float o[32];
+      if (nloc > 0) {
+        uint32_t v[32];
+        tmem_ld32(lane_addr + 64 * m + 32 * hh, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 32; ++h) o[h] = __uint_as_float(v[h]) * den_s[32 * hh + h];
+      } else {
+#pragma unroll
+        for (int h = 0; h < 32; ++h) o[h] = 0.f;
+      }
+      if (m == 3 && q4 >= 2) {  // dims 448..511: rotate each (even, odd) pair back by -t
+        float cs, sn;
+        rope_cs(p, rf.inv_freq[(d - (kD - kDR)) >> 1], -1.0f, cs, sn);
+        const bool odd = d & 1;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          const float partner = __shfl_xor_sync(0xffffffffu, o[h], 1);
+          o[h] = odd ? fmaf(partner, sn, o[h] * cs) : fmaf(-partner, sn, o[h] * cs);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 32; ++h) {
+        const __nv_bfloat16 bv = __float2bfloat16_rn(o[h]);
+        orow[(32 * hh + h) * kD + d] = *reinterpret_cast<const uint16_t*>(&bv);
       }
     }
   }

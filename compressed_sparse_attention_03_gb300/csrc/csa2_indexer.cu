@@ -505,11 +505,20 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(IndexArgs a, i
   const int b = b0 + bl;
   const int64_t row = (int64_t)bl * Tq + tl;
   __shared__ int cnt_s[kMaxChunks];
-  if (threadIdx.x < nchunks) cnt_s[threadIdx.x] = cn[row * nchunks + threadIdx.x];
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    offs[0] = 0;
-    for (int c = 0; c < nchunks; ++c) offs[c + 1] = offs[c] + cnt_s[c];
+  static_assert(kMaxChunks <= 32, "one warp scans the chunk counts");
+  if (threadIdx.x < 32) {  // lane c: chunk c's count and its list's end offset
+    const int v = threadIdx.x < nchunks ? cn[row * nchunks + threadIdx.x] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if ((int)threadIdx.x >= o) incl += y;
+    }
+    if (threadIdx.x < nchunks) {
+      cnt_s[threadIdx.x] = v;
+      offs[threadIdx.x + 1] = incl;
+    }
+    if (threadIdx.x == 0) offs[0] = 0;
   }
   __syncthreads();
   const int n = offs[nchunks];
