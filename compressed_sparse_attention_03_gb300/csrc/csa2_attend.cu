@@ -65,6 +65,15 @@ struct Bars {
   uint64_t tile_free[4];
 };
 
+// 2^x by the hardware approximation (relative error ~2^-22, results below 2^-126 flushed to 0,
+// 2^-inf = 0): P is stored as fp16, whose rounding (2^-11) and smallest subnormal (2^-24)
+// are far coarser.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Reduce v[32] over the 32 lanes of the warp; lane l receives the result for entry l.
 // Each round a lane keeps half of its entries and exchanges the other half.
 template <bool kMax>
@@ -160,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     mbar_init(&bars.q_raw, 1);
     mbar_init(&bars.q_full, 8);
     mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_full, 4);
+    mbar_init(&bars.p_full, 8);  // softmax warps 0-3 and producer warps 4-7
     mbar_init(&bars.l_done, 1);
     for (int i = 0; i < 8; ++i) mbar_init(&bars.atom_full[i], 8);
     for (int i = 0; i < 4; ++i) mbar_init(&bars.tile_free[i], 1);
@@ -195,6 +204,32 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   const int nch = (n + kRows - 1) / kRows;
   const int c_begin = split * chunks_per_split;
   const int nloc = max(0, min(nch, c_begin + chunks_per_split) - c_begin);
+
+  const float scale_log2 = rsqrtf((float)kD) * kLog2e;
+  // P[r, 32hh .. 32hh+31] = exp2(x - m) as fp16 into the MN-major [rows][heads] operand, for the
+  // chunk row r = this thread's TMEM lane (lane quarter warp % 4); true if some score exceeds
+  // its head's reference by more than kTau
+  auto p_half = [&](int hh, int r, uint32_t lane_addr, bool valid) -> bool {
+    uint32_t u[32];
+    tmem_ld32(lane_addr + kSCol + 32 * hh, u);
+    tmem_wait_ld();
+    bool over = false;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int h0 = 8 * q + 2 * k;
+        const float x0 = valid ? __uint_as_float(u[h0]) * scale_log2 : -INFINITY;
+        const float x1 = valid ? __uint_as_float(u[h0 + 1]) * scale_log2 : -INFINITY;
+        const float m0 = m_ref[32 * hh + h0], m1 = m_ref[32 * hh + h0 + 1];
+        over |= (x0 > m0 + kTau) | (x1 > m1 + kTau);
+        w[k] = f2_to_h2(ex2_ftz(x0 - m0), ex2_ftz(x1 - m1));
+      }
+      *reinterpret_cast<uint4*>(sm + kPOff + sw128_off(r, 4 * hh + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return over;
+  };
 
   if (warp >= 4 && warp < 12) {
     // ============================================================ producers
@@ -294,6 +329,24 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         __syncwarp();
         if (lane < 2) mbar_arrive(&bars.atom_full[2 * at + lane]);
       }
+      if (warp < 8) {
+        // warps 4-7 (lane quarters 0-3): heads 32..63 of this chunk's optimistic softmax pass,
+        // from the second chunk on (the barriers as in the softmax warps), then their share of
+        // p_full.  The tiles of the chunk are written, so the raw registers are free until
+        // load(i + 1).
+        if (i > 0) {
+          mbar_wait(&bars.s_full, i & 1, err, 10);
+          tc_fence_after();
+          named_bar_sync(5, 256);
+          const int r = 32 * (warp & 3) + lane;
+          const bool valid = (c_begin + i) * kRows + r < n;
+          bar_red_or(4, 256, p_half(1, r, tmem + ((uint32_t)(32 * (warp & 3)) << 16), valid));
+          fence_proxy_async();
+          tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_full);
+      }
       if (i + 1 < nloc) load(i + 1);
     }
   } else if (warp == 12) {
@@ -345,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     // ============================================================ softmax (warps 0-3)
     const int r = 32 * warp + lane;  // row of the chunk = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
-    const float scale_log2 = rsqrtf((float)kD) * kLog2e;
     // x[32] = scaled scores of heads 32hh..32hh+31 for this thread's row (sum of the S halves)
     auto load_x = [&](int hh, bool valid, float (&x)[32]) {
       uint32_t u[32];
@@ -354,37 +406,21 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
 #pragma unroll
       for (int h = 0; h < 32; ++h) x[h] = valid ? __uint_as_float(u[h]) * scale_log2 : -INFINITY;
     };
-    // P = exp2(x - m) as fp16 into the MN-major [rows][heads] operand; true if some score
-    // exceeds its head's reference by more than kTau
-    auto write_p = [&](bool valid) {
-      bool over = false;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float x[32];
-        load_x(hh, valid, x);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int h0 = 8 * q + 2 * k;
-            const float m0 = m_ref[32 * hh + h0], m1 = m_ref[32 * hh + h0 + 1];
-            over |= (x[h0] > m0 + kTau) | (x[h0 + 1] > m1 + kTau);
-            w[k] = f2_to_h2(exp2f(x[h0] - m0), exp2f(x[h0 + 1] - m1));
-          }
-          *reinterpret_cast<uint4*>(sm + kPOff + sw128_off(r, 4 * hh + q)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-      return over;
-    };
     for (int i = 0; i < nloc; ++i) {
       mbar_wait(&bars.s_full, i & 1, err, 5);
       tc_fence_after();
       const bool valid = (c_begin + i) * kRows + r < n;
-      // Optimistic pass with the current references (for the first chunk they are -inf, so the
-      // check always fails there); one barrier ORs whether any head needs a new reference.
-      const bool over = write_p(valid);
-      if (bar_red_or(1, 128, over)) {
+      // Optimistic pass with the current references: heads 0..31 here, 32..63 in producer warps
+      // 4-7 (same rows: lane quarter warp % 4).  Barrier 5 makes this group's reference updates
+      // of the last chunk visible to them; barrier 4 ORs whether any head needs a new reference
+      // (both: warps 0-7, 256 threads, every chunk after the first).  The first chunk skips the
+      // pass: its references are -inf, so the check would always fail there.
+      bool redo = true;
+      if (i > 0) {
+        named_bar_sync(5, 256);
+        redo = bar_red_or(4, 256, p_half(0, r, lane_addr, valid));
+      }
+      if (redo) {  // new references where needed, O rescaled, then P for all 64 heads
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float x[32];
@@ -419,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
             }
           tmem_wait_st();
         }
-        write_p(valid);
+        p_half(0, r, lane_addr, valid);
+        p_half(1, r, lane_addr, valid);
       }
       fence_proxy_async();
       tc_fence_before();
