@@ -230,6 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     }
     return over;
   };
+  // red_max[warp % 4][32hh + lane] = max over the warp's 32 rows of head 32hh + lane
+  auto warp_max_half = [&](int hh, uint32_t lane_addr, bool valid) {
+    uint32_t u[32];
+    tmem_ld32(lane_addr + kSCol + 32 * hh, u);
+    tmem_wait_ld();
+    float x[32];
+#pragma unroll
+    for (int h = 0; h < 32; ++h) x[h] = valid ? __uint_as_float(u[h]) * scale_log2 : -INFINITY;
+    red_max[warp & 3][32 * hh + lane] = transpose_reduce32<true>(x, lane);
+  };
 
   if (warp >= 4 && warp < 12) {
     // ============================================================ producers
@@ -330,20 +340,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         if (lane < 2) mbar_arrive(&bars.atom_full[2 * at + lane]);
       }
       if (warp < 8) {
-        // warps 4-7 (lane quarters 0-3): heads 32..63 of this chunk's optimistic softmax pass,
-        // from the second chunk on (the barriers as in the softmax warps), then their share of
-        // p_full.  The tiles of the chunk are written, so the raw registers are free until
-        // load(i + 1).
-        if (i > 0) {
-          mbar_wait(&bars.s_full, i & 1, err, 10);
-          tc_fence_after();
+        // warps 4-7 (lane quarters 0-3): heads 32..63 of this chunk's softmax (the barriers as
+        // in the softmax warps), then their share of p_full.  The tiles of the chunk are
+        // written, so the raw registers are free until load(i + 1).
+        mbar_wait(&bars.s_full, i & 1, err, 10);
+        tc_fence_after();
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        const bool valid = (c_begin + i) * kRows + r < n;
+        if (i == 0) {
+          warp_max_half(1, lane_addr, valid);
+          named_bar_sync(5, 256);  // the chunk maximum of every head is in red_max
+          named_bar_sync(4, 256);  // the references are set
+          p_half(1, r, lane_addr, valid);
+        } else {
           named_bar_sync(5, 256);
-          const int r = 32 * (warp & 3) + lane;
-          const bool valid = (c_begin + i) * kRows + r < n;
-          bar_red_or(4, 256, p_half(1, r, tmem + ((uint32_t)(32 * (warp & 3)) << 16), valid));
-          fence_proxy_async();
-          tc_fence_before();
+          bar_red_or(4, 256, p_half(1, r, lane_addr, valid));
         }
+        fence_proxy_async();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.p_full);
       }
@@ -410,13 +425,22 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       mbar_wait(&bars.s_full, i & 1, err, 5);
       tc_fence_after();
       const bool valid = (c_begin + i) * kRows + r < n;
-      // Optimistic pass with the current references: heads 0..31 here, 32..63 in producer warps
-      // 4-7 (same rows: lane quarter warp % 4).  Barrier 5 makes this group's reference updates
-      // of the last chunk visible to them; barrier 4 ORs whether any head needs a new reference
-      // (both: warps 0-7, 256 threads, every chunk after the first).  The first chunk skips the
-      // pass: its references are -inf, so the check would always fail there.
-      bool redo = true;
-      if (i > 0) {
+      // Heads 0..31 here, 32..63 in producer warps 4-7 (same rows: lane quarter warp % 4); barriers
+      // 5 and 4 are taken by warps 0-7 (256 threads) at every chunk.
+      // First chunk: the references are -inf, so they are set to the chunk maxima (each group
+      // reduces its heads; barrier 5: all maxima in red_max; barrier 4: references set).
+      // Later chunks: an optimistic pass with the current references; barrier 5 makes this
+      // group's reference updates of the last chunk visible to warps 4-7, barrier 4 ORs whether
+      // any head needs a new reference.
+      bool redo = false;
+      if (i == 0) {
+        warp_max_half(0, lane_addr, valid);
+        named_bar_sync(5, 256);
+        if (tid < 64)
+          m_ref[tid] = fmaxf(fmaxf(red_max[0][tid], red_max[1][tid]), fmaxf(red_max[2][tid], red_max[3][tid]));
+        named_bar_sync(4, 256);
+        p_half(0, r, lane_addr, valid);
+      } else {
         named_bar_sync(5, 256);
         redo = bar_red_or(4, 256, p_half(0, r, lane_addr, valid));
       }
