@@ -78,7 +78,10 @@ __device__ __forceinline__ float group_sum(DFSum v, float2* red, int g) {
 // grid (entry groups of 4, sequences), 512 threads.  Group g = tid / 128 pools, normalises and
 // quantises entry g (thread = 4 channels); the k^i = c W_IK products are split over the
 // groups by K quarter (thread = output column), each a double-float partial, combined in
-// phase 3 where group g again owns entry g (thread = output column).
+// phase 3 where group g again owns entry g (thread = output column).  NE = 1: launches where
+// no sequence gains more than one entry (decode); the thread's weights then load in two
+// batches of 64, so that their latency is paid twice rather than eight times.
+template <int NE>
 __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArgs a, SeqPos pos, int b0, RopeFreq rf) {
   __shared__ float sc[kEntriesPerBlock][kD];
   __shared__ float2 part[4][kEntriesPerBlock][kDI];  // (s, c) of each K quarter
@@ -168,9 +171,33 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
   __syncthreads();
 
   // ---- phase 2: quarter g of k^i = c W_IK for the block's entries (thread = output column)
-  {
+  if constexpr (NE == 1) {
     const int o = gt;
-    const int nacc = ne == 1 ? 1 : kEntriesPerBlock;  // one entry (decode) skips the empty rows
+    DF acc{0.f, 0.f};
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const int d0 = 128 * g + 64 * hb;
+      float w[64];
+#pragma unroll
+      for (int u = 0; u < 64; ++u) w[u] = bf16_to_f32(__ldg(a.w_ik + (d0 + u) * kDI + o));
+#pragma unroll
+      for (int c = 0; c < 64; c += kChain) {  // the same chains, in the same order, as below
+        float s = 0.f;
+#pragma unroll
+        for (int u = 0; u < kChain; u += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(&sc[0][d0 + c + u]);
+          s = fmaf(x.x, w[c + u], s);
+          s = fmaf(x.y, w[c + u + 1], s);
+          s = fmaf(x.z, w[c + u + 2], s);
+          s = fmaf(x.w, w[c + u + 3], s);
+        }
+        acc.add(s);
+      }
+    }
+    part[g][0][o] = make_float2(acc.s, acc.c);
+  } else {
+    const int o = gt;
+    const int nacc = ne == 1 ? 1 : kEntriesPerBlock;  // one entry skips the empty rows
     DF acc[kEntriesPerBlock];
 #pragma unroll
     for (int e = 0; e < kEntriesPerBlock; ++e) acc[e] = DF{0.f, 0.f};
@@ -292,7 +319,10 @@ cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb
   for (int i = 0; i < nb; ++i) max_new = max(max_new, ((pos.p0[i] + a.T) >> a.rshift) - (pos.p0[i] >> a.rshift));
   if (max_new > 0) {
     dim3 grid((unsigned)((max_new + kEntriesPerBlock - 1) / kEntriesPerBlock), (unsigned)nb);
-    writer_entries_kernel<<<grid, kEntryThreads, 0, st>>>(a, pos, b0, rf);
+    if (max_new == 1)
+      writer_entries_kernel<1><<<grid, kEntryThreads, 0, st>>>(a, pos, b0, rf);
+    else
+      writer_entries_kernel<kEntriesPerBlock><<<grid, kEntryThreads, 0, st>>>(a, pos, b0, rf);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
