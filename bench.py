@@ -22,6 +22,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 from pathlib import Path
 
@@ -120,14 +121,15 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path: str | None = None):
         self.proc = None
         self.gpu = gpu_index
-        self.path = ROOT / "gpurun_out" / f"clocks_rank{gpu_index}.csv"
+        # the raw samples: a file the caller names (--clocks-csv), else one in the temp directory
+        self.path = Path(path) if path else Path(tempfile.gettempdir()) / f"csa2_clocks_gpu{gpu_index}.csv"
 
     def __enter__(self):
         try:
-            self.path.parent.mkdir(exist_ok=True)
+            self.path.parent.mkdir(parents=True, exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
@@ -429,7 +431,7 @@ def run_ours(args, rank, ws):
     hbm, bf16, src = peaks()
     wl = inputs.WORKLOADS[args.workload]
     step = Step(csa2, inputs, wl, seed_for_rank(wl.seed, rank), dev)
-    clocks = ClockSampler(torch.cuda.current_device())
+    clocks = ClockSampler(torch.cuda.current_device(), args.clocks_csv)
     ms, per, launches = time_workload(step, args.steps, args.warmup, ws, flush, clocks)
     ms_max = max_over_ranks(ms, ws)
     att_ms = max_over_ranks(per["attend"], ws)
@@ -585,6 +587,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--clocks-csv", default=None, help="where to keep the raw nvidia-smi samples (default: temp dir)")
     args = ap.parse_args()
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores only; the other ranks exit without work
