@@ -258,6 +258,73 @@ def test_writer_ratio1_ignores_gates_and_splits_anywhere():
         assert np.array_equal(full[k], b[k])
 
 
+# The indexer-key chain of [PG] "Compressed sparse attention": k^i = c W_IK (c is the
+# normalised pooled key before RoPE and FP4), k^n = gamma_IK * RMSNorm(k^i), and dims 64..127
+# of K^I rotated by the entry's position (2j at ratio 2, j at ratio 1).  The inputs below make
+# each stage a closed form: a pair of equal tokens of +-1 values pools to itself (the softmax
+# weights sum to 1) and has mean square 1, so c = gamma_C * k exactly.
+def _pm1_tokens(rng, T):
+    k = np.where(rng.random(512) < 0.5, -1.0, 1.0).astype(np.float32)
+    return np.repeat(k[None], T, axis=0), k.astype(np.float64)
+
+
+def _rot_pairs(x, pos):
+    """Dims 64..127 of x turned pair by pair by pos * 10000^(-2i/64), cos/sin written out."""
+    y = np.array(x, np.float64)
+    for i in range(32):
+        a = pos * 10000.0 ** (-2.0 * i / 64)
+        x0, x1 = x[64 + 2 * i], x[65 + 2 * i]
+        y[64 + 2 * i] = x0 * math.cos(a) - x1 * math.sin(a)
+        y[65 + 2 * i] = x0 * math.sin(a) + x1 * math.cos(a)
+    return y
+
+
+@pytest.mark.parametrize("ratio,p0,T,rope_pos", [(2, 10, 2, 10), (2, 2047, 1, 2046), (1, 7, 1, 7)])
+def test_indexer_key_chain_single_tap_projection(ratio, p0, T, rope_pos):
+    # W_IK with one tap per column: column o reads row r_o with weight a_o = +-0.5.  Columns
+    # 0..63 read the rotated dims 448..511 of c (a permutation of them), so a k^i taken from Z
+    # (after RoPE) would differ; the other columns read distinct rows below 448.  Then
+    # k^i[o] = a_o c[r_o] = +-0.5, its mean square is 0.25, and k^n[o] = gamma_IK[o] * sign.
+    rng = np.random.default_rng(40 + p0)
+    kc, k = _pm1_tokens(rng, T)
+    gc = rng.standard_normal((T, 512)).astype(np.float32) * 3
+    rows = np.concatenate([448 + rng.permutation(64), rng.choice(448, 64, replace=False)])
+    a = np.where(rng.random(128) < 0.5, -0.5, 0.5)
+    w = np.zeros((512, 128), np.float32)
+    w[rows, np.arange(128)] = a
+    g_ik = (1 + 0.2 * rng.standard_normal(128)).astype(np.float32)
+    prm = dict(gamma_c=np.ones(512, np.float32), w_ik=w, gamma_ik=g_ik, gamma_w=np.ones(512, np.float32))
+    pair = dict(pair_k=kc[0], pair_g=gc[0]) if ratio == 2 and p0 % 2 else {}
+    r = oracle.write_seq(kc, gc, kc, p0=p0, cap=p0 // ratio + 1, ratio=ratio, **pair, **prm)
+    assert r["n_entries"] == 1 and r["first_entry"] * ratio == rope_pos
+    kn = g_ik.astype(np.float64) * np.sign(a * k[rows])
+    assert np.allclose(r["ki_pre"][0], _rot_pairs(kn, rope_pos), rtol=0, atol=1e-12)
+
+
+def test_indexer_key_chain_dense_projection():
+    # A dense, non-symmetric W_IK and a non-uniform gamma_C: k^i = (gamma_C * k) W_IK (a
+    # library matmul), and after undoing the rotation of dims 64..127 by 2j (cos/sin written
+    # out) and dividing by gamma_IK, K^I is k^i scaled to unit mean square.
+    rng = np.random.default_rng(41)
+    kc, k = _pm1_tokens(rng, 2)
+    gc = rng.standard_normal((2, 512)).astype(np.float32)
+    g_c = (1 + 0.3 * rng.standard_normal(512)).astype(np.float32)
+    w = (rng.standard_normal((512, 128)) / math.sqrt(512)).astype(np.float32)
+    g_ik = (1 + 0.2 * rng.standard_normal(128)).astype(np.float32)
+    r = oracle.write_seq(kc, gc, kc, g_c, w, g_ik, np.ones(512, np.float32), p0=6, cap=4)
+    j = r["first_entry"]
+    assert j == 3 and r["n_entries"] == 1
+    u = _rot_pairs(r["ki_pre"][0], -2 * j) / g_ik.astype(np.float64)
+    ki = (g_c.astype(np.float64) * k) @ w.astype(np.float64)
+    assert abs(np.mean(u ** 2) - 1.0) < 1e-12
+    cos = u @ ki / (np.linalg.norm(u) * np.linalg.norm(ki))
+    assert abs(cos - 1.0) < 1e-12
+    # Z rows hold c rotated by 2j on dims 448..511 (c = gamma_C * k here)
+    zc = g_c.astype(np.float64) * k
+    z = np.concatenate([zc[:448], _rot_pairs(np.concatenate([np.zeros(64), zc[448:]]), 2 * j)[64:]])
+    assert np.allclose(r["z_pre"][0], z, rtol=0, atol=1e-12)
+
+
 def test_index_causal_bound_ratio1():
     rng = np.random.default_rng(13)
     kc, ks = oracle.mx_quantize(rng.standard_normal((60, 128)))
