@@ -422,6 +422,44 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def decode_object(dw, dms, dper, dlaunches, ws, hbm, src, profile=None):
+    """Throughput and HBM rooflines of a decode workload (T = 1): the whole step and the index call."""
+    by = decode_bytes(dw.B, dw.p0, dw.ratio)
+    idx_ms = dper["index"]
+    return {
+        "workload": dw.name, "B": dw.B, "p0": dw.p0, "ratio": dw.ratio, "value": ws * dw.B / (dms / 1e3),
+        "unit": "tok/s", "ms_per_step": dms, "kernels_ms": dper,
+        "roofline_step": {"bound": "hbm", "achieved": by["step"] / (dms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                          "frac": by["step"] / (dms / 1e3) / 1e9 / hbm, "bytes": by["step"],
+                          "peak_source": f"{src} copy bandwidth"},
+        "roofline_index": {"bound": "hbm", "achieved": by["indexer"] / (idx_ms / 1e3) / 1e9, "peak": hbm,
+                           "unit": "GB/s", "frac": by["indexer"] / (idx_ms / 1e3) / 1e9 / hbm,
+                           "bytes": by["indexer"], "peak_source": f"{src} copy bandwidth",
+                           "traffic": profiled_traffic(profile, INDEX_SOURCES) if profile else None},
+        "gpu_launches": dlaunches,
+    }
+
+
+def prefill_rooflines(wl, per, bf16, src, ws=1):
+    """Tensor rooflines of a prefill workload: attention (bf16 operands), the indexer score GEMM
+    (FP4 values on fp16-operand MMAs, so against the bf16 peak) and the two together."""
+    af = attention_flops(wl.B, wl.p0, wl.T, wl.ratio)
+    xf = 8192.0 * indexer_pairs(wl.B, wl.p0, wl.T, wl.ratio)
+    a_ach = af / (per["attend"] / 1e3) / 1e12
+    x_ach = xf / (per["index"] / 1e3) / 1e12
+    both = (af + xf) / ((per["attend"] + per["index"]) / 1e3) / 1e12
+    peak_src = f"{src} bf16 burst"
+    return {
+        "roofline_attend": {"bound": "tensor", "achieved": a_ach, "peak": bf16, "unit": "TFLOP/s", "frac": a_ach / bf16,
+                            "flops_per_launch": af, "peak_source": peak_src},
+        "roofline_index": {"bound": "tensor", "achieved": x_ach, "peak": bf16, "unit": "TFLOP/s", "frac": x_ach / bf16,
+                           "flops_per_call": xf, "peak_source": peak_src + " (FP4 values on fp16-operand MMAs)",
+                           "note": "whole csa2_index_topk call: score GEMM + fp32 score rows + top-512 select"},
+        "roofline_attend_plus_index": {"bound": "tensor", "achieved": both, "peak": bf16, "unit": "TFLOP/s",
+                                       "frac": both / bf16, "flops": af + xf, "peak_source": peak_src},
+    }
+
+
 def run_ours(args, rank, ws):
     import compressed_sparse_attention_03_gb300 as csa2
     from compressed_sparse_attention_03_gb300 import inputs
@@ -434,7 +472,8 @@ def run_ours(args, rank, ws):
     clocks = ClockSampler(torch.cuda.current_device(), args.clocks_csv)
     ms, per, launches = time_workload(step, args.steps, args.warmup, ws, flush, clocks)
     ms_max = max_over_ranks(ms, ws)
-    att_ms = max_over_ranks(per["attend"], ws)
+    per = {k: max_over_ranks(v, ws) for k, v in per.items()}
+    att_ms = per["attend"]
     flops = attention_flops(wl.B, wl.p0, wl.T, wl.ratio)
     achieved = flops / (att_ms / 1e3) / 1e12
     e2e = time_e2e(step, max(2, args.steps // 2), 1)
@@ -455,31 +494,31 @@ def run_ours(args, rank, ws):
         "gpu_launches": launches,
         "clocks": clocks.summary(),
     }
+    line.update({k: v for k, v in prefill_rooflines(wl, per, bf16, src).items() if k != "roofline_attend"})
     del step
     torch.cuda.empty_cache()
-    # decode objects: the ratio-2 layer at 1M tokens, and a ratio-1 (decoder owner) layer
-    for key, name in (("decode", args.decode_workload), ("decode_ratio1", args.ratio1_workload)):
+    # the other workloads, one object each: decode at 8K (B=1), 128K (B=64) and 1M (B=8) context,
+    # a ratio-1 (decoder owner) layer, and the 32K-token chunk on a 256K-token prefix
+    others = [("decode_8k", args.decode8k_workload, None), ("decode_128k", args.decode128k_workload, None),
+              ("decode", args.decode_workload, "index_decode_decode_1m.md"),
+              ("decode_ratio1", args.ratio1_workload, None), ("chunk_32k", args.chunk_workload, None)]
+    for key, name, prof in others:
         if args.no_decode or not name:
             continue
         dw = inputs.WORKLOADS[name]
         dstep = Step(csa2, inputs, dw, seed_for_rank(dw.seed, rank), dev)
-        dms, dper, dlaunches = time_workload(dstep, args.steps, args.warmup, ws, flush)
+        steps = args.steps if dw.T == 1 else max(3, args.steps // 4)
+        dms, dper, dlaunches = time_workload(dstep, steps, args.warmup, ws, flush)
         dms = max_over_ranks(dms, ws)
-        idx_ms = max_over_ranks(dper["index"], ws)
-        by = decode_bytes(dw.B, dw.p0, dw.ratio)
-        line[key] = {
-            "workload": dw.name, "B": dw.B, "p0": dw.p0, "ratio": dw.ratio, "value": ws * dw.B / (dms / 1e3),
-            "unit": "tok/s", "ms_per_step": dms, "kernels_ms": dper,
-            "roofline_step": {"bound": "hbm", "achieved": by["step"] / (dms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
-                              "frac": by["step"] / (dms / 1e3) / 1e9 / hbm, "bytes": by["step"]},
-            "roofline_index": {"bound": "hbm", "achieved": by["indexer"] / (idx_ms / 1e3) / 1e9, "peak": hbm,
-                               "unit": "GB/s", "frac": by["indexer"] / (idx_ms / 1e3) / 1e9 / hbm,
-                               "bytes": by["indexer"], "peak_source": f"{src} copy bandwidth",
-                               "traffic": profiled_traffic("index_decode_decode_1m.md", INDEX_SOURCES)
-                               if name == "decode_1m" else None},
-            "gpu_launches": dlaunches,
-        }
+        dper = {k: max_over_ranks(v, ws) for k, v in dper.items()}
+        if dw.T == 1:
+            line[key] = decode_object(dw, dms, dper, dlaunches, ws, hbm, src, prof)
+        else:
+            line[key] = {"workload": dw.name, "B": dw.B, "T": dw.T, "p0": dw.p0, "ratio": dw.ratio, "steps": steps,
+                         "value": ws * dw.B * dw.T / (dms / 1e3), "unit": "tok/s", "ms_per_step": dms,
+                         "kernels_ms": dper, "gpu_launches": dlaunches, **prefill_rooflines(dw, dper, bf16, src)}
         del dstep
+        torch.cuda.empty_cache()
     if not args.no_decode and args.hsi_workload:
         hw = inputs.WORKLOADS[args.hsi_workload]
         hstep = Step(csa2, inputs, hw, seed_for_rank(hw.seed, rank), dev)
@@ -506,70 +545,103 @@ def run_ours(args, rank, ws):
 
 
 # ------------------------------------------------------------------ the oracle (CPU baseline / reference arm)
-def cpu_baseline(wl, budget_s: float = 15.0, n_rows: int | None = None) -> dict:
-    """The fp64 oracle, as it stands, on the host cores: the writer over the whole step plus
-    indexer + top-k + attention for a sample of query rows; tokens/s extrapolated from the
-    per-row time.  Inputs are generated on the CPU (same recipe)."""
-    import oracle
-    from compressed_sparse_attention_03_gb300 import inputs
+def oracle_rows(wl, cores: int) -> np.ndarray:
+    """The fixed, seeded query rows both oracle timings sample: 16 per host thread, spread over
+    the step (all rows when the step has fewer)."""
+    n = min(wl.T, 16 * max(1, cores))
+    return np.sort(np.random.default_rng(0).choice(wl.T, size=n, replace=False))
 
-    x = {}
-    x.update(inputs.layer_params(wl.seed, "cpu"))
-    x.update(inputs.step_inputs(wl.B, wl.T, wl.seed, "cpu"))
-    x.update(inputs.cache_state(wl.B, wl.T, wl.p0, wl.cap, wl.seed, "cpu", wl.ratio))
-    f = lambda t: t.float().numpy()
-    cores = os.cpu_count()
-    t0 = time.perf_counter()
-    w = oracle.write_seq(f(x["kc"][0]), f(x["gc"][0]), f(x["wa"][0]), f(x["gamma_c"]), f(x["w_ik"]), f(x["gamma_ik"]),
-                         f(x["gamma_w"]), wl.p0, wl.cap, z_codes=x["z_codes"][0].numpy(),
-                         z_scales=x["z_scales"][0].numpy(), ki_codes=x["ki_codes"][0].numpy(),
-                         ki_scales=x["ki_scales"][0].numpy(), pair_k=f(x["pair_kc"][0]), pair_g=f(x["pair_gc"][0]),
-                         window_prefix=x["window"][0, :127].numpy(), ratio=wl.ratio)
-    t_write = time.perf_counter() - t0
-    # rows: spread over the step; grow the sample until the budget is used
-    rows_done, t_rows = 0, 0.0
-    n = n_rows or 8
-    rng = np.random.default_rng(0)
-    while True:
-        r = np.sort(rng.choice(wl.T, size=min(n, wl.T), replace=False))
-        pos = wl.p0 + r
+
+class OracleStep:
+    """One sampled oracle step: the writer over every token of one sequence, then indexer, top-512
+    and attention for the fixed row sample; the step time is extrapolated per row and sequence."""
+
+    def __init__(self, wl):
+        from compressed_sparse_attention_03_gb300 import inputs
+
+        x = {}
+        x.update(inputs.layer_params(wl.seed, "cpu"))
+        x.update(inputs.step_inputs(wl.B, wl.T, wl.seed, "cpu"))
+        x.update(inputs.cache_state(wl.B, wl.T, wl.p0, wl.cap, wl.seed, "cpu", wl.ratio))
+        self.wl, self.x = wl, x
+        self.cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+        self.rows = oracle_rows(wl, self.cores)
+
+    def run(self):
+        """Returns (writer seconds, row seconds) of one sampled step."""
+        import oracle
+
+        wl, x, r = self.wl, self.x, self.rows
+        f = lambda t: t.float().numpy()
+        t0 = time.perf_counter()
+        w = oracle.write_seq(f(x["kc"][0]), f(x["gc"][0]), f(x["wa"][0]), f(x["gamma_c"]), f(x["w_ik"]),
+                             f(x["gamma_ik"]), f(x["gamma_w"]), wl.p0, wl.cap, z_codes=x["z_codes"][0].numpy().copy(),
+                             z_scales=x["z_scales"][0].numpy().copy(), ki_codes=x["ki_codes"][0].numpy().copy(),
+                             ki_scales=x["ki_scales"][0].numpy().copy(), pair_k=f(x["pair_kc"][0]),
+                             pair_g=f(x["pair_gc"][0]), window_prefix=x["window"][0, :127].numpy(), ratio=wl.ratio)
         t1 = time.perf_counter()
+        pos = wl.p0 + r
         sc = oracle.index_scores(pos, f(x["qi"][0][r]), f(x["wI"][0][r]), w["ki_codes"], w["ki_scales"], wl.cap,
                                  ratio=wl.ratio)
         oidx, _, _ = oracle.topk(sc, (pos + 1) // wl.ratio)
         oracle.attend(pos, f(x["q"][0][r]), f(x["sinks"]), w["z_codes"], w["z_scales"], wl.cap, w["window"],
                       wl.p0 - 127, oidx)
-        t_rows += time.perf_counter() - t1
-        rows_done += len(r)
-        if n_rows or t_write + t_rows > budget_s or rows_done >= wl.T:
-            break
-        n *= 2
-    per_row = t_rows / rows_done
-    t_step = t_write * wl.B + per_row * wl.T * wl.B  # the writer was timed on one sequence
-    return {"value": wl.B * wl.T / t_step, "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": f"writer over all {wl.T} tokens of 1 sequence ({t_write:.2f} s) + indexer/top-k/attention "
-                      f"for {rows_done} sampled query rows ({t_rows:.2f} s); step time extrapolated per row",
-            "seconds": t_write + t_rows}
+        return t1 - t0, time.perf_counter() - t1
+
+    def step_seconds(self, t_write, t_rows):
+        """Extrapolated time of the whole step: the writer timed on one sequence, the rows per row."""
+        return t_write * self.wl.B + t_rows / len(self.rows) * self.wl.T * self.wl.B
+
+    def describe(self, t_write, t_rows, n_steps):
+        wl = self.wl
+        return (f"writer over all {wl.T} tokens of 1 sequence + indexer/top-512/attention for the same fixed "
+                f"{len(self.rows)} query rows (seeded, 16 per thread), {n_steps} timed pass(es); per pass "
+                f"{t_write:.3f} s + {t_rows:.3f} s; step time extrapolated x{wl.T * wl.B / len(self.rows):.1f} "
+                f"over rows and sequences")
+
+
+def cpu_baseline(wl, budget_s: float = 15.0) -> dict:
+    """The fp64 oracle, as it stands, on the host cores: the sampled step of OracleStep, repeated
+    until about budget_s seconds were spent; tokens/s from the mean extrapolated step time."""
+    o = OracleStep(wl)
+    o.run()  # untimed: first touch of the inputs and the oracle library
+    runs, spent = [], 0.0
+    while spent < budget_s or not runs:
+        tw, tr = o.run()
+        runs.append((tw, tr))
+        spent += tw + tr
+    tw = statistics.mean(a for a, _ in runs)
+    tr = statistics.mean(b for _, b in runs)
+    t_step = o.step_seconds(tw, tr)
+    return {"value": wl.B * wl.T / t_step, "unit": "tok/s", "cores": o.cores, "kind": "oracle",
+            "sample": o.describe(tw, tr, len(runs)), "seconds": spent, "extrapolated_step_s": t_step}
 
 
 def run_reference(args, rank, ws):
     from compressed_sparse_attention_03_gb300 import inputs
 
     wl = inputs.WORKLOADS[args.workload]
-    vals = []
+    o = OracleStep(wl)
+    runs = []
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(wl, budget_s=min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)), n_rows=8)
+        tw, tr = o.run()
         if i >= args.warmup:
-            vals.append(cb)
-    v = statistics.mean(c["value"] for c in vals)
-    ms = wl.B * wl.T / v * 1e3
+            runs.append((tw, tr))
+    tw = statistics.mean(a for a, _ in runs)
+    tr = statistics.mean(b for _, b in runs)
+    t_step = o.step_seconds(tw, tr)
+    v = wl.B * wl.T / t_step
+    measured = sum(a + b for a, b in runs)
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "p0": wl.p0, "seed": wl.seed,
                        "parallelism": "host cores (OpenMP)"},
-            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": vals[0]["cores"], "kind": "oracle",
-                             "sample": vals[0]["sample"]},
+            "measured_seconds": measured,
+            "note": "each step runs a fixed sample of the step's query rows; ms_per_step is that sample "
+                    "extrapolated to the whole step (see cpu_baseline.sample)",
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": o.cores, "kind": "oracle",
+                             "sample": o.describe(tw, tr, len(runs))},
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -581,6 +653,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_4k")
     ap.add_argument("--decode-workload", default="decode_1m")
+    ap.add_argument("--decode8k-workload", default="decode_8k", help="empty: skip")
+    ap.add_argument("--decode128k-workload", default="decode_128k", help="empty: skip")
+    ap.add_argument("--chunk-workload", default="chunk_32k", help="empty: skip")
     ap.add_argument("--ratio1-workload", default="decode_512k_r1", help="empty: skip the ratio-1 decode object")
     ap.add_argument("--out-proj-rows", type=int, default=4096, help="0: skip the output-projection object")
     ap.add_argument("--hsi-workload", default="decode_1m", help="empty: skip the hierarchical-indexer object")

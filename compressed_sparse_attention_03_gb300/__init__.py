@@ -16,7 +16,7 @@ import torch
 _PKG = Path(__file__).resolve().parent
 LIB_PATH = _PKG / "_build" / "libcsa2.so"
 
-OP_WRITE_CACHE, OP_INDEX_TOPK, OP_ATTEND, OP_INDEX_POOL, OP_REINDEX_TOPK = 0, 1, 2, 3, 4
+OP_WRITE_CACHE, OP_INDEX_TOPK, OP_ATTEND, OP_INDEX_POOL, OP_REINDEX_TOPK, OP_INDEX_SCORES = 0, 1, 2, 3, 4, 5
 HSI_BLOCKS = 2048  # pool blocks per query row (blocks of 8 entries)
 HEADS, HEAD_DIM, ROPE_DIMS, IDX_HEADS, IDX_DIM, WINDOW, TOPK = 64, 512, 64, 32, 128, 128, 512
 
@@ -39,7 +39,7 @@ class csa2_config(C.Structure):
 
 EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_string", "csa2_kernel_launches",
            "csa2_workspace_bytes",
-           "csa2_write_cache", "csa2_index_topk", "csa2_index_pool", "csa2_reindex_topk", "csa2_attend",
+           "csa2_write_cache", "csa2_roll_window", "csa2_index_topk", "csa2_index_scores", "csa2_index_pool", "csa2_reindex_topk", "csa2_attend",
            "csa2_attend_replay", "csa2_attend_static", "csa2_check", "csa2_selftest_timeout",
            "csa2_out_group_proj")
 
@@ -69,6 +69,10 @@ def lib() -> C.CDLL:
         L.csa2_write_cache.restype = i32
         L.csa2_index_topk.argtypes = [p] * 5 + [i64, p, i32, i32, p, p, p, sz, p]
         L.csa2_index_topk.restype = i32
+        L.csa2_roll_window.argtypes = [p, p, i32, i32, p, i32, p]
+        L.csa2_roll_window.restype = i32
+        L.csa2_index_scores.argtypes = [p] * 5 + [i64, p, i32, i32, p, i64, p, sz, p]
+        L.csa2_index_scores.restype = i32
         L.csa2_out_group_proj.argtypes = [p, p, p, i64, p, p]
         L.csa2_out_group_proj.restype = i32
         L.csa2_check.argtypes = [p, p]
@@ -183,6 +187,17 @@ def csa2_write_cache(h: Handle, kc, gc, wa, gamma_c, w_ik, gamma_ik, gamma_w, p0
         _stream(stream)))
 
 
+def csa2_roll_window(h: Handle, window, nxt, stream=None) -> None:
+    """Rows T .. T+126 of the window view [B, 127+T, 512] -> rows 0 .. 126 of the next call's view
+    [B, 127+T_next, 512] (``nxt`` may be ``window`` itself when T_next == T or B == 1)."""
+    B, rows, _ = window.shape
+    T, T_next = rows - 127, nxt.shape[1] - 127
+    if nxt.shape[0] != B or window.shape[2] != 512 or nxt.shape[2] != 512:
+        raise ValueError("csa2_roll_window: views must be [B, 127+T, 512]")
+    _check("csa2_roll_window", lib().csa2_roll_window(
+        h.ptr, _dev(window, torch.uint8, "window"), B, T, _dev(nxt, torch.uint8, "next"), T_next, _stream(stream)))
+
+
 def csa2_index_topk(h: Handle, qi, wI, ki_codes, ki_scales, p0, idx, top_scores=None, ws=None, stream=None) -> None:
     B, T = qi.shape[:2]
     p0a = _host_p0(p0, B)
@@ -194,6 +209,23 @@ def csa2_index_topk(h: Handle, qi, wI, ki_codes, ki_scales, p0, idx, top_scores=
         _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
         _dev(idx, torch.int32, "idx"), _dev(top_scores, torch.float32, "top_scores"), _dev(ws, torch.uint8, "ws"),
         ws.numel(), _stream(stream)))
+
+
+def csa2_index_scores(h: Handle, qi, wI, ki_codes, ki_scales, p0, scores, ws=None, stream=None) -> None:
+    """S^I of every visible entry: scores f32 [B, T, ld] (ld a multiple of 4, at least the largest
+    visible count); entries beyond a row's visible count are left untouched."""
+    B, T = qi.shape[:2]
+    p0a = _host_p0(p0, B)
+    cap = ki_codes.shape[1]
+    if scores.dim() != 3 or scores.shape[:2] != (B, T):
+        raise ValueError("csa2_index_scores: scores must be [B, T, ld]")
+    if ws is None:
+        ws = workspace(h, OP_INDEX_SCORES, B, T, int(((p0a + T) // h.ratio).max()), qi.device)
+    _check("csa2_index_scores", lib().csa2_index_scores(
+        h.ptr, _dev(qi, torch.bfloat16, "qi"), _dev(wI, torch.bfloat16, "wI"), _dev(ki_codes, torch.uint8, "ki_codes"),
+        _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
+        _dev(scores, torch.float32, "scores"), scores.shape[2], _dev(ws, torch.uint8, "ws"), ws.numel(),
+        _stream(stream)))
 
 
 def csa2_index_pool(h: Handle, qi, wI, ki_codes, ki_scales, p0, idx, pool, top_scores=None, ws=None,
@@ -237,10 +269,11 @@ def csa2_out_group_proj(h: Handle, o, w_oa, out, stream=None) -> None:
 
 
 def csa2_check(h: Handle, stream=None) -> int:
-    """Synchronises the stream and returns the status of the bounded waits since the last
-    check (0, or 8 = a wait gave up).  Does not raise on 8: the caller decides."""
+    """Synchronises the stream and returns what the kernels recorded since the last check: 0,
+    8 (a bounded wait gave up) or 5 (an FP4 scale above 2^13, or a query beyond the fp16
+    range, was read).  Does not raise on 5 or 8: the caller decides."""
     st = lib().csa2_check(h.ptr, _stream(stream))
-    if st not in (0, 8):
+    if st not in (0, 5, 8):
         _check("csa2_check", st)
     return st
 

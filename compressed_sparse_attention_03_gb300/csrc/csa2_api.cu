@@ -131,6 +131,7 @@ size_t csa2_workspace_bytes(const csa2_handle* h, int op, int B, int T, int64_t 
     case CSA2_OP_ATTEND: return csa2::attend_workspace_bytes(B, T, h->num_sms);
     case CSA2_OP_INDEX_POOL: return csa2::index_workspace_bytes(B, T, max_entries, h->num_sms, csa2::kIndexPool);
     case CSA2_OP_REINDEX_TOPK: return csa2::index_workspace_bytes(B, T, max_entries, h->num_sms, csa2::kIndexReindex);
+    case CSA2_OP_INDEX_SCORES: return csa2::index_workspace_bytes(B, T, max_entries, h->num_sms, csa2::kIndexScores);
   }
   return 0;
 }
@@ -178,8 +179,9 @@ namespace {
 csa2_status index_call(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, const uint8_t* ki_codes,
                        const uint8_t* ki_scales, int64_t cap, const int64_t* p0, int B, int T, int32_t* idx,
                        float* top_scores, int32_t* pool_out, const int32_t* pool_in, int mode, void* ws,
-                       size_t ws_bytes, csa2_stream_t stream) {
-  if (!h || !qi || !wI || !ki_codes || !ki_scales || !idx) return CSA2_ERR_INVALID_ARG;
+                       size_t ws_bytes, csa2_stream_t stream, float* scores_out = nullptr, int64_t scores_ld = 0) {
+  const bool so = mode == csa2::kIndexScores;
+  if (!h || !qi || !wI || !ki_codes || !ki_scales || (!idx && !so) || (so && !scores_out)) return CSA2_ERR_INVALID_ARG;
   if ((mode == csa2::kIndexPool && !pool_out) || (mode == csa2::kIndexReindex && !pool_in)) return CSA2_ERR_INVALID_ARG;
   if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
   csa2_status st = check_p0(p0, B, T);
@@ -187,7 +189,8 @@ csa2_status index_call(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, c
   const int64_t emax = max_visible(p0, B, T, h->rshift);
   if (emax > cap) return CSA2_ERR_SHAPE;
   if (emax > (int64_t(1) << 20)) return CSA2_ERR_UNSUPPORTED;
-  const void* ptrs[] = {qi, wI, ki_codes, ki_scales, idx};
+  if (so && (scores_ld < std::max<int64_t>(emax, 1) || scores_ld % 4)) return CSA2_ERR_SHAPE;
+  const void* ptrs[] = {qi, wI, ki_codes, ki_scales, so ? static_cast<const void*>(scores_out) : idx};
   for (const void* p : ptrs)
     if (!aligned16(p)) return CSA2_ERR_ALIGN;
   if (top_scores && !aligned16(top_scores)) return CSA2_ERR_ALIGN;
@@ -201,6 +204,8 @@ csa2_status index_call(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, c
   a.idx = idx; a.top_scores = top_scores;
   a.pool_out = mode == csa2::kIndexPool ? pool_out : nullptr;
   a.pool_in = mode == csa2::kIndexReindex ? pool_in : nullptr;
+  a.scores_out = scores_out;
+  a.scores_ld = scores_ld;
   for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
     const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
     st = cuda_status(csa2::launch_index_topk(a, pack_pos(p0, b0, nb), b0, nb, emax, ws, ws_bytes, h->num_sms,
@@ -217,6 +222,31 @@ csa2_status csa2_index_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* 
                             float* top_scores, void* ws, size_t ws_bytes, csa2_stream_t stream) {
   return index_call(h, qi, wI, ki_codes, ki_scales, cap, p0, B, T, idx, top_scores, nullptr, nullptr,
                     csa2::kIndexTopk, ws, ws_bytes, stream);
+}
+
+// Window roll between calls (include/csa2.h).
+csa2_status csa2_roll_window(csa2_handle* h, const uint8_t* window, int B, int T, uint8_t* next, int T_next,
+                             csa2_stream_t stream) {
+  if (!h || !window || !next) return CSA2_ERR_INVALID_ARG;
+  if (B <= 0 || T <= 0 || T_next <= 0 || T > 65535 || T_next > 65535 || B > (1 << 24)) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(window) || !aligned16(next)) return CSA2_ERR_ALIGN;
+  // one buffer: only with equal strides (or one sequence) does every block stay within its own rows
+  const uintptr_t w0 = reinterpret_cast<uintptr_t>(window), n0 = reinterpret_cast<uintptr_t>(next);
+  const uintptr_t w1 = w0 + (uintptr_t)B * (127 + T) * 512, n1 = n0 + (uintptr_t)B * (127 + T_next) * 512;
+  const bool overlap = w0 < n1 && n0 < w1;
+  if (overlap && !(w0 == n0 && (T == T_next || B == 1))) return CSA2_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (dev != h->device) return CSA2_ERR_INVALID_ARG;
+  return cuda_status(csa2::launch_roll_window(window, B, T, next, T_next, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Indexer scores alone (include/csa2.h): S^I of every visible entry into the caller's rows.
+csa2_status csa2_index_scores(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, const uint8_t* ki_codes,
+                              const uint8_t* ki_scales, int64_t cap, const int64_t* p0, int B, int T, float* scores,
+                              int64_t ld, void* ws, size_t ws_bytes, csa2_stream_t stream) {
+  return index_call(h, qi, wI, ki_codes, ki_scales, cap, p0, B, T, nullptr, nullptr, nullptr, nullptr,
+                    csa2::kIndexScores, ws, ws_bytes, stream, scores, ld);
 }
 
 // Hierarchical Sparse Indexer, owner layer (include/csa2.h): the top-512 plus the block pool.
@@ -337,10 +367,13 @@ csa2_status csa2_check(csa2_handle* h, csa2_stream_t stream) {
   if (dev != h->device) return CSA2_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
   int ea = 0, ei = 0, eo = 0;
+  unsigned da = 0, di = 0;
   if (csa2::take_attend_error(&ea) != cudaSuccess || csa2::take_index_error(&ei) != cudaSuccess ||
-      csa2::take_outproj_error(&eo) != cudaSuccess)
+      csa2::take_outproj_error(&eo) != cudaSuccess || csa2::take_attend_domain(&da) != cudaSuccess ||
+      csa2::take_index_domain(&di) != cudaSuccess)
     return CSA2_ERR_CUDA;
-  return (ea || ei || eo) ? CSA2_ERR_TIMEOUT : CSA2_OK;
+  if (ea || ei || eo) return CSA2_ERR_TIMEOUT;
+  return (da || di) ? CSA2_ERR_UNSUPPORTED : CSA2_OK;
 }
 
 // Test hook for the timeout report (include/csa2.h).

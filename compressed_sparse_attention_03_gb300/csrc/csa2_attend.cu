@@ -58,6 +58,9 @@ static_assert(kPOff - kGOff == kH * kD * 4, "the G area holds one fp32 output ro
 constexpr uint32_t kTmemCols = 512, kLCol = 256, kSCol = 320;
 
 __device__ int g_attend_error;
+// Set when a producer read a Z scale above 2^13 (scale byte > 140), where E2M1 x 2^e overflows
+// the fp16 operand, or a query value that overflows fp16.  csa2_check reports it.
+__device__ unsigned g_attend_domain;
 
 struct Bars {
   uint64_t q_raw, q_full, s_full, p_full, l_done;
@@ -268,6 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
 #pragma unroll
             for (int q = 0; q < 2; ++q) raw[2 * at + q] = src[2 * (2 * at + half) + q];  // 32 FP4 code bytes
           raw[8] = *reinterpret_cast<const uint4*>(a.z_scales + ((int64_t)b * a.cap + j) * 16);  // all 16 scales
+          if (__vcmpgtu4(raw[8].x, 0x8C8C8C8Cu) | __vcmpgtu4(raw[8].y, 0x8C8C8C8Cu) | __vcmpgtu4(raw[8].z, 0x8C8C8C8Cu) |
+              __vcmpgtu4(raw[8].w, 0x8C8C8C8Cu))
+            atomicOr(&g_attend_domain, 1u);
         }
       }
     };
@@ -287,6 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         uint32_t o[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) o[m] = f2_to_h2(bf16_to_f32(w[m] & 0xffffu), bf16_to_f32(w[m] >> 16));
+        // |q| >= 65520 (bf16 exponent field >= 143) becomes inf in fp16
+        const uint32_t big = __vcmpgeu2(qv.x & 0x7f807f80u, 0x47804780u) | __vcmpgeu2(qv.y & 0x7f807f80u, 0x47804780u) |
+                             __vcmpgeu2(qv.z & 0x7f807f80u, 0x47804780u) | __vcmpgeu2(qv.w & 0x7f807f80u, 0x47804780u);
+        if (big) atomicOr(&g_attend_domain, 1u);
         *reinterpret_cast<uint4*>(sm + kQOff + (d0 >> 6) * 8192 + sw128_off(h, (d0 & 63) >> 3)) =
             make_uint4(o[0], o[1], o[2], o[3]);
       }
@@ -685,6 +695,14 @@ cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, const SeqPos& 
 }
 
 // Reads and clears the attention kernels' device error word (0 = no bounded wait gave up).
+// Reads and clears the domain flag of the attention kernel (0: every scale and query fitted fp16).
+cudaError_t take_attend_domain(unsigned* flag) {
+  const unsigned zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_attend_domain, sizeof(unsigned));
+  if (e == cudaSuccess && *flag != 0) e = cudaMemcpyToSymbol(g_attend_domain, &zero, sizeof(unsigned));
+  return e;
+}
+
 cudaError_t take_attend_error(int* code) {
   const int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(code, g_attend_error, sizeof(int));

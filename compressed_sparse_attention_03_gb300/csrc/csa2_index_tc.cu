@@ -36,6 +36,10 @@ constexpr int kThreadsTC = 256;
 constexpr uint32_t kBOff = 0, kAOff = 131072, kWOff = 196608, kDynTC = 196608 + 2048 + 1024;
 
 __device__ int g_index_error;
+// Set when a kernel here read an FP4 scale above 2^13 (scale byte > 140): E2M1 x 2^e no longer
+// fits fp16 (6 x 2^14 > 65504), so the tensor-core operands would overflow.  csa2_check reports it.
+__device__ unsigned g_index_domain;
+constexpr uint32_t kMaxScaleBytes = 0x8C8C8C8Cu;  // 140 in every byte: 2^13, the largest exact fp16 scale
 
 
 // Q^I (bf16) -> FP4 (E2M1, UE8M0 per 32) -> fp16 image.  grid (Tq, nb), 128 threads: warp w
@@ -62,6 +66,7 @@ __global__ void __launch_bounds__(128) qimage_kernel(IndexArgs a, int b0, int t0
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     const int e = mx_scale_exp(amax);
+    if (e > 13 && l == 0) atomicOr(&g_index_domain, 1u);
     const float down = pow2f(-e);  // exact power of two
     uint2 img;
     if (e >= -24 && e <= 15) {  // 2^e is an fp16 number: code x 2^e rounds exactly as via fp32
@@ -95,6 +100,7 @@ __global__ void __launch_bounds__(128) kimage_kernel(IndexArgs a, int b0, int64_
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] = src[i];
     sc = *reinterpret_cast<const uint32_t*>(a.ki_scales + ((int64_t)b * a.cap + j) * 4);
+    if (__vcmpgtu4(sc, kMaxScaleBytes)) atomicOr(&g_index_domain, 1u);
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -308,7 +314,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
 //  - warps 4-19 (decoders, group = (warp - 4) / 4, rows 32 * (warp % 4) ..): the tiles
 //    i = group mod kDGroups, lane = key row; four groups, so that each warp has four tiles'
 //    time for the latency of its decode chain.  The 4 scale bytes of a row come by a plain
-//    load issued two group tiles ahead; the codes from the stage.  Exact decode to fp16 into TMEM
+//    load issued two group tiles ahead; the codes from the stage, which a warp releases to the
+//    producer after a proxy fence (its generic reads, then the next bulk copy's writes).  Exact decode to fp16 into TMEM
 //    (kDSlots tiles); rows past the last key (or naming an entry outside 0..E-1) are zero.
 //  - warps 20 and 21 (one thread each): the MMAs of the even / odd tiles, A from TMEM, B
 //    (Q^I) from shared memory.  A thread that waits stalls until its own MMAs in flight have
@@ -425,6 +432,7 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
       const int e = mx_scale_exp(amax);
+      if (e > 13 && lane == 0) atomicOr(&g_index_domain, 1u);
       float q[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) q[i] = ldexpf(e2m1_to_f32(f32_to_e2m1(ldexpf(v[i], -e))), e);
@@ -469,11 +477,16 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
                                                        (32 * q4 + lane) * 64);
 #pragma unroll
       for (int k = 0; k < 4; ++k) cw[k] = valid ? rc[k] : make_uint4(0u, 0u, 0u, 0u);
+      // The next bulk copy into this stage (async proxy) must not overtake these generic-proxy
+      // reads: without the proxy fence it sometimes did, and the first key row of a stage (the
+      // first bytes the next copy writes) was decoded from the following group's codes.
+      fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.s_empty[s]);  // the codes are in registers
       const int slot = i % kDSlots;
       if (i >= kDSlots) mbar_wait(&bars.done[slot], ((i / kDSlots) - 1) & 1, err, 34);  // slot's last tile done
       tc_fence_after();
+      if (__vcmpgtu4(sa, kMaxScaleBytes)) atomicOr(&g_index_domain, 1u);
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {  // 32 values: 16 code bytes, one scale byte
         const uint32_t s2 = pow2_h2((int)((sa >> (8 * blk)) & 255u) - 127);
@@ -644,6 +657,14 @@ cudaError_t take_index_error(int* code) {
   const int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(code, g_index_error, sizeof(int));
   if (e == cudaSuccess && *code != 0) e = cudaMemcpyToSymbol(g_index_error, &zero, sizeof(int));
+  return e;
+}
+
+// Reads and clears the FP4-scale domain flag of the indexer kernels (0: every scale read fitted).
+cudaError_t take_index_domain(unsigned* flag) {
+  const unsigned zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_index_domain, sizeof(unsigned));
+  if (e == cudaSuccess && *flag != 0) e = cudaMemcpyToSymbol(g_index_domain, &zero, sizeof(unsigned));
   return e;
 }
 

@@ -50,7 +50,9 @@ IndexPlan make_plan(int nb, int T, int64_t max_entries, int mode = kIndexTopk) {
   p.ld = ((max(max_entries, (int64_t)1) + 31) / 32) * 32;
   int64_t per_q = (int64_t)nb * p.ld * 4;
   int64_t tq = (int64_t)(kScoreBudget / (size_t)per_q);
-  p.Tq = (int)max64(1, min64(T, tq));
+  // scores to the caller's array (csa2_index_scores): one pass over all queries, no select
+  const bool so = mode == kIndexScores;
+  p.Tq = so ? T : (int)max64(1, min64(T, tq));
   int64_t c = kMinChunk;
   while (c * kMaxChunks < p.ld && c < kMaxChunk) c *= 2;
   p.chunk = (int)c;
@@ -63,16 +65,16 @@ IndexPlan make_plan(int nb, int T, int64_t max_entries, int mode = kIndexTopk) {
   size_t off = 0;
   p.off_q = off; off += p.tc ? 0 : align256(rows * kHI * kDI * 4);
   p.off_w = off; off += align256(rows * kHI * 4);
-  p.off_s = off; off += align256(rows * (size_t)p.ld * 4);
-  p.off_ck = off; off += align256(rows * p.nchunks * kTopK * 4);
-  p.off_cj = off; off += align256(rows * p.nchunks * kTopK * 4);
-  p.off_cn = off; off += align256(rows * p.nchunks * 4);
+  p.off_s = off; off += so ? 0 : align256(rows * (size_t)p.ld * 4);
+  p.off_ck = off; off += so ? 0 : align256(rows * p.nchunks * kTopK * 4);
+  p.off_cj = off; off += so ? 0 : align256(rows * p.nchunks * kTopK * 4);
+  p.off_cn = off; off += so ? 0 : align256(rows * p.nchunks * 4);
   p.off_img = off; off += p.tc ? align256(index_tc_image_bytes(nb, p.Tq, p.ld)) : 0;
   p.off_rl = off; off += mode == kIndexReindex ? align256(rows * 4) : 0;
   p.off_pk = off; off += align256(rows * p.pnch * kPoolSel * 4);
   p.off_pj = off; off += align256(rows * p.pnch * kPoolSel * 4);
   p.off_pn = off; off += align256(rows * p.pnch * 4);
-  p.off_h = off; off += p.dec ? align256(rows * kHistBins * 4) : 0;
+  p.off_h = off; off += p.dec && !so ? align256(rows * kHistBins * 4) : 0;
   p.total = off;
   return p;
 }
@@ -695,12 +697,14 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
   char* base = static_cast<char*>(ws);
   float* qdq = reinterpret_cast<float*>(base + p.off_q);
   float* wq = reinterpret_cast<float*>(base + p.off_w);
-  float* sc = reinterpret_cast<float*>(base + p.off_s);
+  const bool so = mode == kIndexScores;  // the caller's score rows (this group's part), no select
+  float* sc = so ? a.scores_out + (int64_t)b0 * a.T * a.scores_ld : reinterpret_cast<float*>(base + p.off_s);
+  const int64_t ld = so ? a.scores_ld : p.ld;
   uint32_t* ck = reinterpret_cast<uint32_t*>(base + p.off_ck);
   int32_t* cj = reinterpret_cast<int32_t*>(base + p.off_cj);
   int* cn = reinterpret_cast<int*>(base + p.off_cn);
   int* rowlen = mode == kIndexReindex ? reinterpret_cast<int*>(base + p.off_rl) : nullptr;
-  uint32_t* hist = p.dec ? reinterpret_cast<uint32_t*>(base + p.off_h) : nullptr;
+  uint32_t* hist = p.dec && !so ? reinterpret_cast<uint32_t*>(base + p.off_h) : nullptr;
   uint32_t* pk = reinterpret_cast<uint32_t*>(base + p.off_pk);
   int32_t* pj = reinterpret_cast<int32_t*>(base + p.off_pj);
   int* pn = reinterpret_cast<int*>(base + p.off_pn);
@@ -729,16 +733,16 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
     int64_t emax = 0;
     for (int i = 0; i < nb; ++i) emax = max(emax, (pos.p0[i] + t0 + tq) >> a.rshift);
     if (mode == kIndexReindex) {  // every query row scans its own pool
-      e = launch_index_scores_decode_tc(a, pos, b0, nb, t0, tq, p.Tq, sc, p.ld, rowlen, hist, num_sms, st);
+      e = launch_index_scores_decode_tc(a, pos, b0, nb, t0, tq, p.Tq, sc, ld, rowlen, hist, num_sms, st);
       if (e != cudaSuccess) return e;
       emax = min64(emax, (int64_t)kHsiBlock * kHsiBlocks);
     } else if (p.tc) {
       e = launch_index_scores_tc(a, pos, b0, nb, t0, tq, p.Tq, emax, reinterpret_cast<uint8_t*>(base + p.off_img), wq, sc,
-                                 p.ld, num_sms, st);
+                                 ld, num_sms, st);
       if (e != cudaSuccess) return e;
     } else if (a.T == 1) {
       if (emax > 0) {
-        e = launch_index_scores_decode_tc(a, pos, b0, nb, 0, 1, 1, sc, p.ld, nullptr, hist, num_sms, st);
+        e = launch_index_scores_decode_tc(a, pos, b0, nb, 0, 1, 1, sc, ld, nullptr, hist, num_sms, st);
         if (e != cudaSuccess) return e;
       }
     } else {
@@ -748,10 +752,11 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
     }
     if (mode != kIndexReindex && !p.tc && a.T > 1 && emax > 0) {
       dim3 g((unsigned)((emax + kScoreThreads - 1) / kScoreThreads), (unsigned)((tq + kQT - 1) / kQT), (unsigned)nb);
-      score_kernel<<<g, kScoreThreads, score_smem, st>>>(a, pos, b0, t0, p.Tq, qdq, wq, sc, p.ld);
+      score_kernel<<<g, kScoreThreads, score_smem, st>>>(a, pos, b0, t0, p.Tq, qdq, wq, sc, ld);
       note_launch();
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    if (so) continue;
     const int nch = (int)max64(1, (emax + p.chunk - 1) / p.chunk);
     if (hist)
       topk_chunk_kernel<kTopkThreads><<<dim3(nch, tq, nb), kTopkThreads, chunk_smem, st>>>(

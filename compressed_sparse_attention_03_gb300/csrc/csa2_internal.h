@@ -48,10 +48,13 @@ struct IndexArgs {
   // pool_in [B, T, 2048] restricts the scan to a pool (csa2_reindex_topk)
   int32_t* pool_out;
   const int32_t* pool_in;
+  // csa2_index_scores: the fp32 score rows go to the caller's [B, T, scores_ld] array
+  float* scores_out;
+  int64_t scores_ld;
 };
 
 constexpr int kHsiBlock = 8, kHsiBlocks = 2048;  // blocks of 8 entries, 2048 blocks per pool
-enum IndexMode { kIndexTopk = 0, kIndexPool = 1, kIndexReindex = 2 };
+enum IndexMode { kIndexTopk = 0, kIndexPool = 1, kIndexReindex = 2, kIndexScores = 3 };
 
 struct AttendArgs {
   const uint16_t* q;
@@ -67,6 +70,9 @@ struct AttendArgs {
 // `b0` is the batch index of the first sequence in `pos`, `nb` how many follow.
 cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf,
                           cudaStream_t st);
+// Window roll: rows T .. T+126 of each sequence's view [B, 127+T, 512] -> rows 0 .. 126 of the
+// next view [B, 127+T_next, 512] (one block per sequence; its rows may move within one buffer).
+cudaError_t launch_roll_window(const uint8_t* window, int B, int T, uint8_t* next, int T_next, cudaStream_t st);
 size_t index_workspace_bytes(int B, int T, int64_t max_entries, int num_sms, int mode = kIndexTopk);
 cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int64_t max_entries,
                               void* ws, size_t ws_bytes, int num_sms, cudaStream_t st, int mode = kIndexTopk);
@@ -85,6 +91,10 @@ cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos,
 cudaError_t take_attend_error(int* code);
 cudaError_t take_index_error(int* code);
 cudaError_t take_outproj_error(int* code);
+// Domain flags: set when a kernel read an FP4 scale above 2^13 (or a value that overflows an fp16
+// operand); read and cleared like the error words.
+cudaError_t take_index_domain(unsigned* flag);
+cudaError_t take_attend_domain(unsigned* flag);
 // Grouped output projection: o [M, 64, 512] bf16, w [8, 1024, 4096] bf16 (group, output,
 // input), out [M, 8, 1024] bf16.
 cudaError_t launch_out_group_proj(const uint16_t* o, const uint16_t* w, int64_t M, uint16_t* out, int num_sms,

@@ -312,7 +312,41 @@ __global__ void __launch_bounds__(kWriterThreads) writer_window_kernel(WriterArg
   }
 }
 
+// Window roll between calls ([PG] paragraph "Between forward calls": the window keeps the last
+// 128 positions).  Row r of the next call's view holds position p0 + T - 127 + r, which is row
+// T + r of this call's view: rows T .. T+126 move to rows 0 .. 126.  One block per sequence
+// loads all of its 127 rows (65,024 bytes, 16 per thread and load) before storing any, so a
+// sequence's rows may move within one buffer.
+constexpr int kRollThreads = 512;
+constexpr int kRollVec = 127 * kD / 16;
+constexpr int kRollPer = (kRollVec + kRollThreads - 1) / kRollThreads;
+
+__global__ void __launch_bounds__(kRollThreads) roll_window_kernel(const uint8_t* window, int T, uint8_t* next,
+                                                                   int T_next) {
+  const int b = blockIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(window + ((int64_t)b * (127 + T) + T) * kD);
+  uint4* dst = reinterpret_cast<uint4*>(next + (int64_t)b * (127 + T_next) * kD);
+  uint4 v[kRollPer];
+#pragma unroll
+  for (int k = 0; k < kRollPer; ++k) {
+    const int i = threadIdx.x + k * kRollThreads;
+    if (i < kRollVec) v[k] = src[i];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kRollPer; ++k) {
+    const int i = threadIdx.x + k * kRollThreads;
+    if (i < kRollVec) dst[i] = v[k];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_roll_window(const uint8_t* window, int B, int T, uint8_t* next, int T_next, cudaStream_t st) {
+  roll_window_kernel<<<(unsigned)B, kRollThreads, 0, st>>>(window, T, next, T_next);
+  note_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf, cudaStream_t st) {
   int64_t max_new = 0;

@@ -85,12 +85,17 @@ def _e2m1_nibbles(shape, g, device):
     return mag | sign
 
 
-def random_fp4(rows_shape, n: int, g, device):
-    """Random FP4 rows: (codes [..., n/2] u8, scales [..., n/32] u8)."""
+def random_fp4(rows_shape, n: int, g, device, scale_range=None):
+    """Random FP4 rows: (codes [..., n/2] u8, scales [..., n/32] u8).  Scale bytes follow the
+    table above, or are uniform over scale_range = (lo, hi) inclusive."""
     lo = _e2m1_nibbles((*rows_shape, n // 2), g, device)
     hi = _e2m1_nibbles((*rows_shape, n // 2), g, device)
     codes = (lo | (hi << 4)).to(torch.uint8)
-    scales = _SCALE.to(device)[_bytes((*rows_shape, n // 32), g, device)]
+    if scale_range is None:
+        scales = _SCALE.to(device)[_bytes((*rows_shape, n // 32), g, device)]
+    else:
+        scales = torch.randint(scale_range[0], scale_range[1] + 1, (*rows_shape, n // 32), generator=g, device=device,
+                               dtype=torch.int32).to(torch.uint8)
     return codes, scales
 
 
@@ -139,10 +144,11 @@ def step_inputs(B: int, T: int, seed: int, device="cpu"):
     return dict(kc=kc, gc=gc, wa=wa, q=q, qi=qi, wI=wI)
 
 
-def cache_state(B: int, T: int, p0: int, cap: int, seed: int, device="cpu", ratio: int = 2):
+def cache_state(B: int, T: int, p0: int, cap: int, seed: int, device="cpu", ratio: int = 2, scale_range=None):
     """Synthetic state before the step: FP4 caches with the p0//ratio cached entries drawn at
     random (rest zero), the window view [B,127+T,512] with random E4M3 codes in the rows of
-    positions p0-127..p0-1 that exist, and a random pair buffer (used when p0 is odd)."""
+    positions p0-127..p0-1 that exist, and a random pair buffer (used when p0 is odd).
+    scale_range = (lo, hi): FP4 scale bytes uniform over lo..hi instead of the default table."""
     g = _gen(30_000 + seed, device)
     n = p0 // ratio
     z_codes = torch.zeros(B, cap, D // 2, dtype=torch.uint8, device=device)
@@ -150,8 +156,8 @@ def cache_state(B: int, T: int, p0: int, cap: int, seed: int, device="cpu", rati
     ki_codes = torch.zeros(B, cap, DI // 2, dtype=torch.uint8, device=device)
     ki_scales = torch.zeros(B, cap, DI // 32, dtype=torch.uint8, device=device)
     if n:
-        zc, zs = random_fp4((B, n), D, g, device)
-        kc, ks = random_fp4((B, n), DI, g, device)
+        zc, zs = random_fp4((B, n), D, g, device, scale_range)
+        kc, ks = random_fp4((B, n), DI, g, device, scale_range)
         z_codes[:, :n], z_scales[:, :n], ki_codes[:, :n], ki_scales[:, :n] = zc, zs, kc, ks
     window = torch.zeros(B, 127 + T, D, dtype=torch.uint8, device=device)
     first = max(0, 127 - p0)

@@ -28,6 +28,15 @@
  *    returned before anything is launched; launch errors come back as CSA2_ERR_CUDA.
  *  - Every wait inside a kernel is bounded (about 80 ms).  A wait that gives up records a
  *    code in a device error word and lets its kernel finish; csa2_check reports it.
+ *  - FP4 scale domain.  The tensor-core kernels decode E2M1 x 2^e exactly into fp16
+ *    operands for scale bytes 104..140 (e = -23 .. 13).  Bytes below 104 decode with an
+ *    absolute error under 2^-24 per value (the rest of the row is unaffected); bytes 0 with
+ *    zero codes are exact zeros.  Bytes above 140 would overflow fp16: a kernel that reads
+ *    one (or an indexer query block with e > 13, or an attention query of magnitude 2^16 or
+ *    more) records it, and the next csa2_check returns CSA2_ERR_UNSUPPORTED (the outputs
+ *    since the previous check are not to be trusted).  Rows this library's writer makes stay
+ *    inside: after RMSNorm |value| <= sqrt(512) max|gamma|, so gains of magnitude at most 2^k
+ *    give scale bytes <= 129 + k (k <= 11 keeps every byte <= 140).
  *
  * Storage formats (fixed by this library)
  *  - FP4 cache row of n values: n/2 code bytes (E2M1, element 2i in the low nibble of byte
@@ -99,7 +108,8 @@ enum {
   CSA2_OP_INDEX_TOPK = 1,
   CSA2_OP_ATTEND = 2,
   CSA2_OP_INDEX_POOL = 3,
-  CSA2_OP_REINDEX_TOPK = 4
+  CSA2_OP_REINDEX_TOPK = 4,
+  CSA2_OP_INDEX_SCORES = 5
 };
 
 /* Bytes of workspace the call `op` needs for B sequences of T new tokens whose largest
@@ -134,6 +144,20 @@ csa2_status csa2_write_cache(csa2_handle* h, const uint16_t* kc, const uint16_t*
                              int64_t cap, uint8_t* window, void* ws, size_t ws_bytes,
                              csa2_stream_t stream);
 
+/* (1') Window roll between calls ([PG], paragraph "Between forward calls": the layer keeps
+ * the window of the last 128 positions).  After a call that appended T tokens at p0, the next
+ * call's view must hold positions p0+T-127 .. p0+T-1 in its rows 0..126; these are rows
+ * T .. T+126 of this call's view, and this call copies them:
+ *  window : u8 [B, 127+T, 512]  this call's view (rows 127.. written by csa2_write_cache).
+ *  next   : u8 [B, 127+T_next, 512]  the next call's view; rows 0..126 are written, the rest
+ *           is untouched (the next csa2_write_cache fills rows 127..).
+ * `next` may be `window` itself when T_next == T or B == 1: each sequence's rows then move
+ * within its own rows.  Any other overlap of the two views is CSA2_ERR_INVALID_ARG.  Rows of
+ * negative positions (p0+T < 127) are copied as they are; no call reads them.
+ * Workspace: none. */
+csa2_status csa2_roll_window(csa2_handle* h, const uint8_t* window, int B, int T, uint8_t* next,
+                             int T_next, csa2_stream_t stream);
+
 /* (2)+(3) Lightning indexer and top-512, [PG] equations for S^I and I_t.
  *  qi  : bf16 [B, T, 32, 128]  indexer queries Q^I (quantised here to FP4, scale per 32).
  *  wI  : bf16 [B, T, 32]       head weights w^I (already divided by sqrt(128*32)).
@@ -148,6 +172,21 @@ csa2_status csa2_index_topk(csa2_handle* h, const uint16_t* qi, const uint16_t* 
                             const uint8_t* ki_codes, const uint8_t* ki_scales, int64_t cap,
                             const int64_t* p0, int B, int T, int32_t* idx, float* top_scores,
                             void* ws, size_t ws_bytes, csa2_stream_t stream);
+
+/* (2) Lightning-indexer scores alone, [PG] equation for S^I: the fp32 values that
+ * csa2_index_topk selects from, for a caller that needs every score (a different select, a
+ * check of the scores themselves).  Arguments as csa2_index_topk, plus
+ *  scores : f32 [B, T, ld]; row (b, t) receives S^I_{t,j} for every visible j <
+ *           floor((p0[b]+t+1)/ratio) in the same fp32 arithmetic as csa2_index_topk; the
+ *           rest of the row is left untouched.  16-byte aligned.
+ *  ld     : row stride in floats, a multiple of 4 and at least the largest visible count
+ *           (CSA2_ERR_SHAPE otherwise).
+ * All T queries are scored in one pass, so the caller holds B*T*ld floats at once.
+ * Workspace: csa2_workspace_bytes(h, CSA2_OP_INDEX_SCORES, B, T, max_entries). */
+csa2_status csa2_index_scores(csa2_handle* h, const uint16_t* qi, const uint16_t* wI,
+                              const uint8_t* ki_codes, const uint8_t* ki_scales, int64_t cap,
+                              const int64_t* p0, int B, int T, float* scores, int64_t ld,
+                              void* ws, size_t ws_bytes, csa2_stream_t stream);
 
 /* (2)+(3) Hierarchical Sparse Indexer, owner layer ("Inside DeepSeek V4.1", section "Most
  * layers borrow"; "Deriving the 890-Byte KV Cache", section "Hierarchical indexing bounds the
@@ -190,9 +229,10 @@ csa2_status csa2_out_group_proj(csa2_handle* h, const uint16_t* o, const uint16_
 
 /* Failure report (no counterpart on the pages).  Synchronises `stream`, then reports whether
  * a bounded wait inside any kernel of this library gave up since the last check:
- * CSA2_ERR_TIMEOUT (the outputs of the calls since then are not to be trusted), CSA2_ERR_CUDA
- * if synchronising or reading the error words failed, CSA2_OK otherwise.  Clears the error
- * words.  Call with the handle's device current; while an error word is set, later waits
+ * CSA2_ERR_TIMEOUT (the outputs of the calls since then are not to be trusted); else
+ * CSA2_ERR_UNSUPPORTED if a kernel read an FP4 scale or query outside the fp16 domain (see the
+ * conventions above); CSA2_ERR_CUDA if synchronising or reading the words failed; CSA2_OK
+ * otherwise.  Clears the error words and domain flags.  Call with the handle's device current; while an error word is set, later waits
  * that stay pending give up early, so check before trusting further results.  Not for use
  * inside stream capture (it synchronises). */
 csa2_status csa2_check(csa2_handle* h, csa2_stream_t stream);
@@ -249,6 +289,11 @@ csa2_status csa2_attend_replay(csa2_handle* h, const uint16_t* q, const float* s
  *    later calls reuse the cached address and make no allocating call at all.  Make the
  *    first call on each device before any stream capture.  The handle's device must be the
  *    current device (else CSA2_ERR_INVALID_ARG).
+ *  - The cached address belongs to this process and to the device's current context: it is
+ *    kept with the context's ID, and a call made in another context (after cudaDeviceReset
+ *    ended the old one) resolves the address again, so that first call after a reset is a
+ *    set-up call like the very first one.  Without the driver's context-ID query (CUDA
+ *    drivers before 12.0) every call resolves the address, which allocates only once.
  *  - The array is shared: calls that may overlap in time (different streams, or different
  *    threads without ordering) race on it and corrupt each other's output.  Calls queued on
  *    one stream are ordered and safe. */

@@ -7,6 +7,8 @@ import subprocess
 import sys
 from pathlib import Path
 
+import numpy as np
+
 ROOT = Path(__file__).resolve().parent.parent
 
 WORKER = r"""
@@ -79,3 +81,22 @@ def test_profiled_traffic_is_dropped_when_the_kernel_source_changes(tmp_path, mo
     src.write_text("kernel v2")
     assert bench.profiled_traffic("p.md", ["k.cu"]) is None
     assert bench.profiled_traffic("missing.md", ["k.cu"]) is None
+
+
+def test_reference_arm_runs_the_fixed_oracle_sample():
+    """bench.py --impl reference on the CPU: one JSON line whose sample is the fixed, seeded row set
+    that the GPU arm's cpu_baseline uses too (16 rows per host thread, at most the step's rows)."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="2")
+    out = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference", "--workload", "decode_8k",
+                          "--steps", "2", "--warmup", "1"], env=env, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "tok/s" and line["value"] > 0
+    assert line["cpu_baseline"]["cores"] == 2 and "fixed 1 query rows" in line["cpu_baseline"]["sample"]
+    sys.path.insert(0, str(ROOT))
+    import bench
+    from compressed_sparse_attention_03_gb300 import inputs
+
+    wl = inputs.WORKLOADS["prefill_4k"]
+    a, b = bench.oracle_rows(wl, 16), bench.oracle_rows(wl, 16)
+    assert len(a) == 256 and np.array_equal(a, b) and np.all(np.diff(a) > 0)

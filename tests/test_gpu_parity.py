@@ -111,6 +111,66 @@ def test_writer_workloads(handle, name):
     print(f"writer {name}: boundary exceptions codes/scales/fp8 = {n}")
 
 
+# ------------------------------------------------------------------------ window roll
+@pytest.mark.parametrize("B,T,T_next,inplace", [(2, 1, 1, True), (3, 5, 5, True), (1, 200, 40, True),
+                                                (2, 300, 1, False), (2, 1, 64, False)])
+def test_roll_window(handle, B, T, T_next, inplace):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(1000 * B + T)
+    win = inputs.random_e4m3((B, 127 + T, 512), g, DEV)
+    want = win[:, T:T + 127].clone()
+    if inplace:  # the same buffer: with B = 1 the next view may be shorter
+        nxt = win.view(-1)[: B * (127 + T_next) * 512].view(B, 127 + T_next, 512)
+    else:
+        nxt = inputs.random_e4m3((B, 127 + T_next, 512), g, DEV)
+    keep = nxt[:, 127:].clone()
+    csa2.csa2_roll_window(handle, win, nxt)
+    assert torch.equal(nxt[:, :127], want)
+    assert torch.equal(nxt[:, 127:], keep)
+
+
+def test_roll_window_rejects_shared_rows():
+    h = csa2.csa2_create()
+    win = torch.zeros(2, 127 + 3, 512, dtype=torch.uint8, device=DEV)
+    nxt = win.view(-1)[: 2 * 128 * 512].view(2, 128, 512)  # one buffer, other strides: blocks would collide
+    with pytest.raises(csa2.Csa2Error) as e:
+        csa2.csa2_roll_window(h, win, nxt)
+    assert e.value.status == 1
+
+
+def test_decode_steps_with_roll(handle):
+    """Two decode steps (T = 1 each, the window rolled in between, the pair buffer carried) write
+    the same caches, window rows and pair state as one two-token call of the oracle."""
+    B, p0s = 2, [4001, 300]
+    x, cap = make_state(B, 2, p0s, seed=51)
+    ow = oracle_write(x, p0s, cap)
+    w = {k: x[k].clone() for k in ("z_codes", "z_scales", "ki_codes", "ki_scales", "pair_kc", "pair_gc")}
+    view = x["window"][:, :128].clone()  # rows of positions p0-127 .. p0
+    for t in range(2):
+        p = [q + t for q in p0s]
+        csa2.csa2_write_cache(handle, x["kc"][:, t:t + 1].contiguous(), x["gc"][:, t:t + 1].contiguous(),
+                              x["wa"][:, t:t + 1].contiguous(), x["gamma_c"], x["w_ik"], x["gamma_ik"], x["gamma_w"], p,
+                              w["z_codes"], w["z_scales"], w["ki_codes"], w["ki_scales"], view, w["pair_kc"],
+                              w["pair_gc"])
+        if t == 0:
+            csa2.csa2_roll_window(handle, view, view)
+    for b, r in enumerate(ow):
+        j0, n = r["first_entry"], r["n_entries"]
+        for k in ("z_codes", "z_scales", "ki_codes", "ki_scales"):
+            g = w[k][b].cpu().numpy()
+            assert np.array_equal(g[:j0], r[k][:j0]) and np.array_equal(g[j0 + n:], r[k][j0 + n:])
+        fp4_compare(w["z_codes"][b, j0:j0 + n].cpu().numpy(), w["z_scales"][b, j0:j0 + n].cpu().numpy(),
+                    r["z_codes"][j0:j0 + n], r["z_scales"][j0:j0 + n], r["z_pre"])
+        fp4_compare(w["ki_codes"][b, j0:j0 + n].cpu().numpy(), w["ki_scales"][b, j0:j0 + n].cpu().numpy(),
+                    r["ki_codes"][j0:j0 + n], r["ki_scales"][j0:j0 + n], r["ki_pre"])
+        # the view of the second call holds positions p0-126 .. p0+1 = oracle rows 1 .. 128
+        gv = view[b].cpu().numpy()
+        assert np.array_equal(gv[:126], r["window"][1:127])  # the caller's rows, moved
+        e4m3_compare(gv[126:128], r["window"][127:129], r["win_pre"])  # positions p0, p0+1
+        if (p0s[b] + 2) % 2 == 1:
+            assert np.array_equal(w["pair_kc"][b].cpu().numpy(), r["pair"][0])
+
+
 # ------------------------------------------------------------------------ indexer + top-k
 def run_index(h, x, p0s, T):
     B = x["qi"].shape[0]
@@ -143,6 +203,72 @@ def check_index(idx, top, x, p0s, rows=None, ratio=2):
             assert np.all(np.abs(gt[i, :k] - ref) <= 1e-5 * scale), f"row {r[i]} scores"
             assert np.all(np.isnan(gt[i, k:]))
     return swaps
+
+
+def check_scores(g, x, p0s, ratio=2):
+    """Every visible S^I of every row (GPU fp32, [B, T, ld]) against the oracle's fp64 scores,
+    within 1e-5 of the row's largest |score| (a score is a signed sum of 32 fp32 terms).
+    Returns the oracle's scores per sequence."""
+    B, T = g.shape[:2]
+    out = []
+    for b, p0 in enumerate(p0s):
+        pos = p0 + np.arange(T)
+        E = (pos + 1) // ratio
+        n = max(int(E.max()), 1)
+        sc = oracle.index_scores(pos, np32(x["qi"][b]), np32(x["wI"][b]), x["ki_codes"][b, :n].cpu().numpy(),
+                                 x["ki_scales"][b, :n].cpu().numpy(), n, ratio=ratio)
+        gb = g[b].cpu().numpy().astype(np.float64)
+        for t in range(T):
+            e = int(E[t])
+            if e == 0:
+                continue
+            err = np.abs(gb[t, :e] - sc[t, :e])
+            bound = 1e-5 * np.abs(sc[t, :e]).max()
+            bad = np.nonzero(err > bound)[0]
+            assert not len(bad), (f"sequence {b} query {t}: {len(bad)} scores off, first entries {bad[:4].tolist()} "
+                                  f"gpu {gb[t, bad[:4]].tolist()} oracle {sc[t, bad[:4]].tolist()}")
+        out.append(sc)
+    return out
+
+
+def run_scores(h, x, p0s, T, ratio=2):
+    B = x["qi"].shape[0]
+    ld = ((int(((np.asarray(p0s) + T) // ratio).max()) + 3) // 4) * 4
+    g = torch.full((B, T, max(ld, 4)), float("nan"), dtype=torch.float32, device=DEV)
+    csa2.csa2_index_scores(h, x["qi"], x["wI"], x["ki_codes"], x["ki_scales"], p0s, g)
+    return g
+
+
+@pytest.mark.parametrize("B,T,p0s", [(1, 300, [0]), (2, 5, [1000, 37]), (3, 1, [0, 1, 4001]), (2, 64, [2000, 37]),
+                                     (1, 1, [70001])])
+def test_index_scores_small(handle, B, T, p0s):
+    """S^I alone, every visible entry of every query: the tensor-core prefill scorer (T >= 8),
+    the CUDA-core scorer (T < 8) and the decode scorer (T = 1)."""
+    x, cap = make_state(B, T, p0s, seed=19 + T)
+    g = run_scores(handle, x, p0s, T)
+    check_scores(g, x, p0s)
+    # entries beyond each query's visible count are left untouched
+    for b, p0 in enumerate(p0s):
+        for t in range(T):
+            assert torch.isnan(g[b, t, (p0 + t + 1) // 2:]).all()
+
+
+@pytest.mark.parametrize("name", ["decode_512k_r1", "decode_1m"])
+def test_index_scores_repeated(handle, handle_r1, name):
+    """Every S^I score of the two largest decode workloads (8 x 524288 entries), from ten calls
+    in one process: each call must match the oracle and repeat the first call bit for bit.  The
+    selected sets and their scores alone would miss a wrong score outside the top 512."""
+    wl = inputs.WORKLOADS[name]
+    h = handle_r1 if wl.ratio == 1 else handle
+    x = inputs.workload_inputs(wl, DEV)
+    p0s = [wl.p0] * wl.B
+    first = run_scores(h, x, p0s, 1, wl.ratio)
+    check_scores(first, x, p0s, wl.ratio)
+    E = (wl.p0 + 1) // wl.ratio
+    for k in range(9):
+        g = run_scores(h, x, p0s, 1, wl.ratio)
+        same = torch.equal(g[..., :E].view(torch.int32), first[..., :E].view(torch.int32))
+        assert same, f"call {k + 2}: {(g[..., :E] != first[..., :E]).sum().item()} scores differ from the first call"
 
 
 @pytest.mark.parametrize("B,T,p0s", [(2, 1, [3001, 1000]), (1, 300, [0]), (2, 64, [2000, 37]), (3, 1, [0, 1, 2]),
@@ -199,6 +325,63 @@ def test_tail_group_workspace(handle):
     check_index(idx, top, x, p0s)
     out = run_attend(handle, x, idx, p0s)
     print(f"tail group: max abs / rel L2 = {check_attend(out, x, idx, p0s)}")
+
+
+# ------------------------------------------------------------------------ FP4 scale domain
+def wide_state(B, T, p0s, seed, scale_range):
+    p0s = np.asarray(p0s, np.int64)
+    cap = int(((p0s + T) // 2).max()) + 3
+    x = {}
+    x.update(inputs.layer_params(seed, DEV))
+    x.update(inputs.step_inputs(B, T, seed, DEV))
+    x.update(inputs.cache_state(B, T, int(p0s.max()), cap, seed, DEV, scale_range=scale_range))
+    return x, cap
+
+
+@pytest.mark.parametrize("B,T,p0s", [(2, 1, [6001, 3000]), (1, 40, [2000])])
+def test_index_wide_scale_range(handle, B, T, p0s):
+    """K^I scale bytes uniform over 100..140 (2^-27 .. 2^13, blocks of one key up to 40 binades
+    apart): every score and the top-512 sets still match the oracle.  Scales from 2^-23 up
+    decode exactly; below, values under 2^-24 round away, far inside the score tolerance."""
+    x, cap = wide_state(B, T, p0s, 61 + T, (100, 140))
+    check_scores(run_scores(handle, x, p0s, T), x, p0s)
+    idx, top = run_index(handle, x, p0s, T)
+    print(f"wide-scale index B={B} T={T}: near-tie swaps = {check_index(idx, top, x, p0s)}")
+    assert csa2.csa2_check(handle) == 0
+
+
+def test_attend_wide_scale_range(handle):
+    """Z scale bytes uniform over 100..127 (2^-27 .. 2^0; the bf16 outputs keep the absolute
+    tolerance meaningful): attention still matches the oracle."""
+    B, T, p0s = 3, 1, [9000, 700, 64000]
+    x, cap = wide_state(B, T, p0s, 71, (100, 127))
+    idx = random_indices(B, T, p0s, seed=7, device=DEV)
+    out = run_attend(handle, x, idx, p0s)
+    print(f"wide-scale attend: max abs / rel L2 = {check_attend(out, x, idx, p0s)}")
+    assert csa2.csa2_check(handle) == 0
+
+
+def test_scale_domain_is_reported(handle):
+    """An FP4 scale above 2^13 (byte 141) would overflow the fp16 tensor-core operands: the
+    kernels that read one record it and csa2_check returns CSA2_ERR_UNSUPPORTED once."""
+    B, T, p0s = 1, 1, [5000]
+    x, cap = make_state(B, T, p0s, seed=81)
+    assert csa2.csa2_check(handle) == 0
+    x["ki_scales"][0, 1234, 2] = 140  # the largest supported scale: no report
+    run_index(handle, x, p0s, T)
+    assert csa2.csa2_check(handle) == 0
+    x["ki_scales"][0, 1234, 2] = 141
+    run_index(handle, x, p0s, T)
+    assert csa2.csa2_check(handle) == 5
+    assert csa2.csa2_check(handle) == 0  # cleared
+    x["ki_scales"][0, 1234, 2] = 126
+    idx = random_indices(B, T, p0s, seed=8, device=DEV)
+    x["z_scales"][0, int(idx[0, 0, 3]), 7] = 141
+    run_attend(handle, x, idx, p0s)
+    assert csa2.csa2_check(handle) == 5
+    x["z_scales"][0, int(idx[0, 0, 3]), 7] = 140
+    run_attend(handle, x, idx, p0s)
+    assert csa2.csa2_check(handle) == 0
 
 
 # ------------------------------------------------------------------------ attention
