@@ -14,8 +14,8 @@
 // convert with one hardware instruction per pair; accumulation is fp32 in tensor memory.
 //
 // The per-head row sums l_h = sum_rows P[row, h] come from the tensor core too: a fifth O-phase
-// accumulator multiplies P^T by an all-ones A operand (one 1 KB swizzle atom addressed with a
-// zero row-group stride), so the softmax never reduces across lanes after the first chunk.
+// accumulator multiplies P^T by an all-ones A operand held in tensor memory (so those MMAs read
+// only P from shared memory), and the softmax never reduces across lanes after the first chunk.
 // Measured on GB300: a 128x64x16 fp16 MMA takes ~50 cycles and alternating between
 // accumulators costs more, so each accumulator receives its MMAs consecutively.
 //
@@ -52,10 +52,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.0f;                // lazy-rescale threshold (log2 units)
 // dynamic shared memory (1024-aligned): Q 8 atoms x [64 x 128 B], G 8 atoms x [128 x 128 B],
 // P [128 rows x 128 B], one 1 KB swizzle atom of fp16 ones
-constexpr uint32_t kQOff = 0, kGOff = 65536, kPOff = 196608, kOnesOff = 212992, kDynBytes = 214016 + 1024;
+constexpr uint32_t kQOff = 0, kGOff = 65536, kPOff = 196608, kDynBytes = 212992 + 1024;
 static_assert(kPOff - kGOff == kH * kD * 4, "the G area holds one fp32 output row (split partials)");
-// TMEM columns: O^T tiles at 0, 64, 128, 192; row sums at 256; S^T at 320
-constexpr uint32_t kTmemCols = 512, kLCol = 256, kSCol = 320;
+// TMEM columns: O^T tiles at 0, 64, 128, 192; row sums at 256; S^T at 320; at 384 the all-ones
+// A operand of the row-sum MMAs (128 lanes x 16 fp16 ones = 8 columns, written once per block)
+constexpr uint32_t kTmemCols = 512, kLCol = 256, kSCol = 320, kOnesCol = 384;
 
 __device__ int g_attend_error;
 // Set when a producer read a Z scale above 2^13 (scale byte > 140), where E2M1 x 2^e overflows
@@ -300,7 +301,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         *reinterpret_cast<uint4*>(sm + kQOff + (d0 >> 6) * 8192 + sw128_off(h, (d0 & 63) >> 3)) =
             make_uint4(o[0], o[1], o[2], o[3]);
       }
-      if (pidx < 64) *reinterpret_cast<uint4*>(sm + kOnesOff + 16 * pidx) = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.q_full);
@@ -379,10 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     if (lane == 0 && nloc > 0) {
       const uint32_t idS = idesc_f16(false, false, 128, 64);
       const uint32_t idO = idesc_f16(true, true, 128, 64);
-      const uint32_t idL = idesc_f16(false, true, 128, 64);  // ones (any layout) x P^T (MN-major)
+      const uint32_t idL = idesc_f16(false, true, 128, 64);  // ones (TMEM) x P^T (MN-major)
       const uint32_t gq = sbase + kQOff, gg = sbase + kGOff, gp = sbase + kPOff;
       mbar_wait(&bars.q_full, 0, err, 2);
-      const uint64_t ones_desc = sw128_desc(sbase + kOnesOff, 16, 0);  // every row group reads the same atom
       for (int i = 0; i < nloc; ++i) {
         // S^T = G_c Q^T into one accumulator.  Every wait of this thread stalls until its MMAs in
         // flight drain, so it waits for atoms 2 k2 and 2 k2 + 1 together (the two producer halves
@@ -414,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ss(tmem + kLCol, ones_desc, sw128_desc(gp + kk * 2048, 8192, 1024), idL, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tmem + kLCol, tmem + kOnesCol, sw128_desc(gp + kk * 2048, 8192, 1024), idL, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.l_done);
       }
     }
@@ -431,6 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
 #pragma unroll
       for (int h = 0; h < 32; ++h) x[h] = valid ? __uint_as_float(u[h]) * scale_log2 : -INFINITY;
     };
+    if (nloc > 0) {  // the row-sum MMAs' all-ones A operand; the first p_full arrive publishes it
+      uint32_t ones[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) ones[k] = 0x3C003C00u;
+      tmem_st16(lane_addr + kOnesCol, ones);
+      tmem_wait_st();
+    }
     for (int i = 0; i < nloc; ++i) {
       mbar_wait(&bars.s_full, i & 1, err, 5);
       tc_fence_after();

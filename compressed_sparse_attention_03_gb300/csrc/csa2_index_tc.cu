@@ -477,12 +477,6 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
                                                        (32 * q4 + lane) * 64);
 #pragma unroll
       for (int k = 0; k < 4; ++k) cw[k] = valid ? rc[k] : make_uint4(0u, 0u, 0u, 0u);
-      // The next bulk copy into this stage (async proxy) must not overtake these generic-proxy
-      // reads: without the proxy fence it sometimes did, and the first key row of a stage (the
-      // first bytes the next copy writes) was decoded from the following group's codes.
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_empty[s]);  // the codes are in registers
       const int slot = i % kDSlots;
       if (i >= kDSlots) mbar_wait(&bars.done[slot], ((i / kDSlots) - 1) & 1, err, 34);  // slot's last tile done
       tc_fence_after();
@@ -502,8 +496,17 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
       }
       tmem_wait_st();
       tc_fence_before();
+      // The stage goes back to the producer only now, after a proxy fence: its next bulk copy
+      // (async proxy) must not overtake these generic-proxy reads.  Without the fence it
+      // sometimes did, and the first key row of a stage (the first bytes the next copy writes)
+      // was decoded from the following group's codes.  Here the reads are long complete, so the
+      // fence costs little.
+      fence_proxy_async();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.a_full[slot]);
+      if (lane == 0) {
+        mbar_arrive(&bars.s_empty[s]);
+        mbar_arrive(&bars.a_full[slot]);
+      }
       sa = sb;
       sb = sc_next;
     }

@@ -3,7 +3,8 @@
 A model of the kernel's roles under random interleavings. The pipeline constants are read
 from the kernel source, so that the model follows the kernel.
 - The producer fills a ring of code stages, each holding a pair of key tiles.
-- Four decoder groups take tiles i = group mod 4 into TMEM A slots (i mod kDSlots).
+- Four decoder groups take tiles i = group mod 4 into TMEM A slots (i mod kDSlots), and give
+  a tile's stage back to the producer when they mark its slot full.
 - Two MMA issuers take even and odd tiles into accumulators i mod 4. Each issuer's MMAs
   complete asynchronously and in order.
 - The epilogue reads every accumulator in tile order.
@@ -103,7 +104,6 @@ def simulate(nt: int, seed: int) -> None:
             s = (d["i"] // GROUP) % STAGES
             assert stage[s] == d["i"] // GROUP, f"tile {d['i']}: stage {s} holds group {stage[s]}"
             d["read"] = True
-            s_empty[s].arrive()
         elif kind == "dec_write":
             d = dec[who]
             i, sl = d["i"], d["i"] % SLOTS
@@ -111,6 +111,8 @@ def simulate(nt: int, seed: int) -> None:
             assert prev in (None, i, i - SLOTS), f"slot {sl}: tile {prev} then {i}"
             assert prev in (None, i) or prev in mma_done, f"slot {sl} rewritten before tile {prev}'s MMAs completed"
             slot[sl] = i
+            # the stage is released with the slot (after the TMEM store and a proxy fence)
+            s_empty[(i // GROUP) % STAGES].arrive()
             a_full[sl].arrive()
             d["read"] = False
             d["i"] += GROUPS
