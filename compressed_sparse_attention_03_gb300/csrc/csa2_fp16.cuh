@@ -1,6 +1,6 @@
 // Exact FP4 (E2M1) / FP8 (E4M3) -> fp16 conversions for building tensor-core operands, with
-// power-of-two scales applied in fp16 (E2M1 x 2^e is exact in fp16 for -22 <= e <= 12; E4M3
-// values are always exact).
+// power-of-two scales applied in fp16 (E2M1 x 2^e is exact in fp16 for -23 <= e <= 13; E4M3
+// values are always exact), and the fp32 -> E5M2 conversion of the 8-bit indexer operands.
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -46,6 +46,15 @@ __device__ __forceinline__ uint32_t cvt_f32x2_e2m1x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
   uint32_t r;
   asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n}\n" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// Two fp32 values -> two E5M2 bytes in the low 16 bits, `lo` in the low byte: round to nearest
+// even, saturating at +-57344.  E2M1 x 2^e converts exactly for -15 <= e <= 13 (E5M2 has two
+// mantissa bits and exponents down to 2^-16 as subnormals).
+__device__ __forceinline__ uint32_t cvt_f32x2_e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %2, %1;\n" : "=h"(r) : "f"(lo), "f"(hi));
   return r;
 }
 

@@ -4,17 +4,20 @@
 //
 // As a GEMM: D[j, (t,h)] = K^I_j . Q^I_{t,h} with M = 128 keys, N = 256 = 8 queries x 32 heads,
 // K = 128; the epilogue thread that owns key j (one TMEM lane) forms the 8 scores
-// sum_h w_{t,h} ReLU(D[j, (t,h)]) in registers.  Both operands are the FP4 values decoded to
-// fp16 (E2M1 x 2^e is exact in fp16 for scale exponents -22..12): Q^I is quantised to FP4
-// here exactly as in the CUDA-core path, then written as 64 KB "images" per query tile, K^I
-// as 32 KB images per key tile, each image already in the 128B-swizzled K-major layout the
-// MMA reads, so that one bulk copy (cp.async.bulk) stages it.  Products of two E2M1 values
-// times powers of two are exact, and the fp32 accumulation of 128 of them is exact while
-// the block exponents of a row stay within ~10 of each other, as for the CUDA-core path.
+// sum_h w_{t,h} ReLU(D[j, (t,h)]) in registers.  Both operands are the FP4 values re-encoded
+// one per byte as E5M2 (E2M1 x 2^e is exact in E5M2 for scale exponents -15..13): Q^I is
+// quantised to FP4 here exactly as in the CUDA-core path, then written as 32 KB "images" per
+// query tile, K^I as 16 KB images per key tile, each image already in the 128B-swizzled
+// K-major layout the MMA reads, so that one bulk copy (cp.async.bulk) stages it.  The score
+// GEMM is four kind::f8f6f4 MMAs of K = 32 per key tile, one per 32-value scale block: within
+// one MMA all key values share a scale and so do a head's query values, so each MMA's sum of
+// 32 exact products is exact, and the fp32 accumulation across the four blocks is as for the
+// CUDA-core path.
 //
-// Persistent kernel, 256 threads: warp 0 issues the bulk copies, warp 1 allocates TMEM and
-// issues the MMAs, warps 4-7 run the epilogue.  A query tile's image stays resident
-// (double-buffered) while its causal key tiles stream through a 2-stage ring; accumulators
+// Persistent kernel, 384 threads: warp 0 issues the bulk copies, warp 1 allocates TMEM and
+// issues the MMAs, warps 4-11 run the epilogue (two warps per TMEM lane quarter, each taking
+// four of the tile's eight queries).  A query tile's image stays resident
+// (double-buffered) while its causal key tiles stream through a kAStages ring; accumulators
 // are double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile overlaps the
 // MMAs of the next.
 #include <cuda_fp16.h>
@@ -30,10 +33,14 @@ using namespace sm100;
 
 constexpr int kQPerTile = 8;                       // queries per query tile (N = 256)
 static_assert(kQPerTile % 2 == 0, "the epilogue reads two queries per TMEM wait");
-constexpr uint32_t kQImg = 65536, kKImg = 32768;   // bytes per image
-constexpr int kThreadsTC = 256;
-// dynamic smem: B (query images) 2 x 64 KB, A (key images) 2 x 32 KB, w^I 2 x [8][32] floats
-constexpr uint32_t kBOff = 0, kAOff = 131072, kWOff = 196608, kDynTC = 196608 + 2048 + 1024;
+constexpr uint32_t kQImg = 32768, kKImg = 16384;   // bytes per image: [256 | 128 rows][128 B] E5M2
+constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter, four queries each
+constexpr int kThreadsTC = 128 + 32 * kEpiWarps;
+constexpr int kAStages = 4;                        // key images in flight
+// dynamic smem: B (query images) 2 x 32 KB, A (key images) kAStages x 16 KB, w^I 2 x [8][32] floats,
+// score-key histograms [8 queries][kHistBins] of the current query tile
+constexpr uint32_t kBOff = 0, kAOff = 2 * kQImg, kWOff = kAOff + kAStages * kKImg, kHOff = kWOff + 2048,
+                   kDynTC = kHOff + kQPerTile * kHistBins * 4 + 1024;
 
 __device__ int g_index_error;
 // Set when a kernel here read an FP4 scale above 2^13 (scale byte > 140): E2M1 x 2^e no longer
@@ -42,9 +49,9 @@ __device__ unsigned g_index_domain;
 constexpr uint32_t kMaxScaleBytes = 0x8C8C8C8Cu;  // 140 in every byte: 2^13, the largest exact fp16 scale
 
 
-// Q^I (bf16) -> FP4 (E2M1, UE8M0 per 32) -> fp16 image.  grid (Tq, nb), 128 threads: warp w
+// Q^I (bf16) -> FP4 (E2M1, UE8M0 per 32) -> E5M2 image.  grid (Tq, nb), 128 threads: warp w
 // handles heads 8w..8w+7, lane l values 4l..4l+3.  Query t of the chunk lives in tile t/8,
-// rows (t%8)*32 + h of the tile's [256 x 128] K-major image (2 atoms of 64 dims).
+// rows (t%8)*32 + h of the tile's [256 x 128] K-major image (one 128-byte swizzle atom per row).
 __global__ void __launch_bounds__(128) qimage_kernel(IndexArgs a, int b0, int t0, int Tq, int nqt, uint8_t* qimg,
                                                      float* wq) {
   const int tl = blockIdx.x, bl = blockIdx.y;
@@ -67,26 +74,19 @@ __global__ void __launch_bounds__(128) qimage_kernel(IndexArgs a, int b0, int t0
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     const int e = mx_scale_exp(amax);
     if (e > 13 && l == 0) atomicOr(&g_index_domain, 1u);
-    const float down = pow2f(-e);  // exact power of two
-    uint2 img;
-    if (e >= -24 && e <= 15) {  // 2^e is an fp16 number: code x 2^e rounds exactly as via fp32
-      const uint32_t s2 = pow2_h2(e);
-      img.x = hmul2(cvt_e2m1x2_f16x2(cvt_f32x2_e2m1x2(v[0] * down, v[1] * down)), s2);
-      img.y = hmul2(cvt_e2m1x2_f16x2(cvt_f32x2_e2m1x2(v[2] * down, v[3] * down)), s2);
-    } else {
-      const float up = pow2f(e);
-      float q[4];
+    const float down = pow2f(-e), up = pow2f(e);  // exact powers of two
+    float q[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) q[i] = e2m1_to_f32(f32_to_e2m1(v[i] * down)) * up;
-      img = make_uint2(f2_to_h2(q[0], q[1]), f2_to_h2(q[2], q[3]));
-    }
+    for (int i = 0; i < 4; ++i) q[i] = e2m1_to_f32(f32_to_e2m1(v[i] * down)) * up;
+    const uint32_t img = cvt_f32x2_e5m2x2(q[0], q[1]) | (cvt_f32x2_e5m2x2(q[2], q[3]) << 16);
     const int n = (tl % kQPerTile) * kHI + h, d = 4 * l;
-    *reinterpret_cast<uint2*>(tile + (d >> 6) * 32768 + sw128_off(n, (d & 63) >> 3) + (d & 7) * 2) = img;
+    *reinterpret_cast<uint32_t*>(tile + sw128_off(n, d >> 4) + (d & 15)) = img;
   }
   if (threadIdx.x < kHI) wq[((int64_t)bl * Tq + tl) * kHI + threadIdx.x] = bf16_to_f32(a.wI[src * kHI + threadIdx.x]);
 }
 
-// K^I (FP4) -> fp16 image.  grid (key tiles, nb), 128 threads: thread = key of the tile.
+// K^I (FP4) -> E5M2 image.  grid (key tiles, nb), 128 threads: thread = key of the tile, its 128
+// values one byte each in row r of the tile's [128 x 128] 128B-swizzled image.
 __global__ void __launch_bounds__(128) kimage_kernel(IndexArgs a, int b0, int64_t n_keys, int nkt, uint8_t* kimg) {
   const int kt = blockIdx.x, bl = blockIdx.y;
   const int b = b0 + bl;
@@ -107,24 +107,25 @@ __global__ void __launch_bounds__(128) kimage_kernel(IndexArgs a, int b0, int64_
   }
 #pragma unroll
   for (int blk = 0; blk < 4; ++blk) {  // 32 values: 16 bytes of codes, one scale byte
-    const float s = ldexpf(1.0f, (int)((sc >> (8 * blk)) & 255u) - 127);
+    const float s = pow2f((int)((sc >> (8 * blk)) & 255u) - 127);
     const uint32_t wd[4] = {c[blk].x, c[blk].y, c[blk].z, c[blk].w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {  // 8 values = one 16-byte chunk of fp16
+    for (int q = 0; q < 2; ++q) {  // 16 values = one 16-byte chunk of E5M2
       uint32_t o[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t byte = (wd[q] >> (8 * k)) & 255u;
-        o[k] = f2_to_h2(e2m1_to_f32(byte & 15u) * s, e2m1_to_f32(byte >> 4) * s);
+        const uint32_t word = wd[2 * q + (k >> 1)] >> (16 * (k & 1));  // four values: two code bytes
+        const float v0 = e2m1_to_f32(word & 15u) * s, v1 = e2m1_to_f32((word >> 4) & 15u) * s;
+        const float v2 = e2m1_to_f32((word >> 8) & 15u) * s, v3 = e2m1_to_f32((word >> 12) & 15u) * s;
+        o[k] = cvt_f32x2_e5m2x2(v0, v1) | (cvt_f32x2_e5m2x2(v2, v3) << 16);
       }
-      const int d = 32 * blk + 8 * q;
-      *reinterpret_cast<uint4*>(tile + (d >> 6) * 16384 + sw128_off(r, (d & 63) >> 3)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(tile + sw128_off(r, 2 * blk + q)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
 
 struct TcBars {
-  uint64_t b_full[2], b_free[2], a_full[2], a_free[2], d_full[2], d_free[2];
+  uint64_t b_full[2], b_free[2], a_full[kAStages], a_free[kAStages], d_full[2], d_free[2];
 };
 
 // The static schedule: in round r CTA c takes query tile r*G + c (even rounds) or
@@ -135,16 +136,40 @@ __device__ __forceinline__ int tile_of(int round, int G, int ntiles) {
   return idx < ntiles ? idx : -1;
 }
 
+// Lower edge (a score key) of the histogram bin that holds the K-th largest counted key, found
+// by one warp: every key among the K largest is >= it.  0 when fewer than K keys were counted.
+// Steps of 32 consecutive bins from the top (lane l: bin base - l, so the loads are free of bank
+// conflicts), a running count, and a stop at the first step that reaches K.
+__device__ uint32_t warp_hist_lower(const uint32_t* hist, int K, int lane) {
+  uint32_t carry = 0;
+  for (int base = kHistBins - 1; base >= 0; base -= 32) {
+    const uint32_t c = hist[base - lane];
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const uint32_t hit = __ballot_sync(0xffffffffu, carry + incl >= (uint32_t)K);
+    if (hit) return (uint32_t)(base - (__ffs(hit) - 1)) << kHistShift;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return 0u;
+}
+
+// lower_out (optional) [nb * Tq]: per query row, the histogram lower edge of its top-512 (keys
+// below it cannot be selected), for the select that follows.
 __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexArgs a, SeqPos pos, int t0, int tq, int nqt,
                                                                          int nkt, const uint8_t* qimg, const uint8_t* kimg,
                                                                          const float* wq, float* scores, int64_t ld,
-                                                                         int nb, int Tq) {
+                                                                         int nb, int Tq, uint32_t* lower_out) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ TcBars bars;
   __shared__ uint32_t tmem_base_sh;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   unsigned char* sm = smem_raw + (sbase - smem_u32(smem_raw));
   float* sw = reinterpret_cast<float*>(sm + kWOff);  // [2][8][32]
+  uint32_t* shist = reinterpret_cast<uint32_t*>(sm + kHOff);  // [8][kHistBins]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nqt_act = (tq + kQPerTile - 1) / kQPerTile;  // query tiles of this pass (image stride: nqt)
   const int G = gridDim.x, ntiles = nb * nqt_act;
@@ -154,10 +179,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.b_full[i], 1);
       mbar_init(&bars.b_free[i], 1);
+      mbar_init(&bars.d_full[i], 1);
+      mbar_init(&bars.d_free[i], kEpiWarps);
+    }
+    for (int i = 0; i < kAStages; ++i) {
       mbar_init(&bars.a_full[i], 1);
       mbar_init(&bars.a_free[i], 1);
-      mbar_init(&bars.d_full[i], 1);
-      mbar_init(&bars.d_free[i], 4);
     }
     mbar_fence_init();
   }
@@ -191,13 +218,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
         if (qi >= 2) mbar_wait(&bars.b_free[sB], ((qi >> 1) - 1) & 1, err, 11);
         mbar_arrive_expect_tx(&bars.b_full[sB], kQImg);
         const uint8_t* qsrc = qimg + ((int64_t)bl * nqt + qt) * kQImg;
-        for (int c = 0; c < 4; ++c) bulk_g2s(sm + kBOff + sB * kQImg + c * 16384, qsrc + c * 16384, 16384, &bars.b_full[sB]);
+        for (int c = 0; c < 2; ++c) bulk_g2s(sm + kBOff + sB * kQImg + c * 16384, qsrc + c * 16384, 16384, &bars.b_full[sB]);
         for (int kt = 0; kt < nk; ++kt, ++it) {
-          const int sA = it & 1;
-          if (it >= 2) mbar_wait(&bars.a_free[sA], ((it >> 1) - 1) & 1, err, 12);
+          const int sA = it % kAStages;
+          if (it >= kAStages) mbar_wait(&bars.a_free[sA], ((it / kAStages) - 1) & 1, err, 12);
           mbar_arrive_expect_tx(&bars.a_full[sA], kKImg);
-          const uint8_t* ksrc = kimg + ((int64_t)bl * nkt + kt) * kKImg;
-          for (int c = 0; c < 2; ++c) bulk_g2s(sm + kAOff + sA * kKImg + c * 16384, ksrc + c * 16384, 16384, &bars.a_full[sA]);
+          bulk_g2s(sm + kAOff + sA * kKImg, kimg + ((int64_t)bl * nkt + kt) * kKImg, kKImg, &bars.a_full[sA]);
         }
         ++qi;
       }
@@ -205,7 +231,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(false, false, 128, 256);
+      const uint32_t idesc = idesc_e5m2(128, 256);
       int it = 0, qi = 0, dc = 0;
       for (int k = 0; k * G < ntiles; ++k) {
         const int tile = tile_of(k, G, ntiles);
@@ -216,17 +242,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
         const int sB = qi & 1;
         mbar_wait(&bars.b_full[sB], (qi >> 1) & 1, err, 13);
         for (int kt = 0; kt < nk; ++kt, ++it, ++dc) {
-          const int sA = it & 1, sD = dc & 1;
-          mbar_wait(&bars.a_full[sA], (it >> 1) & 1, err, 14);
+          const int sA = it % kAStages, sD = dc & 1;
+          mbar_wait(&bars.a_full[sA], (it / kAStages) & 1, err, 14);
           if (dc >= 2) mbar_wait(&bars.d_free[sD], ((dc >> 1) - 1) & 1, err, 15);
           tc_fence_after();
           const uint32_t abase = sbase + kAOff + sA * kKImg, bbase = sbase + kBOff + sB * kQImg;
 #pragma unroll
-          for (int k16 = 0; k16 < 8; ++k16) {
-            const uint32_t atom = k16 >> 2, off = (k16 & 3) * 32;
-            mma_f16_ss(tmem + 256 * sD, sw128_desc(abase + atom * 16384 + off, 16, 1024),
-                       sw128_desc(bbase + atom * 32768 + off, 16, 1024), idesc, k16 > 0);
-          }
+          for (int k32 = 0; k32 < 4; ++k32)  // one MMA per 32-value scale block (32 bytes of each row)
+            mma_f8_ss(tmem + 256 * sD, sw128_desc(abase + k32 * 32, 16, 1024), sw128_desc(bbase + k32 * 32, 16, 1024),
+                      idesc, k32 > 0);
           mma_commit(&bars.a_free[sA]);
           mma_commit(&bars.d_full[sD]);
         }
@@ -236,8 +260,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
     }
   } else if (warp >= 4) {
     // ============================================================ epilogue
-    const int ew = warp - 4, r = 32 * ew + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * ew) << 16);
+    // warp 4 + 4*half + quarter: keys 32*quarter .. (its TMEM lane quarter), queries 4*half .. +3
+    const int ew = warp - 4, quarter = ew & 3, half = ew >> 2, r = 32 * quarter + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
+    constexpr int kEpiThreads = 32 * kEpiWarps;
     int dc = 0, qi = 0;
     for (int k = 0; k * G < ntiles; ++k) {
       const int tile = tile_of(k, G, ntiles);
@@ -246,22 +272,28 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
       const int nk = n_key_tiles(bl, qt);
       if (nk == 0) continue;
       float* wsm = sw + (qi & 1) * 256;
-      named_bar_sync(2, 128);  // the previous use of this w buffer is finished
-      for (int i = r; i < 256; i += 128) {
+      named_bar_sync(2, kEpiThreads);  // the previous use of this w buffer and of the histograms is finished
+      for (int i = tid - 128; i < 256; i += kEpiThreads) {
         const int tl = qt * kQPerTile + i / kHI;
         wsm[i] = tl < tq ? wq[((int64_t)bl * Tq + tl) * kHI + (i % kHI)] : 0.f;
       }
-      named_bar_sync(2, 128);
+      if (lower_out)
+        for (int i = tid - 128; i < kQPerTile * kHistBins; i += kEpiThreads) shist[i] = 0u;
+      named_bar_sync(2, kEpiThreads);
       const int64_t p0 = pos.p0[bl] + t0;
+      // key tiles below this bound are visible to all eight queries (the first has the fewest)
+      const int64_t e_first = (p0 + qt * kQPerTile + 1) >> a.rshift;
+      const bool all_queries = qt * kQPerTile + kQPerTile <= tq;
       for (int kt = 0; kt < nk; ++kt, ++dc) {
         const int sD = dc & 1;
         mbar_wait(&bars.d_full[sD], (dc >> 1) & 1, err, 16);
         tc_fence_after();
         const int64_t j = (int64_t)kt * 128 + r;
-        // two queries per TMEM wait, and four independent partial sums per query (heads h mod 4),
-        // so that one warp per sub-partition is not held by load waits and one long FMA chain
+        const bool full = all_queries && (int64_t)(kt + 1) * 128 <= e_first;
+        // two queries per TMEM wait, and four independent partial sums per query (heads h mod 4,
+        // two packed pairs), so that one warp per sub-partition is not held by load waits
 #pragma unroll 1
-        for (int q = 0; q < kQPerTile; q += 2) {
+        for (int q = 4 * half; q < 4 * half + 4; q += 2) {
           uint32_t u[2][32];
           tmem_ld32(lane_addr + 256 * sD + 32 * q, u[0]);
           tmem_ld32(lane_addr + 256 * sD + 32 * (q + 1), u[1]);
@@ -270,22 +302,36 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
           for (int e = 0; e < 2; ++e) {
             const int tl = qt * kQPerTile + q + e;
             const float4* w4 = reinterpret_cast<const float4*>(wsm + 32 * (q + e));
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int h4 = 0; h4 < 8; ++h4) {
               const float4 w = w4[h4];
-              s[0] = fmaf(w.x, fmaxf(__uint_as_float(u[e][4 * h4]), 0.f), s[0]);
-              s[1] = fmaf(w.y, fmaxf(__uint_as_float(u[e][4 * h4 + 1]), 0.f), s[1]);
-              s[2] = fmaf(w.z, fmaxf(__uint_as_float(u[e][4 * h4 + 2]), 0.f), s[2]);
-              s[3] = fmaf(w.w, fmaxf(__uint_as_float(u[e][4 * h4 + 3]), 0.f), s[3]);
+              s01 = fma2(make_float2(w.x, w.y),
+                         make_float2(fmaxf(__uint_as_float(u[e][4 * h4]), 0.f), fmaxf(__uint_as_float(u[e][4 * h4 + 1]), 0.f)),
+                         s01);
+              s23 = fma2(make_float2(w.z, w.w),
+                         make_float2(fmaxf(__uint_as_float(u[e][4 * h4 + 2]), 0.f), fmaxf(__uint_as_float(u[e][4 * h4 + 3]), 0.f)),
+                         s23);
             }
-            if (tl < tq && j < ((p0 + tl + 1) >> a.rshift))
-              scores[((int64_t)bl * Tq + tl) * ld + j] = (s[0] + s[1]) + (s[2] + s[3]);
+            if (full || (tl < tq && j < ((p0 + tl + 1) >> a.rshift))) {
+              const float sc = (s01.x + s01.y) + (s23.x + s23.y);
+              scores[((int64_t)bl * Tq + tl) * ld + j] = sc;
+              if (lower_out) atomicAdd(&shist[(q + e) * kHistBins + (score_key(sc) >> kHistShift)], 1u);
+            }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.d_free[sD]);
+      }
+      if (lower_out) {  // warp ew: the lower edge of query ew's top-512 from its histogram
+        named_bar_sync(2, kEpiThreads);  // every count of this query tile is in
+        const int tl = qt * kQPerTile + ew;
+        if (tl < tq) {
+          const int64_t E = (p0 + tl + 1) >> a.rshift;
+          const uint32_t lo = warp_hist_lower(shist + ew * kHistBins, (int)min64(kTopK, E), lane);
+          if (lane == 0) lower_out[(int64_t)bl * Tq + tl] = lo;
+        }
       }
       ++qi;
     }
@@ -631,26 +677,28 @@ size_t index_tc_image_bytes(int nb, int Tq, int64_t max_entries) {
 }
 
 cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq, int Tq,
-                                   int64_t emax, uint8_t* img, float* wq, float* scores, int64_t ld, int num_sms,
-                                   cudaStream_t st) {
+                                   int64_t emax, int64_t emax_all, bool build_keys, uint8_t* img, float* wq,
+                                   float* scores, int64_t ld, uint32_t* lower, int num_sms, cudaStream_t st) {
   const int nqt = (Tq + kQPerTile - 1) / kQPerTile;
-  const int nkt = (int)((emax + 127) / 128);
+  const int nkt = (int)((emax_all + 127) / 128);  // key images of every pass of the call: one stride
   uint8_t* qimg = img;
   uint8_t* kimg = img + (size_t)nb * nqt * kQImg;
   qimage_kernel<<<dim3((unsigned)tq, (unsigned)nb), 128, 0, st>>>(a, b0, t0, Tq, nqt, qimg, wq);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (nkt > 0) {
-    kimage_kernel<<<dim3((unsigned)nkt, (unsigned)nb), 128, 0, st>>>(a, b0, emax, nkt, kimg);
+  if (build_keys && nkt > 0) {  // once per call, for the entries visible to its last query
+    kimage_kernel<<<dim3((unsigned)nkt, (unsigned)nb), 128, 0, st>>>(a, b0, emax_all, nkt, kimg);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  (void)emax;
   e = cudaFuncSetAttribute(index_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynTC);
   if (e != cudaSuccess) return e;
   const int ntiles = nb * ((tq + kQPerTile - 1) / kQPerTile);
   const int grid = max(1, min(num_sms, ntiles));
-  index_prefill_tc_kernel<<<grid, kThreadsTC, kDynTC, st>>>(a, pos, t0, tq, nqt, nkt, qimg, kimg, wq, scores, ld, nb, Tq);
+  index_prefill_tc_kernel<<<grid, kThreadsTC, kDynTC, st>>>(a, pos, t0, tq, nqt, nkt, qimg, kimg, wq, scores, ld, nb, Tq,
+                                                             lower);
   note_launch();
   return cudaGetLastError();
 }

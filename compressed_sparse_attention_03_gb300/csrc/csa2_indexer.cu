@@ -35,13 +35,14 @@ struct IndexPlan {
   bool tc;          // prefill: tensor-core score GEMM (queries per pass >= kMinTcQueries)
   int pnch;         // hierarchical pool: chunks of kPoolChunk blocks (pool mode)
   bool dec;         // scores from the per-query scan (one query, or a pool), with histograms
-  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, off_img, off_rl, off_pk, off_pj, off_pn, off_h, total;
+  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, off_img, off_rl, off_pk, off_pj, off_pn, off_h, off_lo, total;
 };
 
 constexpr int kPoolChunk = 16384;             // blocks per chunk of the pool select
 constexpr int kPoolSel = kHsiBlocks - 1;      // best other blocks; the newest is always added
 
 constexpr int kMinTcQueries = 8;
+constexpr int64_t kMinHistRow = 16384;  // prefill rows this long get the scorer's histogram filter
 
 IndexPlan make_plan(int nb, int T, int64_t max_entries, int mode = kIndexTopk) {
   IndexPlan p;
@@ -75,6 +76,7 @@ IndexPlan make_plan(int nb, int T, int64_t max_entries, int mode = kIndexTopk) {
   p.off_pj = off; off += align256(rows * p.pnch * kPoolSel * 4);
   p.off_pn = off; off += align256(rows * p.pnch * 4);
   p.off_h = off; off += p.dec && !so ? align256(rows * kHistBins * 4) : 0;
+  p.off_lo = off; off += p.tc && !so ? align256(rows * 4) : 0;  // per-row lower edges from the prefill scorer
   p.total = off;
   return p;
 }
@@ -402,16 +404,17 @@ __device__ uint32_t hist_lower(const uint32_t* hist, int K, SelectShared<kTopkTh
   return sh.bucket;
 }
 
-// With hist (the row's score histogram), a chunk whose keys at or above the K-th largest
-// key's bin number at most 512 passes exactly those on (a superset of its part of the row's
-// top-512, in position order) and skips the radix select.  NT threads per block: rows with a
+// With hist (the row's score histogram) or lower_in (the lower edge of that bin, from the prefill
+// scorer), a chunk whose keys at or above the K-th largest key's bin number at most 512 passes
+// exactly those on (a superset of its part of the row's top-512, in position order) and skips
+// the radix select.  NT threads per block: rows with a
 // histogram take kTopkThreads (hist_lower reads four bins per thread); the others take
 // kTopkSmall, so that several rows share an SM and hide one another's barrier latency.
 template <int NT>
 __global__ void __launch_bounds__(NT) topk_chunk_kernel(IndexArgs a, SeqPos pos, int b0, int t0, int Tq,
                                                         const float* scores, int64_t ld, int chunk, int nchunks,
                                                         uint32_t* ck, int32_t* cj, int* cn, const int* rowlen,
-                                                        const uint32_t* hist) {
+                                                        const uint32_t* hist, const uint32_t* lower_in) {
   extern __shared__ uint32_t skeys[];
   __shared__ SelectShared<NT> sh;
   __shared__ uint32_t okey[kTopK];
@@ -425,11 +428,14 @@ __global__ void __launch_bounds__(NT) topk_chunk_kernel(IndexArgs a, SeqPos pos,
   const int64_t E = rowlen ? rowlen[row] : (pos.p0[bl] + t + 1) >> a.rshift;
   const int64_t cs = (int64_t)c * chunk;
   const int n = (int)max64(0, min64(chunk, E - cs));
-  // the candidates' lower bound, before the loads (the histogram is complete)
+  // the candidates' lower bound, before the loads: from the row's score histogram, or as the
+  // prefill scorer computed it from its own (lower_in)
   uint32_t lower = 0u;
   if constexpr (NT == kTopkThreads)
     if (hist && n > kTopK) lower = hist_lower(hist + row * kHistBins, (int)min64(kTopK, E), sh);
+  if (lower_in && n > kTopK) lower = __ldg(lower_in + row);
   const float* src = scores + row * ld + cs;  // 16-byte aligned: ld and the chunk are multiples of 32
+  int K = min(kTopK, n);  // entries in okey / oj
   const int n4 = n >> 2;
   constexpr int kLB = 4;  // 16-byte loads in flight per thread
   for (int v0 = threadIdx.x; v0 < n4; v0 += kLB * NT) {
@@ -446,7 +452,6 @@ __global__ void __launch_bounds__(NT) topk_chunk_kernel(IndexArgs a, SeqPos pos,
   for (int i = 4 * n4 + threadIdx.x; i < n; i += NT) skeys[i] = score_key(src[i]);
   if (threadIdx.x == 0) cnt_sh = 0;
   __syncthreads();
-  int K = min(kTopK, n);  // entries in okey / oj
   if (n <= kTopK) {  // every candidate is kept, already in position order
     for (int i = threadIdx.x; i < n; i += NT) {
       okey[i] = skeys[i];
@@ -705,6 +710,11 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
   int* cn = reinterpret_cast<int*>(base + p.off_cn);
   int* rowlen = mode == kIndexReindex ? reinterpret_cast<int*>(base + p.off_rl) : nullptr;
   uint32_t* hist = p.dec && !so ? reinterpret_cast<uint32_t*>(base + p.off_h) : nullptr;
+  // Lower edges from the prefill scorer's histograms pay off only for long rows: with a few
+  // thousand keys the select is cheap, and the histograms' set-up per query tile is not.
+  int64_t emax_all = 0;  // entries visible to the call's last query, over this launch's sequences
+  for (int i = 0; i < nb; ++i) emax_all = max(emax_all, (pos.p0[i] + a.T) >> a.rshift);
+  uint32_t* lower = p.tc && !so && emax_all >= kMinHistRow ? reinterpret_cast<uint32_t*>(base + p.off_lo) : nullptr;
   uint32_t* pk = reinterpret_cast<uint32_t*>(base + p.off_pk);
   int32_t* pj = reinterpret_cast<int32_t*>(base + p.off_pj);
   int* pn = reinterpret_cast<int*>(base + p.off_pn);
@@ -737,8 +747,8 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
       if (e != cudaSuccess) return e;
       emax = min64(emax, (int64_t)kHsiBlock * kHsiBlocks);
     } else if (p.tc) {
-      e = launch_index_scores_tc(a, pos, b0, nb, t0, tq, p.Tq, emax, reinterpret_cast<uint8_t*>(base + p.off_img), wq, sc,
-                                 ld, num_sms, st);
+      e = launch_index_scores_tc(a, pos, b0, nb, t0, tq, p.Tq, emax, emax_all, t0 == 0,
+                                 reinterpret_cast<uint8_t*>(base + p.off_img), wq, sc, ld, lower, num_sms, st);
       if (e != cudaSuccess) return e;
     } else if (a.T == 1) {
       if (emax > 0) {
@@ -760,10 +770,10 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
     const int nch = (int)max64(1, (emax + p.chunk - 1) / p.chunk);
     if (hist)
       topk_chunk_kernel<kTopkThreads><<<dim3(nch, tq, nb), kTopkThreads, chunk_smem, st>>>(
-          a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch, ck, cj, cn, rowlen, hist);
+          a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch, ck, cj, cn, rowlen, hist, nullptr);
     else
       topk_chunk_kernel<kTopkSmall><<<dim3(nch, tq, nb), kTopkSmall, chunk_smem, st>>>(
-          a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch, ck, cj, cn, rowlen, nullptr);
+          a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch, ck, cj, cn, rowlen, nullptr, lower);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (nch > 1) {

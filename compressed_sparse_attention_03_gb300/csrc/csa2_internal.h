@@ -77,9 +77,13 @@ size_t index_workspace_bytes(int B, int T, int64_t max_entries, int num_sms, int
 cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int64_t max_entries,
                               void* ws, size_t ws_bytes, int num_sms, cudaStream_t st, int mode = kIndexTopk);
 size_t index_tc_image_bytes(int nb, int Tq, int64_t max_entries);
+// Prefill score GEMM for the pass t0 .. t0+tq-1: emax = visible entries of the pass's last query,
+// emax_all = of the call's last query (the key-image stride); build_keys: write the key images
+// (once per call, on its first pass).  lower (optional) [nb * Tq] receives per query row the
+// lower edge of the score-key histogram bin that holds its 512th largest score.
 cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq, int Tq,
-                                   int64_t emax, uint8_t* img, float* wq, float* scores, int64_t ld, int num_sms,
-                                   cudaStream_t st);
+                                   int64_t emax, int64_t emax_all, bool build_keys, uint8_t* img, float* wq,
+                                   float* scores, int64_t ld, uint32_t* lower, int num_sms, cudaStream_t st);
 // One query row per (sequence, t) of the pass t0 .. t0+tq-1 (T == 1, or a pool scan); row r =
 // bl * Tq + tl.  With a.pool_in, row r's positions are its pool's entries and rowlen[r]
 // receives the number of visible ones.

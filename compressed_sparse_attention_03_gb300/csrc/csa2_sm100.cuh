@@ -1,7 +1,7 @@
 // Blackwell (sm_100 family, built for sm_103a) primitives as inline PTX: mbarriers with
 // bounded waits, tensor memory (TMEM) allocation and loads/stores, shared-memory matrix
-// descriptors for 128-byte-swizzled operands, and tcgen05.mma (kind::f16: f16 or bf16 operands, fp32 accumulate)
-// with tcgen05.commit.
+// descriptors for 128-byte-swizzled operands, and tcgen05.mma (kind::f16: f16 or bf16 operands;
+// kind::f8f6f4 with E5M2 operands; fp32 accumulate) with tcgen05.commit.
 //
 // Every wait is bounded: after kSpinLimit failed polls the waiter records an error code in
 // the library's device error word and gives up, so that a broken pipeline ends instead of
@@ -118,8 +118,8 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
-// (tcgen05.mma operands).
+// Orders this thread's generic-proxy shared-memory accesses before later async-proxy ones: its
+// writes before tcgen05.mma operand reads, its reads before a bulk copy that overwrites them.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -207,6 +207,23 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 __host__ __device__ constexpr uint32_t idesc_f16(bool a_mn_major, bool b_mn_major, int M, int N, bool bf16 = false) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with E5M2 A and B (format 1 in bits 7-9 / 10-12), fp32
+// D, both K-major: the other fields as in idesc_f16.
+__host__ __device__ constexpr uint32_t idesc_e5m2(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T for kind::f8f6f4 (8-bit operands, K = 32 per instruction: 32
+// bytes of each row); one elected thread issues.
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one elected thread issues.
