@@ -19,7 +19,7 @@
 // Measured on GB300: a 128x64x16 fp16 MMA takes ~50 cycles and alternating between
 // accumulators costs more, so each accumulator receives its MMAs consecutively.
 //
-// Warp roles (416 threads):
+// Warp roles (448 threads):
 //   warps 0-3   softmax (thread = TMEM lane = row of S^T), then the row sums and 1/denominator;
 //               with the producers, the output epilogue (thread = TMEM lane = dim of O^T)
 //   warps 4-11  producers: Q -> smem once, then gather + decode 128 rows per chunk, two
@@ -27,7 +27,10 @@
 //               wait in registers while chunk c is consumed and are written as soon as the
 //               O MMAs free each 128-dim tile.  Both threads of a row sit in one warp and
 //               work on the same tile at each step, so no lane waits for a later tile.
-//   warp 12     TMEM allocation and the single MMA-issuing thread
+//   warp 12     TMEM allocation and the thread issuing the S MMAs
+//   warp 13     the thread issuing the O and row-sum MMAs: while one issuer waits (and its MMAs
+//               drain) the other keeps the tensor pipe busy, so the next chunk's S MMAs overlap
+//               this chunk's O MMAs
 // Online softmax with a lazy reference: a head's reference m only moves when a chunk's
 // maximum exceeds it by more than kTau (log2 units), so P <= 2^kTau and O is rescaled in
 // TMEM rarely (in practice only at the first chunk, where there is nothing to rescale).
@@ -44,7 +47,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 416;
+constexpr int kThreads = 448;
 constexpr int kRows = 128;                  // rows per chunk
 constexpr int kMaxRows = kWin + kTopK;      // 640
 constexpr int kMaxChunks = kMaxRows / kRows;
@@ -354,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
         // in the softmax warps), then their share of p_full.  The tiles of the chunk are
         // written, so the raw registers are free until load(i + 1).
         mbar_wait(&bars.s_full, i & 1, err, 10);
+        if (i > 0) mbar_wait(&bars.l_done, (i - 1) & 1, err, 12);  // P of the last chunk has been read
         tc_fence_after();
         const int r = 32 * (warp & 3) + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -375,17 +379,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
       if (i + 1 < nloc) load(i + 1);
     }
   } else if (warp == 12) {
-    // ============================================================ MMA issuer
+    // ============================================================ S issuer
     if (lane == 0 && nloc > 0) {
       const uint32_t idS = idesc_f16(false, false, 128, 64);
-      const uint32_t idO = idesc_f16(true, true, 128, 64);
-      const uint32_t idL = idesc_f16(false, true, 128, 64);  // ones (TMEM) x P^T (MN-major)
-      const uint32_t gq = sbase + kQOff, gg = sbase + kGOff, gp = sbase + kPOff;
+      const uint32_t gq = sbase + kQOff, gg = sbase + kGOff;
       mbar_wait(&bars.q_full, 0, err, 2);
       for (int i = 0; i < nloc; ++i) {
-        // S^T = G_c Q^T into one accumulator.  Every wait of this thread stalls until its MMAs in
-        // flight drain, so it waits for atoms 2 k2 and 2 k2 + 1 together (the two producer halves
-        // write them at the same time).
+        // S^T = G_c Q^T into one accumulator.  The softmax has read the last chunk's S^T by then:
+        // the atoms of chunk c are refilled only after the O MMAs of chunk c-1, which the other
+        // thread issues after p_full.  Every wait of this thread stalls until its MMAs in flight
+        // drain, so it waits for atoms 2 k2 and 2 k2 + 1 together (the two producer halves write
+        // them at the same time); the O issuer's MMAs keep the tensor pipe busy meanwhile.
         for (int k2 = 0; k2 < 4; ++k2) {
           mbar_wait(&bars.atom_full[2 * k2], i & 1, err, 3);
           mbar_wait(&bars.atom_full[2 * k2 + 1], i & 1, err, 3);
@@ -400,6 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
           }
         }
         mma_commit(&bars.s_full);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 13) {
+    // ============================================================ O issuer
+    if (lane == 0 && nloc > 0) {
+      const uint32_t idO = idesc_f16(true, true, 128, 64);
+      const uint32_t idL = idesc_f16(false, true, 128, 64);  // ones (TMEM) x P^T (MN-major)
+      const uint32_t gg = sbase + kGOff, gp = sbase + kPOff;
+      for (int i = 0; i < nloc; ++i) {
         mbar_wait(&bars.p_full, i & 1, err, 4);
         tc_fence_after();
         // O^T tiles one after the other in the order the producers refill them (each frees its
@@ -439,6 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
     }
     for (int i = 0; i < nloc; ++i) {
       mbar_wait(&bars.s_full, i & 1, err, 5);
+      // P is rewritten below: the last chunk's O and row-sum MMAs (the other issuer) must have read it
+      if (i > 0) mbar_wait(&bars.l_done, (i - 1) & 1, err, 11);
       tc_fence_after();
       const bool valid = (c_begin + i) * kRows + r < n;
       // Heads 0..31 here, 32..63 in producer warps 4-7 (same rows: lane quarter warp % 4); barriers

@@ -1,5 +1,5 @@
 """The attention kernel's synchronisation protocol (attend_tc_kernel, one query), checked on
-the CPU: a model of its 13 warps under random interleavings.
+the CPU: a model of its 14 warps under random interleavings.
 
 Roles, as in the kernel:
 - **Producer warps 4-11.** Each converts its share of Q and arrives on q_full, then meets the
@@ -8,9 +8,13 @@ Roles, as in the kernel:
 - **Producer warps 4-7 also** take heads 32-63 of each chunk's softmax.
 - **Softmax warps 0-3** take heads 0-31, and alone run the rare "new reference" path (O and
   the row sums rescaled in TMEM).
-- **One MMA thread.** S over the eight atoms, then (after p_full) the four O tiles and the
-  row sums, with commits to s_full, tile_free[m] and l_done. The MMAs run asynchronously, in
-  issue order.
+- **Two MMA threads.** The S thread issues S over the eight atoms as they fill and commits to
+  s_full (the atoms are refilled only after the last chunk's O MMAs, which follow p_full, so S
+  is overwritten only after every warp read it). The O thread issues the
+  four O tiles and the row sums after p_full, with commits to tile_free[m] and l_done. Each
+  thread's MMAs run asynchronously and in its own issue order; the two streams interleave in
+  any order, and a commit covers only its own thread's MMAs.
+- **Softmax and helpers** wait for l_done of the last chunk before they rewrite P.
 - **Warps 0-11** meet on named barrier 3 and read O.
 
 mbarriers follow `mbarrier.try_wait.parity` semantics. Named barriers follow `bar.sync`:
@@ -20,7 +24,7 @@ means.
 At every hand-off the model asserts the data it sees:
 - atoms are rewritten only after the MMAs that read the last chunk completed;
 - MMAs read the intended chunk's atoms and P;
-- the S accumulator is read for its own chunk;
+- the S accumulator is read for its own chunk, and overwritten only after every warp read it;
 - P is rewritten only after the last chunk's O and row-sum MMAs read it;
 - O is rescaled only between chunks;
 - the softmax references are read only when no warp is writing them;
@@ -29,15 +33,13 @@ At every hand-off the model asserts the data it sees:
 It also asserts that every warp finishes (no deadlock) and that no barrier generation mixes
 phases.
 
-The model orders events; it does not model memory visibility. Two of the kernel's
-synchronisations are therefore redundant here, and planting their removal is not caught:
-- **Barrier 5, for producer warps 4-7.** It makes the softmax warps' reference updates
-  visible to the helpers. The helpers also reach a chunk only after p_full of the last
-  chunk.
-- **The l_done wait before a rescale.** s_full already covers the last chunk's row-sum MMAs,
-  since a commit tracks every earlier MMA of its thread.
-A skipped tile_free wait, a p_full count without the helpers, and an early read of the
-references are caught.
+The model orders events; it does not model memory visibility. Barrier 5, for producer warps
+4-7, is therefore redundant here and planting its removal is not caught: it makes the softmax
+warps' reference updates visible to the helpers, which also reach a chunk only after p_full of
+the last chunk. The l_done waits before P is rewritten are taken by both the softmax warps and
+the helpers, and barrier 5 joins them, so only the removal of both is caught. A skipped
+tile_free wait, a p_full count without the helpers, and an early read of the references are
+caught too.
 """
 import random
 
@@ -93,7 +95,7 @@ class Model:
         self.issued_o = set()          # chunks whose O MMAs were issued
         self.red_max = {}              # (chunk, half) -> writes
         self.m_ref_writers = 0         # warps inside the reference-writing window
-        self.queue = []                # the MMA thread's async operations, in order
+        self.queues = {"S": [], "O": []}  # each MMA thread's async operations, in its order
 
     # -- helpers
     def nsync(self, bid, tag):
@@ -138,6 +140,8 @@ class Model:
                 self.atom_full[2 * at + 1].arrive()
             if helper:
                 yield lambda i=i: self.s_full.ready(i & 1)
+                if i > 0:
+                    yield lambda i=i: self.l_done.ready((i - 1) & 1)
                 self.read_s(i, 4 + w)
                 if i == 0:
                     self.red_max[(0, 1)] = self.red_max.get((0, 1), 0) + 1
@@ -157,6 +161,8 @@ class Model:
     def softmax(self, w):
         for i in range(self.nloc):
             yield lambda i=i: self.s_full.ready(i & 1)
+            if i > 0:
+                yield lambda i=i: self.l_done.ready((i - 1) & 1)
             self.read_s(i, w)
             if i == 0:
                 self.red_max[(0, 0)] = self.red_max.get((0, 0), 0) + 1
@@ -195,28 +201,35 @@ class Model:
         yield from self.nsync(3, "out")
         self.read_output()
 
-    def issuer(self):
+    def issuer_s(self):
         if self.nloc == 0:
             return
+        q = self.queues["S"]
         yield lambda: self.q_full.ready(0)
         for i in range(self.nloc):
             for k2 in range(4):
                 yield lambda k2=k2, i=i: self.atom_full[2 * k2].ready(i & 1) and self.atom_full[2 * k2 + 1].ready(i & 1)
                 for k in (2 * k2, 2 * k2 + 1):
                     assert self.atom_writes.get((k, i)) == 8, f"S of chunk {i} issued on atom {k} not fully written"
-                    self.queue.append(("S", i, k))
-            self.queue.append(("commit", self.s_full))
+                    q.append(("S", i, k))
+            q.append(("commit", self.s_full))
+
+    def issuer_o(self):
+        if self.nloc == 0:
+            return
+        q = self.queues["O"]
+        for i in range(self.nloc):
             yield lambda i=i: self.p_full.ready(i & 1)
             assert self.s_reads.get(i) == 8, "O issued before every warp read S"
             self.issued_o.add(i)
             for m in range(4):
-                self.queue.append(("O", i, m))
-                self.queue.append(("commit", self.tile_free[m]))
-            self.queue.append(("L", i))
-            self.queue.append(("commit", self.l_done))
+                q.append(("O", i, m))
+                q.append(("commit", self.tile_free[m]))
+            q.append(("L", i))
+            q.append(("commit", self.l_done))
 
-    def tensor_step(self):
-        op = self.queue.pop(0)
+    def tensor_step(self, which):
+        op = self.queues[which].pop(0)
         if op[0] == "commit":
             op[1].arrive()
             return
@@ -252,7 +265,8 @@ def simulate(nloc, seed):
     rng = random.Random(seed)
     redo = [False] + [rng.random() < 0.3 for _ in range(1, max(nloc, 1))]
     md = Model(nloc, redo, rng)
-    agents = [md.softmax(w) for w in range(NQ)] + [md.producer(w) for w in range(8)] + [md.issuer()]
+    pace = rng.choice([0.02, 0.1, 0.3, 0.6])
+    agents = [md.softmax(w) for w in range(NQ)] + [md.producer(w) for w in range(8)] + [md.issuer_s(), md.issuer_o()]
     waits = [None] * len(agents)
     live = list(range(len(agents)))
 
@@ -266,20 +280,22 @@ def simulate(nloc, seed):
         advance(a)
     while True:
         ready = [a for a in range(len(agents)) if waits[a] != "end" and waits[a]()]
-        choices = [("agent", a) for a in ready] + ([("tensor", None)] if md.queue else [])
-        if not choices:
+        tensor = [("tensor", k) for k in md.queues if md.queues[k]]
+        agent = [("agent", a) for a in ready]
+        if not tensor and not agent:
             break
-        kind, a = rng.choice(choices)
+        # the tensor pipe's pace relative to the warps varies per run (slow MMAs open the races)
+        kind, a = rng.choice(tensor if tensor and (not agent or rng.random() < pace) else agent)
         if kind == "tensor":
-            md.tensor_step()
+            md.tensor_step(a)
         else:
             advance(a)
     stuck = [a for a in range(len(agents)) if waits[a] != "end"]
     assert not stuck, f"nloc={nloc}: warps {stuck} never finished (deadlock)"
-    assert not md.queue
+    assert not md.queues["S"] and not md.queues["O"]
 
 
 def test_random_interleavings():
     for nloc in (0, 1, 2, 3, 5):
-        for seed in range(60):
-            simulate(nloc, 100 * nloc + seed)
+        for seed in range(60 if nloc < 2 else 300):
+            simulate(nloc, 1000 * nloc + seed)
