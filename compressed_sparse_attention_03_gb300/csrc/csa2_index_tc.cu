@@ -345,68 +345,82 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
 }
 
 // ------------------------------------------------------------------ decode (one query)
-// Scores of one query per sequence against all its visible keys: M = 128 keys, N = 32 heads,
-// K = 128 per tile.  The FP4 keys are decoded inside the kernel (a fp16 image of all keys
-// would cost 4x the key bytes in extra HBM traffic) and the decoded tile goes to tensor
-// memory, where the MMA reads its A operand: staging it in shared memory made the 32 KB
-// store + 32 KB operand read per tile the bottleneck of the shared-memory port.
-//  - warps 0-3 (epilogue, TMEM lane quarter = warp): ReLU, the w^I weighting and the fp32
-//    score stores of every tile (accumulator = tile % 4).
-//  - warp 22 (producer): bulk copies of the code bytes (64 per key) of kDGroup tiles at a
-//    time (one copy of their contiguous keys, or one per pool block of 8) into a ring of
-//    kDStages groups in shared memory.  Per-thread loads could not keep enough bytes in
-//    flight (the load queue filled long before HBM did), and one bulk copy per 8 KB tile ran
-//    at well under the copy bandwidth that 16 KB copies reach.
-//  - warps 4-19 (decoders, group = (warp - 4) / 4, rows 32 * (warp % 4) ..): the tiles
-//    i = group mod kDGroups, lane = key row; four groups, so that each warp has four tiles'
-//    time for the latency of its decode chain.  The 4 scale bytes of a row come by a plain
-//    load issued two group tiles ahead; the codes from the stage, which a warp releases to the
-//    producer after a proxy fence (its generic reads, then the next bulk copy's writes).  Exact decode to fp16 into TMEM
-//    (kDSlots tiles); rows past the last key (or naming an entry outside 0..E-1) are zero.
-//  - warps 20 and 21 (one thread each): the MMAs of the even / odd tiles, A from TMEM, B
-//    (Q^I) from shared memory.  A thread that waits stalls until its own MMAs in flight have
-//    finished; with two issuers one of them keeps the tensor pipe busy meanwhile.  Each A slot
-//    and accumulator stays with one issuer (kDSlots and kDAcc are even), so no slot passes
-//    from one issuing thread's MMAs to another's: a four-issuer variant that did hand slots
-//    over gave an intermittent wrong score and no speedup.
-// Rows: one query (sequence bl, query t0 + tl) each; a row's key tiles are split evenly over
-// gridDim.x / rows persistent blocks.  With hist, each row also gets the histogram of its
-// score keys (kHistBins bins, added up over its blocks) that lets the top-k skip most keys.
-// With a pool (hierarchical indexer, reindex scan) the row's positions p are its pool's
-// entries 8 * pool[p / 8] + p % 8 instead of 0 .. E-1.
-constexpr int kDSlots = 6, kDAcc = 4, kDGroups = 4, kDThreads = 32 * 23;
-constexpr int kDDec0 = 4, kDMma = 20, kDProd = 22;  // MMA issuers: warps 20 (even tiles) and 21 (odd)
-constexpr uint32_t kDACol = 0;                    // TMEM: A tiles kDSlots x 64 columns
-constexpr uint32_t kDDCol = kDSlots * 64;          // TMEM: kDAcc 32-column accumulators
-constexpr uint32_t kDTmemCols = 512;
-constexpr uint32_t kDQOff = 0;                     // smem: Q^I image, 2 atoms x [32 heads x 128 B]
-constexpr int kDGroup = 2;                         // tiles per stage (one copy)
-constexpr int kDStages = 6;                        // stages in the ring
-constexpr uint32_t kDStageOff = kDQOff + 8192;     // smem: codes [kDStages][kDGroup x 128 rows x 64 B]
-constexpr uint32_t kDynDec = kDStageOff + kDStages * kDGroup * 8192 + 1024;
-static_assert(kDGroup == 2, "a stage holds two tiles (of two decoder groups)");
-static_assert(kDSlots % 2 == 0, "a decoder group keeps the parity of its tiles");
-static_assert(kDDCol + 32 * kDAcc <= kDTmemCols, "TMEM columns");
-static_assert(kDAcc == 4, "accumulator = tile & 3");
-static_assert(kDSlots % 2 == 0 && kDAcc % 2 == 0, "slots and accumulators keep the issuer (tile parity)");
+// Scores of one query per sequence against all its visible keys on the block-scaled FP4
+// tensor-core path (tcgen05.mma kind::mxf4): the cached K^I codes and UE8M0 scales are the MMA
+// operands as they are stored, with no decode.  D[key, head] = K^I_key . Q^I_head, M = 128 keys,
+// N = 32 heads, K = 128 per tile as two MMAs of K = 64 (scale bytes 0-1, then 2-3).  Q^I is
+// quantised to FP4 (E2M1, UE8M0 per 32) in the kernel exactly as in the oracle.  Each MMA's
+// products are exact and the fp32 accumulation is the tensor core's.
+// A unit is two tiles (256 positions); units cycle through kMSlots shared-memory stages and
+// TMEM slots (accumulators 2 x 32 columns, A scale words 2 x 4 columns):
+//  - warps 0 and 1 (one thread each): the even / odd units; per unit, one wait (sf_full), four
+//    MMAs and one commit (done).  A thread's wait does not end before its own MMAs in flight
+//    have finished, so one thread alone left the tensor pipe idle for half of each unit; with
+//    two, one issues while the other waits.  A slot (s = u mod kMSlots, kMSlots even) stays with
+//    one thread: a commit tracks only the MMAs of the thread that issues it.
+//  - warp 2 (producer): TMA copies of the unit's code rows (64 bytes each) into a stage with the
+//    64-byte swizzle the MMA reads (one 256-row box, or one 8-row box per pool block), and of its
+//    scale words (4 bytes per key; boxes of 256 + 4 words, or 12 words per pool block, that start
+//    at a multiple of 4 words: a tensor copy must start on a 16-byte boundary, and a sequence's
+//    words start at word cap * b).  Every box lands at a multiple of 128 bytes in shared memory,
+//    as tensor copies require (pool blocks' scale boxes 128 bytes apart).  A stage is refilled once the MMAs that read it have completed
+//    (done of the unit kMSlots before).  Scale words read by each thread with plain loads arrived
+//    too late: with the copies keeping ~100 KB per SM in flight, a load waited behind them for
+//    several units' time.
+//  - warps 3-6 (scale warps, TMEM lane quarter = warp % 4): once the epilogue has read the slot's
+//    accumulators (d_free) and the unit's copies have landed (s_full), the unit's A scale words
+//    from the stage into TMEM, the same words in every quarter (column c, lane i: row 32c + i);
+//    then they release the unit to the MMA thread (sf_full).  They also write Q^I's codes and
+//    scale words.
+//  - warps 7-14 (epilogue, TMEM lane quarter = warp % 4; group (warp - 7) / 4 takes tile 0 or 1
+//    of each unit): ReLU, the w^I weighting and the fp32 score stores.
+// Earlier designs decoded the FP4 keys to fp16 in the kernel (sixteen decoder warps, eight
+// kind::f16 MMAs per tile): every stage ran far below the copy bandwidth, and the chain of
+// handshakes per tile set the pace.  Here a tile costs two MMAs and a unit one wait per role.
+// Rows: one query (sequence bl, query t0 + tl) each; a row's key tiles are split evenly (an even
+// count per block) over gridDim.x / rows persistent blocks.  With hist, each row also gets the
+// histogram of its score keys (kHistBins bins, added up over its blocks) that lets the top-k skip
+// most keys.  With a pool (hierarchical indexer, reindex scan) the row's positions p are its
+// pool's entries 8 * pool[p / 8] + p % 8 instead of 0 .. E-1.  Positions past the row's end are
+// computed from whatever rows the copies brought (or zeros) and never stored.
+constexpr int kMSlots = 6;                          // units in flight: stages = TMEM slots
+constexpr int kMThreads = 32 * 15;
+constexpr int kMMma = 0, kMProd = 2, kMSf0 = 3, kMEpi0 = 7;  // MMA threads: warps 0 (even units) and 1 (odd)
+constexpr uint32_t kMStage = 16384;                 // smem per stage: 256 rows x 64 B of codes
+constexpr uint32_t kMQOff = 0;                      // smem: Q^I codes, 32 rows x 64 B (SW64)
+constexpr uint32_t kMStageOff = 2048;               // smem: stages (1024-aligned)
+constexpr uint32_t kMScw = 4096;                    // smem per stage: scale words (260, or 32 x 12 at 128 B)
+constexpr uint32_t kMScOff = kMStageOff + kMSlots * kMStage;
+constexpr uint32_t kDynMx = kMScOff + kMSlots * kMScw + 1024;
+constexpr uint32_t kMAccCol = 0;                    // TMEM: slot s accumulators at 64 s (tile t: + 32 t)
+constexpr uint32_t kMSfaCol = 64 * kMSlots;         // TMEM: slot s A scale words at kMSfaCol + 8 s (+ 4 t)
+constexpr uint32_t kMSfbCol = kMSfaCol + 8 * kMSlots;  // TMEM: Q^I scale words (one column)
+static_assert(kMSfbCol % 4 == 0 && kMSfbCol + 1 <= 512, "TMEM columns");
+static_assert(kMStageOff % 1024 == 0 && kMStage % 1024 == 0 && kMScOff % 128 == 0 && kMScw % 128 == 0,
+              "tensor-copy destinations: 128-byte aligned (1024 for the swizzled code rows)");
+static_assert(kMEpi0 + 8 == kMThreads / 32 && kMSlots % 2 == 0, "warp roles; a slot keeps its MMA thread");
 
-// a_full[slot]: the tile in a slot is decoded (4 decoder warps).  done[slot]: the MMAs of the
-// tile in a slot completed (one commit): the slot is free and accumulator slot & 1 holds its
-// scores.  d_free[k]: the epilogue group of tile parity k & 1 has read accumulator k (4 warps).
-// s_full[s] / s_empty[s]: stage s holds its tiles' codes (transaction count) / the decoder
-// warps of its tiles (four per tile) have read it.
-struct DecBars {
-  uint64_t a_full[kDSlots], done[kDSlots], d_free[kDAcc], s_full[kDStages], s_empty[kDStages];
+// s_full[s]: the unit's code rows and scale words landed (transaction count).  sf_full[s]: its scale words are
+// in TMEM and its codes landed (4 scale warps).  done[s]: its MMAs completed (one commit): the
+// stage is free and the accumulators hold its scores.  d_free[s]: the epilogue read them (8 warps).
+struct MxBars {
+  uint64_t s_full[kMSlots], sf_full[kMSlots], done[kMSlots], d_free[kMSlots];
 };
 
-__global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs a, SeqPos pos, int b0, int nb,
+__global__ void __launch_bounds__(kMThreads, 1) index_decode_mx_kernel(const __grid_constant__ CUtensorMap map_unit,
+                                                                       const __grid_constant__ CUtensorMap map_block,
+                                                                       const __grid_constant__ CUtensorMap map_sw256,
+                                                                       const __grid_constant__ CUtensorMap map_sw4,
+                                                                       const __grid_constant__ CUtensorMap map_sw12,
+                                                                       IndexArgs a, SeqPos pos, int b0, int nb,
                                                                        int t0, int tq, int Tq, float* scores,
                                                                        int64_t ld, int* rowlen, uint32_t* hist) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ DecBars bars;
+  __shared__ MxBars bars;
   __shared__ uint32_t shist[kHistBins];
   __shared__ uint32_t tmem_base_sh;
   __shared__ float wsh[kHI];
+  __shared__ uint32_t qsf[kHI];  // Q^I scale word per head (byte k: block k)
   __shared__ int32_t spool[kHsiBlocks];
   __shared__ int64_t n_sh;
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -424,9 +438,9 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   const int64_t E = active ? (pos.p0[bl] + t0 + tl + 1) >> a.rshift : 0;  // visible entries of the query
   const int32_t* prow = a.pool_in ? a.pool_in + qrow * kHsiBlocks : nullptr;
   if (active && prow)
-    for (int i = tid; i < kHsiBlocks; i += kDThreads) spool[i] = prow[i];
+    for (int i = tid; i < kHsiBlocks; i += kMThreads) spool[i] = prow[i];
   if (hist)
-    for (int i = tid; i < kHistBins; i += kDThreads) shist[i] = 0u;
+    for (int i = tid; i < kHistBins; i += kMThreads) shist[i] = 0u;
   __syncthreads();
   if (tid == 0) {
     int64_t n = E;
@@ -446,32 +460,29 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   __syncthreads();
   const int64_t n_pos = n_sh;  // positions of the row
   const int ntile = (int)((n_pos + 127) / 128);
-  const int tpb = (ntile + per_row - 1) / per_row;
+  const int tpb = 2 * ((ntile + 2 * per_row - 1) / (2 * per_row));  // even: whole units
   const int t_begin = min(ntile, part * tpb), t_end = min(ntile, t_begin + tpb);
   const int nt = active ? t_end - t_begin : 0;
+  const int nu = (nt + 1) / 2;
 
   if (tid == 0) {
-    for (int i = 0; i < kDSlots; ++i) {
-      mbar_init(&bars.a_full[i], 4);  // the four warps of one decoder group
-      mbar_init(&bars.done[i], 1);
-    }
-    for (int i = 0; i < kDAcc; ++i) mbar_init(&bars.d_free[i], 4);  // the four warps of one epilogue group
-    for (int i = 0; i < kDStages; ++i) {
+    for (int i = 0; i < kMSlots; ++i) {
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.s_empty[i], 4 * kDGroup);
+      mbar_init(&bars.sf_full[i], 4);  // the four scale warps
+      mbar_init(&bars.done[i], 1);
+      mbar_init(&bars.d_free[i], 8);   // the eight epilogue warps
     }
     mbar_fence_init();
   }
-  if (warp == kDMma) {
-    tmem_alloc(&tmem_base_sh, kDTmemCols);
+  if (warp == kMMma) {
+    tmem_alloc(&tmem_base_sh, 512);
     tmem_relinquish();
   }
-  // Q^I -> FP4 -> fp16 image (warps 8-11: warp heads 8(w-8)..+7, lane l values 4l..4l+3), w^I
-  if (warp >= kDDec0 && warp < kDDec0 + 4 && active) {
-    const int hw = warp - kDDec0;
-    const int64_t src = qrow;
+  // Q^I -> FP4 codes (scale warps: warp heads 8(w - kMSf0)..+7, lane l values 4l..4l+3), w^I
+  if (warp >= kMSf0 && warp < kMSf0 + 4 && active) {
+    const int hw = warp - kMSf0;
     for (int h = 8 * hw; h < 8 * hw + 8; ++h) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(a.qi + (src * kHI + h) * kDI + 4 * lane);
+      const uint2 raw = *reinterpret_cast<const uint2*>(a.qi + (qrow * kHI + h) * kDI + 4 * lane);
       float v[4] = {bf16_to_f32(raw.x & 0xffff), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xffff), bf16_to_f32(raw.y >> 16)};
       float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
@@ -479,14 +490,18 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
       const int e = mx_scale_exp(amax);
       if (e > 13 && lane == 0) atomicOr(&g_index_domain, 1u);
-      float q[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) q[i] = ldexpf(e2m1_to_f32(f32_to_e2m1(ldexpf(v[i], -e))), e);
-      const int d = 4 * lane;
-      *reinterpret_cast<uint2*>(sm + kDQOff + (d >> 6) * 4096 + sw128_off(h, (d & 63) >> 3) + (d & 7) * 2) =
-          make_uint2(f2_to_h2(q[0], q[1]), f2_to_h2(q[2], q[3]));
+      const float down = pow2f(-e);  // exact power of two
+      const uint32_t c0 = f32_to_e2m1(v[0] * down), c1 = f32_to_e2m1(v[1] * down);
+      const uint32_t c2 = f32_to_e2m1(v[2] * down), c3 = f32_to_e2m1(v[3] * down);
+      *reinterpret_cast<uint16_t*>(sm + kMQOff + sw64_off(h, lane >> 3) + ((2 * lane) & 15)) =
+          (uint16_t)(c0 | (c1 << 4) | (c2 << 8) | (c3 << 12));
+      // scale byte of block lane / 8 (values 32k .. 32k+31) into byte k of the head's word
+      const uint32_t sb = (uint32_t)(e + 127);
+      const uint32_t w0 = __shfl_sync(0xffffffffu, sb, 0), w1 = __shfl_sync(0xffffffffu, sb, 8);
+      const uint32_t w2 = __shfl_sync(0xffffffffu, sb, 16), w3 = __shfl_sync(0xffffffffu, sb, 24);
+      if (lane == 0) qsf[h] = w0 | (w1 << 8) | (w2 << 16) | (w3 << 24);
     }
-    if (hw == 0) wsh[lane] = bf16_to_f32(a.wI[src * kHI + lane]);
+    if (hw == 0) wsh[lane] = bf16_to_f32(a.wI[qrow * kHI + lane]);
     fence_proxy_async();
   }
   tc_fence_before();
@@ -494,145 +509,118 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp >= kDDec0 && warp < kDDec0 + 4 * kDGroups) {
-    // ============================================================ decoders: thread = key row
-    const int grp = (warp - kDDec0) >> 2, q4 = warp & 3;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint8_t* scl = a.ki_scales + (int64_t)b * a.cap * 4;
-    // the entry at this lane's row of tile i, or -1 (past the last key, or a pool entry
-    // outside 0..E-1)
-    auto entry = [&](int i) -> int64_t {
-      const int64_t pp = (int64_t)(t_begin + i) * 128 + 32 * q4 + lane;
-      if (i >= nt || pp >= n_pos) return -1;
-      const int64_t j = prow ? (int64_t)kHsiBlock * spool[pp >> 3] + (pp & 7) : pp;
-      return j >= 0 && j < E ? j : -1;
-    };
-    auto scale = [&](int i) -> uint32_t {
-      const int64_t j = entry(i);
-      return j >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(scl + j * 4)) : 0u;
-    };
-    uint32_t sa = scale(grp), sb = scale(grp + kDGroups);
-#pragma unroll 1
-    for (int i = grp; i < nt; i += kDGroups) {
-      const uint32_t sc_next = scale(i + 2 * kDGroups);  // two group tiles ahead
-      const int gi = i / kDGroup, s = gi % kDStages;
-      const bool valid = entry(i) >= 0;
-      mbar_wait(&bars.s_full[s], (gi / kDStages) & 1, err, 35);
-      uint4 cw[4];
-      const uint4* rc = reinterpret_cast<const uint4*>(sm + kDStageOff + (s * kDGroup + i % kDGroup) * 8192 +
-                                                       (32 * q4 + lane) * 64);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) cw[k] = valid ? rc[k] : make_uint4(0u, 0u, 0u, 0u);
-      const int slot = i % kDSlots;
-      if (i >= kDSlots) mbar_wait(&bars.done[slot], ((i / kDSlots) - 1) & 1, err, 34);  // slot's last tile done
-      tc_fence_after();
-      if (__vcmpgtu4(sa, kMaxScaleBytes)) atomicOr(&g_index_domain, 1u);
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {  // 32 values: 16 code bytes, one scale byte
-        const uint32_t s2 = pow2_h2((int)((sa >> (8 * blk)) & 255u) - 127);
-        const uint32_t wd[4] = {cw[blk].x, cw[blk].y, cw[blk].z, cw[blk].w};
-        uint32_t o[16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          cvt_e2m1x8_f16x8(wd[q], o + 4 * q);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) o[4 * q + k] = hmul2(o[4 * q + k], s2);
-        }
-        tmem_st16(lane_addr + kDACol + slot * 64 + 16 * blk, o);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      // The stage goes back to the producer only now, after a proxy fence: its next bulk copy
-      // (async proxy) must not overtake these generic-proxy reads.  Without the fence it
-      // sometimes did, and the first key row of a stage (the first bytes the next copy writes)
-      // was decoded from the following group's codes.  Here the reads are long complete, so the
-      // fence costs little.
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars.s_empty[s]);
-        mbar_arrive(&bars.a_full[slot]);
-      }
-      sa = sb;
-      sb = sc_next;
-    }
-  } else if (warp == kDProd) {
-    // ============================================================ producer: code stages
-    const uint8_t* codes = a.ki_codes + (int64_t)b * a.cap * 64;
-    const int64_t p_end = min64(n_pos, (int64_t)(t_begin + nt) * 128);  // this block's positions end here
-    const int ng = (nt + kDGroup - 1) / kDGroup;
-#pragma unroll 1
-    for (int gi = 0; gi < ng; ++gi) {
-      const int s = gi % kDStages;
-      if (gi >= kDStages) mbar_wait(&bars.s_empty[s], ((gi / kDStages) - 1) & 1, err, 36);
-      const int64_t p0g = (int64_t)(t_begin + gi * kDGroup) * 128;  // first position of the group
-      // lane k: the positions 8k .. 8k+7 of the group (one pool block; without a pool the
-      // group's keys are contiguous and lane 0 copies them all)
-      int64_t j0 = -1;
-      uint32_t bytes = 0;
-      const int64_t pp = p0g + 8 * lane;
-      if (pp < p_end) {
-        if (prow) {
-          j0 = (int64_t)kHsiBlock * spool[pp >> 3];
-          const int64_t nv = min64(8, p_end - pp);
-          const int64_t m = j0 >= 0 && j0 < E ? min64(nv, E - j0) : 0;
-          bytes = (uint32_t)(64 * m);
-        } else if (lane == 0) {
-          j0 = pp;
-          bytes = (uint32_t)(64 * min64(kDGroup * 128, p_end - pp));
-        }
-      }
-      const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
-      if (lane == 0) mbar_arrive_expect_tx(&bars.s_full[s], total);
-      __syncwarp();
-      if (bytes) bulk_g2s(sm + kDStageOff + s * kDGroup * 8192 + 8 * lane * 64, codes + j0 * 64, bytes, &bars.s_full[s]);
-    }
-  } else if (warp == kDMma || warp == kDMma + 1) {
-    // ============================================================ MMA issuers
+  if (warp < kMProd) {
+    // ============================================================ MMA threads
     if (lane == 0) {
-      // An MMA thread shares its sub-partition with four busy warps: keep its instruction
-      // stream short (the Q^I descriptors never change; A and D are plain TMEM offsets).
-      const uint32_t idesc = idesc_f16(false, false, 128, 32);
-      uint64_t bdesc[8];
-#pragma unroll
-      for (int k16 = 0; k16 < 8; ++k16)
-        bdesc[k16] = sw128_desc(sbase + kDQOff + (k16 >> 2) * 4096 + (k16 & 3) * 32, 16, 1024);
-      for (int i = warp - kDMma; i < nt; i += 2) {
-        const int slot = i % kDSlots, acc = i & 3;
-        mbar_wait(&bars.a_full[slot], (i / kDSlots) & 1, err, 22);
-        if (i >= kDAcc) mbar_wait(&bars.d_free[acc], ((i >> 2) - 1) & 1, err, 23);
+      const uint32_t id0 = idesc_mxf4(128, 32, 0, 0), id1 = idesc_mxf4(128, 32, 2, 2);
+      const uint64_t bq0 = sw64_desc(sbase + kMQOff), bq1 = sw64_desc(sbase + kMQOff + 32);
+      for (int u = warp - kMMma; u < nu; u += 2) {
+        const int s = u % kMSlots;
+        mbar_wait(&bars.sf_full[s], (u / kMSlots) & 1, err, 22);
         tc_fence_after();
-        const uint32_t ta = tmem + kDACol + slot * 64, td = tmem + kDDCol + 32 * acc;
-        mma_f16_ts(td, ta, bdesc[0], idesc, 0u);
 #pragma unroll
-        for (int k16 = 1; k16 < 8; ++k16) mma_f16_ts(td, ta + 8 * k16, bdesc[k16], idesc, 1u);
-        mma_commit(&bars.done[slot]);
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t d = tmem + kMAccCol + 64 * s + 32 * t, sfa = tmem + kMSfaCol + 8 * s + 4 * t;
+          const uint32_t abase = sbase + kMStageOff + s * kMStage + t * 8192;
+          mma_mxf4(d, sw64_desc(abase), bq0, id0, sfa, tmem + kMSfbCol, 0u);
+          mma_mxf4(d, sw64_desc(abase + 32), bq1, id1, sfa, tmem + kMSfbCol, 1u);
+        }
+        mma_commit(&bars.done[s]);
       }
     }
     __syncwarp();
+  } else if (warp == kMProd) {
+    // ============================================================ producer: code rows
+    const int64_t row0 = (int64_t)bl * a.cap;  // the sequence's first row (and scale word) in the tensor maps
+    const int k0 = (int)(row0 & 3);            // scale boxes start k0 words early, on a 16-byte boundary
+    const int64_t p_end = min64(n_pos, (int64_t)t_end * 128);
+#pragma unroll 1
+    for (int u = 0; u < nu; ++u) {
+      const int s = u % kMSlots;
+      if (u >= kMSlots) mbar_wait(&bars.done[s], ((u / kMSlots) - 1) & 1, err, 36);
+      unsigned char* dst = sm + kMStageOff + s * kMStage;
+      unsigned char* scd = sm + kMScOff + s * kMScw;
+      const int64_t pu = (int64_t)(t_begin + 2 * u) * 128;  // first position of the unit
+      if (!prow) {
+        if (lane == 0) {
+          const int x0 = (int)(row0 + pu - k0);  // words x0 .. x0 + 259 hold the unit's 256 at k0 ..
+          mbar_arrive_expect_tx(&bars.s_full[s], kMStage + 1024 + 16);
+          tma_load_2d(dst, &map_unit, 0, (int)(row0 + pu), &bars.s_full[s]);
+          tma_load_1d(scd, &map_sw256, x0, &bars.s_full[s]);
+          tma_load_1d(scd + 1024, &map_sw4, x0 + 256, &bars.s_full[s]);
+        }
+      } else {
+        // lane k: pool block k of the unit (positions pu + 8k .. + 7, stage rows 8k .. + 7, scale
+        // words 32k + k0 .. + 7)
+        const int64_t pp = pu + 8 * lane;
+        const int32_t blk = pp < p_end ? spool[pp >> 3] : -1;
+        const uint32_t total = __reduce_add_sync(0xffffffffu, blk >= 0 ? 512u + 48u : 0u);
+        if (lane == 0) mbar_arrive_expect_tx(&bars.s_full[s], total);
+        __syncwarp();
+        if (blk >= 0) {
+          const int64_t j0 = row0 + (int64_t)kHsiBlock * blk;
+          tma_load_2d(dst + lane * 512, &map_block, 0, (int)j0, &bars.s_full[s]);
+          tma_load_1d(scd + lane * 128, &map_sw12, (int)(j0 - k0), &bars.s_full[s]);
+        }
+      }
+    }
+  } else if (warp < kMEpi0) {
+    // ============================================================ scale warps: thread = row of column c
+    const int q4 = warp & 3;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16);
+    const int k0 = (int)(((int64_t)bl * a.cap) & 3);  // offset of the stage's first scale word
+    tmem_st1(lane_addr + kMSfbCol, qsf[lane]);         // Q^I row (head) lane, every quarter
+#pragma unroll 1
+    for (int u = 0; u < nu; ++u) {
+      const int s = u % kMSlots;
+      const int64_t pu = (int64_t)(t_begin + 2 * u) * 128;
+      if (u >= kMSlots) mbar_wait(&bars.d_free[s], ((u / kMSlots) - 1) & 1, err, 34);
+      mbar_wait(&bars.s_full[s], (u / kMSlots) & 1, err, 35);
+      tc_fence_after();
+      // tile t, column c -> unit row i = 128t + 32c + lane (1.0 in every byte past the row's end)
+      const uint32_t* wsc = reinterpret_cast<const uint32_t*>(sm + kMScOff + s * kMScw) + k0;
+      uint32_t v[8], big = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = 128 * (k >> 2) + 32 * (k & 3) + lane;
+        v[k] = pu + i < n_pos ? wsc[prow ? 32 * (i >> 3) + (i & 7) : i] : 0x7F7F7F7Fu;
+        big |= __vcmpgtu4(v[k], kMaxScaleBytes);
+      }
+      if (big) atomicOr(&g_index_domain, 1u);
+      tmem_st4(lane_addr + kMSfaCol + 8 * s, v[0], v[1], v[2], v[3]);
+      tmem_st4(lane_addr + kMSfaCol + 8 * s + 4, v[4], v[5], v[6], v[7]);
+      tmem_wait_st();
+      fence_proxy_async();  // these reads of the stage, before the copy that next overwrites it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.sf_full[s]);
+    }
   } else {
     // ============================================================ epilogue: thread = key lane
-    const int q4 = warp & 3;  // TMEM lane quarter
+    const int q4 = warp & 3;            // TMEM lane quarter
+    const int t = (warp - kMEpi0) >> 2;  // tile of the unit
     const int r = 32 * q4 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16) + kDDCol;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * q4) << 16) + kMAccCol + 32 * t;
     float* out = scores + ((int64_t)bl * Tq + tl) * ld;  // indexed by position
     float wr[kHI];
 #pragma unroll
     for (int h = 0; h < kHI; ++h) wr[h] = wsh[h];
-    for (int i = 0; i < nt; ++i) {
-      mbar_wait(&bars.done[i % kDSlots], (i / kDSlots) & 1, err, 24);
+    for (int u = 0; u < nu; ++u) {
+      const int s = u % kMSlots;
+      mbar_wait(&bars.done[s], (u / kMSlots) & 1, err, 24);
       tc_fence_after();
-      uint32_t u[32];
-      tmem_ld32(lane_addr + 32 * (i & 3), u);
+      uint32_t acc[32];
+      tmem_ld32(lane_addr + 64 * s, acc);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.d_free[i & 3]);
+      if (lane == 0) mbar_arrive(&bars.d_free[s]);
       float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains of 8
 #pragma unroll
-      for (int h = 0; h < 32; ++h) s4[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(u[h]), 0.f), s4[h & 3]);
+      for (int h = 0; h < 32; ++h) s4[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(acc[h]), 0.f), s4[h & 3]);
+      const int i = 2 * u + t;
       const int64_t pp = (int64_t)(t_begin + i) * 128 + r;
-      if (pp < n_pos) {
+      if (i < nt && pp < n_pos) {
         const float sc = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         out[pp] = sc;
         if (hist) atomicAdd(&shist[score_key(sc) >> kHistShift], 1u);
@@ -641,13 +629,13 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kDMma) {
+  if (warp == kMMma) {
     tc_fence_after();
-    tmem_dealloc(tmem, kDTmemCols);
+    tmem_dealloc(tmem, 512);
   }
   if (hist && nt > 0) {  // this block's counts into the row's histogram
     uint32_t* hrow = hist + ((int64_t)bl * Tq + tl) * kHistBins;
-    for (int i = tid; i < kHistBins; i += kDThreads)
+    for (int i = tid; i < kHistBins; i += kMThreads)
       if (shist[i]) atomicAdd(hrow + i, shist[i]);
   }
 }
@@ -657,7 +645,22 @@ __global__ void __launch_bounds__(kDThreads, 1) index_decode_tc_kernel(IndexArgs
 cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq,
                                           int Tq, float* scores, int64_t ld, int* rowlen, uint32_t* hist,
                                           int num_sms, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(index_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynDec);
+  // the nb sequences' code rows [nb * cap][64 B]: 256-row boxes (a unit) and 8-row boxes (a pool
+  // block); their scale words [nb * cap] (u32): boxes of 256 + 4 words and of 12 words
+  CUtensorMap map_unit, map_block, map_sw256, map_sw4, map_sw12;
+  const uint8_t* codes = a.ki_codes + (int64_t)b0 * a.cap * 64;
+  const uint8_t* words = a.ki_scales + (int64_t)b0 * a.cap * 4;
+  const uint64_t rows = (uint64_t)nb * a.cap;
+  if (rows + 512 > (uint64_t)INT32_MAX) return cudaErrorInvalidValue;  // coordinates are 32-bit
+  if (!encode_tiled_2d(&map_unit, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, codes, 64, rows, 64, 64, 256,
+                       CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_tiled_2d(&map_block, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, codes, 64, rows, 64, 64, 8,
+                       CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_tiled_1d(&map_sw256, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, words, rows, 256) ||
+      !encode_tiled_1d(&map_sw4, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, words, rows, 4) ||
+      !encode_tiled_1d(&map_sw12, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, words, rows, 12))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(index_decode_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynMx);
   if (e != cudaSuccess) return e;
   const int nrows = nb * tq;
   const int grid = nrows >= num_sms ? nrows : (num_sms / nrows) * nrows;
@@ -665,7 +668,8 @@ cudaError_t launch_index_scores_decode_tc(const IndexArgs& a, const SeqPos& pos,
     e = cudaMemsetAsync(hist, 0, (size_t)nb * Tq * kHistBins * sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
   }
-  index_decode_tc_kernel<<<grid, kDThreads, kDynDec, st>>>(a, pos, b0, nb, t0, tq, Tq, scores, ld, rowlen, hist);
+  index_decode_mx_kernel<<<grid, kMThreads, kDynMx, st>>>(map_unit, map_block, map_sw256, map_sw4, map_sw12, a, pos, b0, nb, t0, tq, Tq, scores, ld,
+                                                          rowlen, hist);
   note_launch();
   return cudaGetLastError();
 }

@@ -1,5 +1,6 @@
 // Internal declarations shared by the C-ABI front end (csa2_api.cu) and the kernel files.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -65,6 +66,17 @@ struct AttendArgs {
   int T;
   uint16_t* out;
 };
+
+// Tiled 2-D tensor map (cuTensorMapEncodeTiled through the runtime's driver entry point) over
+// [rows][cols] elements of elem_bytes with a row pitch of pitch_bytes, box [box_rows][box_cols],
+// rows outside the tensor read as zero.  False if the entry point is missing or the base, pitch
+// or box width breaks the 16-byte rules.
+bool encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t cols,
+                     uint64_t rows, uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle);
+
+// The same for n elements in one dimension, box of `box` elements (box * elem_bytes a multiple of 16).
+bool encode_tiled_1d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t n,
+                     uint32_t box);
 
 // Launchers: each enqueues on `st` and returns the first CUDA launch error (or success).
 // `b0` is the batch index of the first sequence in `pos`, `nb` how many follow.

@@ -43,14 +43,6 @@ struct OutBars {
   uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
 };
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __global__ void __launch_bounds__(kOutThreads, 1) outproj_kernel(const __grid_constant__ CUtensorMap ta,
                                                                  const __grid_constant__ CUtensorMap tw, int64_t M,
                                                                  uint16_t* out) {
@@ -169,7 +161,9 @@ __global__ void __launch_bounds__(kOutThreads, 1) outproj_kernel(const __grid_co
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -182,19 +176,37 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 [rows][cols] row-major (row pitch `pitch` elements), box [box_rows][64], 128-byte swizzle
-bool encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch, uint32_t box_rows) {
+bool encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t cols,
+                     uint64_t rows, uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn || (reinterpret_cast<uintptr_t>(base) & 15u) || (pitch_bytes & 15u) || (box_cols * elem_bytes) % 16u)
+    return false;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {pitch * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint64_t strides[1] = {pitch_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tiled_1d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t n,
+                     uint32_t box) {
+  auto fn = encode_fn();
+  if (!fn || (reinterpret_cast<uintptr_t>(base) & 15u) || (box * elem_bytes) % 16u) return false;
+  const cuuint64_t dims[1] = {n};
+  const cuuint64_t strides[1] = {(cuuint64_t)n * elem_bytes};  // unused for one dimension
+  const cuuint32_t boxd[1] = {box};
+  const cuuint32_t estr[1] = {1};
+  return fn(map, dtype, 1, const_cast<void*>(base), dims, strides, boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+// bf16 [rows][cols] row-major (row pitch `pitch` elements), box [box_rows][64], 128-byte swizzle
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch, uint32_t box_rows) {
+  return encode_tiled_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, pitch * 2, kBK, box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+}
 }  // namespace
 
 cudaError_t launch_out_group_proj(const uint16_t* o, const uint16_t* w, int64_t M, uint16_t* out, int num_sms,

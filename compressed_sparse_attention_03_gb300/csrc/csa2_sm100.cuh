@@ -1,7 +1,8 @@
 // Blackwell (sm_100 family, built for sm_103a) primitives as inline PTX: mbarriers with
-// bounded waits, tensor memory (TMEM) allocation and loads/stores, shared-memory matrix
-// descriptors for 128-byte-swizzled operands, and tcgen05.mma (kind::f16: f16 or bf16 operands;
-// kind::f8f6f4 with E5M2 operands; fp32 accumulate) with tcgen05.commit.
+// bounded waits, bulk and tensor (TMA) copies, tensor memory (TMEM) allocation and
+// loads/stores, shared-memory matrix descriptors for 128- and 64-byte-swizzled operands, and
+// tcgen05.mma (kind::f16: f16 or bf16 operands; kind::f8f6f4 with E5M2 operands;
+// kind::mxf4: block-scaled packed E2M1 with UE8M0 scales; fp32 accumulate) with tcgen05.commit.
 //
 // Every wait is bounded: after kSpinLimit failed polls the waiter records an error code in
 // the library's device error word and gives up, so that a broken pipeline ends instead of
@@ -97,6 +98,27 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
+// Tiled tensor copy (TMA) of the box at coordinates (x, y) of a 2-D tensor map into shared
+// memory, completing its bytes on `bar`.  x * element size must be a multiple of 16 bytes; rows
+// outside the tensor read as zero.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// The same for a 1-D tensor map: the box starting at element x (x * element size a multiple of
+// 16 bytes); elements past the end read as zero.
+__device__ __forceinline__ void tma_load_1d(void* dst, const void* map, int x, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // The same with a source size: src_bytes (0 or the full size) are read, the rest of the
 // destination is zero-filled (src_bytes = 0 reads nothing).
 __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
@@ -181,6 +203,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// Lane (warp's quarter)*32+i of columns taddr.col .. +3 (x4) or taddr.col (x1) <- thread i's values.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr), "r"(v0), "r"(v1), "r"(v2),
+               "r"(v3)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n" ::"r"(taddr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
@@ -202,6 +233,21 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
+// The same for 64-byte-swizzled K-major operands (layout field 4): rows of 64 bytes, 8-row
+// groups of 512 bytes (512-aligned, SBO = 512); a row's 16-byte chunk c sits at chunk
+// c ^ ((row / 2) % 4), the pattern a TMA copy with 64-byte swizzle writes.  Packed E2M1 rows of
+// 128 values (64 bytes) are one swizzle row; the second half of K starts 32 bytes in.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(512u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
+// Byte offset of 16-byte chunk c of row r in a 64B-swizzled region (rows of 64 bytes).
+__device__ __forceinline__ uint32_t sw64_off(uint32_t r, uint32_t c) { return r * 64u + ((c ^ ((r >> 1) & 3u)) << 4); }
+
 // Instruction descriptor for kind::f16 with fp32 D: bits 4-5 D format (1 = f32), 7-9 / 10-12
 // A / B format (0 = f16, 1 = bf16), 15 / 16 A / B major (1 = MN-major), 17-22 N/8, 24-28 M/16.
 __host__ __device__ constexpr uint32_t idesc_f16(bool a_mn_major, bool b_mn_major, int M, int N, bool bf16 = false) {
@@ -213,6 +259,31 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool a_mn_major, bool b_mn_majo
 // D, both K-major: the other fields as in idesc_f16.
 __host__ __device__ constexpr uint32_t idesc_e5m2(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::mxf4 (packed E2M1 A and B, format 1 in bits 7-9 / 10-12;
+// UE8M0 scales, bit 23; K-major; N/8 in bits 17-22, M/16 in bits 24-28) with the scale-factor
+// byte selectors: bits 29-30 for A, 4-5 for B.  With scale_vec::2X an MMA (K = 64) uses the two
+// scale bytes sf_id and sf_id + 1 of each row's 32-bit scale word, so sf_id = 0 and 2 cover
+// the four 32-value blocks of a 128-value row in two MMAs.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int a_sf_id, int b_sf_id) {
+  return ((uint32_t)b_sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | ((uint32_t)a_sf_id << 29);
+}
+
+// D[tmem] (+)= (A * 2^sfa)[smem] * (B * 2^sfb)[smem]^T for kind::mxf4 (K = 64 packed E2M1
+// values, 32 bytes of each row).  The scale words live in TMEM: for M = 128, row 32c + i of A
+// takes column sfa + c, lane i of every 32-lane quarter (the same word in all four quarters);
+// row 32c + i of B (N rows) likewise takes column sfb + c.  The scale columns start at a
+// multiple of 4.  One elected thread issues.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T for kind::f8f6f4 (8-bit operands, K = 32 per instruction: 32
