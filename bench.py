@@ -440,20 +440,34 @@ def decode_object(dw, dms, dper, dlaunches, ws, hbm, src, profile=None):
     }
 
 
-def prefill_rooflines(wl, per, bf16, src, ws=1):
-    """Tensor rooflines of a prefill workload: attention (bf16 operands), the indexer score GEMM
-    (FP4 values on fp16-operand MMAs, so against the bf16 peak) and the two together."""
+def measure_tensor_rates(csa2, iters=8192):
+    """The tensor-core rate of each MMA kind the kernels use, measured here (csa2_tc_rate)."""
+    h = csa2.csa2_create()
+    r = {k: csa2.csa2_tc_rate(h, i, iters) for i, k in enumerate(("f16", "e5m2", "mxf4"))}
+    h.close()
+    r.update({"unit": "TFLOP/s", "source": f"csa2_tc_rate: best of 3 launches, {iters} MMAs M=128 N=256 per SM, "
+                                           "operands in shared memory (burst)"})
+    return r
+
+
+def prefill_rooflines(wl, per, bf16, src, ws=1, e5m2=None):
+    """Tensor rooflines of a prefill workload: attention (fp16 operands, against the bf16 peak),
+    the indexer score GEMM (E5M2 operands on kind::f8f6f4 MMAs: against the measured E5M2 rate
+    when given) and the two together (against the bf16 peak)."""
     af = attention_flops(wl.B, wl.p0, wl.T, wl.ratio)
     xf = 8192.0 * indexer_pairs(wl.B, wl.p0, wl.T, wl.ratio)
     a_ach = af / (per["attend"] / 1e3) / 1e12
     x_ach = xf / (per["index"] / 1e3) / 1e12
     both = (af + xf) / ((per["attend"] + per["index"]) / 1e3) / 1e12
     peak_src = f"{src} bf16 burst"
+    xpeak = e5m2 if e5m2 else 2.0 * bf16
+    xsrc = ("measured kind::f8f6f4 E5M2 MMA rate (csa2_tc_rate, burst)" if e5m2
+            else f"{src} bf16 burst x 2 (the nominal E5M2 / bf16 ratio)")
     return {
         "roofline_attend": {"bound": "tensor", "achieved": a_ach, "peak": bf16, "unit": "TFLOP/s", "frac": a_ach / bf16,
                             "flops_per_launch": af, "peak_source": peak_src},
-        "roofline_index": {"bound": "tensor", "achieved": x_ach, "peak": bf16, "unit": "TFLOP/s", "frac": x_ach / bf16,
-                           "flops_per_call": xf, "peak_source": peak_src + " (FP4 values on fp16-operand MMAs)",
+        "roofline_index": {"bound": "tensor", "achieved": x_ach, "peak": xpeak, "unit": "TFLOP/s", "frac": x_ach / xpeak,
+                           "flops_per_call": xf, "peak_source": xsrc,
                            "note": "whole csa2_index_topk call: score GEMM + fp32 score rows + top-512 select"},
         "roofline_attend_plus_index": {"bound": "tensor", "achieved": both, "peak": bf16, "unit": "TFLOP/s",
                                        "frac": both / bf16, "flops": af + xf, "peak_source": peak_src},
@@ -467,6 +481,7 @@ def run_ours(args, rank, ws):
     dev = "cuda"
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     hbm, bf16, src = peaks()
+    rates = measure_tensor_rates(csa2)
     wl = inputs.WORKLOADS[args.workload]
     step = Step(csa2, inputs, wl, seed_for_rank(wl.seed, rank), dev)
     clocks = ClockSampler(torch.cuda.current_device(), args.clocks_csv)
@@ -493,8 +508,10 @@ def run_ours(args, rank, ws):
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks.summary(),
+        "tensor_rates": rates,
     }
-    line.update({k: v for k, v in prefill_rooflines(wl, per, bf16, src).items() if k != "roofline_attend"})
+    line.update({k: v for k, v in prefill_rooflines(wl, per, bf16, src, e5m2=rates["e5m2"]).items()
+                 if k != "roofline_attend"})
     del step
     torch.cuda.empty_cache()
     # the other workloads, one object each: decode at 8K (B=1), 128K (B=64) and 1M (B=8) context,
@@ -516,7 +533,8 @@ def run_ours(args, rank, ws):
         else:
             line[key] = {"workload": dw.name, "B": dw.B, "T": dw.T, "p0": dw.p0, "ratio": dw.ratio, "steps": steps,
                          "value": ws * dw.B * dw.T / (dms / 1e3), "unit": "tok/s", "ms_per_step": dms,
-                         "kernels_ms": dper, "gpu_launches": dlaunches, **prefill_rooflines(dw, dper, bf16, src)}
+                         "kernels_ms": dper, "gpu_launches": dlaunches,
+                         **prefill_rooflines(dw, dper, bf16, src, e5m2=rates["e5m2"])}
         del dstep
         torch.cuda.empty_cache()
     if not args.no_decode and args.hsi_workload:

@@ -41,7 +41,7 @@ EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_st
            "csa2_workspace_bytes",
            "csa2_write_cache", "csa2_roll_window", "csa2_index_topk", "csa2_index_scores", "csa2_index_pool", "csa2_reindex_topk", "csa2_attend",
            "csa2_attend_replay", "csa2_attend_static", "csa2_check", "csa2_selftest_timeout",
-           "csa2_out_group_proj")
+           "csa2_out_group_proj", "csa2_tc_rate")
 
 _lib = None
 
@@ -75,6 +75,8 @@ def lib() -> C.CDLL:
         L.csa2_index_scores.restype = i32
         L.csa2_out_group_proj.argtypes = [p, p, p, i64, p, p]
         L.csa2_out_group_proj.restype = i32
+        L.csa2_tc_rate.argtypes = [p, i32, i32, C.POINTER(C.c_double), p]
+        L.csa2_tc_rate.restype = i32
         L.csa2_check.argtypes = [p, p]
         L.csa2_check.restype = i32
         L.csa2_selftest_timeout.argtypes = [p, p]
@@ -266,6 +268,14 @@ def csa2_out_group_proj(h: Handle, o, w_oa, out, stream=None) -> None:
     _check("csa2_out_group_proj", lib().csa2_out_group_proj(
         h.ptr, _dev(o, torch.bfloat16, "o"), _dev(w_oa, torch.bfloat16, "w_oa"), M,
         _dev(out, torch.bfloat16, "out"), _stream(stream)))
+
+
+def csa2_tc_rate(h: Handle, kind: int, iters: int = 8192, stream=None) -> float:
+    """Measured tensor-core rate in TFLOP/s: kind 0 kind::f16 (fp16), 1 kind::f8f6f4 (E5M2),
+    2 kind::mxf4 (E2M1 with UE8M0 scales per 32).  Synchronises the stream."""
+    out = C.c_double(0.0)
+    _check("csa2_tc_rate", lib().csa2_tc_rate(h.ptr, int(kind), int(iters), C.byref(out), _stream(stream)))
+    return out.value
 
 
 def csa2_check(h: Handle, stream=None) -> int:

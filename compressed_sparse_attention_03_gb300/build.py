@@ -16,7 +16,7 @@ CSRC = PKG / "csrc"
 OUT = PKG / "_build"
 LIB = OUT / "libcsa2.so"
 SOURCES = ["csa2_api.cu", "csa2_writer.cu", "csa2_indexer.cu", "csa2_index_tc.cu", "csa2_attend.cu",
-           "csa2_attend_static.cu", "csa2_outproj.cu"]
+           "csa2_attend_static.cu", "csa2_outproj.cu", "csa2_tc_rate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -385,6 +385,19 @@ csa2_status csa2_selftest_timeout(csa2_handle* h, csa2_stream_t stream) {
   return cuda_status(csa2::launch_wait_probe(reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Tensor-core rate probe (include/csa2.h).
+csa2_status csa2_tc_rate(csa2_handle* h, int kind, int iters, double* tflops, csa2_stream_t stream) {
+  if (!h || !tflops || kind < 0 || kind > 2 || iters < 1 || iters > 65536) return CSA2_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (dev != h->device) return CSA2_ERR_INVALID_ARG;
+  int timed_out = 0;
+  const csa2_status s = cuda_status(
+      csa2::measure_tc_rate(kind, iters, h->num_sms, reinterpret_cast<cudaStream_t>(stream), tflops, &timed_out));
+  if (s != CSA2_OK) return s;
+  return timed_out ? CSA2_ERR_TIMEOUT : CSA2_OK;
+}
+
 // Grouped output projection W_OA (include/csa2.h).
 csa2_status csa2_out_group_proj(csa2_handle* h, const uint16_t* o, const uint16_t* w_oa, int64_t M, uint16_t* out,
                                 csa2_stream_t stream) {

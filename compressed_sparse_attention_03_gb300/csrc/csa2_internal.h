@@ -78,6 +78,10 @@ bool encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes
 bool encode_tiled_1d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, uint64_t n,
                      uint32_t box);
 
+// Tensor-core rate (csa2_tc_rate): best of three launches of `iters` MMAs per SM, in TFLOP/s;
+// *timed_out is set if a block's bounded wait gave up.
+cudaError_t measure_tc_rate(int kind, int iters, int num_sms, cudaStream_t st, double* tflops, int* timed_out);
+
 // Launchers: each enqueues on `st` and returns the first CUDA launch error (or success).
 // `b0` is the batch index of the first sequence in `pos`, `nb` how many follow.
 cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf,

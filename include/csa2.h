@@ -228,6 +228,19 @@ csa2_status csa2_reindex_topk(csa2_handle* h, const uint16_t* qi, const uint16_t
 csa2_status csa2_out_group_proj(csa2_handle* h, const uint16_t* o, const uint16_t* w_oa,
                                 int64_t M, uint16_t* out, csa2_stream_t stream);
 
+/* Tensor-core rate probe (no counterpart on the pages): the peak that the tensor-bound
+ * kernels here are quoted against, measured on this device for each operand kind they use.
+ * One block per SM; its elected thread issues `iters` MMAs of M = 128, N = 256 back to back on
+ * fixed shared-memory operands into one tensor-memory accumulator (no memory traffic):
+ *   kind 0: tcgen05.mma kind::f16 (fp16, K = 16 per MMA)
+ *   kind 1: kind::f8f6f4 (E5M2, K = 32)
+ *   kind 2: kind::mxf4 (packed E2M1 with UE8M0 scales per 32 values, K = 64)
+ * Times three launches with CUDA events on `stream` (synchronising it) and writes the best
+ * rate, 2 * 128 * 256 * K * iters * SMs / time, in TFLOP/s to *tflops (host).  1 <= iters <=
+ * 65536 and 0 <= kind <= 2, else CSA2_ERR_INVALID_ARG; CSA2_ERR_TIMEOUT if a block's bounded
+ * wait gave up (the number is then not to be trusted).  Not for use inside stream capture. */
+csa2_status csa2_tc_rate(csa2_handle* h, int kind, int iters, double* tflops, csa2_stream_t stream);
+
 /* Failure report (no counterpart on the pages).  Synchronises `stream`, then reports whether
  * a bounded wait inside any kernel of this library gave up since the last check:
  * CSA2_ERR_TIMEOUT (the outputs of the calls since then are not to be trusted); else
