@@ -14,12 +14,16 @@
 // 32 exact products is exact, and the fp32 accumulation across the four blocks is as for the
 // CUDA-core path.
 //
-// Persistent kernel, 384 threads: warp 0 issues the bulk copies, warp 1 allocates TMEM and
-// issues the MMAs, warps 4-11 run the epilogue (two warps per TMEM lane quarter, each taking
-// four of the tile's eight queries).  A query tile's image stays resident
-// (double-buffered) while its causal key tiles stream through a kAStages ring; accumulators
-// are double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile overlaps the
-// MMAs of the next.
+// Persistent kernel, 640 threads: warp 0 issues the bulk copies, warps 1 and 2 issue the MMAs
+// of the even / odd key tiles (warp 1 allocates TMEM), warps 4-19 run the epilogue (four warps
+// per TMEM lane quarter, each taking two of the tile's eight queries).  A query tile's image
+// stays resident (double-buffered) while its causal key tiles stream through a kAStages ring;
+// accumulators are double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile
+// overlaps the MMAs of the next.  Key tile i keeps ring stage i % kAStages and accumulator i % 2
+// with the MMA thread of its parity (a commit tracks only its own thread's MMAs).  A thread's
+// wait does not end before its own MMAs in flight have finished: with one MMA thread the tensor
+// pipe idled during every wait, and with eight epilogue warps each waited out its own TMEM
+// loads; both ran the kernel at well under its MMA time.
 #include <cuda_fp16.h>
 
 #include "csa2_common.cuh"
@@ -34,9 +38,10 @@ using namespace sm100;
 constexpr int kQPerTile = 8;                       // queries per query tile (N = 256)
 static_assert(kQPerTile % 2 == 0, "the epilogue reads two queries per TMEM wait");
 constexpr uint32_t kQImg = 32768, kKImg = 16384;   // bytes per image: [256 | 128 rows][128 B] E5M2
-constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter, four queries each
+constexpr int kEpiWarps = 16;                      // four per TMEM lane quarter, two queries each
 constexpr int kThreadsTC = 128 + 32 * kEpiWarps;
 constexpr int kAStages = 4;                        // key images in flight
+static_assert(kAStages % 2 == 0 && kEpiWarps == 2 * kQPerTile, "stages keep their MMA thread; two queries per warp");
 // dynamic smem: B (query images) 2 x 32 KB, A (key images) kAStages x 16 KB, w^I 2 x [8][32] floats,
 // score-key histograms [8 queries][kHistBins] of the current query tile
 constexpr uint32_t kBOff = 0, kAOff = 2 * kQImg, kWOff = kAOff + kAStages * kKImg, kHOff = kWOff + 2048,
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.b_full[i], 1);
-      mbar_init(&bars.b_free[i], 1);
+      mbar_init(&bars.b_free[i], 2);  // both MMA threads
       mbar_init(&bars.d_full[i], 1);
       mbar_init(&bars.d_free[i], kEpiWarps);
     }
@@ -228,10 +233,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
         ++qi;
       }
     }
-  } else if (warp == 1) {
-    // ============================================================ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ============================================================ MMA threads (key tiles of parity warp - 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_e5m2(128, 256);
+      const int par = warp - 1;
       int it = 0, qi = 0, dc = 0;
       for (int k = 0; k * G < ntiles; ++k) {
         const int tile = tile_of(k, G, ntiles);
@@ -242,6 +248,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
         const int sB = qi & 1;
         mbar_wait(&bars.b_full[sB], (qi >> 1) & 1, err, 13);
         for (int kt = 0; kt < nk; ++kt, ++it, ++dc) {
+          if ((it & 1) != par) continue;
           const int sA = it % kAStages, sD = dc & 1;
           mbar_wait(&bars.a_full[sA], (it / kAStages) & 1, err, 14);
           if (dc >= 2) mbar_wait(&bars.d_free[sD], ((dc >> 1) - 1) & 1, err, 15);
@@ -260,8 +267,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
     }
   } else if (warp >= 4) {
     // ============================================================ epilogue
-    // warp 4 + 4*half + quarter: keys 32*quarter .. (its TMEM lane quarter), queries 4*half .. +3
-    const int ew = warp - 4, quarter = ew & 3, half = ew >> 2, r = 32 * quarter + lane;
+    // warp 4 + 4*pair + quarter: keys 32*quarter .. (its TMEM lane quarter), queries 2*pair, +1
+    const int ew = warp - 4, quarter = ew & 3, pair = ew >> 2, r = 32 * quarter + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
     constexpr int kEpiThreads = 32 * kEpiWarps;
     int dc = 0, qi = 0;
@@ -290,10 +297,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
         tc_fence_after();
         const int64_t j = (int64_t)kt * 128 + r;
         const bool full = all_queries && (int64_t)(kt + 1) * 128 <= e_first;
-        // two queries per TMEM wait, and four independent partial sums per query (heads h mod 4,
-        // two packed pairs), so that one warp per sub-partition is not held by load waits
-#pragma unroll 1
-        for (int q = 4 * half; q < 4 * half + 4; q += 2) {
+        // two queries per TMEM wait, four independent partial sums per query (heads h mod 4, two
+        // packed pairs); four warps per sub-partition hide each other's load waits
+        {
+          const int q = 2 * pair;
           uint32_t u[2][32];
           tmem_ld32(lane_addr + 256 * sD + 32 * q, u[0]);
           tmem_ld32(lane_addr + 256 * sD + 32 * (q + 1), u[1]);
@@ -320,14 +327,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
             }
           }
         }
+        // released after the scores are formed: releasing it right after the TMEM loads let the
+        // MMAs two tiles on run beside these loads and made the kernel slower
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.d_free[sD]);
       }
-      if (lower_out) {  // warp ew: the lower edge of query ew's top-512 from its histogram
+      if (lower_out) {  // warp ew < 8: the lower edge of query ew's top-512 from its histogram
         named_bar_sync(2, kEpiThreads);  // every count of this query tile is in
         const int tl = qt * kQPerTile + ew;
-        if (tl < tq) {
+        if (ew < kQPerTile && tl < tq) {
           const int64_t E = (p0 + tl + 1) >> a.rshift;
           const uint32_t lo = warp_hist_lower(shist + ew * kHistBins, (int)min64(kTopK, E), lane);
           if (lane == 0) lower_out[(int64_t)bl * Tq + tl] = lo;
