@@ -28,14 +28,17 @@
  *    returned before anything is launched; launch errors come back as CSA2_ERR_CUDA.
  *  - Every wait inside a kernel is bounded (about 80 ms).  A wait that gives up records a
  *    code in a device error word and lets its kernel finish; csa2_check reports it.
- *  - FP4 scale domain.  The tensor-core kernels decode E2M1 x 2^e exactly into their
- *    operands: fp16 (decode indexer, attention) for scale bytes 104..140 (e = -23 .. 13),
- *    E5M2 (prefill indexer, T >= 8) for bytes 112..140 (e = -15 .. 13).  Smaller scales decode
- *    with an absolute error under 2^-24 (fp16) or 2^-17 (E5M2) per value, the rest of the row
- *    unaffected; bytes 0 with zero codes are exact zeros.  Bytes above 140 would overflow
- *    those operands: a kernel that reads one (or an indexer query block with e > 13, or an
- *    attention query of magnitude 2^16 or more) records it, and the next csa2_check returns
- *    CSA2_ERR_UNSUPPORTED (the outputs since the previous check are not to be trusted).  Rows this library's writer makes stay
+ *  - FP4 scale domain.  The decode indexer (T = 1, and the reindex scan) multiplies the cached
+ *    E2M1 codes and UE8M0 scales as stored (block-scaled FP4 MMAs), exactly for every scale
+ *    byte.  The other tensor-core kernels decode E2M1 x 2^e exactly into their operands: fp16
+ *    (attention) for scale bytes 104..140 (e = -23 .. 13), E5M2 (prefill indexer, T >= 8) for
+ *    bytes 112..140 (e = -15 .. 13).  Smaller scales decode with an absolute error under 2^-24
+ *    (fp16) or 2^-17 (E5M2) per value, the rest of the row unaffected; bytes 0 with zero codes
+ *    are exact zeros.  Bytes above 140 would overflow those operands: a kernel that reads one
+ *    (the decode indexer too, so that a call's domain does not depend on the path it takes;
+ *    or an indexer query block with e > 13, or an attention query of magnitude 2^16 or more)
+ *    records it, and the next csa2_check returns CSA2_ERR_UNSUPPORTED (the outputs since the
+ *    previous check are not to be trusted).  Rows this library's writer makes stay
  *    inside: after RMSNorm |value| <= sqrt(512) max|gamma|, so gains of magnitude at most 2^k
  *    give scale bytes <= 129 + k (k <= 11 keeps every byte <= 140).
  *
