@@ -144,11 +144,17 @@ __device__ __forceinline__ int tile_of(int round, int G, int ntiles) {
 // Lower edge (a score key) of the histogram bin that holds the K-th largest counted key, found
 // by one warp: every key among the K largest is >= it.  0 when fewer than K keys were counted.
 // Steps of 32 consecutive bins from the top (lane l: bin base - l, so the loads are free of bank
-// conflicts), a running count, and a stop at the first step that reaches K.
+// conflicts), a running count (one warp reduction per step), and a prefix scan only in the first
+// step that reaches K.
 __device__ uint32_t warp_hist_lower(const uint32_t* hist, int K, int lane) {
   uint32_t carry = 0;
   for (int base = kHistBins - 1; base >= 0; base -= 32) {
     const uint32_t c = hist[base - lane];
+    const uint32_t tot = __reduce_add_sync(0xffffffffu, c);
+    if (carry + tot < (uint32_t)K) {
+      carry += tot;
+      continue;
+    }
     uint32_t incl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -164,10 +170,20 @@ __device__ uint32_t warp_hist_lower(const uint32_t* hist, int K, int lane) {
 
 // lower_out (optional) [nb * Tq]: per query row, the histogram lower edge of its top-512 (keys
 // below it cannot be selected), for the select that follows.
+// cand (optional, with lower_out): instead of the dense score rows, each query row gets the list of
+// its candidates, (score key, position) pairs in cand_key / cand_j: four segments of ld / 4 slots
+// from row * ld, segment s for the keys of TMEM lane quarter s (key rows 32s .. 32s+31 of each
+// tile), filled by the one warp that owns that (query, quarter), its count in cand_n[row * 4 + s].
+// A key is a candidate unless it lies below the lower edge of the histogram bin of the K-th
+// largest key counted so far for its query (thr_run, refreshed after 8, 16, 32, ... key tiles, so
+// that each stretch between refreshes adds about K candidates at most, for a few refreshes): that
+// edge only rises, and never above the row's final lower edge, so every key of the row's top-K is
+// listed, and the lists hold all keys at or above the row's final edge.  ld is a multiple of 128.
 __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexArgs a, SeqPos pos, int t0, int tq, int nqt,
                                                                          int nkt, const uint8_t* qimg, const uint8_t* kimg,
                                                                          const float* wq, float* scores, int64_t ld,
-                                                                         int nb, int Tq, uint32_t* lower_out) {
+                                                                         int nb, int Tq, uint32_t* lower_out,
+                                                                         int32_t* cand_j, int* cand_n) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ TcBars bars;
   __shared__ uint32_t tmem_base_sh;
@@ -175,6 +191,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
   unsigned char* sm = smem_raw + (sbase - smem_u32(smem_raw));
   float* sw = reinterpret_cast<float*>(sm + kWOff);  // [2][8][32]
   uint32_t* shist = reinterpret_cast<uint32_t*>(sm + kHOff);  // [8][kHistBins]
+  __shared__ uint32_t thr_run[kQPerTile];                     // candidate bound per query of the tile
+  uint32_t* cand_key = reinterpret_cast<uint32_t*>(scores);   // the score rows' space holds the keys
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nqt_act = (tq + kQPerTile - 1) / kQPerTile;  // query tiles of this pass (image stride: nqt)
   const int G = gridDim.x, ntiles = nb * nqt_act;
@@ -286,11 +304,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
       }
       if (lower_out)
         for (int i = tid - 128; i < kQPerTile * kHistBins; i += kEpiThreads) shist[i] = 0u;
+      if (tid - 128 < kQPerTile) thr_run[tid - 128] = 0u;
       named_bar_sync(2, kEpiThreads);
       const int64_t p0 = pos.p0[bl] + t0;
       // key tiles below this bound are visible to all eight queries (the first has the fewest)
       const int64_t e_first = (p0 + qt * kQPerTile + 1) >> a.rshift;
       const bool all_queries = qt * kQPerTile + kQPerTile <= tq;
+      int ncand[2] = {0, 0};  // this warp's candidates of its two queries (its lane quarter's segment)
       for (int kt = 0; kt < nk; ++kt, ++dc) {
         const int sD = dc & 1;
         mbar_wait(&bars.d_full[sD], (dc >> 1) & 1, err, 16);
@@ -320,10 +340,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
                          make_float2(fmaxf(__uint_as_float(u[e][4 * h4 + 2]), 0.f), fmaxf(__uint_as_float(u[e][4 * h4 + 3]), 0.f)),
                          s23);
             }
-            if (full || (tl < tq && j < ((p0 + tl + 1) >> a.rshift))) {
-              const float sc = (s01.x + s01.y) + (s23.x + s23.y);
-              scores[((int64_t)bl * Tq + tl) * ld + j] = sc;
-              if (lower_out) atomicAdd(&shist[(q + e) * kHistBins + (score_key(sc) >> kHistShift)], 1u);
+            const bool ok = full || (tl < tq && j < ((p0 + tl + 1) >> a.rshift));
+            const float sc = (s01.x + s01.y) + (s23.x + s23.y);
+            const int64_t rq = (int64_t)bl * Tq + tl;
+            if (!cand_j) {
+              if (ok) {
+                scores[rq * ld + j] = sc;
+                if (lower_out) atomicAdd(&shist[(q + e) * kHistBins + (score_key(sc) >> kHistShift)], 1u);
+              }
+            } else {
+              // candidates: keys at or above the query's running bound, appended in warp batches
+              const uint32_t key = score_key(sc);
+              if (ok) atomicAdd(&shist[(q + e) * kHistBins + (key >> kHistShift)], 1u);
+              const bool app = ok && key >= *reinterpret_cast<volatile uint32_t*>(&thr_run[q + e]);
+              const uint32_t bal = __ballot_sync(0xffffffffu, app);
+              if (app) {
+                const int64_t at = rq * ld + quarter * (ld >> 2) + ncand[e] + __popc(bal & ((1u << lane) - 1u));
+                cand_key[at] = key;
+                cand_j[at] = (int32_t)j;
+              }
+              ncand[e] += __popc(bal);
             }
           }
         }
@@ -332,7 +368,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.d_free[sD]);
+        if (cand_j && ew < kQPerTile && kt >= 7 && ((kt + 1) & kt) == 0) {
+          // warp ew: a new bound for query ew from its histogram so far (other warps may still be
+          // adding to it: a histogram with fewer keys only gives a lower bound)
+          const int tl = qt * kQPerTile + ew;
+          if (tl < tq) {
+            const int64_t E = (p0 + tl + 1) >> a.rshift;
+            const uint32_t lo = warp_hist_lower(shist + ew * kHistBins, (int)min64(kTopK, E), lane);
+            if (lane == 0) thr_run[ew] = lo;
+          }
+        }
       }
+      if (cand_j && lane == 0)
+        for (int e = 0; e < 2; ++e) {
+          const int tl = qt * kQPerTile + 2 * pair + e;
+          if (tl < tq) cand_n[((int64_t)bl * Tq + tl) * 4 + quarter] = ncand[e];
+        }
       if (lower_out) {  // warp ew < 8: the lower edge of query ew's top-512 from its histogram
         named_bar_sync(2, kEpiThreads);  // every count of this query tile is in
         const int tl = qt * kQPerTile + ew;
@@ -691,7 +742,8 @@ size_t index_tc_image_bytes(int nb, int Tq, int64_t max_entries) {
 
 cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq, int Tq,
                                    int64_t emax, int64_t emax_all, bool build_keys, uint8_t* img, float* wq,
-                                   float* scores, int64_t ld, uint32_t* lower, int num_sms, cudaStream_t st) {
+                                   float* scores, int64_t ld, uint32_t* lower, int32_t* cand_j, int* cand_n,
+                                   int num_sms, cudaStream_t st) {
   const int nqt = (Tq + kQPerTile - 1) / kQPerTile;
   const int nkt = (int)((emax_all + 127) / 128);  // key images of every pass of the call: one stride
   uint8_t* qimg = img;
@@ -711,7 +763,7 @@ cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0
   const int ntiles = nb * ((tq + kQPerTile - 1) / kQPerTile);
   const int grid = max(1, min(num_sms, ntiles));
   index_prefill_tc_kernel<<<grid, kThreadsTC, kDynTC, st>>>(a, pos, t0, tq, nqt, nkt, qimg, kimg, wq, scores, ld, nb, Tq,
-                                                             lower);
+                                                             lower, cand_j, cand_n);
   note_launch();
   return cudaGetLastError();
 }

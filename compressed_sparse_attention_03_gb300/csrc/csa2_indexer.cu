@@ -35,7 +35,9 @@ struct IndexPlan {
   bool tc;          // prefill: tensor-core score GEMM (queries per pass >= kMinTcQueries)
   int pnch;         // hierarchical pool: chunks of kPoolChunk blocks (pool mode)
   bool dec;         // scores from the per-query scan (one query, or a pool), with histograms
-  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, off_img, off_rl, off_pk, off_pj, off_pn, off_h, off_lo, total;
+  bool cand;        // long prefill rows may take candidate lists instead of dense score rows
+  size_t off_q, off_w, off_s, off_ck, off_cj, off_cn, off_img, off_rl, off_pk, off_pj, off_pn, off_h, off_lo,
+      off_candj, off_candn, total;
 };
 
 constexpr int kPoolChunk = 16384;             // blocks per chunk of the pool select
@@ -48,7 +50,7 @@ IndexPlan make_plan(int nb, int T, int64_t max_entries, int mode = kIndexTopk) {
   IndexPlan p;
   // a reindex row holds the pool's positions (at most 2048 blocks of 8), not all entries
   if (mode == kIndexReindex) max_entries = min64(max_entries, (int64_t)kHsiBlock * kHsiBlocks);
-  p.ld = ((max(max_entries, (int64_t)1) + 31) / 32) * 32;
+  p.ld = ((max(max_entries, (int64_t)1) + 127) / 128) * 128;
   int64_t per_q = (int64_t)nb * p.ld * 4;
   int64_t tq = (int64_t)(kScoreBudget / (size_t)per_q);
   // scores to the caller's array (csa2_index_scores): one pass over all queries, no select
@@ -77,6 +79,11 @@ IndexPlan make_plan(int nb, int T, int64_t max_entries, int mode = kIndexTopk) {
   p.off_pn = off; off += align256(rows * p.pnch * 4);
   p.off_h = off; off += p.dec && !so ? align256(rows * kHistBins * 4) : 0;
   p.off_lo = off; off += p.tc && !so ? align256(rows * 4) : 0;  // per-row lower edges from the prefill scorer
+  // candidate lists (csa2_index_topk on rows of kMinHistRow entries or more): positions beside the
+  // keys, which take the score rows' space, and a count per row
+  p.cand = p.tc && mode == kIndexTopk && max_entries >= kMinHistRow;
+  p.off_candj = off; off += p.cand ? align256(rows * (size_t)p.ld * 4) : 0;
+  p.off_candn = off; off += p.cand ? align256(rows * 4 * 4) : 0;
   p.total = off;
   return p;
 }
@@ -188,6 +195,7 @@ struct SelectShared {
   int warp_tot[2][kWarps];
   uint32_t bucket;
   int krem;
+  int exact;  // radix_select_pairs: the chosen bucket is taken whole
 };
 
 // Radix select over keys[0..n): on return *thr is the K-th largest key and *need_eq the
@@ -573,6 +581,172 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(IndexArgs a, i
   }
 }
 
+// K-th largest of the n pairs (key, j) = pair(i) in the order "larger key first, then lower j": as
+// the composite V = key * 2^32 + (2^32 - 1 - j), distinct for distinct j, so V >= *thr takes exactly
+// the K pairs.  The digits start at the highest bit in which the keys differ (in the position half
+// when every key is equal) and stop as soon as a whole bucket is needed.
+template <int NT, class Pair>
+__device__ void radix_select_pairs(const Pair& pair, int n, int K, SelectShared<NT>& sh, uint64_t* thr) {
+  constexpr int kWarps = NT / 32;
+  const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
+  const bool one_hist = n <= kSmallSelect;
+  const int hw = one_hist ? 0 : w;
+  const int nclear = (one_hist ? 1 : kWarps) * 256;
+  auto val = [&](int i) -> uint64_t {
+    uint32_t k;
+    int32_t j;
+    pair(i, k, j);
+    return ((uint64_t)k << 32) | (uint64_t)(~(uint32_t)j);
+  };
+  uint32_t mn = 0xffffffffu, mx = 0u;
+  for (int i = tid; i < n; i += NT) {
+    const uint32_t k = (uint32_t)(val(i) >> 32);
+    mn = min(mn, k);
+    mx = max(mx, k);
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (l == 0) {
+    sh.red[0][w] = mn;
+    sh.red[1][w] = mx;
+  }
+  __syncthreads();
+  mn = 0xffffffffu;
+  mx = 0u;
+  for (int x = 0; x < kWarps; ++x) {
+    mn = min(mn, sh.red[0][x]);
+    mx = max(mx, sh.red[1][x]);
+  }
+  __syncthreads();
+  const int top = mn == mx ? 31 : 63 - __clz(mn ^ mx);
+  uint64_t mask = top == 63 ? 0ull : ~((2ull << top) - 1ull);
+  uint64_t prefix = ((uint64_t)mx << 32) & mask;
+  int krem = K;
+  for (int hi = top; hi >= 0; hi -= 8) {
+    const int lo = max(hi - 7, 0);
+    const uint64_t dmask = (2ull << (hi - lo)) - 1ull;
+    for (int i = tid; i < nclear; i += NT) (&sh.hist[0][0])[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += NT) {
+      const uint64_t v = val(i);
+      if ((v & mask) == prefix) atomicAdd(&sh.hist[hw][(uint32_t)((v >> lo) & dmask)], 1u);
+    }
+    __syncthreads();
+    if (!one_hist) {
+      for (int b = tid; b < 256; b += NT) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int x = 0; x < kWarps; ++x) c += sh.hist[x][b];
+        sh.hist[0][b] = c;
+      }
+      __syncthreads();
+    }
+    if (tid < 32) {
+      // lane l owns bins 255-8l .. 248-8l (descending)
+      uint32_t c[8], tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { c[i] = sh.hist[0][255 - 8 * tid - i]; tot += c[i]; }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += v;
+      }
+      const uint32_t excl = incl - tot;
+      if (excl < (uint32_t)krem && incl >= (uint32_t)krem) {
+        uint32_t run = excl;
+        for (int i = 0; i < 8; ++i) {
+          if (run + c[i] >= (uint32_t)krem) {
+            sh.bucket = 255 - 8 * tid - i;
+            sh.krem = krem - (int)run;
+            sh.exact = c[i] == (uint32_t)(krem - (int)run);
+            break;
+          }
+          run += c[i];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (uint64_t)sh.bucket << lo;
+    mask |= dmask << lo;
+    krem = sh.krem;
+    const bool exact = sh.exact;
+    __syncthreads();
+    if (exact) break;  // the whole bucket is needed: V >= prefix (lower bits 0) takes it and the rest
+  }
+  *thr = prefix;
+}
+
+// Top-512 of a row from its candidate lists (long prefill rows): grid (rows, nb).  The row's four
+// segments (counts in cand_n[row * 4 ..], segment s at row * ld + s * ld / 4) hold (score key,
+// position) pairs in any order, among them the row's top-K; the K pairs go out in ascending
+// position order, each placed by its rank among them.
+__global__ void __launch_bounds__(kTopkThreads) topk_cand_kernel(IndexArgs a, SeqPos pos, int b0, int t0, int Tq,
+                                                                 const uint32_t* cand_key, const int32_t* cand_j,
+                                                                 const int* cand_n, int64_t ld) {
+  __shared__ SelectShared<kTopkThreads> sh;
+  __shared__ uint32_t okey[kTopK];
+  __shared__ int32_t oj[kTopK];
+  __shared__ int cnt_sh;
+  const int tl = blockIdx.x, bl = blockIdx.y;
+  const int t = t0 + tl;
+  if (t >= a.T) return;
+  const int b = b0 + bl;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t row = (int64_t)bl * Tq + tl;
+  const int64_t E = (pos.p0[bl] + t + 1) >> a.rshift;
+  const int K = (int)min64(kTopK, E);
+  int pre[5];  // the segments' starts in the row's numbering of its candidates
+  pre[0] = 0;
+  for (int q = 0; q < 4; ++q) pre[q + 1] = pre[q] + cand_n[row * 4 + q];
+  const int n = pre[4];
+  const int64_t seg = ld >> 2;
+  auto pair = [&](int i, uint32_t& k, int32_t& j) {
+    const int q = (i >= pre[1]) + (i >= pre[2]) + (i >= pre[3]);
+    const int64_t at = row * ld + q * seg + (i - pre[q]);
+    k = cand_key[at];
+    j = cand_j[at];
+  };
+  uint64_t thr = 0ull;  // n <= K: every candidate
+  if (n > K) radix_select_pairs<kTopkThreads>(pair, n, K, sh, &thr);
+  if (tid == 0) cnt_sh = 0;
+  __syncthreads();
+  const int nround = (n + kTopkThreads - 1) / kTopkThreads * kTopkThreads;  // whole warps take part in the ballots
+  for (int i = tid; i < nround; i += kTopkThreads) {
+    const bool v = i < n;
+    uint32_t k = 0u;
+    int32_t j = 0;
+    if (v) pair(i, k, j);
+    const bool take = v && ((((uint64_t)k << 32) | (uint64_t)(~(uint32_t)j)) >= thr);
+    const uint32_t bal = __ballot_sync(0xffffffffu, take);
+    if (bal) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&cnt_sh, __popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const int at = base + __popc(bal & ((1u << lane) - 1u));
+      if (take && at < kTopK) {
+        okey[at] = k;
+        oj[at] = j;
+      }
+    }
+  }
+  __syncthreads();
+  const int m = min(cnt_sh, kTopK);
+  int32_t* idx = a.idx + ((int64_t)b * a.T + t) * kTopK;
+  float* ts = a.top_scores ? a.top_scores + ((int64_t)b * a.T + t) * kTopK : nullptr;
+  for (int i = tid; i < m; i += kTopkThreads) {  // rank by position (positions are distinct)
+    const int32_t ji = oj[i];
+    int r = 0;
+    for (int q = 0; q < m; ++q) r += oj[q] < ji;
+    idx[r] = ji;
+    if (ts) ts[r] = key_score(okey[i]);
+  }
+  for (int i = m + tid; i < kTopK; i += kTopkThreads) {
+    idx[i] = -1;
+    if (ts) ts[i] = __int_as_float(0x7fc00000);
+  }
+}
+
 // ------------------------------------------------------------------ hierarchical pool
 // "Inside DeepSeek V4.1", section "Most layers borrow": blocks of 8 entries scored by their
 // best entry, 2048 blocks kept, the block holding the newest entries always among them.
@@ -715,6 +889,10 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
   int64_t emax_all = 0;  // entries visible to the call's last query, over this launch's sequences
   for (int i = 0; i < nb; ++i) emax_all = max(emax_all, (pos.p0[i] + a.T) >> a.rshift);
   uint32_t* lower = p.tc && !so && emax_all >= kMinHistRow ? reinterpret_cast<uint32_t*>(base + p.off_lo) : nullptr;
+  // long rows of csa2_index_topk: candidate lists instead of dense score rows
+  const bool use_cand = lower && p.cand;
+  int32_t* cand_j = use_cand ? reinterpret_cast<int32_t*>(base + p.off_candj) : nullptr;
+  int* cand_n = use_cand ? reinterpret_cast<int*>(base + p.off_candn) : nullptr;
   uint32_t* pk = reinterpret_cast<uint32_t*>(base + p.off_pk);
   int32_t* pj = reinterpret_cast<int32_t*>(base + p.off_pj);
   int* pn = reinterpret_cast<int*>(base + p.off_pn);
@@ -747,8 +925,9 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
       if (e != cudaSuccess) return e;
       emax = min64(emax, (int64_t)kHsiBlock * kHsiBlocks);
     } else if (p.tc) {
-      e = launch_index_scores_tc(a, pos, b0, nb, t0, tq, p.Tq, emax, emax_all, t0 == 0,
-                                 reinterpret_cast<uint8_t*>(base + p.off_img), wq, sc, ld, lower, num_sms, st);
+          e = launch_index_scores_tc(a, pos, b0, nb, t0, tq, p.Tq, emax, emax_all, t0 == 0,
+                                 reinterpret_cast<uint8_t*>(base + p.off_img), wq, sc, ld, lower, cand_j, cand_n,
+                                 num_sms, st);
       if (e != cudaSuccess) return e;
     } else if (a.T == 1) {
       if (emax > 0) {
@@ -767,6 +946,13 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (so) continue;
+    if (use_cand) {  // the rows' top-512 from their candidate lists
+      topk_cand_kernel<<<dim3(tq, nb), kTopkThreads, 0, st>>>(a, pos, b0, t0, p.Tq, reinterpret_cast<const uint32_t*>(sc),
+                                                              cand_j, cand_n, p.ld);
+      note_launch();
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      continue;
+    }
     const int nch = (int)max64(1, (emax + p.chunk - 1) / p.chunk);
     if (hist)
       topk_chunk_kernel<kTopkThreads><<<dim3(nch, tq, nb), kTopkThreads, chunk_smem, st>>>(

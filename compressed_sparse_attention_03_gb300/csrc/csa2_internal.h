@@ -99,7 +99,8 @@ size_t index_tc_image_bytes(int nb, int Tq, int64_t max_entries);
 // lower edge of the score-key histogram bin that holds its 512th largest score.
 cudaError_t launch_index_scores_tc(const IndexArgs& a, const SeqPos& pos, int b0, int nb, int t0, int tq, int Tq,
                                    int64_t emax, int64_t emax_all, bool build_keys, uint8_t* img, float* wq,
-                                   float* scores, int64_t ld, uint32_t* lower, int num_sms, cudaStream_t st);
+                                   float* scores, int64_t ld, uint32_t* lower, int32_t* cand_j, int* cand_n,
+                                   int num_sms, cudaStream_t st);
 // One query row per (sequence, t) of the pass t0 .. t0+tq-1 (T == 1, or a pool scan); row r =
 // bl * Tq + tl.  With a.pool_in, row r's positions are its pool's entries and rowlen[r]
 // receives the number of visible ones.

@@ -292,6 +292,22 @@ def test_index_exact_ties(handle):
     assert np.array_equal(idx[0, 0].cpu().numpy(), oidx[0])
 
 
+def test_index_long_prefill_rows_exact_ties(handle):
+    # prefill rows of >= 16,384 entries take candidate lists instead of dense score rows; the first
+    # 10,000 keys are identical, so the 512th score is shared by thousands of entries and the
+    # lower indices must win, as in the oracle's (score desc, j asc) sort
+    T, p0 = 16, 33000
+    x, cap = make_state(1, T, [p0], seed=11)
+    x["ki_codes"][0, :10000] = x["ki_codes"][0, 5]
+    x["ki_scales"][0, :10000] = x["ki_scales"][0, 5]
+    idx, top = run_index(handle, x, [p0], T)
+    pos = p0 + np.arange(T)
+    sc = oracle.index_scores(pos, np32(x["qi"][0]), np32(x["wI"][0]), x["ki_codes"][0].cpu().numpy(),
+                             x["ki_scales"][0].cpu().numpy(), cap)
+    oidx, _, _ = oracle.topk(sc, (pos + 1) // 2)
+    assert np.array_equal(idx[0].cpu().numpy(), oidx)
+
+
 @pytest.mark.parametrize("name", ["decode_8k", "decode_128k", "decode_1m", "prefill_4k"])
 def test_index_workloads(handle, name):
     wl = inputs.WORKLOADS[name]
