@@ -41,7 +41,7 @@ EXPORTS = ("csa2_default_config", "csa2_create", "csa2_destroy", "csa2_status_st
            "csa2_workspace_bytes",
            "csa2_write_cache", "csa2_roll_window", "csa2_index_topk", "csa2_index_scores", "csa2_index_pool", "csa2_reindex_topk", "csa2_attend",
            "csa2_attend_replay", "csa2_attend_static", "csa2_check", "csa2_selftest_timeout",
-           "csa2_out_group_proj", "csa2_tc_rate")
+           "csa2_out_group_proj", "csa2_tc_rate", "csa2_set_device_positions")
 
 _lib = None
 
@@ -91,6 +91,8 @@ def lib() -> C.CDLL:
         L.csa2_attend_replay.restype = i32
         L.csa2_attend_static.argtypes = [p] * 5 + [i64, p, p, p, i32, i32, p, p]
         L.csa2_attend_static.restype = i32
+        L.csa2_set_device_positions.argtypes = [p, p, i64]
+        L.csa2_set_device_positions.restype = i32
         _lib = L
     return _lib
 
@@ -112,13 +114,31 @@ def _dev(t, dtype, name):
     return C.c_void_p(t.data_ptr())
 
 
-def _host_p0(p0, B):
+def _host_p0(p0, B, h=None):
+    """Host positions as int64[B]; None (passed as NULL) when the handle reads device positions
+    and the call gives none."""
+    if p0 is None:
+        if h is not None and h.dev_p0_max is not None:
+            return None
+        raise ValueError("p0: required (the handle reads host positions)")
     a = np.ascontiguousarray(np.asarray(p0.cpu() if isinstance(p0, torch.Tensor) else p0, dtype=np.int64).reshape(-1))
     if a.size == 1 and B > 1:
         a = np.full(B, int(a[0]), np.int64)
     if a.size != B:
         raise ValueError(f"p0: expected {B} positions, got {a.size}")
     return a
+
+
+def _p0_ptr(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _max_entries(h, p0a, T):
+    """Visible entries of the call's last query: from the host positions, else from the bound of
+    the device positions."""
+    if p0a is None:
+        return (h.dev_p0_max + T) // h.ratio
+    return int(((p0a + T) // h.ratio).max())
 
 
 def _stream(stream):
@@ -134,6 +154,7 @@ class Handle:
         lib().csa2_default_config(C.byref(cfg))
         cfg.rope_base, cfg.eps, cfg.ratio = rope_base, eps, ratio
         self.ratio = ratio
+        self.dev_p0_max = None  # set by csa2_set_device_positions
         h = C.c_void_p()
         _check("csa2_create", lib().csa2_create(C.byref(cfg), C.byref(h)))
         self._h = h
@@ -176,13 +197,13 @@ def workspace(h: Handle, op: int, B: int, T: int, max_entries: int, device=None)
 def csa2_write_cache(h: Handle, kc, gc, wa, gamma_c, w_ik, gamma_ik, gamma_w, p0, z_codes, z_scales, ki_codes,
                      ki_scales, window, pair_kc=None, pair_gc=None, stream=None) -> None:
     B, T, _ = kc.shape
-    p0a = _host_p0(p0, B)
+    p0a = _host_p0(p0, B, h)
     cap = z_codes.shape[1]
     _check("csa2_write_cache", lib().csa2_write_cache(
         h.ptr, _dev(kc, torch.bfloat16, "kc"), _dev(gc, torch.bfloat16, "gc"), _dev(wa, torch.bfloat16, "wa"),
         _dev(gamma_c, torch.float32, "gamma_c"), _dev(w_ik, torch.bfloat16, "w_ik"),
         _dev(gamma_ik, torch.float32, "gamma_ik"), _dev(gamma_w, torch.float32, "gamma_w"),
-        p0a.ctypes.data_as(C.c_void_p), B, T, _dev(pair_kc, torch.float32, "pair_kc"),
+        _p0_ptr(p0a), B, T, _dev(pair_kc, torch.float32, "pair_kc"),
         _dev(pair_gc, torch.float32, "pair_gc"), _dev(z_codes, torch.uint8, "z_codes"),
         _dev(z_scales, torch.uint8, "z_scales"), _dev(ki_codes, torch.uint8, "ki_codes"),
         _dev(ki_scales, torch.uint8, "ki_scales"), cap, _dev(window, torch.uint8, "window"), None, 0,
@@ -202,13 +223,13 @@ def csa2_roll_window(h: Handle, window, nxt, stream=None) -> None:
 
 def csa2_index_topk(h: Handle, qi, wI, ki_codes, ki_scales, p0, idx, top_scores=None, ws=None, stream=None) -> None:
     B, T = qi.shape[:2]
-    p0a = _host_p0(p0, B)
+    p0a = _host_p0(p0, B, h)
     cap = ki_codes.shape[1]
     if ws is None:
-        ws = workspace(h, OP_INDEX_TOPK, B, T, int(((p0a + T) // h.ratio).max()), qi.device)
+        ws = workspace(h, OP_INDEX_TOPK, B, T, _max_entries(h, p0a, T), qi.device)
     _check("csa2_index_topk", lib().csa2_index_topk(
         h.ptr, _dev(qi, torch.bfloat16, "qi"), _dev(wI, torch.bfloat16, "wI"), _dev(ki_codes, torch.uint8, "ki_codes"),
-        _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
+        _dev(ki_scales, torch.uint8, "ki_scales"), cap, _p0_ptr(p0a), B, T,
         _dev(idx, torch.int32, "idx"), _dev(top_scores, torch.float32, "top_scores"), _dev(ws, torch.uint8, "ws"),
         ws.numel(), _stream(stream)))
 
@@ -217,15 +238,15 @@ def csa2_index_scores(h: Handle, qi, wI, ki_codes, ki_scales, p0, scores, ws=Non
     """S^I of every visible entry: scores f32 [B, T, ld] (ld a multiple of 4, at least the largest
     visible count); entries beyond a row's visible count are left untouched."""
     B, T = qi.shape[:2]
-    p0a = _host_p0(p0, B)
+    p0a = _host_p0(p0, B, h)
     cap = ki_codes.shape[1]
     if scores.dim() != 3 or scores.shape[:2] != (B, T):
         raise ValueError("csa2_index_scores: scores must be [B, T, ld]")
     if ws is None:
-        ws = workspace(h, OP_INDEX_SCORES, B, T, int(((p0a + T) // h.ratio).max()), qi.device)
+        ws = workspace(h, OP_INDEX_SCORES, B, T, _max_entries(h, p0a, T), qi.device)
     _check("csa2_index_scores", lib().csa2_index_scores(
         h.ptr, _dev(qi, torch.bfloat16, "qi"), _dev(wI, torch.bfloat16, "wI"), _dev(ki_codes, torch.uint8, "ki_codes"),
-        _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
+        _dev(ki_scales, torch.uint8, "ki_scales"), cap, _p0_ptr(p0a), B, T,
         _dev(scores, torch.float32, "scores"), scores.shape[2], _dev(ws, torch.uint8, "ws"), ws.numel(),
         _stream(stream)))
 
@@ -234,13 +255,13 @@ def csa2_index_pool(h: Handle, qi, wI, ki_codes, ki_scales, p0, idx, pool, top_s
                     stream=None) -> None:
     """csa2_index_topk plus the hierarchical block pool [B, T, 2048] of each query."""
     B, T = qi.shape[:2]
-    p0a = _host_p0(p0, B)
+    p0a = _host_p0(p0, B, h)
     cap = ki_codes.shape[1]
     if ws is None:
-        ws = workspace(h, OP_INDEX_POOL, B, T, int(((p0a + T) // h.ratio).max()), qi.device)
+        ws = workspace(h, OP_INDEX_POOL, B, T, _max_entries(h, p0a, T), qi.device)
     _check("csa2_index_pool", lib().csa2_index_pool(
         h.ptr, _dev(qi, torch.bfloat16, "qi"), _dev(wI, torch.bfloat16, "wI"), _dev(ki_codes, torch.uint8, "ki_codes"),
-        _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
+        _dev(ki_scales, torch.uint8, "ki_scales"), cap, _p0_ptr(p0a), B, T,
         _dev(idx, torch.int32, "idx"), _dev(top_scores, torch.float32, "top_scores"), _dev(pool, torch.int32, "pool"),
         _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
 
@@ -249,13 +270,13 @@ def csa2_reindex_topk(h: Handle, qi, wI, ki_codes, ki_scales, p0, pool, idx, top
                       stream=None) -> None:
     """Top-512 of this layer's indexer scores over the entries of a given block pool."""
     B, T = qi.shape[:2]
-    p0a = _host_p0(p0, B)
+    p0a = _host_p0(p0, B, h)
     cap = ki_codes.shape[1]
     if ws is None:
-        ws = workspace(h, OP_REINDEX_TOPK, B, T, int(((p0a + T) // h.ratio).max()), qi.device)
+        ws = workspace(h, OP_REINDEX_TOPK, B, T, _max_entries(h, p0a, T), qi.device)
     _check("csa2_reindex_topk", lib().csa2_reindex_topk(
         h.ptr, _dev(qi, torch.bfloat16, "qi"), _dev(wI, torch.bfloat16, "wI"), _dev(ki_codes, torch.uint8, "ki_codes"),
-        _dev(ki_scales, torch.uint8, "ki_scales"), cap, p0a.ctypes.data_as(C.c_void_p), B, T,
+        _dev(ki_scales, torch.uint8, "ki_scales"), cap, _p0_ptr(p0a), B, T,
         _dev(pool, torch.int32, "pool"), _dev(idx, torch.int32, "idx"), _dev(top_scores, torch.float32, "top_scores"),
         _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
 
@@ -280,12 +301,26 @@ def csa2_tc_rate(h: Handle, kind: int, iters: int = 8192, stream=None) -> float:
 
 def csa2_check(h: Handle, stream=None) -> int:
     """Synchronises the stream and returns what the kernels recorded since the last check: 0,
-    8 (a bounded wait gave up) or 5 (an FP4 scale above 2^13, or a query beyond the fp16
-    range, was read).  Does not raise on 5 or 8: the caller decides."""
+    8 (a bounded wait gave up), 2 (a device position outside 0..p0_max was read and clamped) or
+    5 (an FP4 scale above 2^13, or a query beyond the fp16 range, was read).  Does not raise on
+    2, 5 or 8: the caller decides."""
     st = lib().csa2_check(h.ptr, _stream(stream))
-    if st not in (0, 5, 8):
+    if st not in (0, 2, 5, 8):
         _check("csa2_check", st)
     return st
+
+
+def csa2_set_device_positions(h: Handle, p0_dev, p0_max: int = 0) -> None:
+    """Positions from device memory (int64 CUDA tensor of B values, read by the kernels when they
+    run; the calls may then pass p0=None) with the bound p0_max the host plans with; None returns
+    the handle to host positions.  Call outside stream capture."""
+    if p0_dev is None:
+        _check("csa2_set_device_positions", lib().csa2_set_device_positions(h.ptr, None, 0))
+        h.dev_p0_max = None
+        return
+    _check("csa2_set_device_positions", lib().csa2_set_device_positions(
+        h.ptr, _dev(p0_dev, torch.int64, "p0_dev"), int(p0_max)))
+    h.dev_p0_max = int(p0_max)
 
 
 def csa2_selftest_timeout(h: Handle, stream=None) -> None:
@@ -295,14 +330,14 @@ def csa2_selftest_timeout(h: Handle, stream=None) -> None:
 
 def csa2_attend(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, out, ws=None, stream=None) -> None:
     B, T = q.shape[:2]
-    p0a = _host_p0(p0, B)
+    p0a = _host_p0(p0, B, h)
     cap = z_codes.shape[1]
     if ws is None:
         ws = workspace(h, OP_ATTEND, B, T, 0, q.device)
     _check("csa2_attend", lib().csa2_attend(
         h.ptr, _dev(q, torch.bfloat16, "q"), _dev(sinks, torch.float32, "sinks"), _dev(z_codes, torch.uint8, "z_codes"),
         _dev(z_scales, torch.uint8, "z_scales"), cap, _dev(window, torch.uint8, "window"),
-        _dev(idx, torch.int32, "idx"), p0a.ctypes.data_as(C.c_void_p), B, T, _dev(out, torch.bfloat16, "out"),
+        _dev(idx, torch.int32, "idx"), _p0_ptr(p0a), B, T, _dev(out, torch.bfloat16, "out"),
         _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
 
 
@@ -311,12 +346,12 @@ def csa2_attend_static(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, 
     partials, and no call here allocates device memory (the tensors are the caller's).  Calls
     that can overlap in time share that scratch and race; see include/csa2.h."""
     B, T = q.shape[:2]
-    p0a = _host_p0(p0, B)
+    p0a = _host_p0(p0, B, h)
     cap = z_codes.shape[1]
     _check("csa2_attend_static", lib().csa2_attend_static(
         h.ptr, _dev(q, torch.bfloat16, "q"), _dev(sinks, torch.float32, "sinks"), _dev(z_codes, torch.uint8, "z_codes"),
         _dev(z_scales, torch.uint8, "z_scales"), cap, _dev(window, torch.uint8, "window"),
-        _dev(idx, torch.int32, "idx"), p0a.ctypes.data_as(C.c_void_p), B, T, _dev(out, torch.bfloat16, "out"),
+        _dev(idx, torch.int32, "idx"), _p0_ptr(p0a), B, T, _dev(out, torch.bfloat16, "out"),
         _stream(stream)))
 
 
@@ -325,7 +360,7 @@ def csa2_attend_replay(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, 
     """csa2_attend after a bounded replay: query t of sequence b sees the window positions
     max(win_start[b], t-127)..t."""
     B, T = q.shape[:2]
-    p0a = _host_p0(p0, B)
+    p0a = _host_p0(p0, B, h)
     wsa = _host_p0(win_start, B)
     cap = z_codes.shape[1]
     if ws is None:
@@ -333,5 +368,5 @@ def csa2_attend_replay(h: Handle, q, sinks, z_codes, z_scales, window, idx, p0, 
     _check("csa2_attend_replay", lib().csa2_attend_replay(
         h.ptr, _dev(q, torch.bfloat16, "q"), _dev(sinks, torch.float32, "sinks"), _dev(z_codes, torch.uint8, "z_codes"),
         _dev(z_scales, torch.uint8, "z_scales"), cap, _dev(window, torch.uint8, "window"),
-        _dev(idx, torch.int32, "idx"), p0a.ctypes.data_as(C.c_void_p), wsa.ctypes.data_as(C.c_void_p), B, T,
+        _dev(idx, torch.int32, "idx"), _p0_ptr(p0a), wsa.ctypes.data_as(C.c_void_p), B, T,
         _dev(out, torch.bfloat16, "out"), _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))

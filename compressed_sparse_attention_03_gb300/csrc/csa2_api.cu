@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <vector>
 #include <new>
 
 #include "../../include/csa2.h"
@@ -16,7 +17,16 @@ struct csa2_handle {
   int device;
   int num_sms;
   int rshift;  // log2 of the compression ratio (0: ratio 1, 1: ratio 2)
+  // positions read on the device (csa2_set_device_positions): the caller's array and the bound
+  // the host plans with
+  const int64_t* pos_dev = nullptr;
+  int64_t pos_hi = 0;
 };
+
+namespace {
+// Set by a kernel that read a device position outside 0..bound (every handle's; csa2_check).
+__device__ unsigned g_pos_flag;
+}  // namespace
 
 namespace {
 
@@ -35,6 +45,29 @@ csa2::SeqPos pack_pos(const int64_t* p0, int b0, int nb) {
   std::memset(&s, 0, sizeof s);
   for (int i = 0; i < nb; ++i) s.p0[i] = p0[b0 + i];
   return s;
+}
+
+// The positions of a call's sequences b0 .. b0+nb-1: the host values, or with device positions
+// set, the device array (the host copy then holds the bound, for the launchers' planning).
+csa2::SeqPos call_pos(const csa2_handle* h, const int64_t* p0, int b0, int nb) {
+  if (!h->pos_dev) return pack_pos(p0, b0, nb);
+  csa2::SeqPos s;
+  std::memset(&s, 0, sizeof s);
+  for (int i = 0; i < nb; ++i) s.p0[i] = h->pos_hi;
+  s.dev = h->pos_dev + b0;
+  s.hi = h->pos_hi;
+  void* f = nullptr;
+  cudaGetSymbolAddress(&f, g_pos_flag);
+  s.flag = static_cast<unsigned*>(f);
+  return s;
+}
+
+// The host positions a call validates and plans with: its p0 argument, or with device positions
+// set, the bound for every sequence (the argument is then not read).
+const int64_t* plan_p0(const csa2_handle* h, const int64_t* p0, int B, std::vector<int64_t>& tmp) {
+  if (!h->pos_dev) return p0;
+  tmp.assign((size_t)B, h->pos_hi);
+  return tmp.data();
 }
 
 csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
@@ -106,6 +139,26 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_handle** out) {
 
 void csa2_destroy(csa2_handle* h) { delete h; }
 
+// Positions from device memory (include/csa2.h).
+csa2_status csa2_set_device_positions(csa2_handle* h, const int64_t* p0_dev, int64_t p0_max) {
+  if (!h) return CSA2_ERR_INVALID_ARG;
+  if (!p0_dev) {
+    h->pos_dev = nullptr;
+    h->pos_hi = 0;
+    return CSA2_OK;
+  }
+  if ((reinterpret_cast<uintptr_t>(p0_dev) & 7u) != 0) return CSA2_ERR_ALIGN;
+  if (p0_max < 0 || p0_max + 1 > kMaxPos) return CSA2_ERR_SHAPE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (dev != h->device) return CSA2_ERR_INVALID_ARG;
+  void* f = nullptr;
+  if (cudaGetSymbolAddress(&f, g_pos_flag) != cudaSuccess) return CSA2_ERR_CUDA;  // loads the module now
+  h->pos_dev = p0_dev;
+  h->pos_hi = p0_max;
+  return CSA2_OK;
+}
+
 uint64_t csa2_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* csa2_status_string(csa2_status s) {
@@ -145,10 +198,13 @@ csa2_status csa2_write_cache(csa2_handle* h, const uint16_t* kc, const uint16_t*
       !ki_scales || !window)
     return CSA2_ERR_INVALID_ARG;
   if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  std::vector<int64_t> bound;
+  p0 = plan_p0(h, p0, B, bound);
   csa2_status st = check_p0(p0, B, T);
   if (st != CSA2_OK) return st;
   const int rs = h->rshift;
-  bool need_pair = rs == 1 && (T & 1) != 0;  // the pair buffer exists at ratio 2 only
+  // the pair buffer exists at ratio 2 only; with device positions any position may be odd
+  bool need_pair = rs == 1 && ((T & 1) != 0 || h->pos_dev);
   for (int b = 0; b < B; ++b) {
     if (rs == 1 && (p0[b] & 1)) need_pair = true;
     if ((p0[b] + T) >> rs > cap) return CSA2_ERR_SHAPE;  // last entry floor((p0+T)/ratio)-1 < cap
@@ -166,7 +222,7 @@ csa2_status csa2_write_cache(csa2_handle* h, const uint16_t* kc, const uint16_t*
     a.pair_kc = pair_kc; a.pair_gc = pair_gc;
     a.z_codes = z_codes; a.z_scales = z_scales; a.ki_codes = ki_codes; a.ki_scales = ki_scales; a.window = window;
     a.cap = cap; a.T = T; a.rshift = rs; a.eps = h->cfg.eps;
-    st = cuda_status(csa2::launch_writer(a, pack_pos(p0, b0, nb), b0, nb, h->rf, reinterpret_cast<cudaStream_t>(stream)));
+    st = cuda_status(csa2::launch_writer(a, call_pos(h, p0, b0, nb), b0, nb, h->rf, reinterpret_cast<cudaStream_t>(stream)));
     if (st != CSA2_OK) return st;
   }
   return CSA2_OK;
@@ -184,6 +240,8 @@ csa2_status index_call(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, c
   if (!h || !qi || !wI || !ki_codes || !ki_scales || (!idx && !so) || (so && !scores_out)) return CSA2_ERR_INVALID_ARG;
   if ((mode == csa2::kIndexPool && !pool_out) || (mode == csa2::kIndexReindex && !pool_in)) return CSA2_ERR_INVALID_ARG;
   if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  std::vector<int64_t> bound;
+  p0 = plan_p0(h, p0, B, bound);
   csa2_status st = check_p0(p0, B, T);
   if (st != CSA2_OK) return st;
   const int64_t emax = max_visible(p0, B, T, h->rshift);
@@ -208,7 +266,7 @@ csa2_status index_call(csa2_handle* h, const uint16_t* qi, const uint16_t* wI, c
   a.scores_ld = scores_ld;
   for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
     const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
-    st = cuda_status(csa2::launch_index_topk(a, pack_pos(p0, b0, nb), b0, nb, emax, ws, ws_bytes, h->num_sms,
+    st = cuda_status(csa2::launch_index_topk(a, call_pos(h, p0, b0, nb), b0, nb, emax, ws, ws_bytes, h->num_sms,
                                              reinterpret_cast<cudaStream_t>(stream), mode));
     if (st != CSA2_OK) return st;
   }
@@ -272,6 +330,8 @@ csa2_status csa2_attend(csa2_handle* h, const uint16_t* q, const float* sinks, c
                         csa2_stream_t stream) {
   if (!h || !q || !sinks || !z_codes || !z_scales || !window || !idx || !out) return CSA2_ERR_INVALID_ARG;
   if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  std::vector<int64_t> bound;
+  p0 = plan_p0(h, p0, B, bound);
   csa2_status st = check_p0(p0, B, T);
   if (st != CSA2_OK) return st;
   const void* ptrs[] = {q, sinks, z_codes, z_scales, window, idx, out};
@@ -285,7 +345,7 @@ csa2_status csa2_attend(csa2_handle* h, const uint16_t* q, const float* sinks, c
   a.cap = cap; a.T = T; a.out = out;
   for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
     const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
-    st = cuda_status(csa2::launch_attend(a, pack_pos(p0, b0, nb), no_replay(), b0, nb, h->rf, ws, ws_bytes, h->num_sms,
+    st = cuda_status(csa2::launch_attend(a, call_pos(h, p0, b0, nb), no_replay(), b0, nb, h->rf, ws, ws_bytes, h->num_sms,
                                          reinterpret_cast<cudaStream_t>(stream)));
     if (st != CSA2_OK) return st;
   }
@@ -300,6 +360,7 @@ csa2_status csa2_attend_replay(csa2_handle* h, const uint16_t* q, const float* s
                                size_t ws_bytes, csa2_stream_t stream) {
   if (!h || !q || !sinks || !z_codes || !z_scales || !window || !idx || !out) return CSA2_ERR_INVALID_ARG;
   if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  if (h->pos_dev) return CSA2_ERR_UNSUPPORTED;  // win_start <= p0 is checked on the host
   csa2_status st = check_p0(p0, B, T);
   if (st != CSA2_OK) return st;
   if (!win_start) return CSA2_ERR_INVALID_ARG;
@@ -330,6 +391,8 @@ csa2_status csa2_attend_static(csa2_handle* h, const uint16_t* q, const float* s
                                const int64_t* p0, int B, int T, uint16_t* out, csa2_stream_t stream) {
   if (!h || !q || !sinks || !z_codes || !z_scales || !window || !idx || !out) return CSA2_ERR_INVALID_ARG;
   if (B <= 0 || T <= 0 || cap < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  std::vector<int64_t> bound;
+  p0 = plan_p0(h, p0, B, bound);
   csa2_status st = check_p0(p0, B, T);
   if (st != CSA2_OK) return st;
   const void* ptrs[] = {q, sinks, z_codes, z_scales, window, idx, out};
@@ -350,7 +413,7 @@ csa2_status csa2_attend_static(csa2_handle* h, const uint16_t* q, const float* s
   // Launches of successive groups of sequences reuse the array; they are ordered on `stream`.
   for (int b0 = 0; b0 < B; b0 += csa2::kMaxSeqPerLaunch) {
     const int nb = std::min(B - b0, csa2::kMaxSeqPerLaunch);
-    st = cuda_status(csa2::launch_attend(a, pack_pos(p0, b0, nb), no_replay(), b0, nb, h->rf, ws, need, h->num_sms,
+    st = cuda_status(csa2::launch_attend(a, call_pos(h, p0, b0, nb), no_replay(), b0, nb, h->rf, ws, need, h->num_sms,
                                          reinterpret_cast<cudaStream_t>(stream)));
     if (st != CSA2_OK) return st;
   }
@@ -372,7 +435,12 @@ csa2_status csa2_check(csa2_handle* h, csa2_stream_t stream) {
       csa2::take_outproj_error(&eo) != cudaSuccess || csa2::take_attend_domain(&da) != cudaSuccess ||
       csa2::take_index_domain(&di) != cudaSuccess)
     return CSA2_ERR_CUDA;
+  unsigned pf = 0;
+  const unsigned zero = 0;
+  if (cudaMemcpyFromSymbol(&pf, g_pos_flag, sizeof pf) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (pf && cudaMemcpyToSymbol(g_pos_flag, &zero, sizeof zero) != cudaSuccess) return CSA2_ERR_CUDA;
   if (ea || ei || eo) return CSA2_ERR_TIMEOUT;
+  if (pf) return CSA2_ERR_SHAPE;
   return (da || di) ? CSA2_ERR_UNSUPPORTED : CSA2_OK;
 }
 

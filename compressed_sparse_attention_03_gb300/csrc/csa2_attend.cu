@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   const int t = blockIdx.x, bl = blockIdx.y, split = blockIdx.z;
   const int b = b0 + bl;
   const int T = a.T;
-  const int64_t p = pos.p0[bl] + t;
+  const int64_t p = seq_p0(pos, bl) + t;
   const int64_t qrow = (int64_t)b * T + t;
   int* err = &g_attend_error;
 
@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(128) attend_combine_kernel(AttendArgs a, SeqPo
   const int b = b0 + bl;
   const int64_t qrow = (int64_t)b * a.T + t;
   const int64_t lrow = (int64_t)bl * a.T + t;  // row within this launch's partials
-  const int64_t p = pos.p0[bl] + t;
+  const int64_t p = seq_p0(pos, bl) + t;
   float mstar = a.sinks[h] * kLog2e;
   for (int s = 0; s < nsplit; ++s) {
     const int64_t pr = lrow * nsplit + s;

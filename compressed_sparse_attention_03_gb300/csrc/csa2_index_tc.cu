@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
   // key tiles needed by query tile qt of sequence bl: entries visible to its last query
   auto n_key_tiles = [&](int bl, int qt) {
     const int tlast = min(tq, (qt + 1) * kQPerTile) - 1;
-    const int64_t E = (pos.p0[bl] + t0 + tlast + 1) >> a.rshift;
+    const int64_t E = (seq_p0(pos, bl) + t0 + tlast + 1) >> a.rshift;
     return (int)((E + 127) / 128);
   };
 
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) index_prefill_tc_kernel(IndexAr
         for (int i = tid - 128; i < kQPerTile * kHistBins; i += kEpiThreads) shist[i] = 0u;
       if (tid - 128 < kQPerTile) thr_run[tid - 128] = 0u;
       named_bar_sync(2, kEpiThreads);
-      const int64_t p0 = pos.p0[bl] + t0;
+      const int64_t p0 = seq_p0(pos, bl) + t0;
       // key tiles below this bound are visible to all eight queries (the first has the fewest)
       const int64_t e_first = (p0 + qt * kQPerTile + 1) >> a.rshift;
       const bool all_queries = qt * kQPerTile + kQPerTile <= tq;
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kMThreads, 1) index_decode_mx_kernel(const __g
   const int bl = active ? rr / tq : 0, tl = active ? rr % tq : 0;
   const int b = b0 + bl;
   const int64_t qrow = (int64_t)b * a.T + t0 + tl;
-  const int64_t E = active ? (pos.p0[bl] + t0 + tl + 1) >> a.rshift : 0;  // visible entries of the query
+  const int64_t E = active ? (seq_p0(pos, bl) + t0 + tl + 1) >> a.rshift : 0;  // visible entries of the query
   const int32_t* prow = a.pool_in ? a.pool_in + qrow * kHsiBlocks : nullptr;
   if (active && prow)
     for (int i = tid; i < kHsiBlocks; i += kMThreads) spool[i] = prow[i];

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(IndexArgs a, SeqPo
   __shared__ float sw[kQT][kHI];
   const int bl = blockIdx.z;
   const int b = b0 + bl;
-  const int64_t p0 = pos.p0[bl];
+  const int64_t p0 = seq_p0(pos, bl);
   const int tq0 = blockIdx.y * kQT;
   const int64_t j = (int64_t)blockIdx.x * kScoreThreads + threadIdx.x;
   // visible entries of the last query of the tile bound the whole tile
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(NT) topk_chunk_kernel(IndexArgs a, SeqPos pos,
   if (t >= a.T || tl >= Tq) return;
   const int b = b0 + bl;
   const int64_t row = (int64_t)bl * Tq + tl;
-  const int64_t E = rowlen ? rowlen[row] : (pos.p0[bl] + t + 1) >> a.rshift;
+  const int64_t E = rowlen ? rowlen[row] : (seq_p0(pos, bl) + t + 1) >> a.rshift;
   const int64_t cs = (int64_t)c * chunk;
   const int n = (int)max64(0, min64(chunk, E - cs));
   // the candidates' lower bound, before the loads: from the row's score histogram, or as the
@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_cand_kernel(IndexArgs a, Se
   const int b = b0 + bl;
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t row = (int64_t)bl * Tq + tl;
-  const int64_t E = (pos.p0[bl] + t + 1) >> a.rshift;
+  const int64_t E = (seq_p0(pos, bl) + t + 1) >> a.rshift;
   const int K = (int)min64(kTopK, E);
   int pre[5];  // the segments' starts in the row's numbering of its candidates
   pre[0] = 0;
@@ -765,7 +765,7 @@ __global__ void __launch_bounds__(kTopkThreads) pool_chunk_kernel(IndexArgs a, S
   const int t = t0 + tl;
   if (t >= a.T || tl >= Tq) return;
   const int b = b0 + bl;
-  const int64_t E = (pos.p0[bl] + t + 1) >> a.rshift;
+  const int64_t E = (seq_p0(pos, bl) + t + 1) >> a.rshift;
   const int64_t nblk = (E + kHsiBlock - 1) / kHsiBlock;
   int32_t* pool = a.pool_out + ((int64_t)b * a.T + t) * kHsiBlocks;
   if (nblk <= kHsiBlocks) {  // every block
@@ -829,7 +829,7 @@ __global__ void __launch_bounds__(kTopkThreads) pool_merge_kernel(IndexArgs a, S
   const int t = t0 + tl;
   if (t >= a.T || tl >= Tq) return;
   const int b = b0 + bl;
-  const int64_t E = (pos.p0[bl] + t + 1) >> a.rshift;
+  const int64_t E = (seq_p0(pos, bl) + t + 1) >> a.rshift;
   const int64_t nblk = (E + kHsiBlock - 1) / kHsiBlock;
   const int rnch = (int)((nblk + kPoolChunk - 1) / kPoolChunk);
   if (nblk <= kHsiBlocks || rnch <= 1) return;  // written by stage 1

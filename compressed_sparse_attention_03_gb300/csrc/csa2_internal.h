@@ -16,10 +16,28 @@ constexpr int kWin = 128;    // window rows
 constexpr int kTopK = 512;   // selected entries
 constexpr int kMaxSeqPerLaunch = 128;  // sequences whose p0 travels in one launch's params
 
-// Absolute start positions of up to kMaxSeqPerLaunch sequences, passed by value.
+// Absolute start positions of up to kMaxSeqPerLaunch sequences, passed by value, or (dev not
+// null) read by the kernels from device memory when they run: dev[bl] for the launch's sequence
+// bl, planned for on the host as if it were hi.  A device value outside 0..hi is clamped into it
+// (so every access stays within what the host validated) and sets *flag.
 struct SeqPos {
   int64_t p0[kMaxSeqPerLaunch];
+  const int64_t* dev;
+  int64_t hi;
+  unsigned* flag;
 };
+
+#ifdef __CUDACC__
+__device__ __forceinline__ int64_t seq_p0(const SeqPos& s, int bl) {
+  if (s.dev == nullptr) return s.p0[bl];
+  int64_t v = s.dev[bl];
+  if (v < 0 || v > s.hi) {
+    atomicOr(s.flag, 1u);
+    v = v < 0 ? 0 : s.hi;
+  }
+  return v;
+}
+#endif
 
 // RoPE frequencies theta_i = base^(-2i/64), i < 32, computed on the host in fp64.
 struct RopeFreq {

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
 
   const int bl = blockIdx.y;
   const int b = b0 + bl;
-  const int64_t p0 = pos.p0[bl];
+  const int64_t p0 = seq_p0(pos, bl);
   const int T = a.T;
   const int rs = a.rshift;
   const int64_t n_new = ((p0 + T) >> rs) - (p0 >> rs);
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kWriterThreads) writer_window_kernel(WriterArg
   const int t = blockIdx.x;
   const int bl = blockIdx.y;
   const int b = b0 + bl;
-  const int64_t p0 = pos.p0[bl];
+  const int64_t p0 = seq_p0(pos, bl);
   const int T = a.T;
   const int tid = threadIdx.x;
   const int ch = 4 * tid;
@@ -349,8 +349,13 @@ cudaError_t launch_roll_window(const uint8_t* window, int B, int T, uint8_t* nex
 }
 
 cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb, const RopeFreq& rf, cudaStream_t st) {
+  // new entries per sequence: from the positions, or (positions read on the device) the most any
+  // position can give, T at ratio 1 and ceil(T / 2) at ratio 2; each block checks its own count
   int64_t max_new = 0;
-  for (int i = 0; i < nb; ++i) max_new = max(max_new, ((pos.p0[i] + a.T) >> a.rshift) - (pos.p0[i] >> a.rshift));
+  if (pos.dev)
+    max_new = a.rshift ? (a.T + 1) >> 1 : a.T;
+  else
+    for (int i = 0; i < nb; ++i) max_new = max(max_new, ((pos.p0[i] + a.T) >> a.rshift) - (pos.p0[i] >> a.rshift));
   if (max_new > 0) {
     dim3 grid((unsigned)((max_new + kEntriesPerBlock - 1) / kEntriesPerBlock), (unsigned)nb);
     if (max_new == 1)

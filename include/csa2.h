@@ -23,7 +23,8 @@
  *    workspace (size from csa2_workspace_bytes), except for csa2_attend_static, whose
  *    scratch is a fixed array of the library (see there).
  *  - p0 is a HOST array of B int64 values: the absolute position of the first of the T new
- *    tokens of each sequence (its cached length before the call).
+ *    tokens of each sequence (its cached length before the call), or, after
+ *    csa2_set_device_positions, a device array that the kernels read when they run.
  *  - Every call is asynchronous on `stream` and never synchronises.  Argument errors are
  *    returned before anything is launched; launch errors come back as CSA2_ERR_CUDA.
  *  - Every wait inside a kernel is bounded (about 80 ms).  A wait that gives up records a
@@ -247,12 +248,35 @@ csa2_status csa2_tc_rate(csa2_handle* h, int kind, int iters, double* tflops, cs
 /* Failure report (no counterpart on the pages).  Synchronises `stream`, then reports whether
  * a bounded wait inside any kernel of this library gave up since the last check:
  * CSA2_ERR_TIMEOUT (the outputs of the calls since then are not to be trusted); else
- * CSA2_ERR_UNSUPPORTED if a kernel read an FP4 scale or query outside the fp16 domain (see the
- * conventions above); CSA2_ERR_CUDA if synchronising or reading the words failed; CSA2_OK
- * otherwise.  Clears the error words and domain flags.  Call with the handle's device current; while an error word is set, later waits
- * that stay pending give up early, so check before trusting further results.  Not for use
- * inside stream capture (it synchronises). */
+ * CSA2_ERR_SHAPE if a kernel read a device position outside 0..p0_max (see
+ * csa2_set_device_positions); else CSA2_ERR_UNSUPPORTED if a kernel read an FP4 scale or query
+ * outside the fp16 domain (see the conventions above); CSA2_ERR_CUDA if synchronising or
+ * reading the words failed; CSA2_OK otherwise.  Clears the error words and flags.  Call with
+ * the handle's device current; while an error word is set, later waits that stay pending give
+ * up early, so check before trusting further results.  Not for use inside stream capture (it
+ * synchronises). */
 csa2_status csa2_check(csa2_handle* h, csa2_stream_t stream);
+
+/* Positions from device memory, for a step captured once in a CUDA graph and replayed at every
+ * position (no counterpart on the pages; the positions are the p0 of the calls above).
+ *  - p0_dev: DEVICE array of B int64 (8-byte aligned, owned by the caller) with sequence b's
+ *    p0 at p0_dev[b], for the largest B of the calls that follow; NULL returns the handle to
+ *    host positions.  p0_max: a bound, 0 <= p0_dev[b] <= p0_max (CSA2_ERR_SHAPE unless
+ *    p0_max + 1 <= 2^21 - 2).
+ *  - While set, csa2_write_cache, the indexer calls and csa2_attend / csa2_attend_static do not
+ *    read their p0 argument (it may be NULL): their kernels read p0_dev when they run, and the
+ *    host validates and sizes everything (cache capacity, workspace, grids) as if every p0 were
+ *    p0_max, so workspaces are sized with max_entries = floor((p0_max + T) / ratio).  At ratio 2
+ *    csa2_write_cache then needs the pair buffers for every T.  csa2_attend_replay returns
+ *    CSA2_ERR_UNSUPPORTED.
+ *  - The calls enqueue the same kernels for every position, so a stream capture of one step
+ *    (after one uncaptured step, which loads the library's kernels) replays correctly at any
+ *    positions written to p0_dev before each replay.  Results are bit-identical to the calls
+ *    with those positions on the host.
+ *  - A value outside 0..p0_max is clamped into that range, so that every access stays within
+ *    what was validated, and csa2_check returns CSA2_ERR_SHAPE.
+ *  - Call outside stream capture, with the handle's device current. */
+csa2_status csa2_set_device_positions(csa2_handle* h, const int64_t* p0_dev, int64_t p0_max);
 
 /* Test hook for csa2_check (no counterpart on the pages): enqueues one kernel whose single
  * bounded wait can never complete (nothing arrives at its barrier), so that the next
