@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
   __shared__ float red_max[4][64];
   __shared__ float m_ref[64], alpha_s[64], l_run[64], den_s[64];  // den_s: 1 / denominator
   __shared__ int nrows_sh, nwin_sh;
+  grid_dep_wait();  // launched dependent: nothing is read before the previous kernel has ended
+  grid_dep_trigger();
 
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   unsigned char* sm = smem_raw + (sbase - smem_u32(smem_raw));
@@ -626,6 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendArgs a, Se
 // grid (T, nb, 64 heads), 128 threads x 4 dims.  Merges the split partials with the sink.
 __global__ void __launch_bounds__(128) attend_combine_kernel(AttendArgs a, SeqPos pos, int b0, RopeFreq rf, int nsplit,
                                                              const float* part_o, const float* part_ml) {
+  grid_dep_wait();  // launched dependent on the split blocks
   const int t = blockIdx.x, bl = blockIdx.y, h = blockIdx.z;
   const int b = b0 + bl;
   const int64_t qrow = (int64_t)b * a.T + t;
@@ -704,14 +707,16 @@ cudaError_t launch_attend(const AttendArgs& a, const SeqPos& pos, const SeqPos& 
     po = static_cast<float*>(ws);
     pml = po + rows * kH * kD;
   }
-  attend_tc_kernel<<<dim3((unsigned)a.T, (unsigned)nb, (unsigned)s), kThreads, kDynBytes, st>>>(a, pos, wst, b0, rf, s, cps,
-                                                                                                 po, pml);
+  // dependent launches: the kernel before each may still be ending when it is scheduled
+  e = launch_dependent(attend_tc_kernel, dim3((unsigned)a.T, (unsigned)nb, (unsigned)s), dim3(kThreads), kDynBytes, st, a,
+                       pos, wst, b0, rf, s, cps, po, pml);
   note_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
   if (s > 1) {
-    attend_combine_kernel<<<dim3((unsigned)a.T, (unsigned)nb, kH), 128, 0, st>>>(a, pos, b0, rf, s, po, pml);
+    e = launch_dependent(attend_combine_kernel, dim3((unsigned)a.T, (unsigned)nb, kH), dim3(128), 0, st, a, pos, b0, rf,
+                         s, po, pml);
     note_launch();
-    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
   }
   return e;
 }

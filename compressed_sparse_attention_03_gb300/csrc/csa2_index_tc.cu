@@ -480,6 +480,7 @@ __global__ void __launch_bounds__(kMThreads, 1) index_decode_mx_kernel(const __g
   __shared__ uint32_t shist[kHistBins];
   __shared__ uint32_t tmem_base_sh;
   __shared__ float wsh[kHI];
+  grid_dep_trigger();  // the select that follows may be scheduled as this kernel's blocks end
   __shared__ uint32_t qsf[kHI];  // Q^I scale word per head (byte k: block k)
   __shared__ int32_t spool[kHsiBlocks];
   __shared__ int64_t n_sh;

@@ -428,6 +428,8 @@ __global__ void __launch_bounds__(NT) topk_chunk_kernel(IndexArgs a, SeqPos pos,
   __shared__ uint32_t okey[kTopK];
   __shared__ int32_t oj[kTopK];
   __shared__ int cnt_sh;
+  grid_dep_wait();  // launched dependent on the scorer (histogram rows)
+  grid_dep_trigger();
   const int c = blockIdx.x, tl = blockIdx.y, bl = blockIdx.z;
   const int t = t0 + tl;
   if (t >= a.T || tl >= Tq) return;
@@ -514,6 +516,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(IndexArgs a, i
   __shared__ uint32_t okey[kTopK];
   __shared__ int32_t oj[kTopK];
   __shared__ int offs[kMaxChunks + 1];
+  grid_dep_wait();  // launched dependent on the chunk kernel
+  grid_dep_trigger();
   const int tl = blockIdx.x, bl = blockIdx.y;
   const int t = t0 + tl;
   if (t >= a.T) return;
@@ -954,18 +958,21 @@ cudaError_t launch_index_topk(const IndexArgs& a, const SeqPos& pos, int b0, int
       continue;
     }
     const int nch = (int)max64(1, (emax + p.chunk - 1) / p.chunk);
+    // rows with a histogram (decode) follow the scorer directly: dependent launches (the
+    // launch and block scheduling overlap the previous kernel's end)
     if (hist)
-      topk_chunk_kernel<kTopkThreads><<<dim3(nch, tq, nb), kTopkThreads, chunk_smem, st>>>(
-          a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch, ck, cj, cn, rowlen, hist, nullptr);
+      e = launch_dependent(topk_chunk_kernel<kTopkThreads>, dim3(nch, tq, nb), dim3(kTopkThreads), chunk_smem, st, a,
+                           pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch, ck, cj, cn, rowlen, hist, nullptr);
     else
       topk_chunk_kernel<kTopkSmall><<<dim3(nch, tq, nb), kTopkSmall, chunk_smem, st>>>(
           a, pos, b0, t0, p.Tq, sc, p.ld, p.chunk, nch, ck, cj, cn, rowlen, nullptr, lower);
     note_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     if (nch > 1) {
-      topk_merge_kernel<<<dim3(tq, nb), kTopkThreads, (size_t)nch * kTopK * 8, st>>>(a, b0, t0, p.Tq, nch, ck, cj, cn);
+      e = launch_dependent(topk_merge_kernel, dim3(tq, nb), dim3(kTopkThreads), (size_t)nch * kTopK * 8, st, a, b0, t0,
+                           p.Tq, nch, ck, cj, cn);
       note_launch();
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (mode == kIndexPool) {  // the block pool from this pass's score rows
       const int64_t nblk = (emax + kHsiBlock - 1) / kHsiBlock;

@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
   __shared__ float2 part[4][kEntriesPerBlock][kDI];  // (s, c) of each K quarter
   __shared__ float2 red[kEntriesPerBlock][4];
 
+  grid_dep_trigger();  // the window kernel may be scheduled now (it waits for this one's end)
   const int bl = blockIdx.y;
   const int b = b0 + bl;
   const int64_t p0 = seq_p0(pos, bl);
@@ -259,6 +260,7 @@ __global__ void __launch_bounds__(kEntryThreads) writer_entries_kernel(WriterArg
 __global__ void __launch_bounds__(kWriterThreads) writer_window_kernel(WriterArgs a, SeqPos pos, int b0, RopeFreq rf) {
   __shared__ float2 red[kWriterThreads / 32];
   __shared__ float r_sh;
+  grid_dep_wait();  // launched dependent on the entry kernel (which reads the pair buffer)
   const int t = blockIdx.x;
   const int bl = blockIdx.y;
   const int b = b0 + bl;
@@ -366,9 +368,10 @@ cudaError_t launch_writer(const WriterArgs& a, const SeqPos& pos, int b0, int nb
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  writer_window_kernel<<<dim3((unsigned)a.T, (unsigned)nb), kWriterThreads, 0, st>>>(a, pos, b0, rf);
+  cudaError_t e = launch_dependent(writer_window_kernel, dim3((unsigned)a.T, (unsigned)nb), dim3(kWriterThreads), 0, st, a,
+                                   pos, b0, rf);
   note_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace csa2
