@@ -65,4 +65,30 @@ def test_status_strings_and_config_checks(lib):
     assert lib.csa2_reindex_topk(*([None] * 5), 0, None, 1, 1, None, None, None, None, 0, None) == 1
     assert lib.csa2_check(None, None) == 1
     assert lib.csa2_selftest_timeout(None, None) == 1
+    assert lib.csa2_set_device_positions(None, None, 0) == 1
     assert lib.csa2_kernel_launches() == launches
+
+
+class _FakeHandle:
+    def __init__(self, ratio=2, dev_p0_max=None):
+        self.ratio, self.dev_p0_max = ratio, dev_p0_max
+
+
+def test_binding_positions_host_logic():
+    """The binding's position marshalling: host arrays as int64[B] (a scalar broadcast), None
+    passed as NULL only while the handle reads device positions, and workspace sizing from the
+    host positions or else from the device positions' bound."""
+    from compressed_sparse_attention_03_gb300 import _host_p0, _max_entries, _p0_ptr
+    h = _FakeHandle()
+    a = _host_p0([5, 9], 2, h)
+    assert a.dtype.name == "int64" and list(a) == [5, 9]
+    assert list(_host_p0(7, 3, h)) == [7, 7, 7]
+    with pytest.raises(ValueError):
+        _host_p0([1, 2, 3], 2, h)
+    with pytest.raises(ValueError):  # host positions are required without device positions
+        _host_p0(None, 2, h)
+    assert _max_entries(h, a, 4) == (9 + 4) // 2
+    hd = _FakeHandle(ratio=1, dev_p0_max=1000)
+    assert _host_p0(None, 2, hd) is None and _p0_ptr(None) is None
+    assert _max_entries(hd, None, 1) == 1001
+    assert list(_host_p0([3, 4], 2, hd)) == [3, 4]  # still accepted (the library does not read it)
